@@ -1,0 +1,213 @@
+"""CPU oracle of the routed MoE prefill layer (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its binding) never imports, links or runs anything here, and this package
+imports nothing from the product: the two share only the seeded input
+generator, which holds none of the layer's arithmetic.
+
+The arithmetic lives in ``moe_oracle.c`` (plain C, fp64, -ffp-contract=off);
+this module loads it with ctypes, building it with gcc on first use.  Each
+function cites the passage it follows in the C source:
+
+* ``plan``        -- the routing plan as a stable counting sort ("Round 4 Track
+  C: Prefill MoE Plan ...", section 1 items 1-2 and section 3);
+* ``gather``      -- the row gather (same page, section 1 item 4);
+* ``layer``       -- the flat (token, expert, weight) job pass and the slot-
+  ordered combine ("Batched resident MoE experts on Apple Silicon ...",
+  sections 1 and 3);
+* ``expert_rows`` / ``combine`` -- the same arithmetic cut at the stage
+  boundaries, to check one GPU stage at a time.
+
+Pins (CPU tests): brute force on tiny inputs, closed forms, a dense numpy
+cross-check for a single expert, invariants, and hand-worked fixtures under
+``tests/golden/``.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+GCC_FLAGS = ["-O2", "-std=c11", "-Wall", "-Wextra", "-fPIC", "-shared",
+             "-ffp-contract=off"]
+
+
+def build(force: bool = False) -> str:
+    """Compile moe_oracle.c into liboracle.so (gcc, host only)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *GCC_FLAGS, "-o", tmp, _SRC, "-lm", "-lpthread"],
+                       check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            # MOE_ORACLE_LIB points the tests' planted-mistake runs at a
+            # deliberately broken build of this same source
+            path = os.environ.get("MOE_ORACLE_LIB") or build()
+            lib = C.CDLL(path)
+            P = C.c_void_p
+            lib.oracle_plan.restype = C.c_long
+            lib.oracle_plan.argtypes = [P, P, C.c_int, C.c_int, C.c_int, C.c_int,
+                                        P, P, P, P, P, P, C.c_long]
+            lib.oracle_gather.restype = None
+            lib.oracle_gather.argtypes = [P, C.c_int, C.c_int, P, C.c_long, P]
+            lib.oracle_layer_tokens.restype = C.c_int
+            lib.oracle_layer_tokens.argtypes = [P, C.c_int, P, P, P, P, P, C.c_int,
+                                                C.c_int, C.c_int, C.c_int, C.c_int,
+                                                P, C.c_int, C.c_int, C.c_int, P]
+            lib.oracle_expert_rows.restype = C.c_int
+            lib.oracle_expert_rows.argtypes = [P, C.c_int, C.c_int, C.c_int, P, C.c_int,
+                                               P, P, C.c_int, P, P, P, C.c_int, C.c_int,
+                                               P, P]
+            lib.oracle_combine.restype = None
+            lib.oracle_combine.argtypes = [P, P, C.c_int, C.c_int, C.c_int, P]
+            lib.oracle_round_bf16.restype = C.c_double
+            lib.oracle_round_bf16.argtypes = [C.c_double]
+            lib.oracle_value16.restype = C.c_double
+            lib.oracle_value16.argtypes = [C.c_uint16, C.c_int]
+            _lib = lib
+    return _lib
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(C.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+_ERR = {-1: "bad argument", -2: "expert id outside [-1, E)", -3: "padded rows exceed capacity",
+        -4: "out of memory"}
+
+
+def capacity(T: int, k: int, E: int, tm: int) -> int:
+    """Rows that always hold the padded plan: T*k + min(E, T*k)*(tm-1)."""
+    n = T * k
+    return n + min(E, n) * (tm - 1)
+
+
+def plan(ids, w, E: int, tm: int, cap: int | None = None) -> dict:
+    """Routing plan of ids/w [T,k]: offsets, counts, srt_tok, srt_w, pos,
+    tile_expert (arrays trimmed to R_pad rows / R_pad/tm tiles) and R_pad."""
+    ids = _c(ids, np.int32)
+    w = _c(w, np.float32)
+    T, k = ids.shape
+    if cap is None:
+        cap = capacity(T, k, E, tm)
+    offsets = np.zeros(E + 1, np.int32)
+    counts = np.zeros(E, np.int32)
+    srt_tok = np.full(max(cap, 1), -7, np.int32)
+    srt_w = np.full(max(cap, 1), np.nan, np.float32)
+    pos = np.full(max(T * k, 1), -7, np.int32)
+    tile_expert = np.full(max(cap // tm + 1, 1), -7, np.int32)
+    r = _load().oracle_plan(_p(ids), _p(w), T, k, E, tm, _p(offsets), _p(counts),
+                            _p(srt_tok), _p(srt_w), _p(pos), _p(tile_expert), cap)
+    if r < 0:
+        raise OracleError(_ERR.get(r, str(r)))
+    return dict(R_pad=int(r), offsets=offsets, counts=counts, srt_tok=srt_tok[:r],
+                srt_w=srt_w[:r], pos=pos[:T * k].reshape(T, k),
+                tile_expert=tile_expert[:r // tm])
+
+
+def gather(x, srt_tok) -> np.ndarray:
+    """xs[r] = x[srt_tok[r]] (16-bit rows), zero rows where srt_tok is -1."""
+    x = _c(x, np.uint16)
+    T, d = x.shape
+    srt_tok = _c(srt_tok, np.int32)
+    R = srt_tok.shape[0]
+    xs = np.empty((max(R, 1), d), np.uint16)
+    _load().oracle_gather(_p(x), T, d, _p(srt_tok), R, _p(xs))
+    return xs[:R]
+
+
+def layer(x, ids, w, Wg, Wu, Wd, x_dtype: str = "bf16", tokens=None,
+          mirror: bool = False, nthreads: int | None = None) -> np.ndarray:
+    """Layer output y (fp64 [len(tokens), d]) for the listed tokens (all by
+    default).  ``mirror`` returns the bf16-mirror reference instead."""
+    x = _c(x, np.uint16)
+    ids = _c(ids, np.int32)
+    w = _c(w, np.float32)
+    Wg = _c(Wg, np.uint16)
+    Wu = _c(Wu, np.uint16)
+    Wd = _c(Wd, np.uint16)
+    T, d = x.shape
+    k = ids.shape[1]
+    E, d2, f = Wg.shape
+    assert d2 == d and Wu.shape == Wg.shape and Wd.shape == (E, f, d)
+    if tokens is None:
+        tokens = np.arange(T, dtype=np.int32)
+    tokens = _c(tokens, np.int32)
+    y = np.zeros((max(len(tokens), 1), d), np.float64)
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    rc = _load().oracle_layer_tokens(_p(x), int(x_dtype == "f16"), _p(ids), _p(w),
+                                     _p(Wg), _p(Wu), _p(Wd), T, d, E, k, f, _p(tokens),
+                                     len(tokens), int(bool(mirror)), int(nthreads), _p(y))
+    if rc != 0:
+        raise OracleError(_ERR.get(rc, str(rc)))
+    return y[:len(tokens)]
+
+
+def expert_rows(xs, rows, row_expert, row_w, Wg, Wu, Wd, x_dtype: str = "bf16",
+                mirror: bool = False, nthreads: int | None = None):
+    """For the listed rows of xs: h (fp64 [n, f]) and the weighted down
+    projection ys = w * o (fp64 [n, d])."""
+    xs = _c(xs, np.uint16)
+    d = xs.shape[1]
+    Wg = _c(Wg, np.uint16)
+    Wu = _c(Wu, np.uint16)
+    Wd = _c(Wd, np.uint16)
+    E, _, f = Wg.shape
+    rows = _c(rows, np.int64)
+    row_expert = _c(row_expert, np.int32)
+    row_w = _c(row_w, np.float32)
+    n = len(rows)
+    h = np.zeros((max(n, 1), f), np.float64)
+    ys = np.zeros((max(n, 1), d), np.float64)
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    rc = _load().oracle_expert_rows(_p(xs), int(x_dtype == "f16"), d, f, _p(rows), n,
+                                    _p(row_expert), _p(row_w), E, _p(Wg), _p(Wu), _p(Wd),
+                                    int(bool(mirror)), int(nthreads), _p(h), _p(ys))
+    if rc != 0:
+        raise OracleError(_ERR.get(rc, str(rc)))
+    return h[:n], ys[:n]
+
+
+def combine(Ys, pos) -> np.ndarray:
+    """y[t] = sum_j Ys[pos[t,j]] over j = 0..k-1 in order (fp64)."""
+    Ys = _c(Ys, np.uint16)
+    pos = _c(pos, np.int32)
+    T, k = pos.shape
+    d = Ys.shape[1]
+    y = np.zeros((max(T, 1), d), np.float64)
+    _load().oracle_combine(_p(Ys), _p(pos), T, k, d, _p(y))
+    return y[:T]
+
+
+def round_bf16(v: float) -> float:
+    return _load().oracle_round_bf16(float(v))
+
+
+def value16(bits: int, dtype: str = "bf16") -> float:
+    return _load().oracle_value16(int(bits), int(dtype == "f16"))

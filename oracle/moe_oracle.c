@@ -1,0 +1,498 @@
+/*
+ * CPU oracle of the routed MoE prefill layer.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the package's smoke check and the
+ * CPU-baseline leg of the benchmark load this library.  It shares no code,
+ * header, table or helper with the CUDA path, and the CUDA path never calls
+ * it.  It is written to be read against the pages, not to be fast: plain
+ * loops, fp64 arithmetic, no blocking, no reordering of any sum.  Build with
+ * -ffp-contract=off so that every a*b+c rounds twice, as written.
+ *
+ * Sources (page title, then section):
+ *  [P1] "Round 4 Track C: Prefill MoE Plan (mm_clear + mm_hist + mm_scan +
+ *       mm_place) & Epilogue / Gather Audit" -- section 1 items 1, 2 and 4
+ *       (histogram, padded scan with -1 tail rows, stable place, row gather)
+ *       and section 3 (the plan buffers compared bit for bit).
+ *  [P3] "Batched resident MoE experts on Apple Silicon: a flat parallel
+ *       expert pass" -- section 1 (an immutable (token, expert, weight) job
+ *       list; per job gate/up projection -> gated activation -> weighted down
+ *       projection) and section 3 (the same per-token top-k summation order).
+ *  [P4] "Add --moe-mode sweep-prefill" -- Mechanism (experts walked in
+ *       ascending id over contiguous slices).
+ *
+ * Readings taken where the pages leave a step open:
+ *  - flat entry i = t*k + j (token-major); ties inside an expert keep
+ *    increasing i;
+ *  - id -1 marks a skipped slot: no row, pos = -1, no contribution;
+ *  - an empty expert gets zero rows and zero tiles;
+ *  - pad rows carry srt_tok = -1 and srt_w = +0.0f; gathered pad rows are
+ *    all-zero bits;
+ *  - gated activation is SwiGLU: h = silu(g) * u with silu(z) = z/(1+e^-z),
+ *    g from the gate weight, u from the up weight;
+ *  - the routing weight scales each job's down projection; the token's
+ *    output sums its slots j = 0..k-1 in order starting from zero.
+ *
+ * Every function here is pinned by the CPU tests (brute force on tiny
+ * inputs, closed forms, library cross-checks and invariants).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_ERR_ARG (-1)
+#define ORC_ERR_ID (-2)
+#define ORC_ERR_CAP (-3)
+#define ORC_ERR_MEM (-4)
+
+/* ---- widening of 16-bit inputs (exact) --------------------------------- */
+
+static double bf16_value(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float v;
+    memcpy(&v, &u, sizeof v);
+    return (double)v;
+}
+
+static double f16_value(uint16_t h)
+{
+    int sign = h >> 15, ex = (h >> 10) & 0x1f, man = h & 0x3ff;
+    double v;
+    if (ex == 0)
+        v = ldexp((double)man, -24);               /* subnormal: man * 2^-24 */
+    else if (ex == 31)
+        v = man ? NAN : INFINITY;
+    else
+        v = ldexp((double)(man | 0x400), ex - 25); /* (1024+man) * 2^(ex-25) */
+    return sign ? -v : v;
+}
+
+static double value16(uint16_t b, int is_f16)
+{
+    return is_f16 ? f16_value(b) : bf16_value(b);
+}
+
+/* fp64 -> fp32 (C conversion, nearest) -> bf16 (nearest, ties to even). */
+static double to_bf16(double v)
+{
+    float f = (float)v;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7f800000u) != 0x7f800000u)
+        u += 0x7fffu + ((u >> 16) & 1u);
+    u &= 0xffff0000u;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* ---- routing plan [P1 sec. 1 items 1-2, sec. 3; P4 Mechanism] ---------- */
+
+/*
+ * The plan is a stable counting sort of the flat (token, slot) entries by
+ * expert id.  Its result is what [P1]'s serial rank loop computes ("rank =
+ * number of earlier entries of the block with the same expert", added to the
+ * block's base), which the page's optimised place reproduces bit for bit.
+ *
+ *   counts[e]      = number of entries routed to expert e
+ *   offsets[e]     = sum over e' < e of counts[e'] rounded up to tm
+ *   offsets[E]     = R_pad, the padded row total
+ *   pos[i]         = row of flat entry i (-1 for a skipped slot)
+ *   srt_tok[row]   = token of the entry in that row, -1 in pad rows
+ *   srt_w[row]     = routing weight of that entry (bit copy), +0 in pad rows
+ *   tile_expert[n] = expert owning rows [n*tm, (n+1)*tm)
+ *
+ * Returns R_pad, or ORC_ERR_ID if an id lies outside [-1, E), or
+ * ORC_ERR_CAP if R_pad exceeds cap.
+ */
+long oracle_plan(const int32_t *ids, const float *w, int T, int k, int E, int tm,
+                 int32_t *offsets, int32_t *counts, int32_t *srt_tok, float *srt_w,
+                 int32_t *pos, int32_t *tile_expert, long cap)
+{
+    long n = (long)T * (long)k;
+    long i, r;
+    int e;
+    int32_t *cursor;
+
+    if (T < 0 || k < 1 || E < 1 || tm < 1)
+        return ORC_ERR_ARG;
+
+    /* 1. per-expert row counts (the histogram) */
+    for (e = 0; e < E; e++)
+        counts[e] = 0;
+    for (i = 0; i < n; i++) {
+        int id = ids[i];
+        if (id == -1)
+            continue;
+        if (id < -1 || id >= E)
+            return ORC_ERR_ID;
+        counts[id]++;
+    }
+
+    /* 2. exclusive scan of the tile-padded counts, ascending expert id */
+    offsets[0] = 0;
+    for (e = 0; e < E; e++) {
+        long tiles = ((long)counts[e] + tm - 1) / tm;
+        offsets[e + 1] = (int32_t)(offsets[e] + tiles * tm);
+    }
+    if ((long)offsets[E] > cap)
+        return ORC_ERR_CAP;
+
+    /* 3. stable place: walk the entries in increasing i with one cursor per
+     *    expert that starts at the expert's first row */
+    cursor = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+    if (!cursor)
+        return ORC_ERR_MEM;
+    for (e = 0; e < E; e++)
+        cursor[e] = offsets[e];
+    for (i = 0; i < n; i++) {
+        int id = ids[i];
+        if (id == -1) {
+            pos[i] = -1;
+            continue;
+        }
+        r = cursor[id]++;
+        pos[i] = (int32_t)r;
+        srt_tok[r] = (int32_t)(i / k);
+        srt_w[r] = w[i];
+    }
+    free(cursor);
+
+    /* 4. the tail rows of each expert's last tile */
+    for (e = 0; e < E; e++) {
+        for (r = (long)offsets[e] + counts[e]; r < (long)offsets[e + 1]; r++) {
+            srt_tok[r] = -1;
+            srt_w[r] = 0.0f;
+        }
+    }
+
+    /* 5. tile table */
+    for (e = 0; e < E; e++) {
+        long t;
+        for (t = offsets[e] / tm; t < offsets[e + 1] / tm; t++)
+            tile_expert[t] = e;
+    }
+    return (long)offsets[E];
+}
+
+/* ---- row gather [P1 sec. 1 item 4] ------------------------------------- */
+
+/* xs[r] = x[srt_tok[r]] for a real row, an all-zero row for a pad row. */
+void oracle_gather(const uint16_t *x, int T, int d, const int32_t *srt_tok,
+                   long R_pad, uint16_t *xs)
+{
+    long r;
+    for (r = 0; r < R_pad; r++) {
+        int t = srt_tok[r];
+        if (t >= 0 && t < T)
+            memcpy(xs + r * (long)d, x + (long)t * d, sizeof(uint16_t) * (size_t)d);
+        else
+            memset(xs + r * (long)d, 0, sizeof(uint16_t) * (size_t)d);
+    }
+}
+
+/* ---- one job of the flat expert pass [P3 sec. 1] ----------------------- */
+
+/*
+ * For one routed row x (length d) and expert e:
+ *   g[n] = sum_c x[c] * Wg[e][c][n]      (c = 0..d-1 in order)
+ *   u[n] = sum_c x[c] * Wu[e][c][n]
+ *   h[n] = silu(g[n]) * u[n],  silu(z) = z / (1 + exp(-z))
+ *   o[m] = sum_n h[n] * Wd[e][n][m]      (n = 0..f-1 in order)
+ * Weights are bf16 with layouts Wg, Wu [E][d][f] and Wd [E][f][d].
+ * mirror != 0 rounds h to bf16 before the down projection, as a GPU that
+ * stores h in bf16 does (used only for the second, reported reference).
+ */
+static void expert_job(const uint16_t *xrow, int x_is_f16, const uint16_t *Wg_e,
+                       const uint16_t *Wu_e, const uint16_t *Wd_e, int d, int f,
+                       int mirror, double *xv, double *g, double *u, double *h,
+                       double *o)
+{
+    int c, n, m;
+    for (c = 0; c < d; c++)
+        xv[c] = value16(xrow[c], x_is_f16);
+    for (n = 0; n < f; n++) {
+        g[n] = 0.0;
+        u[n] = 0.0;
+    }
+    for (c = 0; c < d; c++) {
+        const uint16_t *wg = Wg_e + (long)c * f;
+        const uint16_t *wu = Wu_e + (long)c * f;
+        for (n = 0; n < f; n++) {
+            g[n] += xv[c] * bf16_value(wg[n]);
+            u[n] += xv[c] * bf16_value(wu[n]);
+        }
+    }
+    for (n = 0; n < f; n++) {
+        h[n] = g[n] / (1.0 + exp(-g[n])) * u[n];
+        if (mirror)
+            h[n] = to_bf16(h[n]);
+    }
+    for (m = 0; m < d; m++)
+        o[m] = 0.0;
+    for (n = 0; n < f; n++) {
+        const uint16_t *wd = Wd_e + (long)n * d;
+        for (m = 0; m < d; m++)
+            o[m] += h[n] * bf16_value(wd[m]);
+    }
+}
+
+/* A job: one routed row, its expert, and where its results go. */
+typedef struct {
+    const uint16_t *xrow;
+    int e;
+    double *h; /* [f] or NULL */
+    double *o; /* [d] */
+} job_t;
+
+typedef struct {
+    const job_t *jobs;
+    long njobs;
+    int tid, nthreads;
+    int x_is_f16, d, f, mirror;
+    const uint16_t *Wg, *Wu, *Wd;
+    int failed;
+} pass_t;
+
+static void *pass_worker(void *arg)
+{
+    pass_t *p = (pass_t *)arg;
+    long d = p->d, f = p->f, j;
+    double *xv = (double *)malloc(sizeof(double) * (size_t)(d + 3 * f));
+    double *g, *u, *hbuf;
+    if (!xv) {
+        p->failed = 1;
+        return NULL;
+    }
+    g = xv + d;
+    u = g + f;
+    hbuf = u + f;
+    /* jobs are independent; each thread takes every nthreads-th job, so the
+     * arithmetic of a job does not depend on the thread count */
+    for (j = p->tid; j < p->njobs; j += p->nthreads) {
+        const job_t *jb = &p->jobs[j];
+        long eo = (long)jb->e * d * f;
+        expert_job(jb->xrow, p->x_is_f16, p->Wg + eo, p->Wu + eo, p->Wd + eo,
+                   p->d, p->f, p->mirror, xv, g, u, jb->h ? jb->h : hbuf, jb->o);
+    }
+    free(xv);
+    return NULL;
+}
+
+/* Run the flat parallel pass over a job list on nthreads host threads. */
+static int run_pass(const job_t *jobs, long njobs, int x_is_f16, int d, int f,
+                    int mirror, const uint16_t *Wg, const uint16_t *Wu,
+                    const uint16_t *Wd, int nthreads)
+{
+    pthread_t th[256];
+    pass_t ps[256];
+    int started[256];
+    int t, failed = 0;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > 256)
+        nthreads = 256;
+    if ((long)nthreads > njobs)
+        nthreads = njobs > 0 ? (int)njobs : 1;
+    for (t = 0; t < nthreads; t++) {
+        ps[t].jobs = jobs;
+        ps[t].njobs = njobs;
+        ps[t].tid = t;
+        ps[t].nthreads = nthreads;
+        ps[t].x_is_f16 = x_is_f16;
+        ps[t].d = d;
+        ps[t].f = f;
+        ps[t].mirror = mirror;
+        ps[t].Wg = Wg;
+        ps[t].Wu = Wu;
+        ps[t].Wd = Wd;
+        ps[t].failed = 0;
+        started[t] = 0;
+    }
+    for (t = 1; t < nthreads; t++)
+        started[t] = pthread_create(&th[t], NULL, pass_worker, &ps[t]) == 0;
+    pass_worker(&ps[0]);
+    for (t = 1; t < nthreads; t++) {
+        if (started[t])
+            pthread_join(th[t], NULL);
+        else
+            pass_worker(&ps[t]); /* could not start a thread: do its share here */
+    }
+    for (t = 0; t < nthreads; t++)
+        failed |= ps[t].failed;
+    return failed ? ORC_ERR_MEM : ORC_OK;
+}
+
+/* ---- the layer for a set of tokens [P3 sec. 1, sec. 3] ----------------- */
+
+/*
+ * y[ti][m] for the tokens tokens[0..ntok-1] (any subset, any order):
+ *   build the job list of every (token, slot j) with ids[t*k+j] != -1,
+ *   run each job through its expert (expert_job), then for each token
+ *   y = sum over j = 0..k-1 in order of w[t*k+j] * o_(t,j), from 0.0.
+ * mirror != 0 gives the bf16 mirror instead: h rounded to bf16 in the job,
+ * each weighted slot output rounded to bf16, slots summed in fp32 in order,
+ * the sum rounded to bf16.
+ * Returns ORC_OK, ORC_ERR_ID for an id outside [-1, E), ORC_ERR_ARG for a
+ * token outside [0, T), or ORC_ERR_MEM.
+ */
+int oracle_layer_tokens(const uint16_t *x, int x_is_f16, const int32_t *ids,
+                        const float *w, const uint16_t *Wg, const uint16_t *Wu,
+                        const uint16_t *Wd, int T, int d, int E, int k, int f,
+                        const int32_t *tokens, int ntok, int mirror, int nthreads,
+                        double *y)
+{
+    long ti, j, nj = 0, m;
+    job_t *jobs = NULL;
+    double *obuf;
+    long *slot_job;
+    int rc;
+
+    for (ti = 0; ti < ntok; ti++) {
+        int t = tokens[ti];
+        if (t < 0 || t >= T)
+            return ORC_ERR_ARG;
+        for (j = 0; j < k; j++) {
+            int e = ids[(long)t * k + j];
+            if (e == -1)
+                continue;
+            if (e < -1 || e >= E)
+                return ORC_ERR_ID;
+            nj++;
+        }
+    }
+    jobs = (job_t *)calloc((size_t)(nj > 0 ? nj : 1), sizeof(job_t));
+    obuf = (double *)malloc(sizeof(double) * (size_t)(nj > 0 ? nj : 1) * (size_t)d);
+    slot_job = (long *)malloc(sizeof(long) * (size_t)(ntok > 0 ? ntok : 1) * (size_t)k);
+    if (!jobs || !obuf || !slot_job) {
+        free(jobs);
+        free(obuf);
+        free(slot_job);
+        return ORC_ERR_MEM;
+    }
+
+    /* the immutable job list */
+    nj = 0;
+    for (ti = 0; ti < ntok; ti++) {
+        int t = tokens[ti];
+        for (j = 0; j < k; j++) {
+            int e = ids[(long)t * k + j];
+            if (e == -1) {
+                slot_job[ti * k + j] = -1;
+                continue;
+            }
+            jobs[nj].xrow = x + (long)t * d;
+            jobs[nj].e = e;
+            jobs[nj].h = NULL;
+            jobs[nj].o = obuf + nj * (long)d;
+            slot_job[ti * k + j] = nj;
+            nj++;
+        }
+    }
+
+    /* one flat pass over all jobs */
+    rc = run_pass(jobs, nj, x_is_f16, d, f, mirror, Wg, Wu, Wd, nthreads);
+
+    /* per-token combine in slot order */
+    if (rc == ORC_OK) {
+        for (ti = 0; ti < ntok; ti++) {
+            int t = tokens[ti];
+            double *yt = y + ti * (long)d;
+            if (!mirror) {
+                for (m = 0; m < d; m++)
+                    yt[m] = 0.0;
+                for (j = 0; j < k; j++) {
+                    long jb = slot_job[ti * k + j];
+                    double wt;
+                    if (jb < 0)
+                        continue;
+                    wt = (double)w[(long)t * k + j];
+                    for (m = 0; m < d; m++)
+                        yt[m] += wt * jobs[jb].o[m];
+                }
+            } else {
+                for (m = 0; m < d; m++) {
+                    float acc = 0.0f;
+                    for (j = 0; j < k; j++) {
+                        long jb = slot_job[ti * k + j];
+                        if (jb < 0)
+                            continue;
+                        acc += (float)to_bf16((double)w[(long)t * k + j] * jobs[jb].o[m]);
+                    }
+                    yt[m] = to_bf16((double)acc);
+                }
+            }
+        }
+    }
+    free(jobs);
+    free(obuf);
+    free(slot_job);
+    return rc;
+}
+
+/* ---- stage-level views used to check one GPU stage at a time ------------ */
+
+/*
+ * Expert FFN on given routed rows: for each listed row r of xs (16-bit,
+ * [*, d]) with expert row_expert[i] and routing weight row_w[i]:
+ *   h_out[i][n] = h of that job and ys_out[i][m] = row_w[i] * o[m].
+ * Same arithmetic as oracle_layer_tokens' jobs.
+ */
+int oracle_expert_rows(const uint16_t *xs, int x_is_f16, int d, int f,
+                       const int64_t *rows, int nrows, const int32_t *row_expert,
+                       const float *row_w, int E, const uint16_t *Wg,
+                       const uint16_t *Wu, const uint16_t *Wd, int mirror,
+                       int nthreads, double *h_out, double *ys_out)
+{
+    long i, m;
+    job_t *jobs = (job_t *)calloc((size_t)(nrows > 0 ? nrows : 1), sizeof(job_t));
+    int rc;
+    if (!jobs)
+        return ORC_ERR_MEM;
+    for (i = 0; i < nrows; i++) {
+        if (row_expert[i] < 0 || row_expert[i] >= E) {
+            free(jobs);
+            return ORC_ERR_ID;
+        }
+        jobs[i].xrow = xs + rows[i] * (long)d;
+        jobs[i].e = row_expert[i];
+        jobs[i].h = h_out + i * (long)f;
+        jobs[i].o = ys_out + i * (long)d;
+    }
+    rc = run_pass(jobs, nrows, x_is_f16, d, f, mirror, Wg, Wu, Wd, nthreads);
+    if (rc == ORC_OK) {
+        for (i = 0; i < nrows; i++)
+            for (m = 0; m < d; m++)
+                ys_out[i * (long)d + m] *= (double)row_w[i];
+    }
+    free(jobs);
+    return rc;
+}
+
+/*
+ * Combine of given weighted rows: y[t][m] = sum over j = 0..k-1 in order of
+ * Ys[pos[t*k+j]][m] (bf16 rows, skipped when pos is -1), in fp64 from 0.0.
+ */
+void oracle_combine(const uint16_t *Ys, const int32_t *pos, int T, int k, int d,
+                    double *y)
+{
+    long t, j, m;
+    for (t = 0; t < T; t++) {
+        double *yt = y + t * (long)d;
+        for (m = 0; m < d; m++)
+            yt[m] = 0.0;
+        for (j = 0; j < k; j++) {
+            long p = pos[t * k + j];
+            if (p < 0)
+                continue;
+            for (m = 0; m < d; m++)
+                yt[m] += bf16_value(Ys[p * (long)d + m]);
+        }
+    }
+}
+
+/* bf16 rounding as the oracle does it, exposed so the tests can pin it. */
+double oracle_round_bf16(double v) { return to_bf16(v); }
+double oracle_value16(uint16_t b, int is_f16) { return value16(b, is_f16); }

@@ -1,0 +1,50 @@
+"""Planted mistakes: each is a plausible slip in the oracle's C source, built
+on the CPU into a separate library, and the pin tests must fail on every one.
+This shows the pins constrain each step of the oracle, not just its shape."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(os.path.dirname(HERE), "oracle", "moe_oracle.c")
+
+MUTANTS = {
+    "gate_up_swapped": ("h[n] = g[n] / (1.0 + exp(-g[n])) * u[n];",
+                        "h[n] = u[n] / (1.0 + exp(-u[n])) * g[n];"),
+    "sigmoid_sign": ("h[n] = g[n] / (1.0 + exp(-g[n])) * u[n];",
+                     "h[n] = g[n] / (1.0 + exp(g[n])) * u[n];"),
+    "down_transposed": ("o[m] += h[n] * bf16_value(wd[m]);",
+                        "o[m] += h[n] * bf16_value(Wd_e[(long)m * f + n]);"),
+    "weight_dropped": ("yt[m] += wt * jobs[jb].o[m];", "yt[m] += jobs[jb].o[m];"),
+    "no_padding": ("offsets[e + 1] = (int32_t)(offsets[e] + tiles * tm);",
+                   "offsets[e + 1] = (int32_t)(offsets[e] + counts[e]);"),
+    "pad_token_zero": ("            srt_tok[r] = -1;\n            srt_w[r] = 0.0f;",
+                       "            srt_tok[r] = 0;\n            srt_w[r] = 0.0f;"),
+    "token_from_slot": ("srt_tok[r] = (int32_t)(i / k);", "srt_tok[r] = (int32_t)(i % k);"),
+    "unstable_place": ("        r = cursor[id]++;", "        r = offsets[id + 1] - 1 - (cursor[id]++ - offsets[id]) - (offsets[id + 1] - offsets[id] - counts[id]);"),
+    "last_slot_dropped": ("        for (j = 0; j < k; j++) {\n            int e = ids[(long)t * k + j];\n            if (e == -1) {",
+                          "        for (j = 0; j < k; j++) {\n            int e = (j == k - 1 && k > 1) ? -1 : ids[(long)t * k + j];\n            if (e == -1) {"),
+    "f16_exponent_bias": ("v = ldexp((double)(man | 0x400), ex - 25);", "v = ldexp((double)(man | 0x400), ex - 24);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, name
+    mut = tmp_path / f"{name}.c"
+    mut.write_text(src.replace(old, new))
+    lib = tmp_path / f"lib{name}.so"
+    subprocess.run(["gcc", *oracle.GCC_FLAGS, "-o", str(lib), str(mut), "-lm", "-lpthread"],
+                   check=True, capture_output=True)
+    env = dict(os.environ, MOE_ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(HERE, "test_oracle_plan.py"),
+                        os.path.join(HERE, "test_oracle_layer.py")],
+                       env=env, capture_output=True, text=True, cwd=os.path.dirname(HERE))
+    assert r.returncode != 0, f"planted mistake {name} passed every pin:\n{r.stdout[-2000:]}"
