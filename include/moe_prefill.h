@@ -1,0 +1,259 @@
+/*
+ * moe_prefill.h -- C ABI of the GB300 (sm_103a) routed MoE prefill layer.
+ *
+ * The layer of one prefill chunk runs in four stages, each one call below:
+ *
+ *   moe_plan        routing plan: per-block expert histogram, exclusive scan
+ *                   with each expert padded to a multiple of tm (tail rows
+ *                   set to -1), stable place -> srt_tok / srt_w / pos
+ *                   ("Round 4 Track C: Prefill MoE Plan (mm_clear + mm_hist +
+ *                   mm_scan + mm_place) & Epilogue / Gather Audit", section 1
+ *                   items 1-2, section 3)
+ *   moe_gather      token rows copied into expert-sorted order (same page,
+ *                   section 1 item 4)
+ *   moe_expert_ffn  grouped expert FFN: gate/up projection, SwiGLU, down
+ *                   projection scaled by the routing weight ("Batched resident
+ *                   MoE experts on Apple Silicon: a flat parallel expert
+ *                   pass", section 1); split into moe_ffn_gate_up and
+ *                   moe_ffn_down for callers that time or check them apart
+ *   moe_combine     per-token sum of its k weighted rows in slot order
+ *                   (same page, section 3)
+ *
+ * moe_layer_forward runs all four on one stream.
+ *
+ * Conventions shared by every call
+ *  - Tensors are caller-owned DEVICE pointers, row-major and contiguous.
+ *    16-bit tensors are passed as void* and hold bf16 (or fp16 where a
+ *    dtype argument allows it).  16-bit row tensors (x, xs, H, Ys, y and
+ *    the weights) must be 16-byte aligned, int32/fp32 arrays 4-byte aligned
+ *    and workspaces 256-byte aligned (MOE_ERR_ALIGN otherwise).
+ *  - Every call is asynchronous on `stream` (NULL = the legacy default
+ *    stream) and returns once its kernels are enqueued.  The library never
+ *    allocates device memory, never synchronises the host (except
+ *    moe_read_status, on request) and keeps no per-call state.  Kernels are
+ *    chained with programmatic dependent launch.
+ *  - Flat entry i = t*k + j is token t's slot j.  An expert id of -1 marks a
+ *    skipped slot: it gets no row, pos = -1 and adds nothing to y.
+ *  - Sizes that depend on the routing (R_pad = offsets[E], the padded row
+ *    count) stay on the device; kernels size their grids for the capacity
+ *    `cap` and read R_pad on the device.
+ *  - A return value < 0 is an argument error found on the host before
+ *    anything is enqueued (or MOE_ERR_CUDA if a launch failed).  Errors in
+ *    the data (an id outside [-1, E), bad offsets, a wait that ran out its
+ *    time limit) are recorded as bits of a device status word.
+ *
+ * The device must be sm_103 (GB300); the kernels are built for sm_103a only.
+ */
+#ifndef MOE_PREFILL_H
+#define MOE_PREFILL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Entry points are exported from the shared library (built with hidden
+ * default visibility). */
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+/* Same type as cudaStream_t; declared here so that this header needs no
+ * CUDA header. */
+struct CUstream_st;
+typedef struct CUstream_st *moe_stream_t;
+
+/* dtype of 16-bit activation rows */
+#define MOE_DT_BF16 0
+#define MOE_DT_F16 1
+
+/* return codes */
+#define MOE_OK 0
+#define MOE_ERR_NULL (-1)      /* a required pointer is NULL */
+#define MOE_ERR_SHAPE (-2)     /* a size is outside its documented range */
+#define MOE_ERR_CAPACITY (-3)  /* cap < moe_capacity(T, k, E, tm) */
+#define MOE_ERR_WORKSPACE (-4) /* ws_bytes smaller than required */
+#define MOE_ERR_ALIGN (-5)     /* a pointer is not aligned as required */
+#define MOE_ERR_CUDA (-6)      /* a CUDA call or a kernel launch failed */
+#define MOE_ERR_DTYPE (-7)     /* unsupported dtype */
+
+/* bits of the device status word */
+#define MOE_STATUS_BAD_ID 1u      /* an id outside [-1, E): that slot was skipped */
+#define MOE_STATUS_OVERFLOW 2u    /* padded rows exceeded cap: rows >= cap dropped */
+#define MOE_STATUS_BAD_OFFSETS 4u /* offsets not ascending multiples of 16 within cap:
+                                     that expert was skipped by the FFN */
+#define MOE_STATUS_TIMEOUT 8u     /* a pipeline wait inside a GEMM ran out its
+                                     time limit (about 2 s); the kernel stopped */
+
+/* limits */
+#define MOE_MAX_EXPERTS 4096
+#define MOE_MAX_TOPK 256
+#define MOE_MAX_TM 1024
+
+/*
+ * Rows that always hold the padded plan: T*k + min(E, T*k)*(tm-1).
+ * Every expert pads at most tm-1 rows and at most min(E, T*k) experts are
+ * routed to.  srt_tok, srt_w, xs, H and Ys need this many rows.
+ * Returns -1 for negative or out-of-range sizes.
+ */
+MOE_API int64_t moe_capacity(int T, int k, int E, int tm);
+
+/*
+ * Device workspace of moe_plan, in bytes: a 256-byte header holding the
+ * status word (uint32 at offset 0) followed by the per-block expert counts.
+ */
+MOE_API size_t moe_plan_workspace_bytes(int T, int k, int E);
+
+/*
+ * moe_plan -- the routing plan ("Round 4 Track C: Prefill MoE Plan ...",
+ * section 1 items 1-2; buffers as listed in section 3).
+ *
+ * in   ids      int32 [T, k]  expert of each (token, slot); -1 = skipped
+ * in   w        fp32  [T, k]  routing weight of each (token, slot)
+ * out  offsets  int32 [E+1]   offsets[e] = first row of expert e; offsets[E] = R_pad.
+ *                             Each expert owns ceil(counts[e]/tm)*tm rows, in
+ *                             ascending expert id.
+ * out  counts   int32 [E]     routed rows of each expert
+ * out  srt_tok  int32 [cap]   token of each row; -1 in pad rows
+ * out  srt_w    fp32  [cap]   routing weight of each row (bit copy); +0 in pad rows
+ * out  pos      int32 [T, k]  row of each (token, slot); -1 for a skipped slot
+ * out  tile_expert int32 [cap/tm]  expert owning rows [n*tm, (n+1)*tm)
+ * ws                          moe_plan_workspace_bytes(T, k, E) bytes
+ *
+ * Inside an expert, rows keep increasing flat index (token order, then
+ * slot): the plan is a stable counting sort and is unique, so it is
+ * bit-exact.  Only rows < R_pad and tiles < R_pad/tm are written.
+ * Sizes: 0 <= T, 1 <= k <= MOE_MAX_TOPK, 1 <= E <= MOE_MAX_EXPERTS,
+ * 1 <= tm <= MOE_MAX_TM, T*k < 2^31, cap >= moe_capacity(T, k, E, tm).
+ * The status word is reset by every call; ids outside [-1, E) set
+ * MOE_STATUS_BAD_ID and are treated as skipped.
+ */
+MOE_API int moe_plan(const int32_t *ids, const float *w, int T, int k, int E, int tm,
+             int32_t *offsets, int32_t *counts, int32_t *srt_tok, float *srt_w,
+             int32_t *pos, int32_t *tile_expert, int64_t cap, void *ws,
+             size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_gather -- rows into expert-sorted order (same page, section 1 item 4).
+ *
+ * in   x        16-bit [T, d]   token activations (dtype MOE_DT_BF16 or MOE_DT_F16)
+ * in   srt_tok  int32 [cap]     from moe_plan
+ * in   offsets  int32 [E+1]     from moe_plan (R_pad = offsets[E] read on the device)
+ * out  xs       16-bit [cap, d] xs[r] = x[srt_tok[r]]; all-zero bits where srt_tok[r] = -1.
+ *                               Rows >= R_pad are not written.
+ * d must be a positive multiple of 8 (16-byte rows).  A bit copy.
+ */
+MOE_API int moe_gather(const void *x, int dtype, int T, int d, const int32_t *srt_tok,
+               const int32_t *offsets, int E, int64_t cap, void *xs,
+               moe_stream_t stream);
+
+/*
+ * moe_ffn_gate_up -- grouped gate/up projection with SwiGLU.
+ *
+ * For each expert e and each of its rows r in [offsets[e], offsets[e+1]):
+ *   g = xs[r] . Wg[e],  u = xs[r] . Wu[e]   (bf16 operands, fp32 accumulation)
+ *   H[r] = bf16(silu(g) * u),  silu(z) = z / (1 + e^-z)
+ * in   xs       bf16 [cap, d]
+ * in   Wg, Wu   bf16 [E, d, f]
+ * in   offsets  int32 [E+1]   ascending multiples of 16, offsets[E] <= cap
+ * out  H        bf16 [cap, f] rows < R_pad written
+ * in   status   uint32* device word to OR error bits into, or NULL
+ * d and f must be positive multiples of 64.
+ */
+MOE_API int moe_ffn_gate_up(const void *xs, const void *Wg, const void *Wu,
+                    const int32_t *offsets, int E, int d, int f, int64_t cap,
+                    void *H, uint32_t *status, moe_stream_t stream);
+
+/*
+ * moe_ffn_down -- grouped down projection scaled by the routing weight.
+ *
+ *   Ys[r] = bf16(srt_w[r] * (H[r] . Wd[e]))   (fp32 accumulation)
+ * in   H        bf16 [cap, f]
+ * in   Wd       bf16 [E, f, d]
+ * in   offsets  int32 [E+1]
+ * in   srt_w    fp32 [cap]
+ * out  Ys       bf16 [cap, d] rows < R_pad written
+ */
+MOE_API int moe_ffn_down(const void *H, const void *Wd, const int32_t *offsets,
+                 const float *srt_w, int E, int d, int f, int64_t cap, void *Ys,
+                 uint32_t *status, moe_stream_t stream);
+
+/* moe_expert_ffn -- moe_ffn_gate_up then moe_ffn_down; H is caller scratch
+ * of cap*f bf16. */
+MOE_API int moe_expert_ffn(const void *xs, const void *Wg, const void *Wu, const void *Wd,
+                   const int32_t *offsets, const float *srt_w, int E, int d, int f,
+                   int64_t cap, void *H, void *Ys, uint32_t *status,
+                   moe_stream_t stream);
+
+/*
+ * moe_combine -- y[t] = sum over j = 0..k-1, in that order, of Ys[pos[t*k+j]]
+ * ("Batched resident MoE experts on Apple Silicon ...", section 3: the same
+ * per-token top-k summation order).  fp32 accumulation from zero, one bf16
+ * rounding at the end; slots with pos = -1 add nothing.
+ * in   Ys   bf16 [*, d]   weighted expert rows (from moe_ffn_down)
+ * in   pos  int32 [T, k]
+ * out  y    bf16 [T, d]
+ * d must be a positive multiple of 8.
+ */
+MOE_API int moe_combine(const void *Ys, const int32_t *pos, int T, int k, int d, void *y,
+                moe_stream_t stream);
+
+/* Fields of the moe_layer_forward workspace (byte offsets, see
+ * moe_workspace_layout).  The plan's own workspace (status word + counts)
+ * sits at offset 0, so moe_read_status works on either workspace. */
+#define MOE_WS_STATUS 0
+#define MOE_WS_BCNT 1
+#define MOE_WS_OFFSETS 2
+#define MOE_WS_COUNTS 3
+#define MOE_WS_SRT_TOK 4
+#define MOE_WS_SRT_W 5
+#define MOE_WS_POS 6
+#define MOE_WS_TILE_EXPERT 7
+#define MOE_WS_XS 8
+#define MOE_WS_H 9
+#define MOE_WS_YS 10
+#define MOE_WS_TOTAL 11
+#define MOE_WS_FIELDS 12
+
+/* Device workspace of moe_layer_forward, in bytes (0 on bad sizes). */
+MOE_API size_t moe_workspace_bytes(int T, int d, int E, int k, int f, int tm);
+
+/* Byte offset of every MOE_WS_* field inside that workspace (out has
+ * MOE_WS_FIELDS entries; out[MOE_WS_TOTAL] = total bytes).  Host only. */
+MOE_API int moe_workspace_layout(int T, int d, int E, int k, int f, int tm, size_t *out);
+
+/*
+ * moe_layer_forward -- the whole routed MoE layer of one prefill chunk:
+ * moe_plan -> moe_gather -> moe_ffn_gate_up -> moe_ffn_down -> moe_combine.
+ *
+ * in   x        bf16 [T, d]
+ * in   ids, w   [T, k] as in moe_plan
+ * in   Wg, Wu   bf16 [E, d, f];  Wd bf16 [E, f, d]
+ * out  y        bf16 [T, d]
+ * ws            moe_workspace_bytes(T, d, E, k, f, tm) bytes, 256-byte aligned;
+ *               it holds the plan, xs, H and Ys (see moe_workspace_layout)
+ * tm must be a multiple of 16; d and f multiples of 64.
+ */
+MOE_API int moe_layer_forward(const void *x, const int32_t *ids, const float *w,
+                      const void *Wg, const void *Wu, const void *Wd, int T, int d,
+                      int E, int k, int f, int tm, void *y, void *ws, size_t ws_bytes,
+                      moe_stream_t stream);
+
+/*
+ * moe_read_status -- copy the status word at ws (a plan or layer workspace)
+ * to *status, synchronising `stream` only.
+ */
+MOE_API int moe_read_status(const void *ws, moe_stream_t stream, uint32_t *status);
+
+/* Human-readable text of a return code. */
+MOE_API const char *moe_status_str(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_PREFILL_H */

@@ -1,0 +1,301 @@
+"""Thin binding of ``libmoe_prefill.so`` (the C ABI in ``include/moe_prefill.h``).
+
+Argument marshalling only: every step of the layer runs in the library's
+CUDA kernels.  PyTorch provides device memory and the current stream.  There
+is no fallback: if the library is missing or a call fails, this raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libmoe_prefill.so")
+_lock = threading.Lock()
+_lib = None
+
+# return codes and status bits (include/moe_prefill.h)
+MOE_OK = 0
+MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_CAPACITY, MOE_ERR_WORKSPACE = -1, -2, -3, -4
+MOE_ERR_ALIGN, MOE_ERR_CUDA, MOE_ERR_DTYPE = -5, -6, -7
+STATUS_BAD_ID, STATUS_OVERFLOW, STATUS_BAD_OFFSETS, STATUS_TIMEOUT = 1, 2, 4, 8
+DT_BF16, DT_F16 = 0, 1
+WS_FIELDS = ["status", "bcnt", "offsets", "counts", "srt_tok", "srt_w", "pos", "tile_expert",
+             "xs", "H", "Ys", "total"]
+
+_SIGS = {
+    "moe_capacity": (C.c_int64, [C.c_int] * 4),
+    "moe_plan_workspace_bytes": (C.c_size_t, [C.c_int] * 3),
+    "moe_plan": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int,
+                           C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                           C.c_void_p, C.c_int64, C.c_void_p, C.c_size_t, C.c_void_p]),
+    "moe_gather": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p,
+                             C.c_int, C.c_int64, C.c_void_p, C.c_void_p]),
+    "moe_ffn_gate_up": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int,
+                                  C.c_int, C.c_int, C.c_int64, C.c_void_p, C.c_void_p,
+                                  C.c_void_p]),
+    "moe_ffn_down": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int,
+                               C.c_int, C.c_int, C.c_int64, C.c_void_p, C.c_void_p,
+                               C.c_void_p]),
+    "moe_expert_ffn": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                 C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int64, C.c_void_p,
+                                 C.c_void_p, C.c_void_p, C.c_void_p]),
+    "moe_combine": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p,
+                              C.c_void_p]),
+    "moe_workspace_bytes": (C.c_size_t, [C.c_int] * 6),
+    "moe_workspace_layout": (C.c_int, [C.c_int] * 6 + [C.c_void_p]),
+    "moe_layer_forward": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                    C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int,
+                                    C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_size_t,
+                                    C.c_void_p]),
+    "moe_read_status": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p]),
+    "moe_status_str": (C.c_char_p, [C.c_int]),
+}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} failed: {code} ({status_str(code)})")
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m moe_prefill_routing_gb300.build`")
+            L = C.CDLL(LIB_PATH)
+            for name, (res, args) in _SIGS.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def status_str(code: int) -> str:
+    return lib().moe_status_str(int(code)).decode()
+
+
+def _check(fn: str, rc: int):
+    if rc != MOE_OK:
+        raise MoeError(fn, rc)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(device=None) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _dtype_code(t) -> int:
+    if t.dtype in (torch.bfloat16, torch.int16, torch.uint16):
+        return DT_BF16
+    if t.dtype == torch.float16:
+        return DT_F16
+    raise ValueError(f"unsupported 16-bit dtype {t.dtype}")
+
+
+# ---- sizes ----------------------------------------------------------------
+
+def capacity(T: int, k: int, E: int, tm: int) -> int:
+    c = lib().moe_capacity(T, k, E, tm)
+    if c < 0:
+        raise MoeError("moe_capacity", MOE_ERR_SHAPE)
+    return int(c)
+
+
+def plan_workspace_bytes(T: int, k: int, E: int) -> int:
+    return int(lib().moe_plan_workspace_bytes(T, k, E))
+
+
+def workspace_bytes(T: int, d: int, E: int, k: int, f: int, tm: int) -> int:
+    return int(lib().moe_workspace_bytes(T, d, E, k, f, tm))
+
+
+def workspace_layout(T: int, d: int, E: int, k: int, f: int, tm: int) -> dict:
+    out = (C.c_size_t * len(WS_FIELDS))()
+    _check("moe_workspace_layout", lib().moe_workspace_layout(T, d, E, k, f, tm, out))
+    return {name: int(out[i]) for i, name in enumerate(WS_FIELDS)}
+
+
+# ---- stages ---------------------------------------------------------------
+
+def plan(ids, w, E: int, tm: int, cap: int | None = None, out: dict | None = None) -> dict:
+    """moe_plan on device tensors ids int32 [T,k], w fp32 [T,k].
+
+    Returns the output tensors (full capacity; rows >= R_pad unwritten) and
+    the plan workspace ``ws`` (status word at byte 0)."""
+    T, k = ids.shape
+    dev = ids.device
+    if cap is None:
+        cap = capacity(T, k, E, tm)
+    if out is None:
+        out = {}
+    o = dict(out)
+    o.setdefault("offsets", torch.empty(E + 1, dtype=torch.int32, device=dev))
+    o.setdefault("counts", torch.empty(E, dtype=torch.int32, device=dev))
+    o.setdefault("srt_tok", torch.empty(max(cap, 1), dtype=torch.int32, device=dev))
+    o.setdefault("srt_w", torch.empty(max(cap, 1), dtype=torch.float32, device=dev))
+    o.setdefault("pos", torch.empty((T, k), dtype=torch.int32, device=dev))
+    o.setdefault("tile_expert", torch.empty(max(cap // tm, 1), dtype=torch.int32, device=dev))
+    wsb = plan_workspace_bytes(T, k, E)
+    o.setdefault("ws", torch.empty(wsb, dtype=torch.uint8, device=dev))
+    with torch.cuda.device(dev):
+        rc = lib().moe_plan(_ptr(ids), _ptr(w), T, k, E, tm, _ptr(o["offsets"]),
+                            _ptr(o["counts"]), _ptr(o["srt_tok"]), _ptr(o["srt_w"]),
+                            _ptr(o["pos"]), _ptr(o["tile_expert"]), cap, _ptr(o["ws"]),
+                            o["ws"].numel(), _stream(dev))
+    _check("moe_plan", rc)
+    o["cap"] = cap
+    return o
+
+
+def gather(x, srt_tok, offsets, E: int, cap: int, xs=None):
+    """moe_gather: xs [cap, d] (16-bit) from x [T, d]."""
+    T, d = x.shape
+    if xs is None:
+        xs = torch.empty((max(cap, 1), d), dtype=x.dtype, device=x.device)
+    with torch.cuda.device(x.device):
+        rc = lib().moe_gather(_ptr(x), _dtype_code(x), T, d, _ptr(srt_tok), _ptr(offsets), E,
+                              cap, _ptr(xs), _stream(x.device))
+    _check("moe_gather", rc)
+    return xs
+
+
+def ffn_gate_up(xs, Wg, Wu, offsets, cap: int, H=None, status=None):
+    E, d, f = Wg.shape
+    if H is None:
+        H = torch.empty((max(cap, 1), f), dtype=torch.bfloat16, device=xs.device)
+    with torch.cuda.device(xs.device):
+        rc = lib().moe_ffn_gate_up(_ptr(xs), _ptr(Wg), _ptr(Wu), _ptr(offsets), E, d, f, cap,
+                                   _ptr(H), _ptr(status), _stream(xs.device))
+    _check("moe_ffn_gate_up", rc)
+    return H
+
+
+def ffn_down(H, Wd, offsets, srt_w, cap: int, Ys=None, status=None):
+    E, f, d = Wd.shape
+    if Ys is None:
+        Ys = torch.empty((max(cap, 1), d), dtype=torch.bfloat16, device=H.device)
+    with torch.cuda.device(H.device):
+        rc = lib().moe_ffn_down(_ptr(H), _ptr(Wd), _ptr(offsets), _ptr(srt_w), E, d, f, cap,
+                                _ptr(Ys), _ptr(status), _stream(H.device))
+    _check("moe_ffn_down", rc)
+    return Ys
+
+
+def expert_ffn(xs, Wg, Wu, Wd, offsets, srt_w, cap: int, H=None, Ys=None, status=None):
+    E, d, f = Wg.shape
+    dev = xs.device
+    if H is None:
+        H = torch.empty((max(cap, 1), f), dtype=torch.bfloat16, device=dev)
+    if Ys is None:
+        Ys = torch.empty((max(cap, 1), d), dtype=torch.bfloat16, device=dev)
+    with torch.cuda.device(dev):
+        rc = lib().moe_expert_ffn(_ptr(xs), _ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(offsets),
+                                  _ptr(srt_w), E, d, f, cap, _ptr(H), _ptr(Ys), _ptr(status),
+                                  _stream(dev))
+    _check("moe_expert_ffn", rc)
+    return H, Ys
+
+
+def combine(Ys, pos, y=None):
+    T, k = pos.shape
+    d = Ys.shape[1]
+    if y is None:
+        y = torch.empty((T, d), dtype=torch.bfloat16, device=Ys.device)
+    with torch.cuda.device(Ys.device):
+        rc = lib().moe_combine(_ptr(Ys), _ptr(pos), T, k, d, _ptr(y), _stream(Ys.device))
+    _check("moe_combine", rc)
+    return y
+
+
+def layer_forward(x, ids, w, Wg, Wu, Wd, tm: int, y=None, ws=None):
+    """moe_layer_forward: y [T, d] bf16.  ``ws`` (uint8 device tensor of
+    workspace_bytes(...)) may be passed in to reuse it and to inspect the
+    intermediates through workspace_layout(...)."""
+    T, d = x.shape
+    k = ids.shape[1]
+    E, _, f = Wg.shape
+    dev = x.device
+    if y is None:
+        y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    nbytes = workspace_bytes(T, d, E, k, f, tm)
+    if ws is None:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = lib().moe_layer_forward(_ptr(x), _ptr(ids), _ptr(w), _ptr(Wg), _ptr(Wu), _ptr(Wd),
+                                     T, d, E, k, f, tm, _ptr(y), _ptr(ws), ws.numel(),
+                                     _stream(dev))
+    _check("moe_layer_forward", rc)
+    return y
+
+
+def read_status(ws) -> int:
+    """Status word at byte 0 of a plan or layer workspace (syncs the stream)."""
+    v = C.c_uint32(0)
+    with torch.cuda.device(ws.device):
+        rc = lib().moe_read_status(_ptr(ws), _stream(ws.device), C.byref(v))
+    _check("moe_read_status", rc)
+    return int(v.value)
+
+
+class MoeLayer:
+    """A routed MoE layer with its expert weights resident in HBM.
+
+    ``forward`` takes device inputs; ``forward_host`` takes pinned host
+    inputs, copies them in, runs the layer and copies y back, all on the
+    current stream."""
+
+    def __init__(self, Wg, Wu, Wd, tm: int = 16):
+        self.Wg, self.Wu, self.Wd, self.tm = Wg, Wu, Wd, tm
+        self.E, self.d, self.f = Wg.shape
+        self.device = Wg.device
+        self._ws = None
+        self._bufs = None
+
+    def workspace(self, T: int, k: int):
+        n = workspace_bytes(T, self.d, self.E, k, self.f, self.tm)
+        if self._ws is None or self._ws.numel() < n:
+            self._ws = torch.empty(n, dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def forward(self, x, ids, w, y=None):
+        T = x.shape[0]
+        return layer_forward(x, ids, w, self.Wg, self.Wu, self.Wd, self.tm, y=y,
+                             ws=self.workspace(T, ids.shape[1]))
+
+    def forward_host(self, x_h, ids_h, w_h, y_h):
+        """Host (pinned) x, ids, w in; host y out.  Asynchronous on the
+        current stream; synchronize before reading y_h."""
+        T, k = ids_h.shape
+        key = (T, k)
+        if self._bufs is None or self._bufs[0] != key:
+            dev = self.device
+            self._bufs = (key, torch.empty((T, self.d), dtype=torch.bfloat16, device=dev),
+                          torch.empty((T, k), dtype=torch.int32, device=dev),
+                          torch.empty((T, k), dtype=torch.float32, device=dev),
+                          torch.empty((T, self.d), dtype=torch.bfloat16, device=dev))
+        _, x, ids, w, y = self._bufs
+        x.copy_(x_h, non_blocking=True)
+        ids.copy_(ids_h, non_blocking=True)
+        w.copy_(w_h, non_blocking=True)
+        self.forward(x, ids, w, y=y)
+        y_h.copy_(y, non_blocking=True)
+        return y_h

@@ -1,0 +1,511 @@
+// Grouped expert FFN on the 5th-generation tensor cores (tcgen05 + TMEM),
+// operands staged by TMA.
+//
+// "Batched resident MoE experts on Apple Silicon: a flat parallel expert
+// pass", section 1: every routed row goes through its expert's gate/up
+// projection, the gated activation and the weighted down projection.  Here
+// the rows arrive grouped by expert (the plan's offsets), so each expert is
+// one GEMM over its rows, and all experts run in one persistent launch per
+// projection:
+//
+//   gate/up: H[r]  = bf16(silu(xs[r] Wg[e]) * (xs[r] Wu[e]))
+//   down:    Ys[r] = bf16(srt_w[r] * (H[r] Wd[e]))
+//
+// Swap-AB: the weight is the MMA's A operand (M = 128 output features) and
+// the expert's rows are its B operand (N = the unit's rows, a multiple of 16,
+// at most 128), so an expert with few rows still fills the M = 128 tile.
+// Weights are [E, K, M] with M contiguous, i.e. MN-major A tiles read by one
+// 3-D tensor map per weight (the expert is the outer coordinate); activation
+// rows are K-major B tiles.  Both use 128-byte swizzled shared memory.
+//
+// Work unit = (expert chunk of <= 128 rows, 128-feature tile), numbered
+// chunk-major so that the tiles of one chunk (same activation rows) and the
+// chunks of one big expert (same weight tile) run close together in time
+// and share L2.  Each CTA (one per SM) walks units u = blockIdx.x + i*grid.
+//
+// Warp roles: warp 0 issues TMA copies into a ring of shared-memory stages,
+// warp 1 issues tcgen05.mma into one of two TMEM accumulators, warps 2-5
+// read the accumulator with tcgen05.ld, apply the epilogue and store bf16.
+// Every output element is written by one CTA with a fixed K order: results
+// are deterministic.  Every wait is bounded (2 s); on a timeout the CTA
+// stops, lets its copies and MMAs land, frees TMEM and sets
+// MOE_STATUS_TIMEOUT.
+#include "../../include/moe_prefill.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;                           // MMA M: output features per tile
+constexpr int BK = 64;                            // K per stage: 64 bf16 = one 128-byte row
+constexpr int BN = 128;                           // max rows per unit (MMA N)
+constexpr int UMMA_K = 16;                        // K of one kind::f16 MMA
+constexpr int kBoxRows = 16;                      // rows per activation TMA box
+constexpr uint32_t kABoxBytes = 64 * BK * 2;      // 64 features x 64 K rows
+constexpr uint32_t kATileBytes = 2 * kABoxBytes;  // 128 features
+constexpr uint32_t kBTileBytes = BN * BK * 2;     // 128 rows x 64 K
+constexpr uint32_t kBBoxBytes = kBoxRows * BK * 2;
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr uint32_t kFull = 0xffffffffu;
+constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for the stop path
+
+template <bool GATED>
+struct Cfg;
+template <>
+struct Cfg<true> {  // gate/up: A = Wg and Wu, B = xs, two accumulators
+    static constexpr int kStages = 4;
+    static constexpr uint32_t kStageBytes = 2 * kATileBytes + kBTileBytes;
+    static constexpr uint32_t kAccCols = 2 * BN;
+    static constexpr uint32_t kTmemCols = 2 * kAccCols;
+};
+template <>
+struct Cfg<false> {  // down: A = Wd, B = H, one accumulator
+    static constexpr int kStages = 6;
+    static constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
+    static constexpr uint32_t kAccCols = BN;
+    static constexpr uint32_t kTmemCols = 2 * kAccCols;
+};
+
+template <int S>
+struct Ctrl {
+    uint64_t full[S];
+    uint64_t empty[S];
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort_flag;
+    int warp_sum[kThreads / 32];
+};
+
+struct FfnArgs {
+    const int32_t *offsets;
+    const float *srt_w;  // down only
+    uint16_t *out;       // H (gate/up) or Ys (down), bf16 bits, [cap, M]
+    uint32_t *status;    // may be null
+    int64_t cap;
+    int E;
+    int K;  // reduction extent: d (gate/up) or f (down)
+    int M;  // output features: f (gate/up) or d (down)
+};
+
+template <bool GATED>
+constexpr size_t ffn_smem_bytes(int E)
+{
+    return 1024 + size_t(Cfg<GATED>::kStages) * Cfg<GATED>::kStageBytes +
+           sizeof(Ctrl<Cfg<GATED>::kStages>) + size_t(E + 1) * sizeof(int);
+}
+
+// Bounded wait that ignores the abort flag (used while stopping).
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity)
+{
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > kDrainLimitNs)
+            return;
+}
+
+__device__ __forceinline__ int expert_chunks(const int32_t *off, int e, int64_t cap, bool &bad)
+{
+    const int lo = off[e], hi = off[e + 1];
+    if (lo < 0 || hi < lo || int64_t(hi) > cap || (lo & 15) || (hi & 15)) {
+        bad = true;
+        return 0;
+    }
+    return (hi - lo + BN - 1) / BN;
+}
+
+// chunk_start[e] = chunks of experts < e (chunks of <= BN rows); returns the
+// total.  Experts whose offsets are not ascending multiples of 16 inside cap
+// get no chunks and raise MOE_STATUS_BAD_OFFSETS.  All threads take part.
+__device__ int build_chunk_table(const int32_t *off, int E, int64_t cap, int *cs, int *warp_sum,
+                                 uint32_t *status)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (E + kThreads - 1) / kThreads;
+    const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+    bool bad = false;
+    int local = 0;
+    for (int e = e0; e < e1; ++e)
+        local += expert_chunks(off, e, cap, bad);
+    int v = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(kFull, v, o);
+        if (lane >= o)
+            v += t;
+    }
+    if (lane == 31)
+        warp_sum[warp] = v;
+    __syncthreads();
+    int before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+        before += w < warp ? warp_sum[w] : 0;
+        total += warp_sum[w];
+    }
+    int run = before + v - local;
+    for (int e = e0; e < e1; ++e) {
+        cs[e] = run;
+        run += expert_chunks(off, e, cap, bad);
+    }
+    if (tid == 0)
+        cs[E] = total;
+    if (bad && status)
+        atomicOr(status, MOE_STATUS_BAD_OFFSETS);
+    __syncthreads();
+    return total;
+}
+
+struct Unit {
+    int e, row0, nrows, mt;
+};
+
+__device__ __forceinline__ Unit map_unit(int64_t u, int n_mt, const int *cs, int E,
+                                         const int32_t *off)
+{
+    const int c = int(u / n_mt);
+    Unit r;
+    r.mt = int(u - int64_t(c) * n_mt);
+    int lo = 0, hi = E - 1;  // the expert e with cs[e] <= c < cs[e+1]
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cs[mid] <= c)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    r.e = lo;
+    r.row0 = off[lo] + (c - cs[lo]) * BN;
+    r.nrows = min(BN, off[lo + 1] - r.row0);
+    return r;
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float v)
+{
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+template <bool GATED>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_ffn(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
+          const __grid_constant__ CUtensorMap map_b, const FfnArgs p)
+{
+    using C = Cfg<GATED>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    Ctrl<S> *ctl = reinterpret_cast<Ctrl<S> *>(smem + S * C::kStageBytes);
+    int *chunk_start = reinterpret_cast<int *>(ctl + 1);
+    const int warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ctl->tmem_full[b], 1);
+            mbar_init(&ctl->tmem_empty[b], kEpiThreads);
+        }
+        mbar_init(&ctl->mma_done, 1);
+        ctl->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&map_a0);
+        if (GATED)
+            prefetch_tmap(&map_a1);
+        prefetch_tmap(&map_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(&ctl->tmem_base, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = ctl->tmem_base;
+    volatile int *abort_flag = &ctl->abort_flag;
+
+    pdl_wait();
+    pdl_launch_dependents();
+
+    const int total_chunks =
+        build_chunk_table(p.offsets, p.E, p.cap, chunk_start, ctl->warp_sum, p.status);
+    const int n_mt = (p.M + BM - 1) / BM;
+    const int nk = p.K / BK;
+    const int64_t total_units = int64_t(total_chunks) * n_mt;
+
+    if (warp == 0) {
+        // ---- TMA producer ----
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, issued_par = 0;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+                const Unit w = map_unit(u, n_mt, chunk_start, p.E, p.offsets);
+                const int m0 = w.mt * BM;
+                const bool hi_half = m0 + 64 < p.M;  // features m0+64.. exist
+                const uint32_t a_bytes = (hi_half ? 2u : 1u) * kABoxBytes;
+                const uint32_t bytes =
+                    (GATED ? 2u : 1u) * a_bytes + uint32_t(w.nrows) * uint32_t(BK * 2);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint64_t *fb = &ctl->full[stage];
+                    mbar_arrive_expect_tx(fb, bytes);
+                    uint8_t *sa = smem + stage * C::kStageBytes;
+                    const int k0 = kb * BK;
+                    tma_load_3d(sa, &map_a0, fb, m0, k0, w.e);
+                    if (hi_half)
+                        tma_load_3d(sa + kABoxBytes, &map_a0, fb, m0 + 64, k0, w.e);
+                    uint8_t *sb = sa + kATileBytes;
+                    if (GATED) {
+                        tma_load_3d(sb, &map_a1, fb, m0, k0, w.e);
+                        if (hi_half)
+                            tma_load_3d(sb + kABoxBytes, &map_a1, fb, m0 + 64, k0, w.e);
+                        sb += kATileBytes;
+                    }
+                    for (int j = 0; j < w.nrows / kBoxRows; ++j)
+                        tma_load_2d(sb + j * kBBoxBytes, &map_b, fb, k0, w.row0 + j * kBoxRows);
+                    issued |= 1u << stage;
+                    issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // every stage must be released by the MMA side before the CTA exits
+            for (int i = 0; ok && i < S; ++i) {
+                ok = mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag);
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok)  // stopped: let the copies already issued land
+                for (int s = 0; s < S; ++s)
+                    if ((issued >> s) & 1u)
+                        mbar_drain(&ctl->full[s], (issued_par >> s) & 1u);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---- MMA issuer ----
+        if (lane == 0) {
+            int stage = 0, abuf = 0;
+            uint32_t phase = 0, aphase = 0;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+                const Unit w = map_unit(u, n_mt, chunk_start, p.E, p.offsets);
+                if (!mbar_wait(&ctl->tmem_empty[abuf], aphase ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d0 = tmem_base + uint32_t(abuf) * C::kAccCols;
+                const uint32_t idesc = idesc_bf16_f32(BM, uint32_t(w.nrows), 1u, 0u);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(&ctl->full[stage], phase, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t sa = smem_u32(smem + stage * C::kStageBytes);
+                    const uint32_t sb = sa + (GATED ? 2u : 1u) * kATileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        // B: K-major rows of 128 B; the K step moves 32 B inside the row.
+                        const uint64_t bdesc = smem_desc_sw128(sb + kk * UMMA_K * 2, 16, 1024);
+                        // A: MN-major, one 128-byte row per K index; the K step moves 16 rows.
+                        const uint64_t adesc0 =
+                            smem_desc_sw128(sa + kk * UMMA_K * 128, kABoxBytes, 1024);
+                        const uint32_t acc = (kb | kk) != 0;
+                        tc_mma_f16(d0, adesc0, bdesc, idesc, acc);
+                        if (GATED) {
+                            const uint64_t adesc1 = smem_desc_sw128(
+                                sa + kATileBytes + kk * UMMA_K * 128, kABoxBytes, 1024);
+                            tc_mma_f16(d0 + BN, adesc1, bdesc, idesc, acc);
+                        }
+                    }
+                    tc_commit(&ctl->empty[stage]);  // frees the stage once these MMAs finish
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                tc_commit(&ctl->tmem_full[abuf]);
+                abuf ^= 1;
+                if (abuf == 0)
+                    aphase ^= 1u;
+            }
+            // all MMAs issued here have completed once this arrives
+            tc_commit(&ctl->mma_done);
+            mbar_drain(&ctl->mma_done, 0);
+        }
+        __syncwarp();
+    } else {
+        // ---- epilogue: TMEM -> registers -> bf16 global ----
+        const int q = warp & 3;  // TMEM lane quadrant this warp may read
+        const int row_in_tile = q * 32 + int(lane);
+        int abuf = 0;
+        uint32_t aphase = 0;
+        for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
+            const Unit w = map_unit(u, n_mt, chunk_start, p.E, p.offsets);
+            const bool ok = mbar_wait(&ctl->tmem_full[abuf], aphase, abort_flag);
+            if (!__all_sync(kFull, ok))
+                break;
+            tc_fence_after_sync();
+            const int feat = w.mt * BM + row_in_tile;
+            const uint32_t t0 =
+                tmem_base + (uint32_t(q * 32) << 16) + uint32_t(abuf) * C::kAccCols;
+            uint16_t *dst = p.out + int64_t(w.row0) * p.M + feat;
+            for (int c0 = 0; c0 < w.nrows; c0 += 16) {
+                uint32_t a[16];
+                tmem_ld_32x32b_x16(t0 + uint32_t(c0), a);
+                if (GATED) {
+                    uint32_t b[16];
+                    tmem_ld_32x32b_x16(t0 + BN + uint32_t(c0), b);
+                    tmem_ld_wait();
+                    if (feat < p.M) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float g = __uint_as_float(a[j]);
+                            const float up = __uint_as_float(b[j]);
+                            const float h = g / (1.0f + __expf(-g)) * up;
+                            dst[int64_t(c0 + j) * p.M] = bf16_bits(h);
+                        }
+                    }
+                } else {
+                    tmem_ld_wait();
+                    if (feat < p.M) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float wr = p.srt_w[w.row0 + c0 + j];
+                            dst[int64_t(c0 + j) * p.M] = bf16_bits(wr * __uint_as_float(a[j]));
+                        }
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&ctl->tmem_empty[abuf]);
+            abuf ^= 1;
+            if (abuf == 0)
+                aphase ^= 1u;
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+    if (threadIdx.x == 0 && ctl->abort_flag && p.status)
+        atomicOr(p.status, MOE_STATUS_TIMEOUT);
+}
+
+// ---- host: tensor maps ------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+cudaError_t get_encoder()
+{
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode ? cudaSuccess : cudaErrorNotSupported;
+}
+
+// bf16 tensor map with a 128-byte swizzle; dims innermost first.
+cudaError_t encode_bf16(CUtensorMap *m, const void *base, uint32_t rank, const cuuint64_t *dims,
+                        const cuuint64_t *strides_bytes, const cuuint32_t *box)
+{
+    cudaError_t err = get_encoder();
+    if (err != cudaSuccess)
+        return err;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base),
+                                dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Weight [E, K, M] (M contiguous): boxes of 64 features x 64 K rows of one expert.
+cudaError_t weight_map(CUtensorMap *m, const void *W, int E, int K, int M)
+{
+    const cuuint64_t dims[3] = {cuuint64_t(M), cuuint64_t(K), cuuint64_t(E)};
+    const cuuint64_t strides[2] = {cuuint64_t(M) * 2, cuuint64_t(M) * K * 2};
+    const cuuint32_t box[3] = {64, BK, 1};
+    return encode_bf16(m, W, 3, dims, strides, box);
+}
+
+// Rows [cap, K] (K contiguous): boxes of 16 rows x 64 K.
+cudaError_t rows_map(CUtensorMap *m, const void *X, int64_t cap, int K)
+{
+    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(cap)};
+    const cuuint64_t strides[1] = {cuuint64_t(K) * 2};
+    const cuuint32_t box[2] = {BK, kBoxRows};
+    return encode_bf16(m, X, 2, dims, strides, box);
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_gate_up(const void *xs, const void *Wg, const void *Wu,
+                               const int32_t *offsets, int E, int d, int f, int64_t cap,
+                               void *H, uint32_t *status, cudaStream_t stream)
+{
+    CUtensorMap mg, mu, mx;
+    cudaError_t err;
+    if ((err = weight_map(&mg, Wg, E, d, f)) != cudaSuccess ||
+        (err = weight_map(&mu, Wu, E, d, f)) != cudaSuccess ||
+        (err = rows_map(&mx, xs, cap, d)) != cudaSuccess)
+        return err;
+    err = ensure_smem_limit(reinterpret_cast<const void *>(k_ffn<true>), kSlotGateUp,
+                            ffn_smem_bytes<true>(MOE_MAX_EXPERTS));
+    if (err != cudaSuccess)
+        return err;
+    const FfnArgs a{offsets, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f};
+    return launch_pdl(k_ffn<true>, dim3(device_sm_count()), dim3(kThreads),
+                      ffn_smem_bytes<true>(E), stream, mg, mu, mx, a);
+}
+
+cudaError_t launch_ffn_down(const void *H, const void *Wd, const int32_t *offsets,
+                            const float *srt_w, int E, int d, int f, int64_t cap, void *Ys,
+                            uint32_t *status, cudaStream_t stream)
+{
+    CUtensorMap mw, mh;
+    cudaError_t err;
+    if ((err = weight_map(&mw, Wd, E, f, d)) != cudaSuccess ||
+        (err = rows_map(&mh, H, cap, f)) != cudaSuccess)
+        return err;
+    err = ensure_smem_limit(reinterpret_cast<const void *>(k_ffn<false>), kSlotDown,
+                            ffn_smem_bytes<false>(MOE_MAX_EXPERTS));
+    if (err != cudaSuccess)
+        return err;
+    const FfnArgs a{offsets, srt_w, static_cast<uint16_t *>(Ys), status, cap, E, f, d};
+    return launch_pdl(k_ffn<false>, dim3(device_sm_count()), dim3(kThreads),
+                      ffn_smem_bytes<false>(E), stream, mw, mw, mh, a);
+}
+
+}  // namespace moe

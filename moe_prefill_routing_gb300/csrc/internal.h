@@ -1,0 +1,88 @@
+// Internal interface between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <utility>
+
+namespace moe {
+
+// ---- routing plan (plan.cu) ------------------------------------------------
+
+// Flat entries per histogram / place block.  Grows past 512 only when
+// T*k > 512 * kPlanMaxBlocks, so the single-CTA scan reads at most
+// kPlanMaxBlocks * E counts.
+constexpr int kPlanBlockMin = 512;
+constexpr int kPlanMaxBlocks = 256;
+
+inline int64_t plan_block_entries(int64_t n)
+{
+    if (n <= int64_t(kPlanBlockMin) * kPlanMaxBlocks)
+        return kPlanBlockMin;
+    int64_t b = (n + kPlanMaxBlocks - 1) / kPlanMaxBlocks;
+    return (b + kPlanBlockMin - 1) / kPlanBlockMin * kPlanBlockMin;
+}
+
+inline int plan_num_blocks(int64_t n)
+{
+    const int64_t b = plan_block_entries(n);
+    return static_cast<int>((n + b - 1) / b);
+}
+
+cudaError_t launch_plan(const int32_t *ids, const float *w, int T, int k, int E, int tm,
+                        int32_t *offsets, int32_t *counts, int32_t *srt_tok, float *srt_w,
+                        int32_t *pos, int32_t *tile_expert, int64_t cap, uint32_t *status,
+                        int32_t *bcnt, cudaStream_t stream);
+
+// ---- row kernels (rows.cu) ---------------------------------------------------
+
+cudaError_t launch_gather(const void *x, int T, int d, const int32_t *srt_tok,
+                          const int32_t *offsets, int E, int64_t cap, void *xs,
+                          cudaStream_t stream);
+
+cudaError_t launch_combine(const void *Ys, const int32_t *pos, int T, int k, int d, void *y,
+                           cudaStream_t stream);
+
+// ---- grouped expert GEMMs (ffn.cu) -------------------------------------------
+
+cudaError_t launch_ffn_gate_up(const void *xs, const void *Wg, const void *Wu,
+                               const int32_t *offsets, int E, int d, int f, int64_t cap,
+                               void *H, uint32_t *status, cudaStream_t stream);
+
+cudaError_t launch_ffn_down(const void *H, const void *Wd, const int32_t *offsets,
+                            const float *srt_w, int E, int d, int f, int64_t cap, void *Ys,
+                            uint32_t *status, cudaStream_t stream);
+
+// ---- launch helpers (api.cu) -------------------------------------------------
+
+// Streaming multiprocessors of the current device (cached per device).
+int device_sm_count();
+
+// Raise a kernel's dynamic shared-memory limit once per device.
+cudaError_t ensure_smem_limit(const void *kernel, int slot, size_t bytes);
+
+// Launch with programmatic dependent launch allowed: the kernel may begin
+// while its predecessor in the stream finishes; every kernel here calls
+// griddepcontrol.wait before it touches global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Slots of ensure_smem_limit's per-device cache.
+enum SmemSlot { kSlotPlace = 0, kSlotHist, kSlotGateUp, kSlotDown, kSlotCount };
+
+}  // namespace moe

@@ -1,0 +1,158 @@
+// Row kernels: the gather of token rows into expert-sorted order and the
+// slot-ordered combine.  Both are HBM-bound copies/reductions of whole
+// 16-byte-aligned rows, so they move 128-bit vectors with every lane of a
+// warp on consecutive vectors of one row; grids are a multiple of the SM
+// count and loop over rows.
+//
+// Gather: "Round 4 Track C: Prefill MoE Plan ... & Epilogue / Gather Audit",
+// section 1 item 4 (rows read as 16-bit values with vector loads and stored
+// unchanged, bit for bit).  Combine: "Batched resident MoE experts on Apple
+// Silicon: a flat parallel expert pass", section 3 (the same per-token top-k
+// summation order).
+#include "../../include/moe_prefill.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+#include <cuda_bf16.h>
+
+namespace moe {
+namespace {
+
+constexpr int kRowWarps = 8;
+constexpr int kRowThreads = kRowWarps * 32;
+constexpr int kCtasPerSm = 8;
+
+__device__ __forceinline__ uint4 ldg_nc(const uint4 *p)
+{
+    return __ldg(p);
+}
+
+// xs[r] = x[srt_tok[r]] for r < R_pad (= offsets[E]); zero rows where srt_tok = -1.
+__global__ void __launch_bounds__(kRowThreads)
+    k_gather(const uint4 *__restrict__ x, int T, int dvec, const int32_t *__restrict__ srt_tok,
+             const int32_t *__restrict__ offsets, int E, int64_t cap, uint4 *__restrict__ xs)
+{
+    pdl_wait();
+    const int64_t R = min(int64_t(offsets[E]), cap);
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = int64_t(gridDim.x) * kRowWarps;
+    for (int64_t r = int64_t(blockIdx.x) * kRowWarps + (threadIdx.x >> 5); r < R; r += nw) {
+        const int t = srt_tok[r];
+        uint4 *dst = xs + r * dvec;
+        if (t >= 0 && t < T) {
+            const uint4 *src = x + int64_t(t) * dvec;
+            int c = lane;
+            for (; c + 96 < dvec; c += 128) {
+                const uint4 a = ldg_nc(src + c), b = ldg_nc(src + c + 32);
+                const uint4 e = ldg_nc(src + c + 64), g = ldg_nc(src + c + 96);
+                dst[c] = a;
+                dst[c + 32] = b;
+                dst[c + 64] = e;
+                dst[c + 96] = g;
+            }
+            for (; c < dvec; c += 32)
+                dst[c] = ldg_nc(src + c);
+        } else {
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            for (int c = lane; c < dvec; c += 32)
+                dst[c] = z;
+        }
+    }
+    pdl_launch_dependents();
+}
+
+__device__ __forceinline__ void add_bf16x8(float *acc, const uint4 v)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc[2 * i] += __uint_as_float(w[i] << 16);
+        acc[2 * i + 1] += __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float *acc)
+{
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * i]));
+        const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * i + 1]));
+        w[i] = lo | (hi << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// One warp per (token, 512-column segment): y[t] = sum_{j=0..k-1} Ys[pos[t,j]],
+// fp32 from zero in slot order, one bf16 rounding.
+constexpr int kSegVec = 64;  // 16-byte vectors per warp segment (2 per lane)
+
+__global__ void __launch_bounds__(kRowThreads)
+    k_combine(const uint4 *__restrict__ Ys, const int32_t *__restrict__ pos, int T, int k,
+              int dvec, uint4 *__restrict__ y)
+{
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int nseg = (dvec + kSegVec - 1) / kSegVec;
+    const int64_t ntask = int64_t(T) * nseg;
+    const int64_t nw = int64_t(gridDim.x) * kRowWarps;
+    for (int64_t task = int64_t(blockIdx.x) * kRowWarps + (threadIdx.x >> 5); task < ntask;
+         task += nw) {
+        const int64_t t = task / nseg;
+        const int seg = int(task - t * nseg);
+        const int c0 = seg * kSegVec + lane, c1 = c0 + 32;
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            acc[i] = 0.0f;
+        const int32_t *pt = pos + t * k;
+        for (int j = 0; j < k; ++j) {
+            const int p = pt[j];
+            if (p < 0)
+                continue;
+            const uint4 *row = Ys + int64_t(p) * dvec;
+            if (c1 < dvec) {
+                const uint4 a = ldg_nc(row + c0), b = ldg_nc(row + c1);
+                add_bf16x8(acc, a);
+                add_bf16x8(acc + 8, b);
+            } else if (c0 < dvec) {
+                add_bf16x8(acc, ldg_nc(row + c0));
+            }
+        }
+        uint4 *out = y + t * dvec;
+        if (c0 < dvec)
+            out[c0] = pack_bf16x8(acc);
+        if (c1 < dvec)
+            out[c1] = pack_bf16x8(acc + 8);
+    }
+    pdl_launch_dependents();
+}
+
+}  // namespace
+
+cudaError_t launch_gather(const void *x, int T, int d, const int32_t *srt_tok,
+                          const int32_t *offsets, int E, int64_t cap, void *xs,
+                          cudaStream_t stream)
+{
+    const int dvec = d / 8;
+    const int64_t want = (cap + kRowWarps - 1) / kRowWarps;
+    const int64_t cap_grid = int64_t(device_sm_count()) * kCtasPerSm;
+    const int grid = int(want < 1 ? 1 : (want < cap_grid ? want : cap_grid));
+    return launch_pdl(k_gather, dim3(grid), dim3(kRowThreads), 0, stream,
+                      static_cast<const uint4 *>(x), T, dvec, srt_tok, offsets, E, cap,
+                      static_cast<uint4 *>(xs));
+}
+
+cudaError_t launch_combine(const void *Ys, const int32_t *pos, int T, int k, int d, void *y,
+                           cudaStream_t stream)
+{
+    const int dvec = d / 8;
+    const int64_t ntask = int64_t(T) * ((dvec + kSegVec - 1) / kSegVec);
+    const int64_t want = (ntask + kRowWarps - 1) / kRowWarps;
+    const int64_t cap_grid = int64_t(device_sm_count()) * kCtasPerSm;
+    const int grid = int(want < 1 ? 1 : (want < cap_grid ? want : cap_grid));
+    return launch_pdl(k_combine, dim3(grid), dim3(kRowThreads), 0, stream,
+                      static_cast<const uint4 *>(Ys), pos, T, k, dvec, static_cast<uint4 *>(y));
+}
+
+}  // namespace moe

@@ -1,0 +1,118 @@
+"""The C ABI on the CPU: the library loads, exports every entry point the
+header declares, and its host-side logic (sizes, workspace layout, argument
+checks) behaves as documented.  No call here reaches the GPU: every call
+either is host-only or fails its argument checks before anything is
+enqueued (device pointers below are never dereferenced)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from moe_prefill_routing_gb300 import binding as B
+from moe_prefill_routing_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_prefill.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return B.lib()
+
+
+def declared():
+    src = open(HEADER).read()
+    return re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", src)
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared())
+    assert {"moe_plan", "moe_gather", "moe_expert_ffn", "moe_combine", "moe_layer_forward",
+            "moe_ffn_gate_up", "moe_ffn_down", "moe_capacity", "moe_workspace_bytes",
+            "moe_read_status", "moe_status_str"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared():
+        assert hasattr(lib, name), name
+        assert name in B._SIGS, f"binding lacks {name}"
+
+
+def test_capacity(lib):
+    assert B.capacity(2048, 10, 512, 16) == 20480 + 512 * 15
+    assert B.capacity(4, 2, 512, 16) == 8 + 8 * 15
+    assert B.capacity(0, 2, 5, 16) == 0
+    for bad in ((-1, 2, 4, 16), (4, 0, 4, 16), (4, 2, 0, 16), (4, 2, 4097, 16), (4, 2, 4, 0),
+                (4, 2, 4, 1025), (1 << 30, 4, 4, 16)):
+        assert lib.moe_capacity(*bad) == -1
+
+
+def test_workspace_layout(lib):
+    T, d, E, k, f, tm = 2048, 2560, 512, 10, 512, 16
+    L = B.workspace_layout(T, d, E, k, f, tm)
+    offs = [L[n] for n in B.WS_FIELDS]
+    assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    cap = B.capacity(T, k, E, tm)
+    assert L["Ys"] - L["H"] >= cap * f * 2 and L["total"] - L["Ys"] >= cap * d * 2
+    assert L["xs"] - L["tile_expert"] >= (cap // tm) * 4
+    assert B.workspace_bytes(T, d, E, k, f, tm) == L["total"]
+    assert L["bcnt"] == 256 and L["offsets"] == B.plan_workspace_bytes(T, k, E)
+
+
+FAKE = 0x10000  # a 256-byte aligned stand-in device address, never dereferenced
+
+
+def plan_call(lib, **kw):
+    a = dict(ids=FAKE, w=FAKE, T=8, k=2, E=4, tm=16, offsets=FAKE, counts=FAKE, srt_tok=FAKE,
+             srt_w=FAKE, pos=FAKE, tile=FAKE, cap=8 * 2 + 4 * 15, ws=FAKE, ws_bytes=1 << 20,
+             stream=None)
+    a.update(kw)
+    return lib.moe_plan(a["ids"], a["w"], a["T"], a["k"], a["E"], a["tm"], a["offsets"],
+                        a["counts"], a["srt_tok"], a["srt_w"], a["pos"], a["tile"], a["cap"],
+                        a["ws"], a["ws_bytes"], a["stream"])
+
+
+def test_plan_argument_errors(lib):
+    assert plan_call(lib, ids=None) == B.MOE_ERR_NULL
+    assert plan_call(lib, ws=None) == B.MOE_ERR_NULL
+    assert plan_call(lib, E=0) == B.MOE_ERR_SHAPE
+    assert plan_call(lib, E=5000) == B.MOE_ERR_SHAPE
+    assert plan_call(lib, k=300) == B.MOE_ERR_SHAPE
+    assert plan_call(lib, tm=0) == B.MOE_ERR_SHAPE
+    assert plan_call(lib, cap=8 * 2 + 4 * 15 - 1) == B.MOE_ERR_CAPACITY
+    assert plan_call(lib, ws_bytes=16) == B.MOE_ERR_WORKSPACE
+    assert plan_call(lib, ids=FAKE + 2) == B.MOE_ERR_ALIGN
+    assert plan_call(lib, ws=FAKE + 16) == B.MOE_ERR_ALIGN
+
+
+def test_stage_argument_errors(lib):
+    g = lib.moe_gather
+    assert g(FAKE, 2, 8, 64, FAKE, FAKE, 4, 100, FAKE, None) == B.MOE_ERR_DTYPE
+    assert g(FAKE, 0, 8, 60, FAKE, FAKE, 4, 100, FAKE, None) == B.MOE_ERR_SHAPE   # d % 8
+    assert g(None, 0, 8, 64, FAKE, FAKE, 4, 100, FAKE, None) == B.MOE_ERR_NULL
+    assert g(FAKE + 8, 0, 8, 64, FAKE, FAKE, 4, 100, FAKE, None) == B.MOE_ERR_ALIGN
+    assert g(FAKE, 0, 8, 64, FAKE, FAKE, 4, 0, FAKE, None) == B.MOE_OK          # nothing to do
+    gu = lib.moe_ffn_gate_up
+    assert gu(FAKE, FAKE, FAKE, FAKE, 4, 96, 64, 100, FAKE, None, None) == B.MOE_ERR_SHAPE
+    assert gu(FAKE, FAKE, FAKE, FAKE, 4, 64, 32, 100, FAKE, None, None) == B.MOE_ERR_SHAPE
+    assert gu(FAKE, None, FAKE, FAKE, 4, 64, 64, 100, FAKE, None, None) == B.MOE_ERR_NULL
+    assert gu(FAKE, FAKE, FAKE, FAKE, 4, 64, 64, 100, FAKE, FAKE + 2, None) == B.MOE_ERR_ALIGN
+    dn = lib.moe_ffn_down
+    assert dn(FAKE, FAKE, FAKE, None, 4, 64, 64, 100, FAKE, None, None) == B.MOE_ERR_NULL
+    c = lib.moe_combine
+    assert c(FAKE, FAKE, 4, 0, 64, FAKE, None) == B.MOE_ERR_SHAPE
+    assert c(FAKE, FAKE, 0, 2, 64, FAKE, None) == B.MOE_OK
+    assert c(None, FAKE, 4, 2, 64, FAKE, None) == B.MOE_ERR_NULL
+    lf = lib.moe_layer_forward
+    ws = 1 << 40
+    assert lf(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, 64, 4, 2, 64, 8, FAKE, FAKE, ws, None) == B.MOE_ERR_SHAPE
+    assert lf(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, 64, 4, 2, 64, 16, FAKE, FAKE, 10, None) == B.MOE_ERR_WORKSPACE
+    assert lf(FAKE, FAKE, FAKE, None, FAKE, FAKE, 8, 64, 4, 2, 64, 16, FAKE, FAKE, ws, None) == B.MOE_ERR_NULL
+    assert lib.moe_read_status(None, None, None) == B.MOE_ERR_NULL
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, 99):
+        assert isinstance(B.status_str(code), str) and B.status_str(code)

@@ -1,0 +1,147 @@
+"""GPU routing plan vs the oracle: bit-exact (offsets, counts, srt_tok,
+srt_w, pos, tile_expert), with output buffers poisoned first as in "Round 4
+Track C: Prefill MoE Plan ...", section 3 (0xDEADBEEF / 777777), so every
+value compared was written by the kernels and rows >= R_pad are untouched."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_prefill_routing_gb300 import binding as B
+from moe_prefill_routing_gb300 import workload as W
+
+from helpers import dev, inputs
+
+pytestmark = pytest.mark.gpu
+
+POISON_I = np.int32(np.uint32(0xDEADBEEF).view(np.int32))
+POISON_W = np.float32(777777.0)
+
+
+def gpu_plan(ids, w, E, tm):
+    T, k = ids.shape
+    cap = B.capacity(T, k, E, tm)
+    d = "cuda"
+    out = dict(
+        offsets=torch.full((E + 1,), int(POISON_I), dtype=torch.int32, device=d),
+        counts=torch.full((E,), int(POISON_I), dtype=torch.int32, device=d),
+        srt_tok=torch.full((max(cap, 1),), int(POISON_I), dtype=torch.int32, device=d),
+        srt_w=torch.full((max(cap, 1),), float(POISON_W), dtype=torch.float32, device=d),
+        pos=torch.full((T, k), int(POISON_I), dtype=torch.int32, device=d),
+        tile_expert=torch.full((max(cap // tm, 1),), int(POISON_I), dtype=torch.int32, device=d),
+        ws=torch.full((B.plan_workspace_bytes(T, k, E),), 0x5A, dtype=torch.uint8, device=d),
+    )
+    o = B.plan(dev(ids), dev(w), E, tm, cap=cap, out=out)
+    status = B.read_status(o["ws"])
+    return {n: o[n].cpu().numpy() for n in
+            ("offsets", "counts", "srt_tok", "srt_w", "pos", "tile_expert")}, status
+
+
+def assert_same_plan(g, ref, tm):
+    R = ref["R_pad"]
+    assert g["offsets"].tolist() == ref["offsets"].tolist()
+    assert g["counts"].tolist() == ref["counts"].tolist()
+    assert np.array_equal(g["srt_tok"][:R], ref["srt_tok"])
+    assert np.array_equal(g["srt_w"][:R].view(np.uint32), ref["srt_w"].view(np.uint32))
+    assert np.array_equal(g["pos"], ref["pos"])
+    assert np.array_equal(g["tile_expert"][:R // tm], ref["tile_expert"])
+    # nothing past the padded rows / tiles is written
+    assert np.all(g["srt_tok"][R:] == POISON_I)
+    assert np.all(g["srt_w"][R:] == POISON_W)
+    assert np.all(g["tile_expert"][R // tm:] == POISON_I)
+
+
+def check(ids, w, E, tm):
+    g, status = gpu_plan(ids, w, E, tm)
+    ref = oracle.plan(ids, w, E, tm)
+    assert status == 0
+    assert_same_plan(g, ref, tm)
+    return ref
+
+
+@pytest.mark.parametrize("cfg,chunk", [(1, 0), (2, 0), (3, 0), (4, 0), (5, 0), (5, 7)])
+def test_plan_workloads(cfg, chunk):
+    wl = W.workload(cfg)
+    inp = W.make_inputs(wl, chunk=chunk, weights=False)
+    check(inp["ids"], inp["w"], wl.E, wl.tm)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_plan_page1_shape_seeds(seed):
+    ids, w = W.make_routing(2048, 512, 10, "topk_bias", seed=seed)
+    check(ids, w, 512, 16)
+
+
+EDGE = [
+    # T, k, E, tm
+    (1, 1, 1, 1), (1, 10, 512, 16), (7, 2, 3, 16), (1023, 10, 512, 16), (1024, 10, 512, 16),
+    (1025, 10, 512, 16), (300, 8, 31, 32), (300, 8, 33, 64), (777, 2, 1024, 128),
+    (513, 1, 2, 16), (64, 8, 4096, 16), (2049, 10, 512, 1), (100, 3, 5, 1024),
+    (97, 256, 300, 16),
+]
+
+
+@pytest.mark.parametrize("T,k,E,tm", EDGE)
+def test_plan_edges(T, k, E, tm):
+    rng = np.random.default_rng(T * 7919 + k * 31 + E)
+    ids = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    w = rng.standard_normal((T, k)).astype(np.float32)
+    check(ids, w, E, tm)
+
+
+def test_plan_all_tokens_one_expert():
+    ids = np.full((4096, 8), 77, np.int32)
+    w = np.random.default_rng(1).random((4096, 8)).astype(np.float32)
+    ref = check(ids, w, 128, 16)
+    assert ref["counts"][77] == 4096 * 8
+
+
+def test_plan_many_empty_experts_and_skips():
+    rng = np.random.default_rng(2)
+    ids = rng.choice([3, 900, 901, 4000], size=(1500, 6)).astype(np.int32)
+    ids[rng.random(ids.shape) < 0.3] = -1
+    w = rng.standard_normal(ids.shape).astype(np.float32)
+    check(ids, w, 4096, 16)
+
+
+def test_plan_large_block_path():
+    # T*k above 512 * 256 entries: blocks of more than 512 entries
+    ids, w = W.make_routing(70001, 256, 2, "topk", seed=3)
+    check(ids, w, 256, 16)
+
+
+def test_plan_zero_tokens():
+    g, status = gpu_plan(np.zeros((0, 4), np.int32), np.zeros((0, 4), np.float32), 9, 16)
+    assert status == 0
+    assert g["offsets"].tolist() == [0] * 10 and g["counts"].tolist() == [0] * 9
+
+
+def test_plan_bad_ids_flag_status_and_are_skipped():
+    rng = np.random.default_rng(4)
+    ids = rng.integers(0, 40, size=(200, 4)).astype(np.int32)
+    w = rng.standard_normal(ids.shape).astype(np.float32)
+    bad = ids.copy()
+    bad[3, 1], bad[150, 0], bad[199, 3] = 40, -5, 1 << 30
+    g, status = gpu_plan(bad, w, 40, 16)
+    assert status & B.STATUS_BAD_ID
+    fixed = np.where((bad < -1) | (bad >= 40), -1, bad).astype(np.int32)
+    assert_same_plan(g, oracle.plan(fixed, w, 40, 16), 16)
+
+
+def test_plan_weights_copied_bitwise():
+    # NaN payloads, -0.0, denormals and infinities travel unchanged
+    ids = np.array([[0, 1], [1, 0], [0, 0]], np.int32)
+    wb = np.array([[0x7FC01234, 0x80000000], [0x00000001, 0x7F800000], [0xFF800000, 0x3F800000]],
+                  np.uint32)
+    w = wb.view(np.float32)
+    g, status = gpu_plan(ids, w, 2, 16)
+    ref = oracle.plan(ids, w, 2, 16)
+    assert_same_plan(g, ref, 16)
+
+
+def test_plan_repeatable():
+    inp = inputs(2)
+    a, _ = gpu_plan(inp["ids"], inp["w"], 512, 16)
+    b, _ = gpu_plan(inp["ids"], inp["w"], 512, 16)
+    for n in a:
+        assert np.array_equal(a[n], b[n])
