@@ -1,0 +1,380 @@
+#!/usr/bin/env python3
+"""Benchmark of the routed MoE prefill layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+One step is one whole layer call (moe_layer_forward: plan -> gather ->
+gate/up -> down -> combine) over one synthetic chunk already resident in HBM,
+on the full page-1-scale layer: T=2048 tokens, d=2560, E=512 experts, top-10,
+expert FFN f=512, tm=16, skewed routing (router logits N(0,1) plus a
+per-expert N(0,1) bias).  L2 is flushed (256 MiB write) before every timed
+step; the weights alone (4 GB) are far larger than L2 too.
+
+Printed: ONE JSON line with rows/s (T*k routed rows per layer), the plan's
+microseconds per layer, per-stage times, the roofline of the dominant kernel
+(the gate/up GEMM), the end-to-end rows/s through host buffers, SM clocks
+sampled during the timed region, and the CPU oracle timed on a bounded
+sample on this host's cores.
+
+``--impl reference`` times the CPU oracle itself (the only reference this
+method has) on bounded samples of the same workload.
+
+Multi-GPU (torchrun): every rank runs its own independent layer on its own
+chunk of tokens (weak scaling, no collective on the data path); rank 0
+prints the line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as dt
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from moe_prefill_routing_gb300 import binding as B  # noqa: E402
+from moe_prefill_routing_gb300 import replicas  # noqa: E402
+from moe_prefill_routing_gb300 import workload as W  # noqa: E402
+
+METRIC = "MoE layer routed rows/s (plan+gather+FFN+combine); plan µs/layer at T=2048"
+WORKLOAD = 3
+KERNELS_PER_LAYER = 7  # hist, scan+pad, place, gather, gate/up, down, combine
+FLUSH_BYTES = 256 << 20
+PROFILE = os.path.join(ROOT, "profiles", "ffn_gate_up_layer_t2048_d2560_e512_k10_f512.md")
+FFN_SRC = os.path.join(ROOT, "moe_prefill_routing_gb300", "csrc", "ffn.cu")
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---- helpers ----------------------------------------------------------------
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def profile_traffic():
+    """dram bytes per launch of the gate/up kernel from the committed ncu
+    summary, or None when the kernel source changed since the capture."""
+    if not os.path.exists(PROFILE):
+        return None
+    txt = open(PROFILE).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", txt)
+    h = re.search(r"ffn_cu_sha256:\s*([0-9a-f]{64})", txt)
+    if not m or not h:
+        return None
+    cur = hashlib.sha256(open(FFN_SRC, "rb").read()).hexdigest()
+    return int(m.group(1)) if h.group(1) == cur else None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            cmd.insert(1, f"--id={uuid if uuid.startswith('GPU-') else 'GPU-' + uuid}")
+        except Exception:
+            pass
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.seek(0)
+        rows = []
+        for line in self.file.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 9:
+                continue
+            try:
+                ts = dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        inwin = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15]
+        use = inwin or rows
+        reasons = sorted({n for r in use for n, v in zip(self.NAMES, r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use),
+                "window": "timed region" if inwin else "whole run"}
+
+
+def algorithmic(wl, ids):
+    """Algorithmic work of one layer from the routing itself: active experts,
+    real and padded rows, and the bytes / flops each stage must move."""
+    flat = ids.ravel()
+    counts = np.bincount(flat[flat >= 0], minlength=wl.E)
+    active = int((counts > 0).sum())
+    R = int(counts.sum())
+    R_pad = int((-(-counts // wl.tm) * wl.tm).sum())
+    d, f = wl.d, wl.f
+    gate_up = active * 2 * d * f * 2 + R_pad * d * 2 + R_pad * f * 2
+    down = active * f * d * 2 + R_pad * f * 2 + R_pad * d * 2 + R_pad * 4
+    gather = wl.T * d * 2 + R_pad * d * 2 + R_pad * 4
+    combine = R * d * 2 + wl.T * d * 2 + R * 4
+    plan = 8 * wl.T * wl.k + 4 * wl.T * wl.k + 8 * R_pad + 8 * (wl.E + 1)
+    return dict(active=active, R=R, R_pad=R_pad, gate_up=gate_up, down=down, gather=gather,
+                combine=combine, plan=plan, layer=plan + gather + gate_up + down + combine,
+                flops=6 * d * f * R)
+
+
+def d16(a, dev):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+# ---- CPU oracle timing ----------------------------------------------------------
+
+def oracle_sample(inp, wl, budget_s, nthreads):
+    """Times the oracle on a bounded sample of the workload: the full plan
+    (single-threaded by definition) and the layer for the first n tokens,
+    n chosen to take about budget_s.  Returns rows/s and a description."""
+    import oracle  # CPU baseline leg only
+
+    t = time.perf_counter()
+    oracle.plan(inp["ids"], inp["w"], wl.E, wl.tm)
+    t_plan = time.perf_counter() - t
+    args = (inp["x"], inp["ids"], inp["w"], inp["Wg"], inp["Wu"], inp["Wd"])
+    pilot = np.arange(min(4, wl.T), dtype=np.int32)
+    t = time.perf_counter()
+    oracle.layer(*args, x_dtype=wl.x_dtype, tokens=pilot, nthreads=nthreads)
+    per_tok = (time.perf_counter() - t) / len(pilot)
+    n = int(max(len(pilot), min(wl.T, budget_s / max(per_tok, 1e-9))))
+    toks = np.arange(n, dtype=np.int32)
+    t = time.perf_counter()
+    oracle.layer(*args, x_dtype=wl.x_dtype, tokens=toks, nthreads=nthreads)
+    t_layer = time.perf_counter() - t
+    secs = t_layer + t_plan * n / wl.T
+    rows = n * wl.k
+    return rows / secs, secs, f"plan of all {wl.T * wl.k} rows (1 thread) + fp64 FFN/combine of " \
+                              f"the first {n} tokens ({rows} rows) on {nthreads} threads; " \
+                              f"plan time prorated per row"
+
+
+# ---- native arm ------------------------------------------------------------------
+
+def run_native(args, rank, world, local):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = W.workload(WORKLOAD)
+    chunk = replicas.chunk_of_rank(rank, world)
+    log(f"[rank {rank}] generating {wl.name} (chunk {chunk}) ...")
+    inp = W.make_inputs(wl, seed=0, chunk=chunk)
+    alg = algorithmic(wl, inp["ids"])
+    x, ids, w = d16(inp["x"], dev), torch.from_numpy(inp["ids"]).to(dev), torch.from_numpy(inp["w"]).to(dev)
+    Wg, Wu, Wd = (d16(inp[n], dev) for n in ("Wg", "Wu", "Wd"))
+    layer = B.MoeLayer(Wg, Wu, Wd, tm=wl.tm)
+    y = torch.empty((wl.T, wl.d), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    rows = wl.T * wl.k
+
+    def timed(step_fn, K):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            evs[i][0].record(stream)
+            step_fn()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b) for a, b in evs]
+
+    # warm-up, then EXACTLY K timed layer steps
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        layer.forward(x, ids, w, y=y)
+    torch.cuda.synchronize(dev)
+    status = B.read_status(layer._ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status:#x} after warm-up")
+    clocks = ClockSampler(dev) if rank == 0 else None
+    replicas.barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    ms = timed(lambda: layer.forward(x, ids, w, y=y), args.steps)
+    torch.cuda.synchronize(dev)
+    replicas.barrier(world)
+    t1 = time.time()
+    clk = clocks.stop(t0, t1) if clocks else None
+    total_ms = replicas.max_over_ranks(sum(ms), world, dev)
+    value = args.steps * rows * world / (total_ms / 1e3)
+
+    # per-stage breakdown through the stage entry points (same stream)
+    cap = B.capacity(wl.T, wl.k, wl.E, wl.tm)
+    o = B.plan(ids, w, wl.E, wl.tm, cap=cap)
+    xs = B.gather(x, o["srt_tok"], o["offsets"], wl.E, cap)
+    H = torch.empty((cap, wl.f), dtype=torch.bfloat16, device=dev)
+    Ys = torch.empty((cap, wl.d), dtype=torch.bfloat16, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    stages = ("plan", "gather", "gate_up", "down", "combine")
+    calls = (lambda: B.plan(ids, w, wl.E, wl.tm, cap=cap, out=o),
+             lambda: B.gather(x, o["srt_tok"], o["offsets"], wl.E, cap, xs=xs),
+             lambda: B.ffn_gate_up(xs, Wg, Wu, o["offsets"], cap, H=H, status=st),
+             lambda: B.ffn_down(H, Wd, o["offsets"], o["srt_w"], cap, Ys=Ys, status=st),
+             lambda: B.combine(Ys, o["pos"], y=y))
+    K2 = max(3, min(args.steps, 200))
+    per = {s: [] for s in stages}
+    for i in range(K2 + 3):
+        flush.fill_(i & 0xFF)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+        ev[0].record(stream)
+        for j, c in enumerate(calls):
+            c()
+            ev[j + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        if i >= 3:
+            for j, s in enumerate(stages):
+                per[s].append(ev[j].elapsed_time(ev[j + 1]) * 1e3)
+    stage_us = {s: statistics.median(v) for s, v in per.items()}
+    stage_mean_us = {s: statistics.mean(v) for s, v in per.items()}
+
+    # end to end: pinned host inputs in, y out, every step
+    x_h = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    ids_h = torch.from_numpy(inp["ids"]).pin_memory()
+    w_h = torch.from_numpy(inp["w"]).pin_memory()
+    y_h = torch.empty((wl.T, wl.d), dtype=torch.bfloat16).pin_memory()
+    for _ in range(3):
+        layer.forward_host(x_h, ids_h, w_h, y_h)
+    torch.cuda.synchronize(dev)
+    K3 = max(3, min(args.steps, 200))
+    ms_e2e = timed(lambda: layer.forward_host(x_h, ids_h, w_h, y_h), K3)
+    e2e_total = replicas.max_over_ranks(sum(ms_e2e), world, dev)
+    e2e_value = K3 * rows * world / (e2e_total / 1e3)
+    h2d = x_h.numel() * 2 + ids_h.numel() * 4 + w_h.numel() * 4
+    d2h = y_h.numel() * 2
+
+    if rank != 0:
+        return
+    hbm, peak_src = peaks()
+    t_gu = stage_mean_us["gate_up"] * 1e-6
+    achieved = alg["gate_up"] / t_gu / 1e9
+    traffic = profile_traffic()
+    layer_gbs = alg["layer"] / (sum(ms) / len(ms) / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(ms),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded: x~N(0,1), W~N(0,0.02) bf16, skewed top-10 routing)",
+        "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k, "f": wl.f,
+                   "tm": wl.tm, "routing": "top-k of N(0,1) logits + N(0,1) expert bias",
+                   "active_experts": alg["active"], "R_pad": alg["R_pad"],
+                   "l2": "flushed before every timed step (256 MiB write)",
+                   "parallelism": "replicas (one independent layer per GPU)"},
+        "plan_us_per_layer": stage_us["plan"],
+        "stages_us": stage_us,
+        "layer_hbm_gbs": layer_gbs,
+        "roofline": {"kernel": "k_ffn<gate/up> (tcgen05 grouped GEMM + SwiGLU)", "bound": "hbm",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": alg["gate_up"],
+                     "traffic": traffic},
+        "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(ms_e2e)},
+        "clocks": clk,
+        "gpu_launches": KERNELS_PER_LAYER * args.steps,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        nth = os.cpu_count() or 1
+        log("timing the CPU oracle on a bounded sample ...")
+        v, secs, desc = oracle_sample(inp, wl, args.cpu_budget, nth)
+        line["cpu_baseline"] = {"value": v, "unit": "rows/s", "cores": nth, "kind": "oracle",
+                                "sample": desc, "seconds": secs}
+    print(json.dumps(line), flush=True)
+
+
+# ---- reference arm: the CPU oracle ------------------------------------------------
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    wl = W.workload(WORKLOAD)
+    log(f"reference (CPU oracle): generating {wl.name} ...")
+    inp = W.make_inputs(wl, seed=0)
+    nth = os.cpu_count() or 1
+    budget = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(inp, wl, budget, nth)
+    vals, secs = [], []
+    desc = ""
+    for _ in range(args.steps):
+        v, s, desc = oracle_sample(inp, wl, budget, nth)
+        vals.append(v)
+        secs.append(s)
+    value = sum(v * s for v, s in zip(vals, secs)) / sum(secs)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.mean(secs), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k, "f": wl.f,
+                   "tm": wl.tm},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": nth, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("native", "reference"), default="native")
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = replicas.init_from_env(backend="nccl" if args.impl == "native" else "gloo")
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_native(args, rank, world, local)
+    finally:
+        replicas.finalize(world)
+
+
+if __name__ == "__main__":
+    main()
