@@ -1,0 +1,69 @@
+"""A short, self-contained run of one stage for profilers (ncu).
+
+    python -m moe_prefill_routing_gb300.profile_run --workload 3 --experts 128 \
+        --stage gate_up --iters 3
+
+Generates the named workload (optionally with fewer experts, routing redrawn
+for that expert count, so that the device holds a few GB at most), runs the
+whole layer once through the stage entry points, then runs the chosen stage
+``--iters`` more times.  Every stage call goes through the C ABI.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import sys
+
+import numpy as np
+import torch
+
+from . import binding as B
+from . import workload as W
+
+STAGES = ("plan", "gather", "gate_up", "down", "combine", "layer")
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", type=int, default=3)
+    ap.add_argument("--experts", type=int, default=0, help="override E (0: the workload's)")
+    ap.add_argument("--stage", choices=STAGES, default="gate_up")
+    ap.add_argument("--iters", type=int, default=3)
+    a = ap.parse_args(argv)
+    wl = W.workload(a.workload)
+    if a.experts:
+        wl = dataclasses.replace(wl, E=a.experts, name=f"{wl.name}_E{a.experts}")
+    dev = torch.device("cuda", 0)
+    inp = W.make_inputs(wl)
+
+    def d16(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    x = d16(inp["x"])
+    ids = torch.from_numpy(inp["ids"]).to(dev)
+    w = torch.from_numpy(inp["w"]).to(dev)
+    Wg, Wu, Wd = (d16(inp[n]) for n in ("Wg", "Wu", "Wd"))
+    cap = B.capacity(wl.T, wl.k, wl.E, wl.tm)
+    o = B.plan(ids, w, wl.E, wl.tm, cap=cap)
+    xs = B.gather(x, o["srt_tok"], o["offsets"], wl.E, cap)
+    H, Ys = B.expert_ffn(xs, Wg, Wu, Wd, o["offsets"], o["srt_w"], cap)
+    y = B.combine(Ys, o["pos"])
+    calls = {
+        "plan": lambda: B.plan(ids, w, wl.E, wl.tm, cap=cap, out=o),
+        "gather": lambda: B.gather(x, o["srt_tok"], o["offsets"], wl.E, cap, xs=xs),
+        "gate_up": lambda: B.ffn_gate_up(xs, Wg, Wu, o["offsets"], cap, H=H),
+        "down": lambda: B.ffn_down(H, Wd, o["offsets"], o["srt_w"], cap, Ys=Ys),
+        "combine": lambda: B.combine(Ys, o["pos"], y=y),
+        "layer": lambda: B.layer_forward(x, ids, w, Wg, Wu, Wd, wl.tm, y=y),
+    }
+    for _ in range(a.iters):
+        calls[a.stage]()
+    torch.cuda.synchronize(dev)
+    flat = inp["ids"].ravel()
+    counts = np.bincount(flat[flat >= 0], minlength=wl.E)
+    print(f"{wl.name}: stage {a.stage} x{a.iters}; active experts {(counts > 0).sum()}, "
+          f"R_pad {int((-(-counts // wl.tm) * wl.tm).sum())}", file=sys.stderr)
+
+
+if __name__ == "__main__":
+    main()
