@@ -138,6 +138,42 @@ MOE_API int moe_plan(const int32_t *ids, const float *w, int T, int k, int E, in
              size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * moe_plan_noalloc -- moe_plan for callers that cannot allocate device memory.
+ *
+ * The paper has no counterpart: this is an interface addition.  moe_plan
+ * needs a caller-provided workspace for its per-block expert counts.  Some
+ * callers cannot obtain one: a serving process whose memory manager has
+ * already reserved all of the GPU's memory for its own pool, or a plug-in
+ * that is handed buffers by a host application and has no allocator of its
+ * own.  This entry point computes exactly what moe_plan computes (same
+ * kernels, same outputs, bit for bit) but keeps that scratch in a fixed
+ * array inside the library, MOE_PLAN_NOALLOC_SCRATCH_BYTES of device memory
+ * that every GPU which loads the library holds until the process exits.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Arguments are those of moe_plan, without ws / ws_bytes and with
+ *   status   uint32* device word that receives the MOE_STATUS_* bits of this
+ *            call (reset by the call), or NULL to leave them in the library.
+ * Limit: plan blocks x E <= MOE_PLAN_NOALLOC_MAX_COUNTS, where the plan
+ * uses ceil(T*k / 512) blocks (at most 256): any T with E <= 1024, or
+ * T*k <= 32768 with E = 4096.  Larger sizes return MOE_ERR_WORKSPACE.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any
+ * stream capture.  Every call on a device shares the same array and leaves
+ * its contents behind; nothing in it has to start at zero (every count the
+ * kernels read is written first by the same call), but calls that overlap on
+ * the GPU (on different streams without ordering) race on it and must not
+ * be issued.
+ */
+#define MOE_PLAN_NOALLOC_MAX_COUNTS 262144
+#define MOE_PLAN_NOALLOC_SCRATCH_BYTES (256 + 4 * MOE_PLAN_NOALLOC_MAX_COUNTS)
+MOE_API int moe_plan_noalloc(const int32_t *ids, const float *w, int T, int k, int E, int tm,
+                             int32_t *offsets, int32_t *counts, int32_t *srt_tok, float *srt_w,
+                             int32_t *pos, int32_t *tile_expert, int64_t cap, uint32_t *status,
+                             moe_stream_t stream);
+
+/*
  * moe_gather -- rows into expert-sorted order (same page, section 1 item 4).
  *
  * in   x        16-bit [T, d]   token activations (dtype MOE_DT_BF16 or MOE_DT_F16)

@@ -32,6 +32,9 @@ _SIGS = {
     "moe_plan": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int,
                            C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                            C.c_void_p, C.c_int64, C.c_void_p, C.c_size_t, C.c_void_p]),
+    "moe_plan_noalloc": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int,
+                                   C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                   C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p]),
     "moe_gather": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p,
                              C.c_int, C.c_int64, C.c_void_p, C.c_void_p]),
     "moe_ffn_gate_up": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int,
@@ -162,6 +165,33 @@ def plan(ids, w, E: int, tm: int, cap: int | None = None, out: dict | None = Non
                             _ptr(o["pos"]), _ptr(o["tile_expert"]), cap, _ptr(o["ws"]),
                             o["ws"].numel(), _stream(dev))
     _check("moe_plan", rc)
+    o["cap"] = cap
+    return o
+
+
+def plan_noalloc(ids, w, E: int, tm: int, cap: int | None = None, out: dict | None = None,
+                 status=None) -> dict:
+    """moe_plan_noalloc: the same plan as ``plan`` with the library's own
+    scratch instead of a workspace (for callers that cannot allocate device
+    memory).  Output tensors are allocated here only when ``out`` lacks
+    them; ``status`` is an optional int32 device tensor of one element."""
+    T, k = ids.shape
+    dev = ids.device
+    if cap is None:
+        cap = capacity(T, k, E, tm)
+    o = dict(out or {})
+    o.setdefault("offsets", torch.empty(E + 1, dtype=torch.int32, device=dev))
+    o.setdefault("counts", torch.empty(E, dtype=torch.int32, device=dev))
+    o.setdefault("srt_tok", torch.empty(max(cap, 1), dtype=torch.int32, device=dev))
+    o.setdefault("srt_w", torch.empty(max(cap, 1), dtype=torch.float32, device=dev))
+    o.setdefault("pos", torch.empty((T, k), dtype=torch.int32, device=dev))
+    o.setdefault("tile_expert", torch.empty(max(cap // tm, 1), dtype=torch.int32, device=dev))
+    with torch.cuda.device(dev):
+        rc = lib().moe_plan_noalloc(_ptr(ids), _ptr(w), T, k, E, tm, _ptr(o["offsets"]),
+                                    _ptr(o["counts"]), _ptr(o["srt_tok"]), _ptr(o["srt_w"]),
+                                    _ptr(o["pos"]), _ptr(o["tile_expert"]), cap, _ptr(status),
+                                    _stream(dev))
+    _check("moe_plan_noalloc", rc)
     o["cap"] = cap
     return o
 
