@@ -14,18 +14,23 @@
 // Swap-AB: the weight is the MMA's A operand (M = 128 output features) and
 // the expert's rows are its B operand (N = the unit's rows, a multiple of 16,
 // at most 128), so an expert with few rows still fills the M = 128 tile.
+// Each stage holds two A tiles and one B tile and feeds two accumulators:
+// gate/up uses (Wg, Wu) over the same 128 features; down uses two adjacent
+// 128-feature tiles of Wd, so one H tile serves 256 output features.
 // Weights are [E, K, M] with M contiguous, i.e. MN-major A tiles read by one
 // 3-D tensor map per weight (the expert is the outer coordinate); activation
 // rows are K-major B tiles.  Both use 128-byte swizzled shared memory.
 //
-// Work unit = (expert chunk of <= 128 rows, 128-feature tile), numbered
+// Work unit = (expert chunk of <= 128 rows, 128 (gate/up) or 256 (down)
+// output features), numbered
 // chunk-major so that the tiles of one chunk (same activation rows) and the
 // chunks of one big expert (same weight tile) run close together in time
 // and share L2.  Each CTA (one per SM) walks units u = blockIdx.x + i*grid.
 //
 // Warp roles: warp 0 issues TMA copies into a ring of shared-memory stages,
 // warp 1 issues tcgen05.mma into one of two TMEM accumulators, warps 2-5
-// read the accumulator with tcgen05.ld, apply the epilogue and store bf16.
+// read the accumulator with tcgen05.ld, apply the epilogue, stage 16 rows of
+// bf16 in shared memory and write them out as whole-row 16-byte vectors.
 // Every output element is written by one CTA with a fixed K order: results
 // are deterministic.  Every wait is bounded (2 s); on a timeout the CTA
 // stops, lets its copies and MMAs land, frees TMEM and sets
@@ -56,21 +61,18 @@ constexpr int kEpiThreads = 128;
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for the stop path
 
+constexpr int kStages = 4;
+constexpr uint32_t kStageBytes = 2 * kATileBytes + kBTileBytes;  // two A tiles + one B tile
+constexpr uint32_t kAccCols = 2 * BN;                            // two accumulators per buffer
+constexpr uint32_t kTmemCols = 2 * kAccCols;                     // double-buffered
+constexpr int kStageRows = 16;                                   // rows per epilogue chunk
+constexpr uint32_t kStgBytes = 2 * kStageRows * 256 * 2;         // two chunks of <= 256 features
+
+// GATED: gate/up (A tiles = Wg and Wu over the same 128 features, output H).
+// !GATED: down (A tiles = Wd over features m0 and m0 + 128, output Ys).
 template <bool GATED>
-struct Cfg;
-template <>
-struct Cfg<true> {  // gate/up: A = Wg and Wu, B = xs, two accumulators
-    static constexpr int kStages = 4;
-    static constexpr uint32_t kStageBytes = 2 * kATileBytes + kBTileBytes;
-    static constexpr uint32_t kAccCols = 2 * BN;
-    static constexpr uint32_t kTmemCols = 2 * kAccCols;
-};
-template <>
-struct Cfg<false> {  // down: A = Wd, B = H, one accumulator
-    static constexpr int kStages = 6;
-    static constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
-    static constexpr uint32_t kAccCols = BN;
-    static constexpr uint32_t kTmemCols = 2 * kAccCols;
+struct Kind {
+    static constexpr int kUnitM = GATED ? BM : 2 * BM;  // output features per unit
 };
 
 template <int S>
@@ -82,6 +84,7 @@ struct Ctrl {
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
+    int epi_stop;  // set only by epilogue threads; read by all four warps after a barrier
     int warp_sum[kThreads / 32];
 };
 
@@ -96,11 +99,10 @@ struct FfnArgs {
     int M;  // output features: f (gate/up) or d (down)
 };
 
-template <bool GATED>
 constexpr size_t ffn_smem_bytes(int E)
 {
-    return 1024 + size_t(Cfg<GATED>::kStages) * Cfg<GATED>::kStageBytes +
-           sizeof(Ctrl<Cfg<GATED>::kStages>) + size_t(E + 1) * sizeof(int);
+    return 1024 + size_t(kStages) * kStageBytes + kStgBytes + sizeof(Ctrl<kStages>) +
+           size_t(E + 1) * sizeof(int);
 }
 
 // Bounded wait that ignores the abort flag (used while stopping).
@@ -193,17 +195,23 @@ __device__ __forceinline__ uint16_t bf16_bits(float v)
     return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
+__device__ __forceinline__ void epi_bar()
+{
+    asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
+}
+
 template <bool GATED>
 __global__ void __launch_bounds__(kThreads, 1)
     k_ffn(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
           const __grid_constant__ CUtensorMap map_b, const FfnArgs p)
 {
-    using C = Cfg<GATED>;
-    constexpr int S = C::kStages;
+    constexpr int S = kStages;
+    constexpr int UM = Kind<GATED>::kUnitM;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
-    Ctrl<S> *ctl = reinterpret_cast<Ctrl<S> *>(smem + S * C::kStageBytes);
+    uint16_t *stg = reinterpret_cast<uint16_t *>(smem + S * kStageBytes);
+    Ctrl<S> *ctl = reinterpret_cast<Ctrl<S> *>(smem + S * kStageBytes + kStgBytes);
     int *chunk_start = reinterpret_cast<int *>(ctl + 1);
     const int warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
@@ -219,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&ctl->mma_done, 1);
         ctl->abort_flag = 0;
+        ctl->epi_stop = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -228,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&map_b);
     }
     if (warp == 1) {
-        tmem_alloc(&ctl->tmem_base, C::kTmemCols);
+        tmem_alloc(&ctl->tmem_base, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before_sync();
@@ -242,9 +251,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int total_chunks =
         build_chunk_table(p.offsets, p.E, p.cap, chunk_start, ctl->warp_sum, p.status);
-    const int n_mt = (p.M + BM - 1) / BM;
+    const int n_mt = (p.M + UM - 1) / UM;
     const int nk = p.K / BK;
     const int64_t total_units = int64_t(total_chunks) * n_mt;
+
+    // first feature of A tile t of a unit starting at feature m0
+    auto tile_base = [](int m0, int t) { return GATED ? m0 : m0 + t * BM; };
 
     if (warp == 0) {
         // ---- TMA producer ----
@@ -254,11 +266,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int64_t u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
                 const Unit w = map_unit(u, n_mt, chunk_start, p.E, p.offsets);
-                const int m0 = w.mt * BM;
-                const bool hi_half = m0 + 64 < p.M;  // features m0+64.. exist
-                const uint32_t a_bytes = (hi_half ? 2u : 1u) * kABoxBytes;
-                const uint32_t bytes =
-                    (GATED ? 2u : 1u) * a_bytes + uint32_t(w.nrows) * uint32_t(BK * 2);
+                const int m0 = w.mt * UM;
+                uint32_t boxes = 0;  // 64-feature boxes per stage that hold real features
+                for (int t = 0; t < 2; ++t)
+                    for (int h = 0; h < 2; ++h)
+                        boxes += tile_base(m0, t) + 64 * h < p.M;
+                const uint32_t bytes = boxes * kABoxBytes + uint32_t(w.nrows) * uint32_t(BK * 2);
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag)) {
                         ok = false;
@@ -266,18 +279,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     uint64_t *fb = &ctl->full[stage];
                     mbar_arrive_expect_tx(fb, bytes);
-                    uint8_t *sa = smem + stage * C::kStageBytes;
+                    uint8_t *sa = smem + stage * kStageBytes;
                     const int k0 = kb * BK;
-                    tma_load_3d(sa, &map_a0, fb, m0, k0, w.e);
-                    if (hi_half)
-                        tma_load_3d(sa + kABoxBytes, &map_a0, fb, m0 + 64, k0, w.e);
-                    uint8_t *sb = sa + kATileBytes;
-                    if (GATED) {
-                        tma_load_3d(sb, &map_a1, fb, m0, k0, w.e);
-                        if (hi_half)
-                            tma_load_3d(sb + kABoxBytes, &map_a1, fb, m0 + 64, k0, w.e);
-                        sb += kATileBytes;
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const CUtensorMap *m = (GATED && t == 1) ? &map_a1 : &map_a0;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int f0 = tile_base(m0, t) + 64 * h;
+                            if (f0 < p.M)
+                                tma_load_3d(sa + t * kATileBytes + h * kABoxBytes, m, fb, f0, k0,
+                                            w.e);
+                        }
                     }
+                    uint8_t *sb = sa + 2 * kATileBytes;
                     for (int j = 0; j < w.nrows / kBoxRows; ++j)
                         tma_load_2d(sb + j * kBBoxBytes, &map_b, fb, k0, w.row0 + j * kBoxRows);
                     issued |= 1u << stage;
@@ -310,12 +325,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int64_t u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
                 const Unit w = map_unit(u, n_mt, chunk_start, p.E, p.offsets);
+                const int m0 = w.mt * UM;
+                const bool use1 = tile_base(m0, 1) < p.M;  // second A tile holds real features
                 if (!mbar_wait(&ctl->tmem_empty[abuf], aphase ^ 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t d0 = tmem_base + uint32_t(abuf) * C::kAccCols;
+                const uint32_t d0 = tmem_base + uint32_t(abuf) * kAccCols;
                 const uint32_t idesc = idesc_bf16_f32(BM, uint32_t(w.nrows), 1u, 0u);
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait(&ctl->full[stage], phase, abort_flag)) {
@@ -323,22 +340,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t sa = smem_u32(smem + stage * C::kStageBytes);
-                    const uint32_t sb = sa + (GATED ? 2u : 1u) * kATileBytes;
+                    const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+                    const uint32_t sb = sa + 2 * kATileBytes;
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                         // B: K-major rows of 128 B; the K step moves 32 B inside the row.
                         const uint64_t bdesc = smem_desc_sw128(sb + kk * UMMA_K * 2, 16, 1024);
                         // A: MN-major, one 128-byte row per K index; the K step moves 16 rows.
-                        const uint64_t adesc0 =
-                            smem_desc_sw128(sa + kk * UMMA_K * 128, kABoxBytes, 1024);
                         const uint32_t acc = (kb | kk) != 0;
-                        tc_mma_f16(d0, adesc0, bdesc, idesc, acc);
-                        if (GATED) {
-                            const uint64_t adesc1 = smem_desc_sw128(
-                                sa + kATileBytes + kk * UMMA_K * 128, kABoxBytes, 1024);
-                            tc_mma_f16(d0 + BN, adesc1, bdesc, idesc, acc);
-                        }
+                        tc_mma_f16(d0, smem_desc_sw128(sa + kk * UMMA_K * 128, kABoxBytes, 1024),
+                                   bdesc, idesc, acc);
+                        if (use1)
+                            tc_mma_f16(d0 + BN,
+                                       smem_desc_sw128(sa + kATileBytes + kk * UMMA_K * 128,
+                                                       kABoxBytes, 1024),
+                                       bdesc, idesc, acc);
                     }
                     tc_commit(&ctl->empty[stage]);  // frees the stage once these MMAs finish
                     if (++stage == S) {
@@ -359,46 +375,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // ---- epilogue: TMEM -> registers -> bf16 global ----
+        // ---- epilogue: TMEM -> registers -> shared (16 rows) -> global rows ----
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
-        const int row_in_tile = q * 32 + int(lane);
+        const int fq = q * 32 + int(lane);
+        const int et = int(threadIdx.x) - 64;  // 0..127
+        constexpr int kVecPerRow = UM / 8;
+        constexpr int kVecPerThread = kStageRows * kVecPerRow / kEpiThreads;
         int abuf = 0;
-        uint32_t aphase = 0;
+        uint32_t aphase = 0, chunk = 0;
         for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
             const Unit w = map_unit(u, n_mt, chunk_start, p.E, p.offsets);
-            const bool ok = mbar_wait(&ctl->tmem_full[abuf], aphase, abort_flag);
-            if (!__all_sync(kFull, ok))
+            const int m0 = w.mt * UM;
+            const bool use1 = tile_base(m0, 1) < p.M;
+            // The four warps stop together or not at all: they meet at named
+            // barriers below.  epi_stop is written before this barrier and read
+            // after it; the next write can only come after the unit's chunk
+            // barriers, which every thread reaches after its read.
+            if (!mbar_wait(&ctl->tmem_full[abuf], aphase, abort_flag))
+                *reinterpret_cast<volatile int *>(&ctl->epi_stop) = 1;
+            epi_bar();
+            if (*reinterpret_cast<volatile int *>(&ctl->epi_stop))
                 break;
             tc_fence_after_sync();
-            const int feat = w.mt * BM + row_in_tile;
             const uint32_t t0 =
-                tmem_base + (uint32_t(q * 32) << 16) + uint32_t(abuf) * C::kAccCols;
-            uint16_t *dst = p.out + int64_t(w.row0) * p.M + feat;
-            for (int c0 = 0; c0 < w.nrows; c0 += 16) {
-                uint32_t a[16];
+                tmem_base + (uint32_t(q * 32) << 16) + uint32_t(abuf) * kAccCols;
+            for (int c0 = 0; c0 < w.nrows; c0 += kStageRows, ++chunk) {
+                uint16_t *sg = stg + (chunk & 1u) * (kStageRows * 256);
+                uint32_t a[16], b[16];
                 tmem_ld_32x32b_x16(t0 + uint32_t(c0), a);
-                if (GATED) {
-                    uint32_t b[16];
+                if (GATED || use1)
                     tmem_ld_32x32b_x16(t0 + BN + uint32_t(c0), b);
-                    tmem_ld_wait();
-                    if (feat < p.M) {
+                tmem_ld_wait();
+                if (GATED) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float g = __uint_as_float(a[j]);
-                            const float up = __uint_as_float(b[j]);
-                            const float h = g / (1.0f + __expf(-g)) * up;
-                            dst[int64_t(c0 + j) * p.M] = bf16_bits(h);
-                        }
+                    for (int j = 0; j < 16; ++j) {
+                        const float g = __uint_as_float(a[j]);
+                        const float up = __uint_as_float(b[j]);
+                        sg[j * UM + fq] = bf16_bits(g / (1.0f + __expf(-g)) * up);
                     }
                 } else {
-                    tmem_ld_wait();
-                    if (feat < p.M) {
+                    const float *wr = p.srt_w + w.row0 + c0;
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float wr = p.srt_w[w.row0 + c0 + j];
-                            dst[int64_t(c0 + j) * p.M] = bf16_bits(wr * __uint_as_float(a[j]));
-                        }
+                    for (int j = 0; j < 16; ++j) {
+                        const float s = wr[j];
+                        sg[j * UM + fq] = bf16_bits(s * __uint_as_float(a[j]));
+                        sg[j * UM + BM + fq] = use1 ? bf16_bits(s * __uint_as_float(b[j])) : 0;
                     }
+                }
+                epi_bar();
+                // 16 rows x UM features leave as 16-byte vectors, a whole row
+                // segment per group of UM/8 threads
+#pragma unroll
+                for (int i = 0; i < kVecPerThread; ++i) {
+                    const int v = et + i * kEpiThreads;
+                    const int row = v / kVecPerRow, cv = v - row * kVecPerRow;
+                    const int fo = m0 + cv * 8;
+                    if (fo < p.M)
+                        *reinterpret_cast<uint4 *>(p.out + int64_t(w.row0 + c0 + row) * p.M + fo) =
+                            *reinterpret_cast<const uint4 *>(sg + row * UM + cv * 8);
                 }
             }
             tc_fence_before_sync();
@@ -412,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, C::kTmemCols);
+        tmem_dealloc(tmem_base, kTmemCols);
     }
     if (threadIdx.x == 0 && ctl->abort_flag && p.status)
         atomicOr(p.status, MOE_STATUS_TIMEOUT);
@@ -482,12 +516,12 @@ cudaError_t launch_ffn_gate_up(const void *xs, const void *Wg, const void *Wu,
         (err = rows_map(&mx, xs, cap, d)) != cudaSuccess)
         return err;
     err = ensure_smem_limit(reinterpret_cast<const void *>(k_ffn<true>), kSlotGateUp,
-                            ffn_smem_bytes<true>(MOE_MAX_EXPERTS));
+                            ffn_smem_bytes(MOE_MAX_EXPERTS));
     if (err != cudaSuccess)
         return err;
     const FfnArgs a{offsets, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f};
     return launch_pdl(k_ffn<true>, dim3(device_sm_count()), dim3(kThreads),
-                      ffn_smem_bytes<true>(E), stream, mg, mu, mx, a);
+                      ffn_smem_bytes(E), stream, mg, mu, mx, a);
 }
 
 cudaError_t launch_ffn_down(const void *H, const void *Wd, const int32_t *offsets,
@@ -500,12 +534,12 @@ cudaError_t launch_ffn_down(const void *H, const void *Wd, const int32_t *offset
         (err = rows_map(&mh, H, cap, f)) != cudaSuccess)
         return err;
     err = ensure_smem_limit(reinterpret_cast<const void *>(k_ffn<false>), kSlotDown,
-                            ffn_smem_bytes<false>(MOE_MAX_EXPERTS));
+                            ffn_smem_bytes(MOE_MAX_EXPERTS));
     if (err != cudaSuccess)
         return err;
     const FfnArgs a{offsets, srt_w, static_cast<uint16_t *>(Ys), status, cap, E, f, d};
     return launch_pdl(k_ffn<false>, dim3(device_sm_count()), dim3(kThreads),
-                      ffn_smem_bytes<false>(E), stream, mw, mw, mh, a);
+                      ffn_smem_bytes(E), stream, mw, mw, mh, a);
 }
 
 }  // namespace moe
