@@ -30,6 +30,13 @@ inline int plan_num_blocks(int64_t n)
     return static_cast<int>((n + b - 1) / b);
 }
 
+// The per-block counts are stored expert-major, one row of this many int32
+// per expert (the block count rounded up to 4, so rows load as int4).
+inline int plan_count_stride(int64_t n)
+{
+    return (plan_num_blocks(n) + 3) / 4 * 4;
+}
+
 cudaError_t launch_plan(const int32_t *ids, const float *w, int T, int k, int E, int tm,
                         int32_t *offsets, int32_t *counts, int32_t *srt_tok, float *srt_w,
                         int32_t *pos, int32_t *tile_expert, int64_t cap, uint32_t *status,

@@ -27,12 +27,15 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", type=int, default=3)
     ap.add_argument("--experts", type=int, default=0, help="override E (0: the workload's)")
+    ap.add_argument("--tokens", type=int, default=0, help="override T (0: the workload's)")
     ap.add_argument("--stage", choices=STAGES, default="gate_up")
     ap.add_argument("--iters", type=int, default=3)
     a = ap.parse_args(argv)
     wl = W.workload(a.workload)
     if a.experts:
         wl = dataclasses.replace(wl, E=a.experts, name=f"{wl.name}_E{a.experts}")
+    if a.tokens:
+        wl = dataclasses.replace(wl, T=a.tokens, name=f"{wl.name}_T{a.tokens}")
     dev = torch.device("cuda", 0)
     inp = W.make_inputs(wl)
 
