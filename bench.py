@@ -264,6 +264,22 @@ def run_native(args, rank, world, local):
         if i >= 3:
             for j, s in enumerate(stages):
                 per[s].append(ev[j].elapsed_time(ev[j + 1]) * 1e3)
+    # the plan alone, 48 layers per CUDA graph replay (the pages' plan figure is
+    # a 48-layer graph median per layer); inputs stay in L2 between layers
+    plan_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(plan_graph):
+        for _ in range(48):
+            B.plan(ids, w, wl.E, wl.tm, cap=cap, out=o)
+    plan_graph.replay()
+    torch.cuda.synchronize(dev)
+    reps = 50
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(reps):
+        plan_graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize(dev)
+    plan_graph_us = g0.elapsed_time(g1) * 1e3 / (48 * reps)
     stage_us = {s: statistics.median(v) for s, v in per.items()}
     stage_mean_us = {s: statistics.mean(v) for s, v in per.items()}
 
@@ -299,10 +315,13 @@ def run_native(args, rank, world, local):
                    "active_experts": alg["active"], "R_pad": alg["R_pad"],
                    "l2": "flushed before every timed step (256 MiB write)",
                    "parallelism": "replicas (one independent layer per GPU)"},
-        "plan_us_per_layer": stage_us["plan"],
+        "plan_us_per_layer": plan_graph_us,
+        "plan_us_per_layer_method": "48 moe_plan calls per CUDA graph replay, mean per call",
+        "plan_us_cold": stage_us["plan"],
         "stages_us": stage_us,
         "layer_hbm_gbs": layer_gbs,
-        "roofline": {"kernel": "k_ffn<gate/up> (tcgen05 grouped GEMM + SwiGLU)", "bound": "hbm",
+        "roofline": {"kernel": "k_ffn<gate/up> (tcgen05 grouped GEMM + SwiGLU)",
+                     "bound": "hbm",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": alg["gate_up"],

@@ -206,6 +206,22 @@ MOE_API int moe_ffn_gate_up(const void *xs, const void *Wg, const void *Wu,
                     void *H, uint32_t *status, moe_stream_t stream);
 
 /*
+ * moe_ffn_gate_up_rows -- moe_ffn_gate_up reading each routed row straight
+ * from the token activations: row r of expert e is x[srt_tok[r]] (a zero
+ * row where srt_tok[r] = -1), fetched four rows at a time by TMA gather4,
+ * so the gathered copy xs is never written.  Same arithmetic and result as
+ * moe_gather followed by moe_ffn_gate_up, bit for bit.  On GB300 the
+ * gather4 loads make this slower than the separate 128-bit gather plus tiled
+ * loads, so moe_layer_forward does not use it.
+ * in   x        bf16 [T, d]
+ * in   srt_tok  int32 [cap]   from moe_plan
+ * other arguments as in moe_ffn_gate_up.
+ */
+MOE_API int moe_ffn_gate_up_rows(const void *x, int T, const int32_t *srt_tok, const void *Wg,
+                                 const void *Wu, const int32_t *offsets, int E, int d, int f,
+                                 int64_t cap, void *H, uint32_t *status, moe_stream_t stream);
+
+/*
  * moe_ffn_down -- grouped down projection scaled by the routing weight.
  *
  *   Ys[r] = bf16(srt_w[r] * (H[r] . Wd[e]))   (fp32 accumulation)

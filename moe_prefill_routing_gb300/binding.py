@@ -40,6 +40,9 @@ _SIGS = {
     "moe_ffn_gate_up": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int,
                                   C.c_int, C.c_int, C.c_int64, C.c_void_p, C.c_void_p,
                                   C.c_void_p]),
+    "moe_ffn_gate_up_rows": (C.c_int, [C.c_void_p, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p,
+                                       C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int64,
+                                       C.c_void_p, C.c_void_p, C.c_void_p]),
     "moe_ffn_down": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int,
                                C.c_int, C.c_int, C.c_int64, C.c_void_p, C.c_void_p,
                                C.c_void_p]),
@@ -216,6 +219,20 @@ def ffn_gate_up(xs, Wg, Wu, offsets, cap: int, H=None, status=None):
         rc = lib().moe_ffn_gate_up(_ptr(xs), _ptr(Wg), _ptr(Wu), _ptr(offsets), E, d, f, cap,
                                    _ptr(H), _ptr(status), _stream(xs.device))
     _check("moe_ffn_gate_up", rc)
+    return H
+
+
+def ffn_gate_up_rows(x, srt_tok, Wg, Wu, offsets, cap: int, H=None, status=None):
+    """gate/up with the routed rows read from x [T, d] by srt_tok (no xs)."""
+    T = x.shape[0]
+    E, d, f = Wg.shape
+    if H is None:
+        H = torch.empty((max(cap, 1), f), dtype=torch.bfloat16, device=x.device)
+    with torch.cuda.device(x.device):
+        rc = lib().moe_ffn_gate_up_rows(_ptr(x), T, _ptr(srt_tok), _ptr(Wg), _ptr(Wu),
+                                        _ptr(offsets), E, d, f, cap, _ptr(H), _ptr(status),
+                                        _stream(x.device))
+    _check("moe_ffn_gate_up_rows", rc)
     return H
 
 

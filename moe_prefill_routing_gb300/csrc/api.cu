@@ -196,6 +196,25 @@ int moe_ffn_gate_up(const void *xs, const void *Wg, const void *Wu, const int32_
                                            as_stream(stream)));
 }
 
+int moe_ffn_gate_up_rows(const void *x, int T, const int32_t *srt_tok, const void *Wg,
+                         const void *Wu, const int32_t *offsets, int E, int d, int f, int64_t cap,
+                         void *H, uint32_t *status, moe_stream_t stream)
+{
+    int rc = ffn_checks(x, Wg, Wu, offsets, E, d, f, cap, H);
+    if (rc != MOE_OK)
+        return rc;
+    if (T < 0)
+        return MOE_ERR_SHAPE;
+    if (!srt_tok)
+        return MOE_ERR_NULL;
+    if (!aligned(status, 4) || !aligned(srt_tok, 4))
+        return MOE_ERR_ALIGN;
+    if (cap == 0 || T == 0)
+        return MOE_OK;
+    return cuda_rc(moe::launch_ffn_gate_up_rows(x, T, srt_tok, Wg, Wu, offsets, E, d, f, cap, H,
+                                                status, as_stream(stream)));
+}
+
 int moe_ffn_down(const void *H, const void *Wd, const int32_t *offsets, const float *srt_w,
                  int E, int d, int f, int64_t cap, void *Ys, uint32_t *status,
                  moe_stream_t stream)

@@ -90,6 +90,7 @@ struct Ctrl {
 
 struct FfnArgs {
     const int32_t *offsets;
+    const int32_t *srt_tok;  // gate/up with gathered rows: token of each row, -1 for pad rows
     const float *srt_w;  // down only
     uint16_t *out;       // H (gate/up) or Ys (down), bf16 bits, [cap, M]
     uint32_t *status;    // may be null
@@ -102,7 +103,7 @@ struct FfnArgs {
 constexpr size_t ffn_smem_bytes(int E)
 {
     return 1024 + size_t(kStages) * kStageBytes + kStgBytes + sizeof(Ctrl<kStages>) +
-           size_t(E + 1) * sizeof(int);
+           BN * sizeof(int) + size_t(E + 1) * sizeof(int);
 }
 
 // Bounded wait that ignores the abort flag (used while stopping).
@@ -200,7 +201,9 @@ __device__ __forceinline__ void epi_bar()
     asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
 }
 
-template <bool GATED>
+// GATHER: the B rows of a unit are token rows of x fetched by index
+// (srt_tok, four rows per TMA gather4) instead of consecutive rows of xs.
+template <bool GATED, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1)
     k_ffn(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
           const __grid_constant__ CUtensorMap map_b, const FfnArgs p)
@@ -212,7 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                 ~uintptr_t(1023));
     uint16_t *stg = reinterpret_cast<uint16_t *>(smem + S * kStageBytes);
     Ctrl<S> *ctl = reinterpret_cast<Ctrl<S> *>(smem + S * kStageBytes + kStgBytes);
-    int *chunk_start = reinterpret_cast<int *>(ctl + 1);
+    int *row_tok = reinterpret_cast<int *>(ctl + 1);  // [BN] tokens of the unit's rows
+    int *chunk_start = row_tok + BN;
     const int warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
 
@@ -259,13 +263,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto tile_base = [](int m0, int t) { return GATED ? m0 : m0 + t * BM; };
 
     if (warp == 0) {
-        // ---- TMA producer ----
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0, issued = 0, issued_par = 0;
-            bool ok = true;
-            for (int64_t u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-                const Unit w = map_unit(u, n_mt, chunk_start, p.E, p.offsets);
+        // ---- TMA producer (lane 0 issues; with GATHER the warp loads row indices) ----
+        int stage = 0;
+        uint32_t phase = 0, issued = 0, issued_par = 0;
+        bool ok = true;
+        for (int64_t u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+            const Unit w = map_unit(u, n_mt, chunk_start, p.E, p.offsets);
+            if (GATHER) {
+                // the previous unit's gather4s took their rows as operands at issue
+                for (int r = int(lane); r < w.nrows; r += 32)
+                    row_tok[r] = p.srt_tok[w.row0 + r];
+                __syncwarp();
+            }
+            if (lane == 0) {
                 const int m0 = w.mt * UM;
                 uint32_t boxes = 0;  // 64-feature boxes per stage that hold real features
                 for (int t = 0; t < 2; ++t)
@@ -293,8 +303,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     uint8_t *sb = sa + 2 * kATileBytes;
-                    for (int j = 0; j < w.nrows / kBoxRows; ++j)
-                        tma_load_2d(sb + j * kBBoxBytes, &map_b, fb, k0, w.row0 + j * kBoxRows);
+                    if (GATHER) {
+                        for (int j = 0; j < w.nrows; j += 4)
+                            tma_gather4(sb + j * (BK * 2), &map_b, fb, k0, row_tok[j],
+                                        row_tok[j + 1], row_tok[j + 2], row_tok[j + 3]);
+                    } else {
+                        for (int j = 0; j < w.nrows / kBoxRows; ++j)
+                            tma_load_2d(sb + j * kBBoxBytes, &map_b, fb, k0,
+                                        w.row0 + j * kBoxRows);
+                    }
                     issued |= 1u << stage;
                     issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == S) {
@@ -303,6 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            ok = __shfl_sync(kFull, ok, 0);
+            __syncwarp();
+        }
+        if (lane == 0) {
             // every stage must be released by the MMA side before the CTA exits
             for (int i = 0; ok && i < S; ++i) {
                 ok = mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag);
@@ -503,6 +524,15 @@ cudaError_t rows_map(CUtensorMap *m, const void *X, int64_t cap, int K)
     return encode_bf16(m, X, 2, dims, strides, box);
 }
 
+// Token rows [T, K] read four at a time by index: one-row boxes of 64 K.
+cudaError_t token_rows_map(CUtensorMap *m, const void *X, int T, int K)
+{
+    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(T)};
+    const cuuint64_t strides[1] = {cuuint64_t(K) * 2};
+    const cuuint32_t box[2] = {BK, 1};
+    return encode_bf16(m, X, 2, dims, strides, box);
+}
+
 }  // namespace
 
 cudaError_t launch_ffn_gate_up(const void *xs, const void *Wg, const void *Wu,
@@ -515,12 +545,31 @@ cudaError_t launch_ffn_gate_up(const void *xs, const void *Wg, const void *Wu,
         (err = weight_map(&mu, Wu, E, d, f)) != cudaSuccess ||
         (err = rows_map(&mx, xs, cap, d)) != cudaSuccess)
         return err;
-    err = ensure_smem_limit(reinterpret_cast<const void *>(k_ffn<true>), kSlotGateUp,
+    err = ensure_smem_limit(reinterpret_cast<const void *>(k_ffn<true, false>), kSlotGateUp,
                             ffn_smem_bytes(MOE_MAX_EXPERTS));
     if (err != cudaSuccess)
         return err;
-    const FfnArgs a{offsets, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f};
-    return launch_pdl(k_ffn<true>, dim3(device_sm_count()), dim3(kThreads),
+    const FfnArgs a{offsets, nullptr, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f};
+    return launch_pdl(k_ffn<true, false>, dim3(device_sm_count()), dim3(kThreads),
+                      ffn_smem_bytes(E), stream, mg, mu, mx, a);
+}
+
+cudaError_t launch_ffn_gate_up_rows(const void *x, int T, const int32_t *srt_tok, const void *Wg,
+                                    const void *Wu, const int32_t *offsets, int E, int d, int f,
+                                    int64_t cap, void *H, uint32_t *status, cudaStream_t stream)
+{
+    CUtensorMap mg, mu, mx;
+    cudaError_t err;
+    if ((err = weight_map(&mg, Wg, E, d, f)) != cudaSuccess ||
+        (err = weight_map(&mu, Wu, E, d, f)) != cudaSuccess ||
+        (err = token_rows_map(&mx, x, T, d)) != cudaSuccess)
+        return err;
+    err = ensure_smem_limit(reinterpret_cast<const void *>(k_ffn<true, true>), kSlotGateUpRows,
+                            ffn_smem_bytes(MOE_MAX_EXPERTS));
+    if (err != cudaSuccess)
+        return err;
+    const FfnArgs a{offsets, srt_tok, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f};
+    return launch_pdl(k_ffn<true, true>, dim3(device_sm_count()), dim3(kThreads),
                       ffn_smem_bytes(E), stream, mg, mu, mx, a);
 }
 
@@ -533,12 +582,12 @@ cudaError_t launch_ffn_down(const void *H, const void *Wd, const int32_t *offset
     if ((err = weight_map(&mw, Wd, E, f, d)) != cudaSuccess ||
         (err = rows_map(&mh, H, cap, f)) != cudaSuccess)
         return err;
-    err = ensure_smem_limit(reinterpret_cast<const void *>(k_ffn<false>), kSlotDown,
+    err = ensure_smem_limit(reinterpret_cast<const void *>(k_ffn<false, false>), kSlotDown,
                             ffn_smem_bytes(MOE_MAX_EXPERTS));
     if (err != cudaSuccess)
         return err;
-    const FfnArgs a{offsets, srt_w, static_cast<uint16_t *>(Ys), status, cap, E, f, d};
-    return launch_pdl(k_ffn<false>, dim3(device_sm_count()), dim3(kThreads),
+    const FfnArgs a{offsets, nullptr, srt_w, static_cast<uint16_t *>(Ys), status, cap, E, f, d};
+    return launch_pdl(k_ffn<false, false>, dim3(device_sm_count()), dim3(kThreads),
                       ffn_smem_bytes(E), stream, mw, mw, mh, a);
 }
 

@@ -57,6 +57,11 @@ cudaError_t launch_ffn_gate_up(const void *xs, const void *Wg, const void *Wu,
                                const int32_t *offsets, int E, int d, int f, int64_t cap,
                                void *H, uint32_t *status, cudaStream_t stream);
 
+// gate/up with the B rows gathered from x [T, d] by srt_tok (no xs).
+cudaError_t launch_ffn_gate_up_rows(const void *x, int T, const int32_t *srt_tok, const void *Wg,
+                                    const void *Wu, const int32_t *offsets, int E, int d, int f,
+                                    int64_t cap, void *H, uint32_t *status, cudaStream_t stream);
+
 cudaError_t launch_ffn_down(const void *H, const void *Wd, const int32_t *offsets,
                             const float *srt_w, int E, int d, int f, int64_t cap, void *Ys,
                             uint32_t *status, cudaStream_t stream);
@@ -90,6 +95,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // Slots of ensure_smem_limit's per-device cache.
-enum SmemSlot { kSlotPlace = 0, kSlotHist, kSlotGateUp, kSlotDown, kSlotCount };
+enum SmemSlot { kSlotPlace = 0, kSlotHist, kSlotGateUp, kSlotGateUpRows, kSlotDown, kSlotCount };
 
 }  // namespace moe

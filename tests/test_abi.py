@@ -56,7 +56,7 @@ def test_workspace_layout(lib):
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     cap = B.capacity(T, k, E, tm)
     assert L["Ys"] - L["H"] >= cap * f * 2 and L["total"] - L["Ys"] >= cap * d * 2
-    assert L["xs"] - L["tile_expert"] >= (cap // tm) * 4
+    assert L["xs"] - L["tile_expert"] >= (cap // tm) * 4 and L["H"] - L["xs"] >= cap * d * 2
     assert B.workspace_bytes(T, d, E, k, f, tm) == L["total"]
     assert L["bcnt"] == 256 and L["offsets"] == B.plan_workspace_bytes(T, k, E)
 
@@ -99,6 +99,10 @@ def test_stage_argument_errors(lib):
     assert gu(FAKE, FAKE, FAKE, FAKE, 4, 64, 32, 100, FAKE, None, None) == B.MOE_ERR_SHAPE
     assert gu(FAKE, None, FAKE, FAKE, 4, 64, 64, 100, FAKE, None, None) == B.MOE_ERR_NULL
     assert gu(FAKE, FAKE, FAKE, FAKE, 4, 64, 64, 100, FAKE, FAKE + 2, None) == B.MOE_ERR_ALIGN
+    gr = lib.moe_ffn_gate_up_rows
+    assert gr(FAKE, 8, None, FAKE, FAKE, FAKE, 4, 64, 64, 100, FAKE, None, None) == B.MOE_ERR_NULL
+    assert gr(FAKE, -1, FAKE, FAKE, FAKE, FAKE, 4, 64, 64, 100, FAKE, None, None) == B.MOE_ERR_SHAPE
+    assert gr(FAKE, 8, FAKE, FAKE, FAKE, FAKE, 4, 64, 64, 0, FAKE, None, None) == B.MOE_OK
     dn = lib.moe_ffn_down
     assert dn(FAKE, FAKE, FAKE, None, 4, 64, 64, 100, FAKE, None, None) == B.MOE_ERR_NULL
     c = lib.moe_combine

@@ -49,6 +49,12 @@ def run_case(inp, E, d, f, tm, Wg, Wu, Wd, nsample=None):
     cap = B.capacity(T, k, E, tm)
     offsets = dev(p["offsets"])
     H = B.ffn_gate_up(dev16(to_cap(xs, cap)), Wg, Wu, offsets, cap)
+    # the same stage reading the rows straight from x by srt_tok (TMA gather4)
+    # computes the same arithmetic on the same shared-memory tiles: bit-equal
+    Hr = B.ffn_gate_up_rows(dev16(inp["x"]), dev(to_cap(p["srt_tok"], cap, fill=-1)), Wg, Wu,
+                            offsets, cap)
+    R = p["R_pad"]
+    assert torch.equal(H[:R].view(torch.int16), Hr[:R].view(torch.int16))
     rows = real if nsample is None else sample_rows(p, real, row_e, nsample)
     host = inputs_host(inp)
     h_ref, _ = oracle.expert_rows(xs, rows, row_e[rows], p["srt_w"][rows], *host)
