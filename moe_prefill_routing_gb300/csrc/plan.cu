@@ -16,10 +16,20 @@
 //    on top-k.  The place kernel is then a parallel scatter: row = block
 //    base of the expert + rank.
 //  - item 3: one CTA for the whole histogram+scan was slower than a multi-CTA
-//    histogram plus a one-CTA scan; the same split is kept.
+//    histogram plus a one-CTA scan, because one CTA cannot use the whole GPU.
+//    On GB300 the launch and completion gaps between three small kernels
+//    cost more than the work, so chunks of up to 64K entries run the whole
+//    plan in ONE launch of a thread-block cluster (16 CTAs of 1024 threads
+//    where the GPU can place them, else 8): each CTA counts and ranks its
+//    share of the entries, then, through distributed shared memory and
+//    hardware cluster barriers, each CTA scans a share of the experts and
+//    hands every CTA the first row of each expert for its share of entries.
+//    Larger inputs use the three kernels below.
 #include "../../include/moe_prefill.h"
 #include "internal.h"
 #include "ptx.cuh"
+
+#include <atomic>
 
 namespace moe {
 namespace {
@@ -222,6 +232,239 @@ __global__ void __launch_bounds__(kPlaceThreads)
         atomicOr(status, MOE_STATUS_BAD_ID);
 }
 
+// ---- one-launch plan for a thread-block cluster --------------------------------
+
+constexpr int kCThreads = 1024;
+constexpr int kCWarps = kCThreads / 32;
+constexpr int kCPasses = 4;       // 1024-entry passes per CTA, held in registers
+constexpr int kClusterMax = 16;
+
+constexpr size_t cluster_smem_bytes(int E)
+{
+    return size_t(kCWarps) * E + 2 * sizeof(int) * size_t(E) + (kClusterMax + kCWarps) * sizeof(int);
+}
+
+// CTA c of the cluster owns flat entries [c*chunk, (c+1)*chunk) and experts
+// [c*epc, (c+1)*epc).  Phase 1: per-expert counts of the CTA's entries and
+// each entry's rank among the CTA's earlier entries of its expert.  Phase 2
+// (owners): the expert's count over all CTAs, its padded size, offsets by a
+// scan over the owned experts plus the totals of the CTAs before, the tail
+// fill, the tile table, and for every CTA the first row of the expert's
+// entries in that CTA.  Phase 3: every entry's row = that first row + rank.
+__global__ void __launch_bounds__(kCThreads, 1)
+    k_plan_cluster(const int32_t *__restrict__ ids, const float *__restrict__ w, int64_t n, int k,
+                   int E, int tm, int64_t cap, int64_t chunk, int32_t *__restrict__ offsets,
+                   int32_t *__restrict__ counts, int32_t *__restrict__ srt_tok,
+                   float *__restrict__ srt_w, int32_t *__restrict__ pos,
+                   int32_t *__restrict__ tile_expert, uint32_t *__restrict__ status)
+{
+    extern __shared__ __align__(16) uint8_t csm[];
+    uint8_t *cnt = csm;                                        // [32 warps][E]
+    int *carry = reinterpret_cast<int *>(csm + kCWarps * E);  // [E] counts of this CTA
+    int *rowbase = carry + E;                                  // [E] first row, this CTA
+    int *tot = rowbase + E;                                    // [16] padded rows per CTA
+    int *warp_incl = tot + kClusterMax;                        // [32]
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const uint32_t lane = tid & 31, lt = lanemask_lt();
+    const int C = int(cluster_nctarank()), c = int(cluster_ctarank());
+
+    pdl_launch_dependents();
+    for (int e = tid; e < E; e += kCThreads)
+        carry[e] = 0;
+    pdl_wait();
+    if (c == 0 && tid == 0)
+        *status = 0u;
+
+    // ---- phase 1: counts and in-CTA ranks -------------------------------------
+    const int64_t start = int64_t(c) * chunk;
+    const int64_t end = min(n, start + chunk);
+    int my_id[kCPasses], my_rank[kCPasses];
+#pragma unroll
+    for (int p = 0; p < kCPasses; ++p) {
+        my_id[p] = -1;
+        my_rank[p] = -1;
+        const int64_t s0 = start + int64_t(p) * kCThreads;
+        if (s0 < end) {  // the same for every thread of the CTA
+            for (int v = tid; v < 2 * E; v += kCThreads)  // 32*E bytes = 2E vectors
+                reinterpret_cast<uint4 *>(cnt)[v] = make_uint4(0u, 0u, 0u, 0u);
+            __syncthreads();
+            const int64_t i = s0 + tid;
+            const int id = i < end ? ids[i] : -1;
+            const bool ok = id >= 0 && id < E;
+            const uint32_t key = ok ? uint32_t(id) : (0x80000000u | lane);
+            const uint32_t peers = __match_any_sync(kFull, key);
+            if (ok && lane == uint32_t(__ffs(peers) - 1))
+                cnt[warp * E + id] = uint8_t(__popc(peers));
+            __syncthreads();
+            if (i < end) {
+                my_id[p] = id;
+                if (ok) {
+                    int r = carry[id] + __popc(peers & lt);
+                    for (int w2 = 0; w2 < warp; ++w2)
+                        r += cnt[w2 * E + id];
+                    my_rank[p] = r;
+                }
+            }
+            __syncthreads();
+            for (int e = tid; e < E; e += kCThreads) {
+                int cs = 0;
+#pragma unroll 8
+                for (int w2 = 0; w2 < kCWarps; ++w2)
+                    cs += cnt[w2 * E + e];
+                carry[e] += cs;
+            }
+            __syncthreads();
+        }
+    }
+    cluster_sync();  // every CTA's counts are final
+
+    // ---- phase 2: owners scan their experts ------------------------------------
+    const int epc = (E + C - 1) / C;
+    const int e = c * epc + tid;
+    const bool own = tid < epc && e < E;
+    int cc[kClusterMax];
+    int ce = 0;
+#pragma unroll
+    for (int c2 = 0; c2 < kClusterMax; ++c2) {
+        cc[c2] = 0;
+        if (own && c2 < C) {
+            cc[c2] = dsmem_ld(dsmem_addr(&carry[e], uint32_t(c2)));
+            ce += cc[c2];
+        }
+    }
+    const int P = own ? (ce + tm - 1) / tm * tm : 0;
+    int v = P;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(kFull, v, o);
+        if (int(lane) >= o)
+            v += t;
+    }
+    if (lane == 31)
+        warp_incl[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int wv = warp_incl[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(kFull, wv, o);
+            if (int(lane) >= o)
+                wv += t;
+        }
+        warp_incl[lane] = wv;
+    }
+    __syncthreads();
+    const int local_excl = (v - P) + (warp > 0 ? warp_incl[warp - 1] : 0);
+    if (tid == 0) {
+        const int S = warp_incl[kCWarps - 1];
+        for (int c2 = 0; c2 < C; ++c2)
+            dsmem_st(dsmem_addr(&tot[c], uint32_t(c2)), S);
+    }
+    cluster_sync();  // every CTA knows every CTA's padded total
+
+    int64_t base = 0, total = 0;
+    for (int c2 = 0; c2 < C; ++c2) {
+        base += c2 < c ? tot[c2] : 0;
+        total += tot[c2];
+    }
+    if (own) {
+        const int64_t off = base + local_excl;
+        offsets[e] = int32_t(off);
+        counts[e] = ce;
+        int64_t run = off;
+#pragma unroll
+        for (int c2 = 0; c2 < kClusterMax; ++c2) {
+            if (c2 < C) {
+                dsmem_st(dsmem_addr(&rowbase[e], uint32_t(c2)), int(run));
+                run += cc[c2];
+            }
+        }
+        for (int64_t r = off + ce; r < off + P && r < cap; ++r) {
+            srt_tok[r] = -1;
+            srt_w[r] = 0.0f;
+        }
+        const int64_t n_tiles_cap = cap / tm;
+        for (int64_t t = off / tm; t < (off + P) / tm && t < n_tiles_cap; ++t)
+            tile_expert[t] = e;
+    }
+    if (c == C - 1 && tid == 0) {
+        offsets[E] = int32_t(total);
+        if (total > cap)
+            atomicOr(status, MOE_STATUS_OVERFLOW);
+    }
+    cluster_sync();  // every CTA holds the first row of each expert's entries
+
+    // ---- phase 3: place ----------------------------------------------------------
+    bool bad = false;
+#pragma unroll
+    for (int p = 0; p < kCPasses; ++p) {
+        const int64_t i = start + int64_t(p) * kCThreads + tid;
+        if (i < end) {
+            const int id = my_id[p];
+            if (id >= 0 && id < E) {
+                const int row = rowbase[id] + my_rank[p];
+                pos[i] = row;
+                if (row < cap) {
+                    srt_tok[row] = int32_t(i / k);
+                    srt_w[row] = w[i];
+                }
+            } else {
+                pos[i] = -1;
+                bad |= id != -1;
+            }
+        }
+    }
+    if (__any_sync(kFull, bad) && lane == 0)
+        atomicOr(status, MOE_STATUS_BAD_ID);
+}
+
+// Cluster size that fits this device (16, else 8, else 0 = none); once per device.
+int plan_cluster_size()
+{
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 0;
+    const int v = cached[dev].load(std::memory_order_acquire);
+    if (v != 0)
+        return v > 0 ? v : 0;
+    int chosen = -1;
+    bool refused = false;
+    const void *fn = reinterpret_cast<const void *>(k_plan_cluster);
+    const size_t smem = cluster_smem_bytes(MOE_MAX_EXPERTS);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess) {
+        refused = true;
+    } else {
+        for (int C : {16, 8}) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(C);
+            cfg.blockDim = dim3(kCThreads);
+            cfg.dynamicSmemBytes = smem;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = C;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int nclusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&nclusters, fn, &cfg) != cudaSuccess) {
+                refused = true;
+            } else if (nclusters >= 1) {
+                chosen = C;
+                break;
+            }
+        }
+    }
+    if (refused)
+        cudaGetLastError();  // a refused cluster size is not the caller's error
+    cached[dev].store(chosen, std::memory_order_release);
+    return chosen > 0 ? chosen : 0;
+}
+
 }  // namespace
 
 cudaError_t launch_plan(const int32_t *ids, const float *w, int T, int k, int E, int tm,
@@ -230,6 +473,26 @@ cudaError_t launch_plan(const int32_t *ids, const float *w, int T, int k, int E,
                         int32_t *bcnt, cudaStream_t stream)
 {
     const int64_t n = int64_t(T) * k;
+    const int C = n > 0 ? plan_cluster_size() : 0;
+    if (C > 0 && n <= int64_t(C) * kCThreads * kCPasses) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(C);
+        cfg.blockDim = dim3(kCThreads);
+        cfg.dynamicSmemBytes = cluster_smem_bytes(E);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        const int64_t chunk = (n + C - 1) / C;
+        return cudaLaunchKernelEx(&cfg, k_plan_cluster, ids, w, n, k, E, tm, cap, chunk, offsets,
+                                  counts, srt_tok, srt_w, pos, tile_expert, status);
+    }
     const int64_t B = plan_block_entries(n);
     const int nblk = plan_num_blocks(n);
     const int stride = plan_count_stride(n);
