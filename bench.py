@@ -49,7 +49,8 @@ from moe_prefill_routing_gb300 import workload as W  # noqa: E402
 
 METRIC = "MoE layer routed rows/s (plan+gather+FFN+combine); plan µs/layer at T=2048"
 WORKLOAD = 3
-KERNELS_PER_LAYER = 7  # hist, scan+pad, place, gather, gate/up, down, combine
+# plan (one cluster launch at this size), gather, gate/up, down, combine
+KERNELS_PER_LAYER = 5
 FLUSH_BYTES = 256 << 20
 PROFILE = os.path.join(ROOT, "profiles", "ffn_gate_up_layer_t2048_d2560_e512_k10_f512.md")
 FFN_SRC = os.path.join(ROOT, "moe_prefill_routing_gb300", "csrc", "ffn.cu")

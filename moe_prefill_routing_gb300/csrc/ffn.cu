@@ -103,7 +103,7 @@ struct FfnArgs {
 constexpr size_t ffn_smem_bytes(int E)
 {
     return 1024 + size_t(kStages) * kStageBytes + kStgBytes + sizeof(Ctrl<kStages>) +
-           BN * sizeof(int) + size_t(E + 1) * sizeof(int);
+           2 * BN * sizeof(int) + size_t(E + 1) * sizeof(int);
 }
 
 // Bounded wait that ignores the abort flag (used while stopping).
@@ -216,7 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint16_t *stg = reinterpret_cast<uint16_t *>(smem + S * kStageBytes);
     Ctrl<S> *ctl = reinterpret_cast<Ctrl<S> *>(smem + S * kStageBytes + kStgBytes);
     int *row_tok = reinterpret_cast<int *>(ctl + 1);  // [BN] tokens of the unit's rows
-    int *chunk_start = row_tok + BN;
+    float *row_w = reinterpret_cast<float *>(row_tok + BN);  // [BN] routing weights (down)
+    int *chunk_start = row_tok + 2 * BN;
     const int warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
 
@@ -412,6 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // barriers below.  epi_stop is written before this barrier and read
             // after it; the next write can only come after the unit's chunk
             // barriers, which every thread reaches after its read.
+            if (!GATED && et < w.nrows)  // read by every thread of the unit's chunks
+                row_w[et] = p.srt_w[w.row0 + et];
             if (!mbar_wait(&ctl->tmem_full[abuf], aphase, abort_flag))
                 *reinterpret_cast<volatile int *>(&ctl->epi_stop) = 1;
             epi_bar();
@@ -435,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sg[j * UM + fq] = bf16_bits(g / (1.0f + __expf(-g)) * up);
                     }
                 } else {
-                    const float *wr = p.srt_w + w.row0 + c0;
+                    const float *wr = row_w + c0;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const float s = wr[j];

@@ -19,12 +19,12 @@
 //    histogram plus a one-CTA scan, because one CTA cannot use the whole GPU.
 //    On GB300 the launch and completion gaps between three small kernels
 //    cost more than the work, so chunks of up to 64K entries run the whole
-//    plan in ONE launch of a thread-block cluster (16 CTAs of 1024 threads
-//    where the GPU can place them, else 8): each CTA counts and ranks its
-//    share of the entries, then, through distributed shared memory and
-//    hardware cluster barriers, each CTA scans a share of the experts and
-//    hands every CTA the first row of each expert for its share of entries.
-//    Larger inputs use the three kernels below.
+//    plan in ONE launch of a thread-block cluster (16 CTAs
+//    where the GPU can place them, else 8; 256 threads each): each CTA counts
+//    and ranks its share of the entries, then, through distributed shared
+//    memory and hardware cluster barriers, each CTA scans a share of the
+//    experts and hands every CTA the first row of each expert for its share
+//    of entries.  Larger inputs use the three kernels below.
 #include "../../include/moe_prefill.h"
 #include "internal.h"
 #include "ptx.cuh"
@@ -234,23 +234,29 @@ __global__ void __launch_bounds__(kPlaceThreads)
 
 // ---- one-launch plan for a thread-block cluster --------------------------------
 
-constexpr int kCThreads = 1024;
+constexpr int kCThreads = 256;
 constexpr int kCWarps = kCThreads / 32;
-constexpr int kCPasses = 4;       // 1024-entry passes per CTA, held in registers
+constexpr int kCSteps = 16;  // 32-entry steps per warp, held in registers
 constexpr int kClusterMax = 16;
+constexpr int kCEntriesPerCta = kCWarps * kCSteps * 32;  // 4096
 
 constexpr size_t cluster_smem_bytes(int E)
 {
-    return size_t(kCWarps) * E + 2 * sizeof(int) * size_t(E) + (kClusterMax + kCWarps) * sizeof(int);
+    return size_t(kCWarps) * E * sizeof(uint16_t) + 2 * sizeof(int) * size_t(E) +
+           (kClusterMax + kCWarps) * sizeof(int);
 }
 
-// CTA c of the cluster owns flat entries [c*chunk, (c+1)*chunk) and experts
-// [c*epc, (c+1)*epc).  Phase 1: per-expert counts of the CTA's entries and
-// each entry's rank among the CTA's earlier entries of its expert.  Phase 2
-// (owners): the expert's count over all CTAs, its padded size, offsets by a
-// scan over the owned experts plus the totals of the CTAs before, the tail
-// fill, the tile table, and for every CTA the first row of the expert's
-// entries in that CTA.  Phase 3: every entry's row = that first row + rank.
+// CTA c of the cluster owns flat entries [c*chunk, (c+1)*chunk), split into
+// eight contiguous warp ranges, and experts [c*epc, (c+1)*epc).
+// Phase 1: each warp walks its range 32 entries at a time with a running
+// count per expert (match_any peers share one update), which gives each
+// entry its rank in the warp range; an in-place prefix of the eight warp
+// counts per expert turns that into the rank in the CTA range and leaves the
+// CTA's count per expert.  Phase 2 (owners, over distributed shared memory):
+// the expert's count over all CTAs, its padded size, its first row by a scan
+// over the owned experts plus the totals of the CTAs before, the tail fill,
+// the tile table, and for every CTA the first row of the expert's entries in
+// that CTA.  Phase 3: row = that first row + rank.
 __global__ void __launch_bounds__(kCThreads, 1)
     k_plan_cluster(const int32_t *__restrict__ ids, const float *__restrict__ w, int64_t n, int k,
                    int E, int tm, int64_t cap, int64_t chunk, int32_t *__restrict__ offsets,
@@ -259,81 +265,96 @@ __global__ void __launch_bounds__(kCThreads, 1)
                    int32_t *__restrict__ tile_expert, uint32_t *__restrict__ status)
 {
     extern __shared__ __align__(16) uint8_t csm[];
-    uint8_t *cnt = csm;                                        // [32 warps][E]
-    int *carry = reinterpret_cast<int *>(csm + kCWarps * E);  // [E] counts of this CTA
-    int *rowbase = carry + E;                                  // [E] first row, this CTA
-    int *tot = rowbase + E;                                    // [16] padded rows per CTA
-    int *warp_incl = tot + kClusterMax;                        // [32]
+    uint16_t *cntw = reinterpret_cast<uint16_t *>(csm);                   // [8 warps][E]
+    int *carry = reinterpret_cast<int *>(csm + kCWarps * E * sizeof(uint16_t));  // [E]
+    int *rowbase = carry + E;                                             // [E]
+    int *tot = rowbase + E;                                               // [16]
+    int *warp_tot = tot + kClusterMax;                                    // [8]
     const int tid = threadIdx.x, warp = tid >> 5;
     const uint32_t lane = tid & 31, lt = lanemask_lt();
     const int C = int(cluster_nctarank()), c = int(cluster_ctarank());
 
     pdl_launch_dependents();
-    for (int e = tid; e < E; e += kCThreads)
-        carry[e] = 0;
+    for (int v = tid; v < E; v += kCThreads)  // 16*E bytes = E vectors of 16
+        reinterpret_cast<uint4 *>(cntw)[v] = make_uint4(0u, 0u, 0u, 0u);
     pdl_wait();
     if (c == 0 && tid == 0)
         *status = 0u;
 
-    // ---- phase 1: counts and in-CTA ranks -------------------------------------
-    const int64_t start = int64_t(c) * chunk;
-    const int64_t end = min(n, start + chunk);
-    int my_id[kCPasses], my_rank[kCPasses];
+    // ---- phase 1: ranks inside the warp range, then inside the CTA range -------
+    const int64_t cta_lo = int64_t(c) * chunk;
+    const int64_t cta_hi = min(n, cta_lo + chunk);
+    const int64_t wchunk = (chunk + kCWarps - 1) / kCWarps;
+    const int64_t w_lo = min(cta_hi, cta_lo + warp * wchunk);
+    const int64_t w_hi = min(cta_hi, w_lo + wchunk);
+    int my_id[kCSteps], my_rank[kCSteps];
 #pragma unroll
-    for (int p = 0; p < kCPasses; ++p) {
-        my_id[p] = -1;
-        my_rank[p] = -1;
-        const int64_t s0 = start + int64_t(p) * kCThreads;
-        if (s0 < end) {  // the same for every thread of the CTA
-            for (int v = tid; v < 2 * E; v += kCThreads)  // 32*E bytes = 2E vectors
-                reinterpret_cast<uint4 *>(cnt)[v] = make_uint4(0u, 0u, 0u, 0u);
-            __syncthreads();
-            const int64_t i = s0 + tid;
-            const int id = i < end ? ids[i] : -1;
-            const bool ok = id >= 0 && id < E;
+    for (int s = 0; s < kCSteps; ++s) {
+        const int64_t i = w_lo + s * 32 + lane;
+        my_id[s] = i < w_hi ? ids[i] : -1;
+        my_rank[s] = -1;
+    }
+    __syncthreads();  // counters zeroed
+    uint16_t *mycnt = cntw + warp * E;
+#pragma unroll
+    for (int s = 0; s < kCSteps; ++s) {
+        if (w_lo + s * 32 < w_hi) {  // the same for the whole warp
+            const int id = my_id[s];
+            const bool ok = w_lo + s * 32 + lane < w_hi && id >= 0 && id < E;
             const uint32_t key = ok ? uint32_t(id) : (0x80000000u | lane);
             const uint32_t peers = __match_any_sync(kFull, key);
-            if (ok && lane == uint32_t(__ffs(peers) - 1))
-                cnt[warp * E + id] = uint8_t(__popc(peers));
-            __syncthreads();
-            if (i < end) {
-                my_id[p] = id;
-                if (ok) {
-                    int r = carry[id] + __popc(peers & lt);
-                    for (int w2 = 0; w2 < warp; ++w2)
-                        r += cnt[w2 * E + id];
-                    my_rank[p] = r;
-                }
+            const int leader = __ffs(peers) - 1;
+            int first = 0;
+            if (ok && lane == uint32_t(leader)) {
+                first = mycnt[id];
+                mycnt[id] = uint16_t(first + __popc(peers));
             }
-            __syncthreads();
-            for (int e = tid; e < E; e += kCThreads) {
-                int cs = 0;
-#pragma unroll 8
-                for (int w2 = 0; w2 < kCWarps; ++w2)
-                    cs += cnt[w2 * E + e];
-                carry[e] += cs;
-            }
-            __syncthreads();
+            first = __shfl_sync(kFull, first, leader);
+            if (ok)
+                my_rank[s] = first + __popc(peers & lt);
+            __syncwarp();
         }
     }
+    __syncthreads();
+    for (int e = tid; e < E; e += kCThreads) {  // warp counts -> prefix over warps
+        int run = 0;
+#pragma unroll
+        for (int w2 = 0; w2 < kCWarps; ++w2) {
+            const int t = cntw[w2 * E + e];
+            cntw[w2 * E + e] = uint16_t(run);
+            run += t;
+        }
+        carry[e] = run;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int s = 0; s < kCSteps; ++s)
+        if (my_rank[s] >= 0)
+            my_rank[s] += mycnt[my_id[s]];
     cluster_sync();  // every CTA's counts are final
 
     // ---- phase 2: owners scan their experts ------------------------------------
     const int epc = (E + C - 1) / C;
-    const int e = c * epc + tid;
-    const bool own = tid < epc && e < E;
-    int cc[kClusterMax];
-    int ce = 0;
+    const int J = (epc + kCThreads - 1) / kCThreads;  // experts per thread (1 or 2)
+    int cc[2][kClusterMax], ce[2] = {0, 0}, P[2] = {0, 0};
+    int tsum = 0;
 #pragma unroll
-    for (int c2 = 0; c2 < kClusterMax; ++c2) {
-        cc[c2] = 0;
-        if (own && c2 < C) {
-            cc[c2] = dsmem_ld(dsmem_addr(&carry[e], uint32_t(c2)));
-            ce += cc[c2];
+    for (int j = 0; j < 2; ++j) {
+        const int li = tid * J + j;
+        const int e = c * epc + li;
+        const bool own = j < J && li < epc && e < E;
+#pragma unroll
+        for (int c2 = 0; c2 < kClusterMax; ++c2) {
+            cc[j][c2] = 0;
+            if (own && c2 < C) {
+                cc[j][c2] = dsmem_ld(dsmem_addr(&carry[e], uint32_t(c2)));
+                ce[j] += cc[j][c2];
+            }
         }
+        P[j] = own ? (ce[j] + tm - 1) / tm * tm : 0;
+        tsum += P[j];
     }
-    const int P = own ? (ce + tm - 1) / tm * tm : 0;
-    int v = P;
+    int v = tsum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int t = __shfl_up_sync(kFull, v, o);
@@ -341,25 +362,18 @@ __global__ void __launch_bounds__(kCThreads, 1)
             v += t;
     }
     if (lane == 31)
-        warp_incl[warp] = v;
+        warp_tot[warp] = v;
     __syncthreads();
-    if (warp == 0) {
-        int wv = warp_incl[lane];
+    int before = 0, S = 0;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(kFull, wv, o);
-            if (int(lane) >= o)
-                wv += t;
-        }
-        warp_incl[lane] = wv;
+    for (int w2 = 0; w2 < kCWarps; ++w2) {
+        before += w2 < warp ? warp_tot[w2] : 0;
+        S += warp_tot[w2];
     }
-    __syncthreads();
-    const int local_excl = (v - P) + (warp > 0 ? warp_incl[warp - 1] : 0);
-    if (tid == 0) {
-        const int S = warp_incl[kCWarps - 1];
+    const int t_excl = before + v - tsum;
+    if (tid == 0)
         for (int c2 = 0; c2 < C; ++c2)
             dsmem_st(dsmem_addr(&tot[c], uint32_t(c2)), S);
-    }
     cluster_sync();  // every CTA knows every CTA's padded total
 
     int64_t base = 0, total = 0;
@@ -367,25 +381,31 @@ __global__ void __launch_bounds__(kCThreads, 1)
         base += c2 < c ? tot[c2] : 0;
         total += tot[c2];
     }
-    if (own) {
-        const int64_t off = base + local_excl;
-        offsets[e] = int32_t(off);
-        counts[e] = ce;
-        int64_t run = off;
+    int64_t off = base + t_excl;
+    const int64_t n_tiles_cap = cap / tm;
 #pragma unroll
-        for (int c2 = 0; c2 < kClusterMax; ++c2) {
-            if (c2 < C) {
-                dsmem_st(dsmem_addr(&rowbase[e], uint32_t(c2)), int(run));
-                run += cc[c2];
+    for (int j = 0; j < 2; ++j) {
+        const int li = tid * J + j;
+        const int e = c * epc + li;
+        if (j < J && li < epc && e < E) {
+            offsets[e] = int32_t(off);
+            counts[e] = ce[j];
+            int64_t run = off;
+#pragma unroll
+            for (int c2 = 0; c2 < kClusterMax; ++c2) {
+                if (c2 < C) {
+                    dsmem_st(dsmem_addr(&rowbase[e], uint32_t(c2)), int(run));
+                    run += cc[j][c2];
+                }
             }
+            for (int64_t r = off + ce[j]; r < off + P[j] && r < cap; ++r) {
+                srt_tok[r] = -1;
+                srt_w[r] = 0.0f;
+            }
+            for (int64_t t = off / tm; t < (off + P[j]) / tm && t < n_tiles_cap; ++t)
+                tile_expert[t] = e;
         }
-        for (int64_t r = off + ce; r < off + P && r < cap; ++r) {
-            srt_tok[r] = -1;
-            srt_w[r] = 0.0f;
-        }
-        const int64_t n_tiles_cap = cap / tm;
-        for (int64_t t = off / tm; t < (off + P) / tm && t < n_tiles_cap; ++t)
-            tile_expert[t] = e;
+        off += P[j];
     }
     if (c == C - 1 && tid == 0) {
         offsets[E] = int32_t(total);
@@ -397,12 +417,12 @@ __global__ void __launch_bounds__(kCThreads, 1)
     // ---- phase 3: place ----------------------------------------------------------
     bool bad = false;
 #pragma unroll
-    for (int p = 0; p < kCPasses; ++p) {
-        const int64_t i = start + int64_t(p) * kCThreads + tid;
-        if (i < end) {
-            const int id = my_id[p];
-            if (id >= 0 && id < E) {
-                const int row = rowbase[id] + my_rank[p];
+    for (int s = 0; s < kCSteps; ++s) {
+        const int64_t i = w_lo + s * 32 + lane;
+        if (i < w_hi) {
+            const int id = my_id[s];
+            if (my_rank[s] >= 0) {
+                const int row = rowbase[id] + my_rank[s];
                 pos[i] = row;
                 if (row < cap) {
                     srt_tok[row] = int32_t(i / k);
@@ -474,7 +494,7 @@ cudaError_t launch_plan(const int32_t *ids, const float *w, int T, int k, int E,
 {
     const int64_t n = int64_t(T) * k;
     const int C = n > 0 ? plan_cluster_size() : 0;
-    if (C > 0 && n <= int64_t(C) * kCThreads * kCPasses) {
+    if (C > 0 && n <= int64_t(C) * kCEntriesPerCta && E <= C * 2 * kCThreads) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(C);
         cfg.blockDim = dim3(kCThreads);

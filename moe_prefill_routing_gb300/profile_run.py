@@ -37,7 +37,8 @@ def main(argv=None):
     if a.tokens:
         wl = dataclasses.replace(wl, T=a.tokens, name=f"{wl.name}_T{a.tokens}")
     dev = torch.device("cuda", 0)
-    inp = W.make_inputs(wl)
+    plan_only = a.stage in ("plan", "gather")
+    inp = W.make_inputs(wl, weights=not plan_only)
 
     def d16(x):
         return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev).view(torch.bfloat16)
@@ -45,12 +46,13 @@ def main(argv=None):
     x = d16(inp["x"])
     ids = torch.from_numpy(inp["ids"]).to(dev)
     w = torch.from_numpy(inp["w"]).to(dev)
-    Wg, Wu, Wd = (d16(inp[n]) for n in ("Wg", "Wu", "Wd"))
     cap = B.capacity(wl.T, wl.k, wl.E, wl.tm)
     o = B.plan(ids, w, wl.E, wl.tm, cap=cap)
     xs = B.gather(x, o["srt_tok"], o["offsets"], wl.E, cap)
-    H, Ys = B.expert_ffn(xs, Wg, Wu, Wd, o["offsets"], o["srt_w"], cap)
-    y = B.combine(Ys, o["pos"])
+    if not plan_only:
+        Wg, Wu, Wd = (d16(inp[n]) for n in ("Wg", "Wu", "Wd"))
+        H, Ys = B.expert_ffn(xs, Wg, Wu, Wd, o["offsets"], o["srt_w"], cap)
+        y = B.combine(Ys, o["pos"])
     calls = {
         "plan": lambda: B.plan(ids, w, wl.E, wl.tm, cap=cap, out=o),
         "gather": lambda: B.gather(x, o["srt_tok"], o["offsets"], wl.E, cap, xs=xs),
