@@ -30,7 +30,7 @@
 // Warp roles: warp 0 issues TMA copies into a ring of shared-memory stages,
 // warp 1 issues tcgen05.mma into one of two TMEM accumulators, warps 2-5
 // read the accumulator with tcgen05.ld, apply the epilogue, stage 16 rows of
-// bf16 in shared memory and write them out as whole-row 16-byte vectors.
+// bf16 in shared memory, and one thread writes them out with a TMA store.
 // Every output element is written by one CTA with a fixed K order: results
 // are deterministic.  Every wait is bounded (2 s); on a timeout the CTA
 // stops, lets its copies and MMAs land, frees TMEM and sets
@@ -206,7 +206,8 @@ __device__ __forceinline__ void epi_bar()
 template <bool GATED, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1)
     k_ffn(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
-          const __grid_constant__ CUtensorMap map_b, const FfnArgs p)
+          const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_out,
+          const FfnArgs p)
 {
     constexpr int S = kStages;
     constexpr int UM = Kind<GATED>::kUnitM;
@@ -240,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (GATED)
             prefetch_tmap(&map_a1);
         prefetch_tmap(&map_b);
+        prefetch_tmap(&map_out);
     }
     if (warp == 1) {
         tmem_alloc(&ctl->tmem_base, kTmemCols);
@@ -397,12 +399,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // ---- epilogue: TMEM -> registers -> shared (16 rows) -> global rows ----
+        // ---- epilogue: TMEM -> registers -> shared (16 rows) -> TMA store ----
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
         const int fq = q * 32 + int(lane);
-        const int et = int(threadIdx.x) - 64;  // 0..127
-        constexpr int kVecPerRow = UM / 8;
-        constexpr int kVecPerThread = kStageRows * kVecPerRow / kEpiThreads;
+        const int et = int(threadIdx.x) - 64;  // 0..127; thread 0 issues the stores
         int abuf = 0;
         uint32_t aphase = 0, chunk = 0;
         for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
@@ -430,33 +430,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (GATED || use1)
                     tmem_ld_32x32b_x16(t0 + BN + uint32_t(c0), b);
                 tmem_ld_wait();
+                float v0[16], v1[16];
                 if (GATED) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const float g = __uint_as_float(a[j]);
-                        const float up = __uint_as_float(b[j]);
-                        sg[j * UM + fq] = bf16_bits(g / (1.0f + __expf(-g)) * up);
+                        v0[j] = __fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(b[j]);
                     }
                 } else {
                     const float *wr = row_w + c0;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const float s = wr[j];
-                        sg[j * UM + fq] = bf16_bits(s * __uint_as_float(a[j]));
-                        sg[j * UM + BM + fq] = use1 ? bf16_bits(s * __uint_as_float(b[j])) : 0;
+                        v0[j] = wr[j] * __uint_as_float(a[j]);
+                        v1[j] = use1 ? wr[j] * __uint_as_float(b[j]) : 0.0f;
                     }
                 }
+                // the bulk store that last read this staging buffer (two chunks
+                // back) must be done with it before it is overwritten
+                if (et == 0)
+                    bulk_wait_read<1>();
                 epi_bar();
-                // 16 rows x UM features leave as 16-byte vectors, a whole row
-                // segment per group of UM/8 threads
 #pragma unroll
-                for (int i = 0; i < kVecPerThread; ++i) {
-                    const int v = et + i * kEpiThreads;
-                    const int row = v / kVecPerRow, cv = v - row * kVecPerRow;
-                    const int fo = m0 + cv * 8;
-                    if (fo < p.M)
-                        *reinterpret_cast<uint4 *>(p.out + int64_t(w.row0 + c0 + row) * p.M + fo) =
-                            *reinterpret_cast<const uint4 *>(sg + row * UM + cv * 8);
+                for (int j = 0; j < 16; ++j) {
+                    sg[j * UM + fq] = bf16_bits(v0[j]);
+                    if (!GATED)
+                        sg[j * UM + BM + fq] = bf16_bits(v1[j]);
+                }
+                fence_proxy_async_smem();  // staged rows -> visible to the bulk copy
+                epi_bar();
+                // 16 rows x UM features leave as one TMA store; features past M
+                // fall outside the tensor and are not written
+                if (et == 0) {
+                    tma_store_2d(&map_out, sg, m0, w.row0 + c0);
+                    bulk_commit();
                 }
             }
             tc_fence_before_sync();
@@ -465,6 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (abuf == 0)
                 aphase ^= 1u;
         }
+        if (et == 0)
+            bulk_wait<0>();  // every store written before the CTA (and its smem) goes
     }
 
     __syncthreads();
@@ -494,9 +502,9 @@ cudaError_t get_encoder()
     return g_encode ? cudaSuccess : cudaErrorNotSupported;
 }
 
-// bf16 tensor map with a 128-byte swizzle; dims innermost first.
+// bf16 tensor map (128-byte swizzle unless `plain`); dims innermost first.
 cudaError_t encode_bf16(CUtensorMap *m, const void *base, uint32_t rank, const cuuint64_t *dims,
-                        const cuuint64_t *strides_bytes, const cuuint32_t *box)
+                        const cuuint64_t *strides_bytes, const cuuint32_t *box, bool plain = false)
 {
     cudaError_t err = get_encoder();
     if (err != cudaSuccess)
@@ -504,7 +512,8 @@ cudaError_t encode_bf16(CUtensorMap *m, const void *base, uint32_t rank, const c
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base),
                                 dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                plain ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -536,17 +545,28 @@ cudaError_t token_rows_map(CUtensorMap *m, const void *X, int T, int K)
     return encode_bf16(m, X, 2, dims, strides, box);
 }
 
+// Output rows [cap, M] written 16 rows x `width` features at a time from a
+// dense (unswizzled) staging tile.
+cudaError_t out_map(CUtensorMap *m, void *Y, int64_t cap, int M, int width)
+{
+    const cuuint64_t dims[2] = {cuuint64_t(M), cuuint64_t(cap)};
+    const cuuint64_t strides[1] = {cuuint64_t(M) * 2};
+    const cuuint32_t box[2] = {cuuint32_t(width), cuuint32_t(kStageRows)};
+    return encode_bf16(m, Y, 2, dims, strides, box, true);
+}
+
 }  // namespace
 
 cudaError_t launch_ffn_gate_up(const void *xs, const void *Wg, const void *Wu,
                                const int32_t *offsets, int E, int d, int f, int64_t cap,
                                void *H, uint32_t *status, cudaStream_t stream)
 {
-    CUtensorMap mg, mu, mx;
+    CUtensorMap mg, mu, mx, mo;
     cudaError_t err;
     if ((err = weight_map(&mg, Wg, E, d, f)) != cudaSuccess ||
         (err = weight_map(&mu, Wu, E, d, f)) != cudaSuccess ||
-        (err = rows_map(&mx, xs, cap, d)) != cudaSuccess)
+        (err = rows_map(&mx, xs, cap, d)) != cudaSuccess ||
+        (err = out_map(&mo, H, cap, f, Kind<true>::kUnitM)) != cudaSuccess)
         return err;
     err = ensure_smem_limit(reinterpret_cast<const void *>(k_ffn<true, false>), kSlotGateUp,
                             ffn_smem_bytes(MOE_MAX_EXPERTS));
@@ -554,18 +574,19 @@ cudaError_t launch_ffn_gate_up(const void *xs, const void *Wg, const void *Wu,
         return err;
     const FfnArgs a{offsets, nullptr, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f};
     return launch_pdl(k_ffn<true, false>, dim3(device_sm_count()), dim3(kThreads),
-                      ffn_smem_bytes(E), stream, mg, mu, mx, a);
+                      ffn_smem_bytes(E), stream, mg, mu, mx, mo, a);
 }
 
 cudaError_t launch_ffn_gate_up_rows(const void *x, int T, const int32_t *srt_tok, const void *Wg,
                                     const void *Wu, const int32_t *offsets, int E, int d, int f,
                                     int64_t cap, void *H, uint32_t *status, cudaStream_t stream)
 {
-    CUtensorMap mg, mu, mx;
+    CUtensorMap mg, mu, mx, mo;
     cudaError_t err;
     if ((err = weight_map(&mg, Wg, E, d, f)) != cudaSuccess ||
         (err = weight_map(&mu, Wu, E, d, f)) != cudaSuccess ||
-        (err = token_rows_map(&mx, x, T, d)) != cudaSuccess)
+        (err = token_rows_map(&mx, x, T, d)) != cudaSuccess ||
+        (err = out_map(&mo, H, cap, f, Kind<true>::kUnitM)) != cudaSuccess)
         return err;
     err = ensure_smem_limit(reinterpret_cast<const void *>(k_ffn<true, true>), kSlotGateUpRows,
                             ffn_smem_bytes(MOE_MAX_EXPERTS));
@@ -573,17 +594,18 @@ cudaError_t launch_ffn_gate_up_rows(const void *x, int T, const int32_t *srt_tok
         return err;
     const FfnArgs a{offsets, srt_tok, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f};
     return launch_pdl(k_ffn<true, true>, dim3(device_sm_count()), dim3(kThreads),
-                      ffn_smem_bytes(E), stream, mg, mu, mx, a);
+                      ffn_smem_bytes(E), stream, mg, mu, mx, mo, a);
 }
 
 cudaError_t launch_ffn_down(const void *H, const void *Wd, const int32_t *offsets,
                             const float *srt_w, int E, int d, int f, int64_t cap, void *Ys,
                             uint32_t *status, cudaStream_t stream)
 {
-    CUtensorMap mw, mh;
+    CUtensorMap mw, mh, mo;
     cudaError_t err;
     if ((err = weight_map(&mw, Wd, E, f, d)) != cudaSuccess ||
-        (err = rows_map(&mh, H, cap, f)) != cudaSuccess)
+        (err = rows_map(&mh, H, cap, f)) != cudaSuccess ||
+        (err = out_map(&mo, Ys, cap, d, Kind<false>::kUnitM)) != cudaSuccess)
         return err;
     err = ensure_smem_limit(reinterpret_cast<const void *>(k_ffn<false, false>), kSlotDown,
                             ffn_smem_bytes(MOE_MAX_EXPERTS));
@@ -591,7 +613,7 @@ cudaError_t launch_ffn_down(const void *H, const void *Wd, const int32_t *offset
         return err;
     const FfnArgs a{offsets, nullptr, srt_w, static_cast<uint16_t *>(Ys), status, cap, E, f, d};
     return launch_pdl(k_ffn<false, false>, dim3(device_sm_count()), dim3(kThreads),
-                      ffn_smem_bytes(E), stream, mw, mw, mh, a);
+                      ffn_smem_bytes(E), stream, mw, mw, mh, mo, a);
 }
 
 }  // namespace moe
