@@ -104,6 +104,14 @@ def test_plan_many_empty_experts_and_skips():
     check(ids, w, 4096, 16)
 
 
+@pytest.mark.parametrize("T,k,E", [(8192, 8, 128), (8193, 8, 128), (4096, 8, 4096), (4097, 8, 4096)])
+def test_plan_one_launch_limit(T, k, E):
+    # up to 16 x 4096 entries the plan runs as one cluster launch, above it as
+    # three kernels; both sides of the limit must match the oracle
+    ids, w = W.make_routing(T, E, k, "topk", seed=T)
+    check(ids, w, E, 16)
+
+
 def test_plan_large_block_path():
     # T*k above 512 * 256 entries: blocks of more than 512 entries
     ids, w = W.make_routing(70001, 256, 2, "topk", seed=3)
