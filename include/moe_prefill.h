@@ -302,6 +302,20 @@ MOE_API int moe_layer_forward(const void *x, const int32_t *ids, const float *w,
  */
 MOE_API int moe_read_status(const void *ws, moe_stream_t stream, uint32_t *status);
 
+/*
+ * moe_selftest_wait_limit -- failure-detection self-test of the GEMMs'
+ * bounded waits.  Runs moe_ffn_gate_up on the given arguments with one
+ * change: CTA `cta`'s first pipeline stage expects 16 bytes that never
+ * arrive, so that CTA's waits run out their time limit (about 2 s), it lets
+ * its issued copies and MMAs land, frees its tensor memory and stops; the
+ * other CTAs finish normally.  Afterwards *status has MOE_STATUS_TIMEOUT set
+ * and the context stays usable.  status must not be NULL.  Rows of the
+ * stopped CTA's work units are left unwritten in H.  For tests only.
+ */
+MOE_API int moe_selftest_wait_limit(const void *xs, const void *Wg, const void *Wu,
+                                    const int32_t *offsets, int E, int d, int f, int64_t cap,
+                                    void *H, uint32_t *status, int cta, moe_stream_t stream);
+
 /* Human-readable text of a return code. */
 MOE_API const char *moe_status_str(int code);
 

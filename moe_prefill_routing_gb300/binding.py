@@ -58,6 +58,9 @@ _SIGS = {
                                     C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_size_t,
                                     C.c_void_p]),
     "moe_read_status": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p]),
+    "moe_selftest_wait_limit": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                          C.c_int, C.c_int, C.c_int, C.c_int64, C.c_void_p,
+                                          C.c_void_p, C.c_int, C.c_void_p]),
     "moe_status_str": (C.c_char_p, [C.c_int]),
 }
 
@@ -292,6 +295,20 @@ def layer_forward(x, ids, w, Wg, Wu, Wd, tm: int, y=None, ws=None):
                                      _stream(dev))
     _check("moe_layer_forward", rc)
     return y
+
+
+def selftest_wait_limit(xs, Wg, Wu, offsets, cap: int, status, cta: int = 0, H=None):
+    """Gate/up GEMM with CTA `cta` made to wait for bytes that never come:
+    its bounded waits run out, it stops, and `status` gets STATUS_TIMEOUT."""
+    E, d, f = Wg.shape
+    if H is None:
+        H = torch.empty((max(cap, 1), f), dtype=torch.bfloat16, device=xs.device)
+    with torch.cuda.device(xs.device):
+        rc = lib().moe_selftest_wait_limit(_ptr(xs), _ptr(Wg), _ptr(Wu), _ptr(offsets), E, d, f,
+                                           cap, _ptr(H), _ptr(status), int(cta),
+                                           _stream(xs.device))
+    _check("moe_selftest_wait_limit", rc)
+    return H
 
 
 def read_status(ws) -> int:

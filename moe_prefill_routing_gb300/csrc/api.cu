@@ -316,6 +316,23 @@ int moe_layer_forward(const void *x, const int32_t *ids, const float *w, const v
     return cuda_rc(e);
 }
 
+int moe_selftest_wait_limit(const void *xs, const void *Wg, const void *Wu,
+                            const int32_t *offsets, int E, int d, int f, int64_t cap, void *H,
+                            uint32_t *status, int cta, moe_stream_t stream)
+{
+    const int rc = ffn_checks(xs, Wg, Wu, offsets, E, d, f, cap, H);
+    if (rc != MOE_OK)
+        return rc;
+    if (!status)
+        return MOE_ERR_NULL;
+    if (!aligned(status, 4))
+        return MOE_ERR_ALIGN;
+    if (cta < 0 || cap == 0)
+        return MOE_ERR_SHAPE;
+    return cuda_rc(moe::launch_ffn_gate_up(xs, Wg, Wu, offsets, E, d, f, cap, H, status,
+                                           as_stream(stream), cta));
+}
+
 int moe_read_status(const void *ws, moe_stream_t stream, uint32_t *status)
 {
     if (!ws || !status)

@@ -98,6 +98,8 @@ struct FfnArgs {
     int E;
     int K;  // reduction extent: d (gate/up) or f (down)
     int M;  // output features: f (gate/up) or d (down)
+    int stall_cta;  // self-test only: this CTA's first stage waits for 16 bytes
+                    // that never come; -1 in every normal launch
 };
 
 constexpr size_t ffn_smem_bytes(int E)
@@ -270,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int stage = 0;
         uint32_t phase = 0, issued = 0, issued_par = 0;
         bool ok = true;
+        uint32_t stall_bytes = int(blockIdx.x) == p.stall_cta ? 16u : 0u;
         for (int64_t u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
             const Unit w = map_unit(u, n_mt, chunk_start, p.E, p.offsets);
             if (GATHER) {
@@ -291,7 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     uint64_t *fb = &ctl->full[stage];
-                    mbar_arrive_expect_tx(fb, bytes);
+                    mbar_arrive_expect_tx(fb, bytes + stall_bytes);
+                    stall_bytes = 0;
                     uint8_t *sa = smem + stage * kStageBytes;
                     const int k0 = kb * BK;
 #pragma unroll
@@ -559,7 +563,7 @@ cudaError_t out_map(CUtensorMap *m, void *Y, int64_t cap, int M, int width)
 
 cudaError_t launch_ffn_gate_up(const void *xs, const void *Wg, const void *Wu,
                                const int32_t *offsets, int E, int d, int f, int64_t cap,
-                               void *H, uint32_t *status, cudaStream_t stream)
+                               void *H, uint32_t *status, cudaStream_t stream, int stall_cta)
 {
     CUtensorMap mg, mu, mx, mo;
     cudaError_t err;
@@ -572,7 +576,8 @@ cudaError_t launch_ffn_gate_up(const void *xs, const void *Wg, const void *Wu,
                             ffn_smem_bytes(MOE_MAX_EXPERTS));
     if (err != cudaSuccess)
         return err;
-    const FfnArgs a{offsets, nullptr, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f};
+    const FfnArgs a{offsets, nullptr, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f,
+                    stall_cta};
     return launch_pdl(k_ffn<true, false>, dim3(device_sm_count()), dim3(kThreads),
                       ffn_smem_bytes(E), stream, mg, mu, mx, mo, a);
 }
@@ -592,7 +597,7 @@ cudaError_t launch_ffn_gate_up_rows(const void *x, int T, const int32_t *srt_tok
                             ffn_smem_bytes(MOE_MAX_EXPERTS));
     if (err != cudaSuccess)
         return err;
-    const FfnArgs a{offsets, srt_tok, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f};
+    const FfnArgs a{offsets, srt_tok, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f, -1};
     return launch_pdl(k_ffn<true, true>, dim3(device_sm_count()), dim3(kThreads),
                       ffn_smem_bytes(E), stream, mg, mu, mx, mo, a);
 }
@@ -611,7 +616,7 @@ cudaError_t launch_ffn_down(const void *H, const void *Wd, const int32_t *offset
                             ffn_smem_bytes(MOE_MAX_EXPERTS));
     if (err != cudaSuccess)
         return err;
-    const FfnArgs a{offsets, nullptr, srt_w, static_cast<uint16_t *>(Ys), status, cap, E, f, d};
+    const FfnArgs a{offsets, nullptr, srt_w, static_cast<uint16_t *>(Ys), status, cap, E, f, d, -1};
     return launch_pdl(k_ffn<false, false>, dim3(device_sm_count()), dim3(kThreads),
                       ffn_smem_bytes(E), stream, mw, mw, mh, mo, a);
 }

@@ -53,9 +53,11 @@ cudaError_t launch_combine(const void *Ys, const int32_t *pos, int T, int k, int
 
 // ---- grouped expert GEMMs (ffn.cu) -------------------------------------------
 
+// stall_cta >= 0 only in the failure-detection self-test (moe_selftest_wait_limit).
 cudaError_t launch_ffn_gate_up(const void *xs, const void *Wg, const void *Wu,
                                const int32_t *offsets, int E, int d, int f, int64_t cap,
-                               void *H, uint32_t *status, cudaStream_t stream);
+                               void *H, uint32_t *status, cudaStream_t stream,
+                               int stall_cta = -1);
 
 // gate/up with the B rows gathered from x [T, d] by srt_tok (no xs).
 cudaError_t launch_ffn_gate_up_rows(const void *x, int T, const int32_t *srt_tok, const void *Wg,

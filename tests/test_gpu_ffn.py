@@ -132,3 +132,24 @@ def test_ffn_status_bad_offsets():
     B.ffn_gate_up(xs, Wg, Wg, offsets, 64, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) & B.STATUS_BAD_OFFSETS
+
+
+def test_ffn_wait_limit_stops_cleanly_and_reports():
+    # Failure detection without a GPU fault: CTA 0's first stage waits for 16
+    # bytes that never arrive, so its bounded waits run out (about 2 s), it
+    # stops after letting its copies and MMAs land, and the status word says
+    # so.  The other CTAs finish, and the context keeps working afterwards.
+    import time
+    wl = W.workload(1)
+    inp = inputs(1)
+    p, xs, real, row_e = staged_inputs(inp, wl.E, wl.tm)
+    cap = B.capacity(wl.T, wl.k, wl.E, wl.tm)
+    Wg, Wu, Wd = dev_weights(1)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.time()
+    B.selftest_wait_limit(dev16(to_cap(xs, cap)), Wg, Wu, dev(p["offsets"]), cap, status, cta=0)
+    torch.cuda.synchronize()
+    elapsed = time.time() - t0
+    assert int(status.item()) & B.STATUS_TIMEOUT
+    assert 1.0 < elapsed < 60.0
+    run_case(inp, wl.E, wl.d, wl.f, wl.tm, Wg, Wu, Wd)
