@@ -48,7 +48,9 @@ from moe_prefill_routing_gb300 import replicas  # noqa: E402
 from moe_prefill_routing_gb300 import workload as W  # noqa: E402
 
 METRIC = "MoE layer routed rows/s (plan+gather+FFN+combine); plan µs/layer at T=2048"
-WORKLOAD = 3
+WORKLOAD = 3  # the full page-1-scale layer
+ROUTING = {"topk": "top-k of N(0,1) logits", "topk_bias": "top-k of N(0,1) logits + N(0,1) expert bias",
+           "zipf": "Zipf (rank^-1.2) popularity, k distinct experts per token"}
 # plan (one cluster launch at this size), gather, gate/up, down, combine
 KERNELS_PER_LAYER = 5
 FLUSH_BYTES = 256 << 20
@@ -63,13 +65,17 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
 def peaks():
+    """(HBM GB/s, bf16 TFLOP/s for a kernel timed alone, source)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             j = json.load(f)
-        return float(j["hbm_gbs"]), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def profile_traffic():
@@ -149,11 +155,13 @@ def algorithmic(wl, ids):
     R_pad = int((-(-counts // wl.tm) * wl.tm).sum())
     d, f = wl.d, wl.f
     gate_up = active * 2 * d * f * 2 + R_pad * d * 2 + R_pad * f * 2
+    gate_up_flops = 4 * d * f * R
     down = active * f * d * 2 + R_pad * f * 2 + R_pad * d * 2 + R_pad * 4
     gather = wl.T * d * 2 + R_pad * d * 2 + R_pad * 4
     combine = R * d * 2 + wl.T * d * 2 + R * 4
     plan = 8 * wl.T * wl.k + 4 * wl.T * wl.k + 8 * R_pad + 8 * (wl.E + 1)
-    return dict(active=active, R=R, R_pad=R_pad, gate_up=gate_up, down=down, gather=gather,
+    return dict(active=active, R=R, R_pad=R_pad, gate_up=gate_up, gate_up_flops=gate_up_flops,
+                down=down, gather=gather,
                 combine=combine, plan=plan, layer=plan + gather + gate_up + down + combine,
                 flops=6 * d * f * R)
 
@@ -195,8 +203,8 @@ def oracle_sample(inp, wl, budget_s, nthreads):
 def run_native(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl = W.workload(WORKLOAD)
-    chunk = replicas.chunk_of_rank(rank, world)
+    wl = W.workload(args.workload)
+    chunk = replicas.chunk_of_rank(rank, world) % wl.n_chunks
     log(f"[rank {rank}] generating {wl.name} (chunk {chunk}) ...")
     inp = W.make_inputs(wl, seed=0, chunk=chunk)
     alg = algorithmic(wl, inp["ids"])
@@ -301,18 +309,23 @@ def run_native(args, rank, world, local):
 
     if rank != 0:
         return
-    hbm, peak_src = peaks()
+    hbm, tflops, peak_src = peaks()
     t_gu = stage_mean_us["gate_up"] * 1e-6
-    achieved = alg["gate_up"] / t_gu / 1e9
+    # the bound is whichever of the two floors is longer for this kernel
+    tensor_bound = alg["gate_up_flops"] / (tflops * 1e12) > alg["gate_up"] / (hbm * 1e9)
+    if tensor_bound:
+        achieved, peak, unit = alg["gate_up_flops"] / t_gu / 1e12, tflops, "TFLOP/s"
+    else:
+        achieved, peak, unit = alg["gate_up"] / t_gu / 1e9, hbm, "GB/s"
     traffic = profile_traffic()
     layer_gbs = alg["layer"] / (sum(ms) / len(ms) / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(ms),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded: x~N(0,1), W~N(0,0.02) bf16, skewed top-10 routing)",
+        "data": "synthetic (seeded: x~N(0,1), W~N(0,0.02) bf16, " + ROUTING[wl.routing] + ")",
         "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k, "f": wl.f,
-                   "tm": wl.tm, "routing": "top-k of N(0,1) logits + N(0,1) expert bias",
+                   "tm": wl.tm, "routing": ROUTING[wl.routing],
                    "active_experts": alg["active"], "R_pad": alg["R_pad"],
                    "l2": "flushed before every timed step (256 MiB write)",
                    "parallelism": "replicas (one independent layer per GPU)"},
@@ -322,11 +335,12 @@ def run_native(args, rank, world, local):
         "stages_us": stage_us,
         "layer_hbm_gbs": layer_gbs,
         "roofline": {"kernel": "k_ffn<gate/up> (tcgen05 grouped GEMM + SwiGLU)",
-                     "bound": "hbm",
-                     "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "peak_source": peak_src,
+                     "bound": "tensor" if tensor_bound else "hbm",
+                     "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": alg["gate_up"],
-                     "traffic": traffic},
+                     "algorithmic_flops_per_launch": alg["gate_up_flops"],
+                     "traffic": traffic if args.workload == WORKLOAD else None},
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(ms_e2e)},
         "clocks": clk,
@@ -346,7 +360,7 @@ def run_native(args, rank, world, local):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    wl = W.workload(WORKLOAD)
+    wl = W.workload(args.workload)
     log(f"reference (CPU oracle): generating {wl.name} ...")
     inp = W.make_inputs(wl, seed=0)
     nth = os.cpu_count() or 1
@@ -380,12 +394,16 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("native", "reference"), default="native")
+    ap.add_argument("--workload", type=int, default=WORKLOAD,
+                    help="layer workload 1, 3, 4 or 5 (default 3, the full page-1-scale layer)")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if not W.workload(args.workload).ffn:
+        ap.error("that workload has no expert FFN (plan + gather only)")
     rank, world, local = replicas.init_from_env(backend="nccl" if args.impl == "native" else "gloo")
     try:
         if args.impl == "reference":

@@ -89,6 +89,20 @@ def test_plan_edges(T, k, E, tm):
     check(ids, w, E, tm)
 
 
+@pytest.mark.parametrize("T", [1, 7, 1023, 1025])
+@pytest.mark.parametrize("E", [1, 2, 31, 33, 512, 1024])
+@pytest.mark.parametrize("k", [1, 2, 8, 10])
+@pytest.mark.parametrize("tm", [16, 128])
+def test_plan_sweep(T, E, k, tm):
+    # every combination of the ragged sizes; ids uniform over the experts
+    # (duplicates inside a token allowed), a tenth of the slots skipped
+    rng = np.random.default_rng(T * 1_000_003 + E * 1009 + k * 31 + tm)
+    ids = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    ids[rng.random(ids.shape) < 0.1] = -1
+    w = rng.standard_normal((T, k)).astype(np.float32)
+    check(ids, w, E, tm)
+
+
 def test_plan_all_tokens_one_expert():
     ids = np.full((4096, 8), 77, np.int32)
     w = np.random.default_rng(1).random((4096, 8)).astype(np.float32)
