@@ -23,13 +23,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
-__device__ __forceinline__ uint32_t lane_id()
-{
-    uint32_t l;
-    asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
-    return l;
-}
-
 __device__ __forceinline__ uint32_t lanemask_lt()
 {
     uint32_t m;
