@@ -19,10 +19,12 @@
  *   moe_combine     per-token sum of its k weighted rows in slot order
  *                   (same page, section 3)
  *
- * moe_layer_forward runs all four on one stream.
+ * moe_layer_forward runs all four on one stream; moe_prefill_forward_host
+ * runs it over a sequence of chunks held in host memory.
  *
  * Conventions shared by every call
- *  - Tensors are caller-owned DEVICE pointers, row-major and contiguous.
+ *  - Tensors are caller-owned DEVICE pointers, row-major and contiguous
+ *    (moe_prefill_forward_host alone takes host buffers for x, ids, w, y).
  *    16-bit tensors are passed as void* and hold bf16 (or fp16 where a
  *    dtype argument allows it).  16-bit row tensors (x, xs, H, Ys, y and
  *    the weights) must be 16-byte aligned, int32/fp32 arrays 4-byte aligned
@@ -30,8 +32,10 @@
  *  - Every call is asynchronous on `stream` (NULL = the legacy default
  *    stream) and returns once its kernels are enqueued.  The library never
  *    allocates device memory, never synchronises the host (except
- *    moe_read_status, on request) and keeps no per-call state.  Kernels are
- *    chained with programmatic dependent launch.
+ *    moe_read_status, on request) and keeps no per-call state (the one
+ *    exception: moe_prefill_forward_host creates two copy streams per device
+ *    on first use and a few events per call).  Kernels are chained with
+ *    programmatic dependent launch.
  *  - Flat entry i = t*k + j is token t's slot j.  An expert id of -1 marks a
  *    skipped slot: it gets no row, pos = -1 and adds nothing to y.
  *  - Sizes that depend on the routing (R_pad = offsets[E], the padded row
@@ -295,6 +299,41 @@ MOE_API int moe_layer_forward(const void *x, const int32_t *ids, const float *w,
                       const void *Wg, const void *Wu, const void *Wd, int T, int d,
                       int E, int k, int f, int tm, void *y, void *ws, size_t ws_bytes,
                       moe_stream_t stream);
+
+/*
+ * moe_prefill_forward_host -- moe_layer_forward over n_chunks prefill
+ * chunks of T tokens each, taken from and returned to HOST memory.  The
+ * pages run the layer chunk by chunk over a prompt ("Round 4 Track C:
+ * Prefill MoE Plan ...", Table 2.1; "#372 Prompt path ...", prompts of
+ * 2K-32K tokens); the host transfers and their overlap have no counterpart
+ * there.  For every chunk c: x_h[c], ids_h[c], w_h[c] are copied to the
+ * device, the layer runs on `stream`, and y is copied to y_h[c].  Two copy
+ * streams (created once per device, shared by every call) and two sets of
+ * staging buffers in ws let chunk c+1's inputs come in and chunk c-1's y go
+ * out while chunk c runs.
+ * in   x_h[c]    bf16 [T, d]  host memory, page-locked for the copies to overlap
+ * in   ids_h[c]  int32 [T, k], w_h[c] fp32 [T, k]  host memory, as in moe_plan
+ * out  y_h[c]    bf16 [T, d]  host memory
+ * in   Wg, Wu, Wd, T, d, E, k, f, tm  device weights and shapes as in
+ *                moe_layer_forward (T is the size of every chunk)
+ * ws            moe_prefill_host_workspace_bytes(...) device bytes, 256-byte
+ *               aligned: the layer's workspace (moe_workspace_bytes, at offset
+ *               0, so moe_read_status works on it) then the staging buffers
+ * The pointer arrays are read during the call only; the host buffers must
+ * stay valid, and x/ids/w unchanged, until `stream` has completed, which is
+ * also when every y_h[c] is written.  Chunks may share input pointers; if
+ * several y_h[c] are the same buffer it ends holding the last of them.
+ * Returns MOE_ERR_* from the argument checks before anything is enqueued;
+ * MOE_ERR_CUDA if a CUDA call fails part-way (synchronize the device before
+ * reusing ws or the host buffers).  Calls from several host threads on one
+ * device share the copy streams and so serialize their copies.
+ */
+MOE_API size_t moe_prefill_host_workspace_bytes(int T, int d, int E, int k, int f, int tm);
+MOE_API int moe_prefill_forward_host(int n_chunks, const void *const *x_h,
+                                     const int32_t *const *ids_h, const float *const *w_h,
+                                     void *const *y_h, const void *Wg, const void *Wu,
+                                     const void *Wd, int T, int d, int E, int k, int f, int tm,
+                                     void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
  * moe_read_status -- copy the status word at ws (a plan or layer workspace)

@@ -57,6 +57,11 @@ _SIGS = {
                                     C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int,
                                     C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_size_t,
                                     C.c_void_p]),
+    "moe_prefill_host_workspace_bytes": (C.c_size_t, [C.c_int] * 6),
+    "moe_prefill_forward_host": (C.c_int, [C.c_int, C.c_void_p, C.c_void_p, C.c_void_p,
+                                           C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                           C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
+                                           C.c_void_p, C.c_size_t, C.c_void_p]),
     "moe_read_status": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p]),
     "moe_selftest_wait_limit": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                           C.c_int, C.c_int, C.c_int, C.c_int64, C.c_void_p,
@@ -297,6 +302,42 @@ def layer_forward(x, ids, w, Wg, Wu, Wd, tm: int, y=None, ws=None):
     return y
 
 
+def prefill_host_workspace_bytes(T: int, d: int, E: int, k: int, f: int, tm: int) -> int:
+    return lib().moe_prefill_host_workspace_bytes(T, d, E, k, f, tm)
+
+
+def _host_ptrs(ts, name):
+    for t in ts:
+        if t.is_cuda:
+            raise ValueError(f"{name}: host tensors expected")
+        if not t.is_contiguous():
+            raise ValueError(f"{name}: contiguous tensors expected")
+    return (C.c_void_p * max(len(ts), 1))(*[t.data_ptr() for t in ts])
+
+
+def prefill_forward_host(x_hs, ids_hs, w_hs, y_hs, Wg, Wu, Wd, tm: int, ws=None):
+    """moe_prefill_forward_host over len(x_hs) chunks: host (preferably
+    pinned) x [T, d] bf16, ids/w [T, k] in; host y [T, d] bf16 out.
+    Asynchronous on the current stream; synchronize before reading y_hs."""
+    n = len(x_hs)
+    if not (len(ids_hs) == len(w_hs) == len(y_hs) == n):
+        raise ValueError("one ids, w and y per chunk")
+    E, d, f = Wg.shape
+    T, k = (ids_hs[0].shape if n else (0, 1))
+    dev = Wg.device
+    nbytes = prefill_host_workspace_bytes(T, d, E, k, f, tm)
+    if ws is None:
+        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    arrays = [_host_ptrs(x_hs, "x"), _host_ptrs(ids_hs, "ids"), _host_ptrs(w_hs, "w"),
+              _host_ptrs(y_hs, "y")]
+    with torch.cuda.device(dev):
+        rc = lib().moe_prefill_forward_host(n, *[C.cast(a, C.c_void_p) for a in arrays],
+                                            _ptr(Wg), _ptr(Wu), _ptr(Wd), T, d, E, k, f, tm,
+                                            _ptr(ws), ws.numel(), _stream(dev))
+    _check("moe_prefill_forward_host", rc)
+    return y_hs
+
+
 def selftest_wait_limit(xs, Wg, Wu, offsets, cap: int, status, cta: int = 0, H=None):
     """Gate/up GEMM with CTA `cta` made to wait for bytes that never come:
     its bounded waits run out, it stops, and `status` gets STATUS_TIMEOUT."""
@@ -323,16 +364,18 @@ def read_status(ws) -> int:
 class MoeLayer:
     """A routed MoE layer with its expert weights resident in HBM.
 
-    ``forward`` takes device inputs; ``forward_host`` takes pinned host
-    inputs, copies them in, runs the layer and copies y back, all on the
-    current stream."""
+    ``forward`` takes device inputs.  ``forward_host`` (one chunk) and
+    ``forward_host_chunks`` (a sequence of chunks) take pinned host inputs
+    and go through moe_prefill_forward_host: the inputs are copied in and y
+    copied back on the library's copy streams, overlapped with the layer,
+    which runs on the current stream."""
 
     def __init__(self, Wg, Wu, Wd, tm: int = 16):
         self.Wg, self.Wu, self.Wd, self.tm = Wg, Wu, Wd, tm
         self.E, self.d, self.f = Wg.shape
         self.device = Wg.device
         self._ws = None
-        self._bufs = None
+        self._host_ws = None
 
     def workspace(self, T: int, k: int):
         n = workspace_bytes(T, self.d, self.E, k, self.f, self.tm)
@@ -346,20 +389,18 @@ class MoeLayer:
                              ws=self.workspace(T, ids.shape[1]))
 
     def forward_host(self, x_h, ids_h, w_h, y_h):
-        """Host (pinned) x, ids, w in; host y out.  Asynchronous on the
-        current stream; synchronize before reading y_h."""
-        T, k = ids_h.shape
-        key = (T, k)
-        if self._bufs is None or self._bufs[0] != key:
-            dev = self.device
-            self._bufs = (key, torch.empty((T, self.d), dtype=torch.bfloat16, device=dev),
-                          torch.empty((T, k), dtype=torch.int32, device=dev),
-                          torch.empty((T, k), dtype=torch.float32, device=dev),
-                          torch.empty((T, self.d), dtype=torch.bfloat16, device=dev))
-        _, x, ids, w, y = self._bufs
-        x.copy_(x_h, non_blocking=True)
-        ids.copy_(ids_h, non_blocking=True)
-        w.copy_(w_h, non_blocking=True)
-        self.forward(x, ids, w, y=y)
-        y_h.copy_(y, non_blocking=True)
-        return y_h
+        """Host (pinned) x, ids, w in; host y out, through the C ABI's host
+        entry point.  Asynchronous on the current stream; synchronize before
+        reading y_h."""
+        return self.forward_host_chunks([x_h], [ids_h], [w_h], [y_h])[0]
+
+    def forward_host_chunks(self, x_hs, ids_hs, w_hs, y_hs):
+        """A sequence of prefill chunks of equal T from host memory: chunk
+        c+1's inputs are copied in and chunk c-1's y copied out while chunk
+        c runs.  Asynchronous on the current stream."""
+        T, k = ids_hs[0].shape
+        n = prefill_host_workspace_bytes(T, self.d, self.E, k, self.f, self.tm)
+        if self._host_ws is None or self._host_ws.numel() < n:
+            self._host_ws = torch.empty(n, dtype=torch.uint8, device=self.device)
+        return prefill_forward_host(x_hs, ids_hs, w_hs, y_hs, self.Wg, self.Wu, self.Wd, self.tm,
+                                    ws=self._host_ws)

@@ -117,6 +117,46 @@ def test_stage_argument_errors(lib):
     assert lib.moe_read_status(None, None, None) == B.MOE_ERR_NULL
 
 
+def test_prefill_host_workspace(lib):
+    T, d, E, k, f, tm = 4096, 2816, 128, 8, 704, 16
+    layer = B.workspace_bytes(T, d, E, k, f, tm)
+    up = lambda v: (v + 255) // 256 * 256
+    staging = up(T * d * 2) + 2 * up(T * k * 4) + up(T * d * 2)
+    assert B.prefill_host_workspace_bytes(T, d, E, k, f, tm) == up(layer) + 2 * staging
+    assert B.prefill_host_workspace_bytes(T, d, 0, k, f, tm) == 0
+
+
+def prefill_host_call(lib, n=2, ptrs=None, **kw):
+    # host pointer arrays of stand-in addresses: only checked for NULL here
+    arr = (C.c_void_p * max(n, 1))(*([FAKE] * max(n, 1)))
+    a = dict(x=arr, ids=arr, w=arr, y=arr, Wg=FAKE, Wu=FAKE, Wd=FAKE, T=8, d=64, E=4, k=2,
+             f=64, tm=16, ws=FAKE, ws_bytes=1 << 30)
+    a.update(ptrs or {})
+    a.update(kw)
+    cast = lambda v: C.cast(v, C.c_void_p) if isinstance(v, C.Array) else v
+    return lib.moe_prefill_forward_host(n, cast(a["x"]), cast(a["ids"]), cast(a["w"]),
+                                        cast(a["y"]), a["Wg"], a["Wu"], a["Wd"], a["T"], a["d"],
+                                        a["E"], a["k"], a["f"], a["tm"], a["ws"], a["ws_bytes"],
+                                        None)
+
+
+def test_prefill_host_argument_errors(lib):
+    assert prefill_host_call(lib, n=-1) == B.MOE_ERR_SHAPE
+    assert prefill_host_call(lib, tm=8) == B.MOE_ERR_SHAPE
+    assert prefill_host_call(lib, d=96) == B.MOE_ERR_SHAPE
+    assert prefill_host_call(lib, E=0) == B.MOE_ERR_SHAPE
+    assert prefill_host_call(lib, Wd=None) == B.MOE_ERR_NULL
+    assert prefill_host_call(lib, ptrs={"y": None}) == B.MOE_ERR_NULL
+    holed = (C.c_void_p * 2)(FAKE, None)  # chunk 1 has no x
+    assert prefill_host_call(lib, ptrs={"x": holed}) == B.MOE_ERR_NULL
+    assert prefill_host_call(lib, ws_bytes=1024) == B.MOE_ERR_WORKSPACE
+    assert prefill_host_call(lib, ws=FAKE + 128) == B.MOE_ERR_ALIGN
+    assert prefill_host_call(lib, Wg=FAKE + 8) == B.MOE_ERR_ALIGN
+    # nothing to do: returns before any CUDA call
+    assert prefill_host_call(lib, n=0) == B.MOE_OK
+    assert prefill_host_call(lib, T=0) == B.MOE_OK
+
+
 def test_status_strings(lib):
     for code in (0, -1, -2, -3, -4, -5, -6, -7, 99):
         assert isinstance(B.status_str(code), str) and B.status_str(code)

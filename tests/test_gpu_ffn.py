@@ -33,12 +33,12 @@ def to_cap(a, cap, fill=0):
 
 
 def sample_rows(p, real, row_e, n, seed=0):
-    """First and last real row of every expert with the most rows, plus
-    chunk boundaries (rows 127/128 of the biggest expert) and a random draw."""
+    """First and last real row of the expert with the most rows, plus the
+    MMA-half and unit boundaries inside it and a random draw."""
     rng = np.random.default_rng(seed)
     big = int(np.argmax(p["counts"]))
     lo, c = int(p["offsets"][big]), int(p["counts"][big])
-    picks = [lo, lo + c - 1] + [lo + r for r in (127, 128, 255, 256) if r < c]
+    picks = [lo, lo + c - 1] + [lo + r for r in (127, 128, 255, 256, 383, 384, 511, 512) if r < c]
     picks += list(rng.choice(real, size=min(n, len(real)), replace=False))
     return np.unique(np.array(picks, np.int64))
 
@@ -102,6 +102,21 @@ def test_ffn_shapes_all_rows(T, d, E, k, f, tm):
     inp = W.make_layer(T, d, E, k, f, tm=tm, seed=T + f)
     Wg, Wu, Wd = (dev16(inp[n]) for n in ("Wg", "Wu", "Wd"))
     run_case(inp, E, d, f, tm, Wg, Wu, Wd)
+
+
+@pytest.mark.parametrize("d,f", [(128, 192), (64, 512)])
+def test_ffn_unit_heights(d, f):
+    # expert sizes on both sides of every unit-height boundary: one MMA half
+    # (<= 128 rows), two halves (the second of only 16 rows, or full), and
+    # experts split into a 256-row unit plus a ragged one
+    counts = [16, 112, 128, 144, 240, 256, 272, 400, 528, 0, 784]
+    E = len(counts)
+    T = sum(counts)
+    inp = W.make_layer(T, d, E, 1, f, tm=16, seed=d + f)
+    ids = np.repeat(np.arange(E, dtype=np.int32), counts)
+    inp["ids"] = np.random.default_rng(5).permutation(ids).reshape(T, 1)
+    Wg, Wu, Wd = (dev16(inp[n]) for n in ("Wg", "Wu", "Wd"))
+    run_case(inp, E, d, f, 16, Wg, Wu, Wd)
 
 
 @pytest.mark.parametrize("cfg", [3, 4, 5])

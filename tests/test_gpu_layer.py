@@ -134,3 +134,75 @@ def test_layer_moe_layer_host_path():
     torch.cuda.synchronize()
     y, _ = run_layer(inp, *dev_weights(1), wl.tm)
     assert torch.equal(y_h.view(torch.int16), y.cpu().view(torch.int16))
+
+
+def host_chunks(chunks, d):
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    xs = [torch.from_numpy(c["x"].view(np.int16)).view(torch.bfloat16).pin_memory() for c in chunks]
+    ids = [pin(c["ids"]) for c in chunks]
+    ws = [pin(c["w"]) for c in chunks]
+    ys = [torch.full((c["x"].shape[0], d), float("nan"), dtype=torch.bfloat16).pin_memory()
+          for c in chunks]
+    return xs, ids, ws, ys
+
+
+@pytest.mark.parametrize("n_chunks", [1, 2, 3, 6])
+def test_prefill_host_chunks(n_chunks):
+    # a prompt as n chunks in host memory: every chunk's y equals the device
+    # layer's bit for bit and meets the oracle's bar
+    T, d, E, k, f, tm = 300, 256, 16, 4, 192, 16
+    chunks = [W.make_layer(T, d, E, k, f, tm=tm, seed=40 + c, skip_frac=0.05)
+              for c in range(n_chunks)]
+    Wg, Wu, Wd = (dev16(chunks[0][n]) for n in ("Wg", "Wu", "Wd"))
+    layer = B.MoeLayer(Wg, Wu, Wd, tm=tm)
+    xs, ids, ws, ys = host_chunks(chunks, d)
+    layer.forward_host_chunks(xs, ids, ws, ys)
+    torch.cuda.synchronize()
+    assert B.read_status(layer._host_ws) == 0
+    for c, inp in enumerate(chunks):
+        ref_dev = layer.forward(dev16(inp["x"]), dev(inp["ids"]), dev(inp["w"]))
+        torch.cuda.synchronize()
+        assert torch.equal(ys[c].view(torch.int16), ref_dev.cpu().view(torch.int16)), c
+        ref = oracle.layer(inp["x"], inp["ids"], inp["w"], chunks[0]["Wg"], chunks[0]["Wu"],
+                           chunks[0]["Wd"])
+        ok, err, bound = layer_tolerance(host_f(ys[c]), ref)
+        assert ok, (c, err, bound)
+
+
+def test_prefill_host_chunks_shared_buffers():
+    # the same input chunk five times into one output buffer: it holds that
+    # chunk's y; a later call on the same layer reuses the workspace
+    T, d, E, k, f, tm = 64, 128, 8, 2, 128, 16
+    inp = W.make_layer(T, d, E, k, f, tm=tm, seed=7)
+    Wg, Wu, Wd = (dev16(inp[n]) for n in ("Wg", "Wu", "Wd"))
+    layer = B.MoeLayer(Wg, Wu, Wd, tm=tm)
+    xs, ids, ws, ys = host_chunks([inp], d)
+    layer.forward_host_chunks(xs * 5, ids * 5, ws * 5, ys * 5)
+    torch.cuda.synchronize()
+    ref = layer.forward(dev16(inp["x"]), dev(inp["ids"]), dev(inp["w"])).cpu()
+    assert torch.equal(ys[0].view(torch.int16), ref.view(torch.int16))
+    other = W.make_layer(T, d, E, k, f, tm=tm, seed=8)
+    xs2, ids2, ws2, ys2 = host_chunks([other], d)
+    layer.forward_host_chunks(xs2, ids2, ws2, ys2)
+    torch.cuda.synchronize()
+    ref2 = layer.forward(dev16(other["x"]), dev(other["ids"]), dev(other["w"])).cpu()
+    assert torch.equal(ys2[0].view(torch.int16), ref2.view(torch.int16))
+
+
+def test_prefill_host_long_prompt_chunks_sampled():
+    # the long-prompt workload's chunks through the host path, two of them,
+    # sampled tokens against the oracle
+    wl = W.workload(5)
+    host_w = inputs(5)
+    chunks = [W.make_inputs(wl, chunk=c, weights=False) for c in (0, 1)]
+    layer = B.MoeLayer(*dev_weights(5), tm=wl.tm)
+    xs, ids, ws, ys = host_chunks(chunks, wl.d)
+    layer.forward_host_chunks(xs, ids, ws, ys)
+    torch.cuda.synchronize()
+    assert B.read_status(layer._host_ws) == 0
+    for c, inp in enumerate(chunks):
+        toks = sample_tokens(inp["ids"], 24, seed=c)
+        ref = oracle.layer(inp["x"], inp["ids"], inp["w"], host_w["Wg"], host_w["Wu"],
+                           host_w["Wd"], tokens=toks)
+        ok, err, bound = layer_tolerance(host_f(ys[c])[toks], ref)
+        assert ok, (c, err, bound)
