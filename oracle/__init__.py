@@ -17,7 +17,12 @@ function cites the passage it follows in the C source:
   ordered combine ("Batched resident MoE experts on Apple Silicon ...",
   sections 1 and 3);
 * ``expert_rows`` / ``combine`` -- the same arithmetic cut at the stage
-  boundaries, to check one GPU stage at a time.
+  boundaries, to check one GPU stage at a time;
+* ``quantize_e4m3`` -- expert weights as E4M3 codes with one fp32 scale per
+  (expert, output feature) ("Round 4 Track C ...", section 2 runs the
+  experts from quantized packs; E4M3 is the OCP 8-bit floating point
+  format).  ``layer`` and ``expert_rows`` take such weights as
+  ``(codes, scales)`` pairs in place of bf16 arrays.
 
 Pins (CPU tests): brute force on tiny inputs, closed forms, a dense numpy
 cross-check for a single expert, invariants, and hand-worked fixtures under
@@ -80,6 +85,20 @@ def _load():
             lib.oracle_round_bf16.argtypes = [C.c_double]
             lib.oracle_value16.restype = C.c_double
             lib.oracle_value16.argtypes = [C.c_uint16, C.c_int]
+            lib.oracle_e4m3_value.restype = C.c_double
+            lib.oracle_e4m3_value.argtypes = [C.c_uint8]
+            lib.oracle_e4m3_encode.restype = C.c_uint8
+            lib.oracle_e4m3_encode.argtypes = [C.c_float]
+            lib.oracle_quantize_e4m3.restype = None
+            lib.oracle_quantize_e4m3.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P]
+            lib.oracle_layer_tokens_e4m3.restype = C.c_int
+            lib.oracle_layer_tokens_e4m3.argtypes = [P, C.c_int, P, P, P, P, P, P, P, P,
+                                                     C.c_int, C.c_int, C.c_int, C.c_int,
+                                                     C.c_int, P, C.c_int, C.c_int, C.c_int, P]
+            lib.oracle_expert_rows_e4m3.restype = C.c_int
+            lib.oracle_expert_rows_e4m3.argtypes = [P, C.c_int, C.c_int, C.c_int, P, C.c_int,
+                                                    P, P, C.c_int, P, P, P, P, P, P, C.c_int,
+                                                    C.c_int, P, P]
             _lib = lib
     return _lib
 
@@ -140,29 +159,46 @@ def gather(x, srt_tok) -> np.ndarray:
     return xs[:R]
 
 
+def _weights(Wg, Wu, Wd):
+    """bf16 bit arrays, or (E4M3 codes, fp32 scales) pairs: the arrays the C
+    side takes, the shapes (E, d, f), and whether they are E4M3."""
+    q8 = isinstance(Wg, tuple)
+    if q8:
+        (g, sg), (u, su), (dn, sd) = Wg, Wu, Wd
+        g, u, dn = _c(g, np.uint8), _c(u, np.uint8), _c(dn, np.uint8)
+        sg, su, sd = _c(sg, np.float32), _c(su, np.float32), _c(sd, np.float32)
+        E, d, f = g.shape
+        assert sg.shape == (E, f) and su.shape == (E, f) and sd.shape == (E, d)
+        arrs = (g, sg, u, su, dn, sd)
+    else:
+        g, u, dn = _c(Wg, np.uint16), _c(Wu, np.uint16), _c(Wd, np.uint16)
+        E, d, f = g.shape
+        arrs = (g, u, dn)
+    assert u.shape == g.shape and dn.shape == (E, f, d)
+    return arrs, (E, d, f), q8
+
+
 def layer(x, ids, w, Wg, Wu, Wd, x_dtype: str = "bf16", tokens=None,
           mirror: bool = False, nthreads: int | None = None) -> np.ndarray:
     """Layer output y (fp64 [len(tokens), d]) for the listed tokens (all by
-    default).  ``mirror`` returns the bf16-mirror reference instead."""
+    default).  ``mirror`` returns the bf16-mirror reference instead.  The
+    weights are bf16 bit arrays or, all three, (E4M3 codes, scales) pairs."""
     x = _c(x, np.uint16)
     ids = _c(ids, np.int32)
     w = _c(w, np.float32)
-    Wg = _c(Wg, np.uint16)
-    Wu = _c(Wu, np.uint16)
-    Wd = _c(Wd, np.uint16)
+    warrs, (E, d2, f), q8 = _weights(Wg, Wu, Wd)
     T, d = x.shape
     k = ids.shape[1]
-    E, d2, f = Wg.shape
-    assert d2 == d and Wu.shape == Wg.shape and Wd.shape == (E, f, d)
+    assert d2 == d
     if tokens is None:
         tokens = np.arange(T, dtype=np.int32)
     tokens = _c(tokens, np.int32)
     y = np.zeros((max(len(tokens), 1), d), np.float64)
     if nthreads is None:
         nthreads = os.cpu_count() or 1
-    rc = _load().oracle_layer_tokens(_p(x), int(x_dtype == "f16"), _p(ids), _p(w),
-                                     _p(Wg), _p(Wu), _p(Wd), T, d, E, k, f, _p(tokens),
-                                     len(tokens), int(bool(mirror)), int(nthreads), _p(y))
+    fn = _load().oracle_layer_tokens_e4m3 if q8 else _load().oracle_layer_tokens
+    rc = fn(_p(x), int(x_dtype == "f16"), _p(ids), _p(w), *[_p(a) for a in warrs],
+            T, d, E, k, f, _p(tokens), len(tokens), int(bool(mirror)), int(nthreads), _p(y))
     if rc != 0:
         raise OracleError(_ERR.get(rc, str(rc)))
     return y[:len(tokens)]
@@ -174,10 +210,7 @@ def expert_rows(xs, rows, row_expert, row_w, Wg, Wu, Wd, x_dtype: str = "bf16",
     projection ys = w * o (fp64 [n, d])."""
     xs = _c(xs, np.uint16)
     d = xs.shape[1]
-    Wg = _c(Wg, np.uint16)
-    Wu = _c(Wu, np.uint16)
-    Wd = _c(Wd, np.uint16)
-    E, _, f = Wg.shape
+    warrs, (E, _, f), q8 = _weights(Wg, Wu, Wd)
     rows = _c(rows, np.int64)
     row_expert = _c(row_expert, np.int32)
     row_w = _c(row_w, np.float32)
@@ -186,9 +219,9 @@ def expert_rows(xs, rows, row_expert, row_w, Wg, Wu, Wd, x_dtype: str = "bf16",
     ys = np.zeros((max(n, 1), d), np.float64)
     if nthreads is None:
         nthreads = os.cpu_count() or 1
-    rc = _load().oracle_expert_rows(_p(xs), int(x_dtype == "f16"), d, f, _p(rows), n,
-                                    _p(row_expert), _p(row_w), E, _p(Wg), _p(Wu), _p(Wd),
-                                    int(bool(mirror)), int(nthreads), _p(h), _p(ys))
+    fn = _load().oracle_expert_rows_e4m3 if q8 else _load().oracle_expert_rows
+    rc = fn(_p(xs), int(x_dtype == "f16"), d, f, _p(rows), n, _p(row_expert), _p(row_w), E,
+            *[_p(a) for a in warrs], int(bool(mirror)), int(nthreads), _p(h), _p(ys))
     if rc != 0:
         raise OracleError(_ERR.get(rc, str(rc)))
     return h[:n], ys[:n]
@@ -211,3 +244,32 @@ def round_bf16(v: float) -> float:
 
 def value16(bits: int, dtype: str = "bf16") -> float:
     return _load().oracle_value16(int(bits), int(dtype == "f16"))
+
+
+def e4m3_value(code: int) -> float:
+    """Value of an E4M3 code (NaN for S.1111.111)."""
+    return _load().oracle_e4m3_value(int(code) & 0xFF)
+
+
+def e4m3_encode(v: float) -> int:
+    """Nearest E4M3 code to the fp32 value v, ties to even, saturating at 448."""
+    return int(_load().oracle_e4m3_encode(float(v)))
+
+
+def quantize_e4m3(W):
+    """bf16 weights [E, K, M] -> (E4M3 codes uint8 [E, K, M], fp32 scales
+    [E, M]) with scale = max_k |W| / 448 (1 where that is 0) and code =
+    e4m3_encode(W / scale)."""
+    W = _c(W, np.uint16)
+    E, K, M = W.shape
+    q = np.empty((E, K, M), np.uint8)
+    s = np.empty((E, M), np.float32)
+    _load().oracle_quantize_e4m3(_p(W), E, K, M, _p(q), _p(s))
+    return q, s
+
+
+def dequantize_e4m3(q, s) -> np.ndarray:
+    """fp64 weights e4m3_value(q) * scale (exact)."""
+    table = np.array([e4m3_value(c) for c in range(256)], np.float64)
+    q = np.asarray(q, np.uint8)
+    return table[q] * np.asarray(s, np.float64)[:, None, :]

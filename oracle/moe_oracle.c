@@ -19,6 +19,12 @@
  *       projection) and section 3 (the same per-token top-k summation order).
  *  [P4] "Add --moe-mode sweep-prefill" -- Mechanism (experts walked in
  *       ascending id over contiguous slices).
+ *  [P1] again, section 2: the benchmarks run the experts from quantized
+ *       weight packs (8-, 4- and 2-bit block formats).  The quantized form
+ *       here is 8-bit floating point E4M3 (the OCP 8-bit floating point
+ *       format: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+ *       infinities, S.1111.111 = NaN, largest finite 448) with one fp32
+ *       scale per expert and output feature.
  *
  * Readings taken where the pages leave a step open:
  *  - flat entry i = t*k + j (token-major); ties inside an expert keep
@@ -86,6 +92,82 @@ static double to_bf16(double v)
     u &= 0xffff0000u;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* ---- E4M3 weights [P1 sec. 2; the OCP E4M3 definition] ----------------- */
+
+/* Value of an E4M3 code: exponent field 0 is subnormal (m/8 * 2^-6), the
+ * rest normal ((1 + m/8) * 2^(e-7)); S.1111.111 is NaN. */
+static double e4m3_value(uint8_t c)
+{
+    int sign = c >> 7, ex = (c >> 3) & 15, man = c & 7;
+    double v;
+    if (ex == 15 && man == 7)
+        return NAN;
+    if (ex == 0)
+        v = ldexp((double)man, -9);
+    else
+        v = ldexp((double)(8 + man), ex - 10);
+    return sign ? -v : v;
+}
+
+/* Nearest E4M3 code to v, ties to the even code (the one whose mantissa
+ * field is even), magnitudes past 448 saturated to 448; the sign is kept
+ * (a negative value that rounds to zero gives -0).  Written as a search
+ * over the 127 non-negative finite magnitudes, which are in increasing
+ * order of their codes. */
+static uint8_t e4m3_encode(float v)
+{
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs((double)v);
+    int c, best = 0;
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7e);
+    for (c = 1; c <= 0x7e; c++) {
+        double lo = e4m3_value((uint8_t)(c - 1)), hi = e4m3_value((uint8_t)c);
+        if (a > hi)
+            continue;
+        /* lo <= a <= hi */
+        if (a - lo < hi - a)
+            best = c - 1;
+        else if (a - lo > hi - a)
+            best = c;
+        else
+            best = ((c - 1) & 1) == 0 ? c - 1 : c;
+        break;
+    }
+    return (uint8_t)(sign | best);
+}
+
+/*
+ * Quantize bf16 weights W [E][K][M] (M the output feature, contiguous) to
+ * E4M3 codes q [E][K][M] with one fp32 scale per (expert, output feature):
+ *   amax = max over k of |W[e][k][m]|
+ *   scale[e][m] = amax / 448 (fp32 division), or 1 when that is 0
+ *   q[e][k][m] = e4m3_encode(W[e][k][m] / scale[e][m]) (fp32 division)
+ * so the dequantized weight is e4m3_value(q) * scale.  W must be finite.
+ */
+void oracle_quantize_e4m3(const uint16_t *W, int E, int K, int M, uint8_t *q, float *scale)
+{
+    long e, k, m;
+    for (e = 0; e < E; e++) {
+        for (m = 0; m < M; m++) {
+            float amax = 0.0f, s;
+            for (k = 0; k < K; k++) {
+                float a = (float)fabs(bf16_value(W[(e * K + k) * M + m]));
+                if (a > amax)
+                    amax = a;
+            }
+            s = amax / 448.0f;
+            if (s == 0.0f)
+                s = 1.0f;
+            scale[e * M + m] = s;
+            for (k = 0; k < K; k++) {
+                long i = (e * K + k) * M + m;
+                q[i] = e4m3_encode((float)bf16_value(W[i]) / s);
+            }
+        }
+    }
 }
 
 /* ---- routing plan [P1 sec. 1 items 1-2, sec. 3; P4 Mechanism] ---------- */
@@ -201,12 +283,29 @@ void oracle_gather(const uint16_t *x, int T, int d, const int32_t *srt_tok,
  *   u[n] = sum_c x[c] * Wu[e][c][n]
  *   h[n] = silu(g[n]) * u[n],  silu(z) = z / (1 + exp(-z))
  *   o[m] = sum_n h[n] * Wd[e][n][m]      (n = 0..f-1 in order)
- * Weights are bf16 with layouts Wg, Wu [E][d][f] and Wd [E][f][d].
+ * Weights have layouts Wg, Wu [E][d][f] and Wd [E][f][d], either bf16 or
+ * E4M3 codes with scales [E][f] (gate, up) and [E][d] (down): a weight
+ * matrix is read through wmat_t, whose value is exact in fp64 either way.
  * mirror != 0 rounds h to bf16 before the down projection, as a GPU that
  * stores h in bf16 does (used only for the second, reported reference).
  */
-static void expert_job(const uint16_t *xrow, int x_is_f16, const uint16_t *Wg_e,
-                       const uint16_t *Wu_e, const uint16_t *Wd_e, int d, int f,
+typedef struct {
+    const uint16_t *b16; /* bf16 weights, or NULL */
+    const uint8_t *q8;   /* E4M3 codes when b16 is NULL */
+    const float *scale;  /* [E][cols] with q8 */
+    long rows, cols;     /* per expert */
+} wmat_t;
+
+static double wval(const wmat_t *W, long e, long r, long c)
+{
+    long i = (e * W->rows + r) * W->cols + c;
+    if (W->b16)
+        return bf16_value(W->b16[i]);
+    return e4m3_value(W->q8[i]) * (double)W->scale[e * W->cols + c];
+}
+
+static void expert_job(const uint16_t *xrow, int x_is_f16, const wmat_t *Wg,
+                       const wmat_t *Wu, const wmat_t *Wd, long e, int d, int f,
                        int mirror, double *xv, double *g, double *u, double *h,
                        double *o)
 {
@@ -218,11 +317,9 @@ static void expert_job(const uint16_t *xrow, int x_is_f16, const uint16_t *Wg_e,
         u[n] = 0.0;
     }
     for (c = 0; c < d; c++) {
-        const uint16_t *wg = Wg_e + (long)c * f;
-        const uint16_t *wu = Wu_e + (long)c * f;
         for (n = 0; n < f; n++) {
-            g[n] += xv[c] * bf16_value(wg[n]);
-            u[n] += xv[c] * bf16_value(wu[n]);
+            g[n] += xv[c] * wval(Wg, e, c, n);
+            u[n] += xv[c] * wval(Wu, e, c, n);
         }
     }
     for (n = 0; n < f; n++) {
@@ -232,11 +329,9 @@ static void expert_job(const uint16_t *xrow, int x_is_f16, const uint16_t *Wg_e,
     }
     for (m = 0; m < d; m++)
         o[m] = 0.0;
-    for (n = 0; n < f; n++) {
-        const uint16_t *wd = Wd_e + (long)n * d;
+    for (n = 0; n < f; n++)
         for (m = 0; m < d; m++)
-            o[m] += h[n] * bf16_value(wd[m]);
-    }
+            o[m] += h[n] * wval(Wd, e, n, m);
 }
 
 /* A job: one routed row, its expert, and where its results go. */
@@ -252,7 +347,7 @@ typedef struct {
     long njobs;
     int tid, nthreads;
     int x_is_f16, d, f, mirror;
-    const uint16_t *Wg, *Wu, *Wd;
+    const wmat_t *Wg, *Wu, *Wd;
     int failed;
 } pass_t;
 
@@ -273,9 +368,8 @@ static void *pass_worker(void *arg)
      * arithmetic of a job does not depend on the thread count */
     for (j = p->tid; j < p->njobs; j += p->nthreads) {
         const job_t *jb = &p->jobs[j];
-        long eo = (long)jb->e * d * f;
-        expert_job(jb->xrow, p->x_is_f16, p->Wg + eo, p->Wu + eo, p->Wd + eo,
-                   p->d, p->f, p->mirror, xv, g, u, jb->h ? jb->h : hbuf, jb->o);
+        expert_job(jb->xrow, p->x_is_f16, p->Wg, p->Wu, p->Wd, jb->e, p->d, p->f,
+                   p->mirror, xv, g, u, jb->h ? jb->h : hbuf, jb->o);
     }
     free(xv);
     return NULL;
@@ -283,8 +377,8 @@ static void *pass_worker(void *arg)
 
 /* Run the flat parallel pass over a job list on nthreads host threads. */
 static int run_pass(const job_t *jobs, long njobs, int x_is_f16, int d, int f,
-                    int mirror, const uint16_t *Wg, const uint16_t *Wu,
-                    const uint16_t *Wd, int nthreads)
+                    int mirror, const wmat_t *Wg, const wmat_t *Wu,
+                    const wmat_t *Wd, int nthreads)
 {
     pthread_t th[256];
     pass_t ps[256];
@@ -338,9 +432,9 @@ static int run_pass(const job_t *jobs, long njobs, int x_is_f16, int d, int f,
  * Returns ORC_OK, ORC_ERR_ID for an id outside [-1, E), ORC_ERR_ARG for a
  * token outside [0, T), or ORC_ERR_MEM.
  */
-int oracle_layer_tokens(const uint16_t *x, int x_is_f16, const int32_t *ids,
-                        const float *w, const uint16_t *Wg, const uint16_t *Wu,
-                        const uint16_t *Wd, int T, int d, int E, int k, int f,
+static int layer_tokens(const uint16_t *x, int x_is_f16, const int32_t *ids,
+                        const float *w, const wmat_t *Wg, const wmat_t *Wu,
+                        const wmat_t *Wd, int T, int d, int E, int k, int f,
                         const int32_t *tokens, int ntok, int mirror, int nthreads,
                         double *y)
 {
@@ -432,6 +526,43 @@ int oracle_layer_tokens(const uint16_t *x, int x_is_f16, const int32_t *ids,
     return rc;
 }
 
+static wmat_t bf16_mat(const uint16_t *W, long rows, long cols)
+{
+    wmat_t m = {W, NULL, NULL, rows, cols};
+    return m;
+}
+
+static wmat_t e4m3_mat(const uint8_t *q, const float *scale, long rows, long cols)
+{
+    wmat_t m = {NULL, q, scale, rows, cols};
+    return m;
+}
+
+int oracle_layer_tokens(const uint16_t *x, int x_is_f16, const int32_t *ids,
+                        const float *w, const uint16_t *Wg, const uint16_t *Wu,
+                        const uint16_t *Wd, int T, int d, int E, int k, int f,
+                        const int32_t *tokens, int ntok, int mirror, int nthreads,
+                        double *y)
+{
+    wmat_t g = bf16_mat(Wg, d, f), u = bf16_mat(Wu, d, f), dn = bf16_mat(Wd, f, d);
+    return layer_tokens(x, x_is_f16, ids, w, &g, &u, &dn, T, d, E, k, f, tokens, ntok,
+                        mirror, nthreads, y);
+}
+
+/* The same layer with E4M3 weights: Wg, Wu codes [E][d][f] with scales
+ * [E][f], Wd codes [E][f][d] with scales [E][d]. */
+int oracle_layer_tokens_e4m3(const uint16_t *x, int x_is_f16, const int32_t *ids,
+                             const float *w, const uint8_t *Wg, const float *sg,
+                             const uint8_t *Wu, const float *su, const uint8_t *Wd,
+                             const float *sd, int T, int d, int E, int k, int f,
+                             const int32_t *tokens, int ntok, int mirror, int nthreads,
+                             double *y)
+{
+    wmat_t g = e4m3_mat(Wg, sg, d, f), u = e4m3_mat(Wu, su, d, f), dn = e4m3_mat(Wd, sd, f, d);
+    return layer_tokens(x, x_is_f16, ids, w, &g, &u, &dn, T, d, E, k, f, tokens, ntok,
+                        mirror, nthreads, y);
+}
+
 /* ---- stage-level views used to check one GPU stage at a time ------------ */
 
 /*
@@ -440,10 +571,10 @@ int oracle_layer_tokens(const uint16_t *x, int x_is_f16, const int32_t *ids,
  *   h_out[i][n] = h of that job and ys_out[i][m] = row_w[i] * o[m].
  * Same arithmetic as oracle_layer_tokens' jobs.
  */
-int oracle_expert_rows(const uint16_t *xs, int x_is_f16, int d, int f,
+static int expert_rows(const uint16_t *xs, int x_is_f16, int d, int f,
                        const int64_t *rows, int nrows, const int32_t *row_expert,
-                       const float *row_w, int E, const uint16_t *Wg,
-                       const uint16_t *Wu, const uint16_t *Wd, int mirror,
+                       const float *row_w, int E, const wmat_t *Wg,
+                       const wmat_t *Wu, const wmat_t *Wd, int mirror,
                        int nthreads, double *h_out, double *ys_out)
 {
     long i, m;
@@ -471,6 +602,29 @@ int oracle_expert_rows(const uint16_t *xs, int x_is_f16, int d, int f,
     return rc;
 }
 
+int oracle_expert_rows(const uint16_t *xs, int x_is_f16, int d, int f,
+                       const int64_t *rows, int nrows, const int32_t *row_expert,
+                       const float *row_w, int E, const uint16_t *Wg,
+                       const uint16_t *Wu, const uint16_t *Wd, int mirror,
+                       int nthreads, double *h_out, double *ys_out)
+{
+    wmat_t g = bf16_mat(Wg, d, f), u = bf16_mat(Wu, d, f), dn = bf16_mat(Wd, f, d);
+    return expert_rows(xs, x_is_f16, d, f, rows, nrows, row_expert, row_w, E, &g, &u, &dn,
+                       mirror, nthreads, h_out, ys_out);
+}
+
+int oracle_expert_rows_e4m3(const uint16_t *xs, int x_is_f16, int d, int f,
+                            const int64_t *rows, int nrows, const int32_t *row_expert,
+                            const float *row_w, int E, const uint8_t *Wg, const float *sg,
+                            const uint8_t *Wu, const float *su, const uint8_t *Wd,
+                            const float *sd, int mirror, int nthreads, double *h_out,
+                            double *ys_out)
+{
+    wmat_t g = e4m3_mat(Wg, sg, d, f), u = e4m3_mat(Wu, su, d, f), dn = e4m3_mat(Wd, sd, f, d);
+    return expert_rows(xs, x_is_f16, d, f, rows, nrows, row_expert, row_w, E, &g, &u, &dn,
+                       mirror, nthreads, h_out, ys_out);
+}
+
 /*
  * Combine of given weighted rows: y[t][m] = sum over j = 0..k-1 in order of
  * Ys[pos[t*k+j]][m] (bf16 rows, skipped when pos is -1), in fp64 from 0.0.
@@ -496,3 +650,5 @@ void oracle_combine(const uint16_t *Ys, const int32_t *pos, int T, int k, int d,
 /* bf16 rounding as the oracle does it, exposed so the tests can pin it. */
 double oracle_round_bf16(double v) { return to_bf16(v); }
 double oracle_value16(uint16_t b, int is_f16) { return value16(b, is_f16); }
+double oracle_e4m3_value(uint8_t c) { return e4m3_value(c); }
+uint8_t oracle_e4m3_encode(float v) { return e4m3_encode(v); }

@@ -17,8 +17,8 @@ MUTANTS = {
                         "h[n] = u[n] / (1.0 + exp(-u[n])) * g[n];"),
     "sigmoid_sign": ("h[n] = g[n] / (1.0 + exp(-g[n])) * u[n];",
                      "h[n] = g[n] / (1.0 + exp(g[n])) * u[n];"),
-    "down_transposed": ("o[m] += h[n] * bf16_value(wd[m]);",
-                        "o[m] += h[n] * bf16_value(Wd_e[(long)m * f + n]);"),
+    "down_transposed": ("o[m] += h[n] * wval(Wd, e, n, m);",
+                        "o[m] += h[n] * wval(Wd, e, ((long)m * f + n) / d, ((long)m * f + n) % d);"),
     "weight_dropped": ("yt[m] += wt * jobs[jb].o[m];", "yt[m] += jobs[jb].o[m];"),
     "no_padding": ("offsets[e + 1] = (int32_t)(offsets[e] + tiles * tm);",
                    "offsets[e + 1] = (int32_t)(offsets[e] + counts[e]);"),
@@ -29,6 +29,16 @@ MUTANTS = {
     "last_slot_dropped": ("        for (j = 0; j < k; j++) {\n            int e = ids[(long)t * k + j];\n            if (e == -1) {",
                           "        for (j = 0; j < k; j++) {\n            int e = (j == k - 1 && k > 1) ? -1 : ids[(long)t * k + j];\n            if (e == -1) {"),
     "f16_exponent_bias": ("v = ldexp((double)(man | 0x400), ex - 25);", "v = ldexp((double)(man | 0x400), ex - 24);"),
+    "e4m3_exponent_bias": ("v = ldexp((double)(8 + man), ex - 10);", "v = ldexp((double)(8 + man), ex - 9);"),
+    "e4m3_subnormal_step": ("v = ldexp((double)man, -9);", "v = ldexp((double)man, -10);"),
+    "e4m3_ties_up": ("best = ((c - 1) & 1) == 0 ? c - 1 : c;", "best = c;"),
+    "e4m3_no_saturation": ("    if (a >= 448.0)\n        return (uint8_t)(sign | 0x7e);",
+                           "    if (a > 464.0)\n        return (uint8_t)(sign | 0x7e);"),
+    "scale_per_expert": ("return e4m3_value(W->q8[i]) * (double)W->scale[e * W->cols + c];",
+                         "return e4m3_value(W->q8[i]) * (double)W->scale[e * W->cols];"),
+    "scale_divisor": ("s = amax / 448.0f;", "s = amax / 256.0f;"),
+    "quantize_amax_axis": ("float a = (float)fabs(bf16_value(W[(e * K + k) * M + m]));",
+                           "float a = (float)fabs(bf16_value(W[(e * K + m % K) * M + k % M]));"),
 }
 
 
@@ -45,6 +55,7 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     env = dict(os.environ, MOE_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(HERE, "test_oracle_plan.py"),
-                        os.path.join(HERE, "test_oracle_layer.py")],
+                        os.path.join(HERE, "test_oracle_layer.py"),
+                        os.path.join(HERE, "test_oracle_e4m3.py")],
                        env=env, capture_output=True, text=True, cwd=os.path.dirname(HERE))
     assert r.returncode != 0, f"planted mistake {name} passed every pin:\n{r.stdout[-2000:]}"
