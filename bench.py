@@ -145,25 +145,28 @@ class ClockSampler:
                 "window": "timed region" if inwin else "whole run"}
 
 
-def algorithmic(wl, ids):
+def algorithmic(wl, ids, wbytes=2):
     """Algorithmic work of one layer from the routing itself: active experts,
-    real and padded rows, and the bytes / flops each stage must move."""
+    real and padded rows, and the bytes / flops each stage must move.
+    ``wbytes`` is the size of one weight element (2 bf16, 1 E4M3, which also
+    reads one fp32 scale per expert and output feature)."""
     flat = ids.ravel()
     counts = np.bincount(flat[flat >= 0], minlength=wl.E)
     active = int((counts > 0).sum())
     R = int(counts.sum())
     R_pad = int((-(-counts // wl.tm) * wl.tm).sum())
     d, f = wl.d, wl.f
-    gate_up = active * 2 * d * f * 2 + R_pad * d * 2 + R_pad * f * 2
+    sc = 4 if wbytes == 1 else 0  # E4M3 scales
+    gate_up = active * 2 * (d * f * wbytes + f * sc) + R_pad * d * 2 + R_pad * f * 2
     gate_up_flops = 4 * d * f * R
-    down = active * f * d * 2 + R_pad * f * 2 + R_pad * d * 2 + R_pad * 4
+    down = active * (f * d * wbytes + d * sc) + R_pad * f * 2 + R_pad * d * 2 + R_pad * 4
     gather = wl.T * d * 2 + R_pad * d * 2 + R_pad * 4
     combine = R * d * 2 + wl.T * d * 2 + R * 4
     plan = 8 * wl.T * wl.k + 4 * wl.T * wl.k + 8 * R_pad + 8 * (wl.E + 1)
     return dict(active=active, R=R, R_pad=R_pad, gate_up=gate_up, gate_up_flops=gate_up_flops,
                 down=down, gather=gather,
                 combine=combine, plan=plan, layer=plan + gather + gate_up + down + combine,
-                flops=6 * d * f * R, weights=active * 3 * d * f * 2)
+                flops=6 * d * f * R, weights=active * 3 * d * f * wbytes)
 
 
 def d16(a, dev):
@@ -207,10 +210,18 @@ def run_native(args, rank, world, local):
     chunk = replicas.chunk_of_rank(rank, world) % wl.n_chunks
     log(f"[rank {rank}] generating {wl.name} (chunk {chunk}) ...")
     inp = W.make_inputs(wl, seed=0, chunk=chunk)
-    alg = algorithmic(wl, inp["ids"])
+    e4m3 = args.weights == "e4m3"
+    alg = algorithmic(wl, inp["ids"], wbytes=1 if e4m3 else 2)
     x, ids, w = d16(inp["x"], dev), torch.from_numpy(inp["ids"]).to(dev), torch.from_numpy(inp["w"]).to(dev)
     Wg, Wu, Wd = (d16(inp[n], dev) for n in ("Wg", "Wu", "Wd"))
-    layer = B.MoeLayer(Wg, Wu, Wd, tm=wl.tm)
+    if e4m3:
+        # the experts' weights as E4M3 codes + per-feature scales (quantized
+        # once on the device, before anything is timed)
+        layer = B.MoeLayer.quantized(Wg, Wu, Wd, tm=wl.tm)
+        Wg, Wu, Wd = layer.Wg, layer.Wu, layer.Wd
+        torch.cuda.synchronize(dev)
+    else:
+        layer = B.MoeLayer(Wg, Wu, Wd, tm=wl.tm)
     y = torch.empty((wl.T, wl.d), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -257,8 +268,11 @@ def run_native(args, rank, world, local):
     stages = ("plan", "gather", "gate_up", "down", "combine")
     calls = (lambda: B.plan(ids, w, wl.E, wl.tm, cap=cap, out=o),
              lambda: B.gather(x, o["srt_tok"], o["offsets"], wl.E, cap, xs=xs),
-             lambda: B.ffn_gate_up(xs, Wg, Wu, o["offsets"], cap, H=H, status=st),
-             lambda: B.ffn_down(H, Wd, o["offsets"], o["srt_w"], cap, Ys=Ys, status=st),
+             (lambda: B.ffn_gate_up_e4m3(xs, Wg, Wu, o["offsets"], cap, H=H, status=st)) if e4m3
+             else (lambda: B.ffn_gate_up(xs, Wg, Wu, o["offsets"], cap, H=H, status=st)),
+             (lambda: B.ffn_down_e4m3(H, Wd, o["offsets"], o["srt_w"], cap, Ys=Ys, status=st))
+             if e4m3 else (lambda: B.ffn_down(H, Wd, o["offsets"], o["srt_w"], cap, Ys=Ys,
+                                               status=st)),
              lambda: B.combine(Ys, o["pos"], y=y))
     K2 = max(3, min(args.steps, 200))
     per = {s: [] for s in stages}
@@ -336,11 +350,14 @@ def run_native(args, rank, world, local):
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(ms),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 (E4M3 weights widened to bf16)" if e4m3 else "bf16",
         "data": "synthetic (seeded: x~N(0,1), W~N(0,0.02) bf16, " + ROUTING[wl.routing] + ")",
         "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k, "f": wl.f,
                    "tm": wl.tm, "routing": ROUTING[wl.routing],
                    "active_experts": alg["active"], "R_pad": alg["R_pad"],
+                   "weights": ("E4M3 codes + fp32 scale per expert and output feature" if e4m3
+                               else "bf16"),
                    "l2": "flushed before every timed step (256 MiB write)",
                    "parallelism": "replicas (one independent layer per GPU)"},
         "plan_us_per_layer": plan_graph_us,
@@ -348,13 +365,15 @@ def run_native(args, rank, world, local):
         "plan_us_cold": stage_us["plan"],
         "stages_us": stage_us,
         "layer_hbm_gbs": layer_gbs,
-        "roofline": {"kernel": "k_ffn<gate/up> (tcgen05 grouped GEMM + SwiGLU)",
+        "roofline": {"kernel": ("k_ffn<gate/up, E4M3 weights> (widened to bf16 in shared memory; "
+                               "tcgen05 grouped GEMM + SwiGLU)") if e4m3
+                     else "k_ffn<gate/up> (tcgen05 grouped GEMM + SwiGLU)",
                      "bound": "tensor" if tensor_bound else "hbm",
                      "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": alg["gate_up"],
                      "algorithmic_flops_per_launch": alg["gate_up_flops"],
-                     "traffic": traffic if args.workload == WORKLOAD else None},
+                     "traffic": traffic if args.workload == WORKLOAD and not e4m3 else None},
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_total / K3, "steps": K3,
                 "api": "moe_prefill_forward_host (host buffers; copies overlap the layer)",
@@ -365,7 +384,7 @@ def run_native(args, rank, world, local):
         "clocks": clk,
         "gpu_launches": KERNELS_PER_LAYER * args.steps,
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not e4m3:
         nth = os.cpu_count() or 1
         log("timing the CPU oracle on a bounded sample ...")
         v, secs, desc = oracle_sample(inp, wl, args.cpu_budget, nth)
@@ -418,6 +437,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--weights", choices=("bf16", "e4m3"), default="bf16",
+                    help="expert weights: bf16 (the default measurement) or E4M3 codes with "
+                         "per-feature scales")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

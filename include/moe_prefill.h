@@ -301,6 +301,47 @@ MOE_API int moe_layer_forward(const void *x, const int32_t *ids, const float *w,
                       moe_stream_t stream);
 
 /*
+ * E4M3 expert weights.  "Round 4 Track C: Prefill MoE Plan ...", section 2,
+ * runs the experts from quantized weight packs (8-, 4- and 2-bit block
+ * formats).  The GEMMs stream the expert weights from HBM, so holding them
+ * in 8 bits halves the layer's dominant traffic.  The packed form is the
+ * OCP E4M3 format (1 sign, 4 exponent bits with bias 7, 3 mantissa bits,
+ * largest finite 448) with one fp32 scale per expert and output feature:
+ *   scale[e][m] = max_k |W[e][k][m]| / 448   (1 when that is 0)
+ *   q[e][k][m]  = E4M3 nearest to W[e][k][m] / scale[e][m] (ties to even,
+ *                 saturated at +-448), both divisions IEEE fp32
+ * and the weight the GEMMs use is value(q) * scale.  Activations, H, Ys and
+ * y stay bf16; accumulation is fp32.  The GEMMs widen each 8-bit tile to
+ * bf16 in shared memory (exact) and apply the scale in their epilogue.
+ *
+ * moe_quantize_e4m3 -- W bf16 [E, K, M] (M = output features, contiguous)
+ * -> q uint8 [E, K, M], scale fp32 [E, M].  W must be finite.  A one-time
+ * preparation (two passes over W), not part of the layer.
+ */
+MOE_API int moe_quantize_e4m3(const void *W, int E, int K, int M, uint8_t *q, float *scale,
+                              moe_stream_t stream);
+
+/* moe_ffn_gate_up / moe_ffn_down with E4M3 weights: Wg, Wu uint8 [E, d, f]
+ * with scales sg, su fp32 [E, f]; Wd uint8 [E, f, d] with scales sd fp32
+ * [E, d] (16-byte aligned codes, 4-byte aligned scales).  Everything else
+ * as in the bf16 calls. */
+MOE_API int moe_ffn_gate_up_e4m3(const void *xs, const uint8_t *Wg, const float *sg,
+                                 const uint8_t *Wu, const float *su, const int32_t *offsets,
+                                 int E, int d, int f, int64_t cap, void *H, uint32_t *status,
+                                 moe_stream_t stream);
+MOE_API int moe_ffn_down_e4m3(const void *H, const uint8_t *Wd, const float *sd,
+                              const int32_t *offsets, const float *srt_w, int E, int d, int f,
+                              int64_t cap, void *Ys, uint32_t *status, moe_stream_t stream);
+
+/* moe_layer_forward with E4M3 weights (as above); same workspace
+ * (moe_workspace_bytes) and outputs. */
+MOE_API int moe_layer_forward_e4m3(const void *x, const int32_t *ids, const float *w,
+                                   const uint8_t *Wg, const float *sg, const uint8_t *Wu,
+                                   const float *su, const uint8_t *Wd, const float *sd, int T,
+                                   int d, int E, int k, int f, int tm, void *y, void *ws,
+                                   size_t ws_bytes, moe_stream_t stream);
+
+/*
  * moe_prefill_forward_host -- moe_layer_forward over n_chunks prefill
  * chunks of T tokens each, taken from and returned to HOST memory.  The
  * pages run the layer chunk by chunk over a prompt ("Round 4 Track C:
@@ -316,6 +357,8 @@ MOE_API int moe_layer_forward(const void *x, const int32_t *ids, const float *w,
  * out  y_h[c]    bf16 [T, d]  host memory
  * in   Wg, Wu, Wd, T, d, E, k, f, tm  device weights and shapes as in
  *                moe_layer_forward (T is the size of every chunk)
+ * in   sg, su, sd  NULL for bf16 weights; with E4M3 weights (codes in Wg,
+ *                Wu, Wd) their scales, as in moe_layer_forward_e4m3
  * ws            moe_prefill_host_workspace_bytes(...) device bytes, 256-byte
  *               aligned: the layer's workspace (moe_workspace_bytes, at offset
  *               0, so moe_read_status works on it) then the staging buffers
@@ -332,7 +375,8 @@ MOE_API size_t moe_prefill_host_workspace_bytes(int T, int d, int E, int k, int 
 MOE_API int moe_prefill_forward_host(int n_chunks, const void *const *x_h,
                                      const int32_t *const *ids_h, const float *const *w_h,
                                      void *const *y_h, const void *Wg, const void *Wu,
-                                     const void *Wd, int T, int d, int E, int k, int f, int tm,
+                                     const void *Wd, const float *sg, const float *su,
+                                     const float *sd, int T, int d, int E, int k, int f, int tm,
                                      void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /*

@@ -60,8 +60,22 @@ _SIGS = {
     "moe_prefill_host_workspace_bytes": (C.c_size_t, [C.c_int] * 6),
     "moe_prefill_forward_host": (C.c_int, [C.c_int, C.c_void_p, C.c_void_p, C.c_void_p,
                                            C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                           C.c_void_p, C.c_void_p, C.c_void_p,
                                            C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
                                            C.c_void_p, C.c_size_t, C.c_void_p]),
+    "moe_quantize_e4m3": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p,
+                                    C.c_void_p, C.c_void_p]),
+    "moe_ffn_gate_up_e4m3": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                       C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
+                                       C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p]),
+    "moe_ffn_down_e4m3": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                    C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int64,
+                                    C.c_void_p, C.c_void_p, C.c_void_p]),
+    "moe_layer_forward_e4m3": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                         C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                         C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int,
+                                         C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_size_t,
+                                         C.c_void_p]),
     "moe_read_status": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p]),
     "moe_selftest_wait_limit": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                           C.c_int, C.c_int, C.c_int, C.c_int64, C.c_void_p,
@@ -317,11 +331,13 @@ def _host_ptrs(ts, name):
 
 def prefill_forward_host(x_hs, ids_hs, w_hs, y_hs, Wg, Wu, Wd, tm: int, ws=None):
     """moe_prefill_forward_host over len(x_hs) chunks: host (preferably
-    pinned) x [T, d] bf16, ids/w [T, k] in; host y [T, d] bf16 out.
+    pinned) x [T, d] bf16, ids/w [T, k] in; host y [T, d] bf16 out.  The
+    weights are bf16 tensors or, all three, (E4M3 codes, scales) pairs.
     Asynchronous on the current stream; synchronize before reading y_hs."""
     n = len(x_hs)
     if not (len(ids_hs) == len(w_hs) == len(y_hs) == n):
         raise ValueError("one ids, w and y per chunk")
+    (Wg, Wu, Wd), scales = _split_weights(Wg, Wu, Wd)
     E, d, f = Wg.shape
     T, k = (ids_hs[0].shape if n else (0, 1))
     dev = Wg.device
@@ -332,10 +348,75 @@ def prefill_forward_host(x_hs, ids_hs, w_hs, y_hs, Wg, Wu, Wd, tm: int, ws=None)
               _host_ptrs(y_hs, "y")]
     with torch.cuda.device(dev):
         rc = lib().moe_prefill_forward_host(n, *[C.cast(a, C.c_void_p) for a in arrays],
-                                            _ptr(Wg), _ptr(Wu), _ptr(Wd), T, d, E, k, f, tm,
+                                            _ptr(Wg), _ptr(Wu), _ptr(Wd),
+                                            *[_ptr(t) for t in scales], T, d, E, k, f, tm,
                                             _ptr(ws), ws.numel(), _stream(dev))
     _check("moe_prefill_forward_host", rc)
     return y_hs
+
+
+def _split_weights(Wg, Wu, Wd):
+    """(codes, scales) pairs -> the code tensors and the scale tensors;
+    bf16 tensors -> themselves and three Nones."""
+    if isinstance(Wg, tuple):
+        return (Wg[0], Wu[0], Wd[0]), (Wg[1], Wu[1], Wd[1])
+    return (Wg, Wu, Wd), (None, None, None)
+
+
+def quantize_e4m3(W):
+    """moe_quantize_e4m3: bf16 W [E, K, M] -> (uint8 codes [E, K, M], fp32
+    scales [E, M]), the pair the *_e4m3 calls and MoeLayer take."""
+    E, K, M = W.shape
+    q = torch.empty((E, K, M), dtype=torch.uint8, device=W.device)
+    s = torch.empty((E, M), dtype=torch.float32, device=W.device)
+    with torch.cuda.device(W.device):
+        rc = lib().moe_quantize_e4m3(_ptr(W), E, K, M, _ptr(q), _ptr(s), _stream(W.device))
+    _check("moe_quantize_e4m3", rc)
+    return q, s
+
+
+def ffn_gate_up_e4m3(xs, Wg, Wu, offsets, cap: int, H=None, status=None):
+    (qg, sg), (qu, su) = Wg, Wu
+    E, d, f = qg.shape
+    if H is None:
+        H = torch.empty((max(cap, 1), f), dtype=torch.bfloat16, device=xs.device)
+    with torch.cuda.device(xs.device):
+        rc = lib().moe_ffn_gate_up_e4m3(_ptr(xs), _ptr(qg), _ptr(sg), _ptr(qu), _ptr(su),
+                                        _ptr(offsets), E, d, f, cap, _ptr(H), _ptr(status),
+                                        _stream(xs.device))
+    _check("moe_ffn_gate_up_e4m3", rc)
+    return H
+
+
+def ffn_down_e4m3(H, Wd, offsets, srt_w, cap: int, Ys=None, status=None):
+    qd, sd = Wd
+    E, f, d = qd.shape
+    if Ys is None:
+        Ys = torch.empty((max(cap, 1), d), dtype=torch.bfloat16, device=H.device)
+    with torch.cuda.device(H.device):
+        rc = lib().moe_ffn_down_e4m3(_ptr(H), _ptr(qd), _ptr(sd), _ptr(offsets), _ptr(srt_w), E,
+                                     d, f, cap, _ptr(Ys), _ptr(status), _stream(H.device))
+    _check("moe_ffn_down_e4m3", rc)
+    return Ys
+
+
+def layer_forward_e4m3(x, ids, w, Wg, Wu, Wd, tm: int, y=None, ws=None):
+    """moe_layer_forward_e4m3 with (codes, scales) weight pairs."""
+    T, d = x.shape
+    k = ids.shape[1]
+    (qg, sg), (qu, su), (qd, sd) = Wg, Wu, Wd
+    E, _, f = qg.shape
+    dev = x.device
+    if y is None:
+        y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    if ws is None:
+        ws = torch.empty(workspace_bytes(T, d, E, k, f, tm), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = lib().moe_layer_forward_e4m3(_ptr(x), _ptr(ids), _ptr(w), _ptr(qg), _ptr(sg),
+                                          _ptr(qu), _ptr(su), _ptr(qd), _ptr(sd), T, d, E, k, f,
+                                          tm, _ptr(y), _ptr(ws), ws.numel(), _stream(dev))
+    _check("moe_layer_forward_e4m3", rc)
+    return y
 
 
 def selftest_wait_limit(xs, Wg, Wu, offsets, cap: int, status, cta: int = 0, H=None):
@@ -364,6 +445,8 @@ def read_status(ws) -> int:
 class MoeLayer:
     """A routed MoE layer with its expert weights resident in HBM.
 
+    The weights are bf16 tensors or, all three, (E4M3 codes, fp32 scales)
+    pairs from ``quantize_e4m3`` (``MoeLayer.quantized`` makes them).
     ``forward`` takes device inputs.  ``forward_host`` (one chunk) and
     ``forward_host_chunks`` (a sequence of chunks) take pinned host inputs
     and go through moe_prefill_forward_host: the inputs are copied in and y
@@ -372,10 +455,17 @@ class MoeLayer:
 
     def __init__(self, Wg, Wu, Wd, tm: int = 16):
         self.Wg, self.Wu, self.Wd, self.tm = Wg, Wu, Wd, tm
-        self.E, self.d, self.f = Wg.shape
-        self.device = Wg.device
+        self.e4m3 = isinstance(Wg, tuple)
+        codes = Wg[0] if self.e4m3 else Wg
+        self.E, self.d, self.f = codes.shape
+        self.device = codes.device
         self._ws = None
         self._host_ws = None
+
+    @classmethod
+    def quantized(cls, Wg, Wu, Wd, tm: int = 16):
+        """The same layer with its bf16 weights quantized to E4M3 on the device."""
+        return cls(quantize_e4m3(Wg), quantize_e4m3(Wu), quantize_e4m3(Wd), tm=tm)
 
     def workspace(self, T: int, k: int):
         n = workspace_bytes(T, self.d, self.E, k, self.f, self.tm)
@@ -385,8 +475,9 @@ class MoeLayer:
 
     def forward(self, x, ids, w, y=None):
         T = x.shape[0]
-        return layer_forward(x, ids, w, self.Wg, self.Wu, self.Wd, self.tm, y=y,
-                             ws=self.workspace(T, ids.shape[1]))
+        fn = layer_forward_e4m3 if self.e4m3 else layer_forward
+        return fn(x, ids, w, self.Wg, self.Wu, self.Wd, self.tm, y=y,
+                  ws=self.workspace(T, ids.shape[1]))
 
     def forward_host(self, x_h, ids_h, w_h, y_h):
         """Host (pinned) x, ids, w in; host y out, through the C ABI's host

@@ -270,14 +270,22 @@ int moe_workspace_layout(int T, int d, int E, int k, int f, int tm, size_t *out)
     return layout(T, d, E, k, f, tm, out);
 }
 
-int moe_layer_forward(const void *x, const int32_t *ids, const float *w, const void *Wg,
-                      const void *Wu, const void *Wd, int T, int d, int E, int k, int f, int tm,
-                      void *y, void *ws, size_t ws_bytes, moe_stream_t stream)
+// The expert weights of a layer: bf16, or E4M3 codes with per-feature scales.
+struct LayerWeights {
+    const void *Wg, *Wu, *Wd;
+    const float *sg, *su, *sd;  // all null for bf16
+};
+
+static int layer_forward(const void *x, const int32_t *ids, const float *w,
+                         const LayerWeights &W, int T, int d, int E, int k, int f, int tm, void *y,
+                         void *ws, size_t ws_bytes, moe_stream_t stream)
 {
+    const bool e4m3 = W.sg != nullptr;
     if (!base_sizes_ok(T, k, E) || tm < 16 || tm > MOE_MAX_TM || tm % 16 != 0 || d <= 0 ||
         f <= 0 || d % 64 != 0 || f % 64 != 0)
         return MOE_ERR_SHAPE;
-    if (!Wg || !Wu || !Wd || !ws || (T > 0 && (!x || !ids || !w || !y)))
+    if (!W.Wg || !W.Wu || !W.Wd || !ws || (T > 0 && (!x || !ids || !w || !y)) ||
+        (e4m3 && (!W.su || !W.sd)))
         return MOE_ERR_NULL;
     size_t L[MOE_WS_FIELDS];
     int rc = layout(T, d, E, k, f, tm, L);
@@ -285,8 +293,9 @@ int moe_layer_forward(const void *x, const int32_t *ids, const float *w, const v
         return rc;
     if (ws_bytes < L[MOE_WS_TOTAL])
         return MOE_ERR_WORKSPACE;
-    if (!aligned(ws, 256) || !aligned(x, 16) || !aligned(y, 16) || !aligned(Wg, 16) ||
-        !aligned(Wu, 16) || !aligned(Wd, 16) || !aligned(ids, 4) || !aligned(w, 4))
+    if (!aligned(ws, 256) || !aligned(x, 16) || !aligned(y, 16) || !aligned(W.Wg, 16) ||
+        !aligned(W.Wu, 16) || !aligned(W.Wd, 16) || !aligned(ids, 4) || !aligned(w, 4) ||
+        !aligned(W.sg, 4) || !aligned(W.su, 4) || !aligned(W.sd, 4))
         return MOE_ERR_ALIGN;
     if (T == 0)
         return MOE_OK;
@@ -308,12 +317,78 @@ int moe_layer_forward(const void *x, const int32_t *ids, const float *w, const v
     if (e == cudaSuccess)
         e = moe::launch_gather(x, T, d, srt_tok, offsets, E, cap, xs, s);
     if (e == cudaSuccess)
-        e = moe::launch_ffn_gate_up(xs, Wg, Wu, offsets, E, d, f, cap, H, status, s);
+        e = e4m3 ? moe::launch_ffn_gate_up_e4m3(xs, static_cast<const uint8_t *>(W.Wg), W.sg,
+                                                static_cast<const uint8_t *>(W.Wu), W.su, offsets,
+                                                E, d, f, cap, H, status, s)
+                 : moe::launch_ffn_gate_up(xs, W.Wg, W.Wu, offsets, E, d, f, cap, H, status, s);
     if (e == cudaSuccess)
-        e = moe::launch_ffn_down(H, Wd, offsets, srt_w, E, d, f, cap, Ys, status, s);
+        e = e4m3 ? moe::launch_ffn_down_e4m3(H, static_cast<const uint8_t *>(W.Wd), W.sd, offsets,
+                                             srt_w, E, d, f, cap, Ys, status, s)
+                 : moe::launch_ffn_down(H, W.Wd, offsets, srt_w, E, d, f, cap, Ys, status, s);
     if (e == cudaSuccess)
         e = moe::launch_combine(Ys, pos, T, k, d, y, s);
     return cuda_rc(e);
+}
+
+int moe_layer_forward(const void *x, const int32_t *ids, const float *w, const void *Wg,
+                      const void *Wu, const void *Wd, int T, int d, int E, int k, int f, int tm,
+                      void *y, void *ws, size_t ws_bytes, moe_stream_t stream)
+{
+    const LayerWeights W{Wg, Wu, Wd, nullptr, nullptr, nullptr};
+    return layer_forward(x, ids, w, W, T, d, E, k, f, tm, y, ws, ws_bytes, stream);
+}
+
+int moe_layer_forward_e4m3(const void *x, const int32_t *ids, const float *w, const uint8_t *Wg,
+                           const float *sg, const uint8_t *Wu, const float *su,
+                           const uint8_t *Wd, const float *sd, int T, int d, int E, int k, int f,
+                           int tm, void *y, void *ws, size_t ws_bytes, moe_stream_t stream)
+{
+    if (!sg)
+        return MOE_ERR_NULL;
+    const LayerWeights W{Wg, Wu, Wd, sg, su, sd};
+    return layer_forward(x, ids, w, W, T, d, E, k, f, tm, y, ws, ws_bytes, stream);
+}
+
+int moe_quantize_e4m3(const void *W, int E, int K, int M, uint8_t *q, float *scale,
+                      moe_stream_t stream)
+{
+    if (E < 1 || E > MOE_MAX_EXPERTS || K < 1 || M < 1)
+        return MOE_ERR_SHAPE;
+    if (!W || !q || !scale)
+        return MOE_ERR_NULL;
+    if (!aligned(W, 2) || !aligned(scale, 4))
+        return MOE_ERR_ALIGN;
+    return cuda_rc(moe::launch_quantize_e4m3(W, E, K, M, q, scale, as_stream(stream)));
+}
+
+int moe_ffn_gate_up_e4m3(const void *xs, const uint8_t *Wg, const float *sg, const uint8_t *Wu,
+                         const float *su, const int32_t *offsets, int E, int d, int f,
+                         int64_t cap, void *H, uint32_t *status, moe_stream_t stream)
+{
+    int rc = ffn_checks(xs, Wg, Wu, offsets, E, d, f, cap, H);
+    if (rc == MOE_OK && (!sg || !su))
+        rc = MOE_ERR_NULL;
+    if (rc == MOE_OK && (!aligned(sg, 4) || !aligned(su, 4) || !aligned(status, 4)))
+        rc = MOE_ERR_ALIGN;
+    if (rc != MOE_OK || cap == 0)
+        return rc;
+    return cuda_rc(moe::launch_ffn_gate_up_e4m3(xs, Wg, sg, Wu, su, offsets, E, d, f, cap, H,
+                                                status, as_stream(stream)));
+}
+
+int moe_ffn_down_e4m3(const void *H, const uint8_t *Wd, const float *sd, const int32_t *offsets,
+                      const float *srt_w, int E, int d, int f, int64_t cap, void *Ys,
+                      uint32_t *status, moe_stream_t stream)
+{
+    int rc = ffn_checks(H, Wd, srt_w, offsets, E, d, f, cap, Ys);
+    if (rc == MOE_OK && !sd)
+        rc = MOE_ERR_NULL;
+    if (rc == MOE_OK && (!aligned(sd, 4) || !aligned(status, 4)))
+        rc = MOE_ERR_ALIGN;
+    if (rc != MOE_OK || cap == 0)
+        return rc;
+    return cuda_rc(moe::launch_ffn_down_e4m3(H, Wd, sd, offsets, srt_w, E, d, f, cap, Ys, status,
+                                             as_stream(stream)));
 }
 
 int moe_selftest_wait_limit(const void *xs, const void *Wg, const void *Wu,

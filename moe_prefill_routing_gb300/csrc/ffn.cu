@@ -31,6 +31,13 @@
 // warp 1 issues tcgen05.mma into one of two TMEM accumulators, warps 2-5
 // read the accumulator with tcgen05.ld, apply the epilogue, stage 16 rows of
 // bf16 in shared memory, and one thread writes them out with a TMA store.
+// W8: the weights are E4M3 codes with a per-(expert, output feature) scale
+// (see quant.cu).  TMA brings the 8-bit tiles into the stage ring (half the
+// bytes of bf16), eight more warps (6-13) widen them to bf16 -- exactly: every
+// E4M3 value is a bf16 value -- into a second ring laid out as the bf16
+// tiles would be (MN-major, 128-byte swizzle), and the epilogue multiplies
+// each accumulator row (one output feature) by its scale.  The MMAs are the
+// same bf16 MMAs.
 // Every output element is written by one CTA with a fixed K order: results
 // are deterministic.  Every wait is bounded (2 s); on a timeout the CTA
 // stops, lets its copies and MMAs land, frees TMEM and sets
@@ -40,6 +47,8 @@
 #include "ptx.cuh"
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -56,7 +65,10 @@ constexpr uint32_t kABoxBytes = 64 * BK * 2;      // 64 features x 64 K rows
 constexpr uint32_t kATileBytes = 2 * kABoxBytes;  // 128 features
 constexpr uint32_t kBTileBytes = BN * BK * 2;     // 128 rows x 64 K
 constexpr uint32_t kBBoxBytes = kBoxRows * BK * 2;
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;      // producer, MMA, four epilogue warps
+constexpr int kConvThreads = 256;  // eight warps widening E4M3 tiles (W8)
+constexpr int kThreadsW8 = kThreads + kConvThreads;
+constexpr int kMaxWarps = kThreadsW8 / 32;
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for the stop path
@@ -67,6 +79,21 @@ constexpr uint32_t kAccCols = 2 * BN;                            // two accumula
 constexpr uint32_t kTmemCols = 2 * kAccCols;                     // double-buffered
 constexpr int kStageRows = 16;                                   // rows per epilogue chunk
 constexpr uint32_t kStgBytes = 2 * kStageRows * 256 * 2;         // two chunks of <= 256 features
+// W8: a stage holds two E4M3 tiles (128 features x 64 K, 1 byte each, rows
+// of 128 bytes unswizzled) and the B tile; two more slots hold the widened
+// bf16 A tiles.  Shared memory in stages is the same 192 KB either way.
+constexpr uint32_t kA8TileBytes = BM * BK;                       // 8 KB
+constexpr uint32_t kStageBytesW8 = 2 * kA8TileBytes + kBTileBytes;
+constexpr int kConvSlots = 2;
+constexpr uint32_t kConvSlotBytes = 2 * kATileBytes;
+
+template <bool W8>
+struct Cfg {
+    static constexpr int kThreadsK = W8 ? kThreadsW8 : kThreads;
+    static constexpr uint32_t kStageB = W8 ? kStageBytesW8 : kStageBytes;
+    static constexpr uint32_t kRingBytes =
+        kStages * kStageB + (W8 ? kConvSlots * kConvSlotBytes : 0u);
+};
 
 // GATED: gate/up (A tiles = Wg and Wu over the same 128 features, output H).
 // !GATED: down (A tiles = Wd over features m0 and m0 + 128, output Ys).
@@ -81,11 +108,13 @@ struct Ctrl {
     uint64_t empty[S];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
+    uint64_t conv_full[kConvSlots];   // W8: widened A tiles ready (kConvThreads arrivals)
+    uint64_t conv_empty[kConvSlots];  // W8: the MMAs are done with a slot
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
     int epi_stop;  // set only by epilogue threads; read by all four warps after a barrier
-    int warp_sum[kThreads / 32];
+    int warp_sum[kMaxWarps];
 };
 
 struct FfnArgs {
@@ -100,13 +129,18 @@ struct FfnArgs {
     int M;  // output features: f (gate/up) or d (down)
     int stall_cta;  // self-test only: this CTA's first stage waits for 16 bytes
                     // that never come; -1 in every normal launch
+    const float *scale0;  // W8: scales [E, M] of A tile 0's weight (Wg or Wd)
+    const float *scale1;  // W8: scales [E, M] of A tile 1's weight (Wu or Wd)
 };
 
+template <bool W8>
 constexpr size_t ffn_smem_bytes(int E)
 {
-    return 1024 + size_t(kStages) * kStageBytes + kStgBytes + sizeof(Ctrl<kStages>) +
+    return 1024 + size_t(Cfg<W8>::kRingBytes) + kStgBytes + sizeof(Ctrl<kStages>) +
            2 * BN * sizeof(int) + size_t(E + 1) * sizeof(int);
 }
+static_assert(ffn_smem_bytes<true>(MOE_MAX_EXPERTS) <= 227 * 1024, "shared memory per CTA");
+static_assert(ffn_smem_bytes<false>(MOE_MAX_EXPERTS) <= 227 * 1024, "shared memory per CTA");
 
 // Bounded wait that ignores the abort flag (used while stopping).
 __device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity)
@@ -134,7 +168,8 @@ __device__ int build_chunk_table(const int32_t *off, int E, int64_t cap, int *cs
                                  uint32_t *status)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int per = (E + kThreads - 1) / kThreads;
+    const int nthr = blockDim.x, nwarps = nthr >> 5;
+    const int per = (E + nthr - 1) / nthr;
     const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
     bool bad = false;
     int local = 0;
@@ -151,8 +186,7 @@ __device__ int build_chunk_table(const int32_t *off, int E, int64_t cap, int *cs
         warp_sum[warp] = v;
     __syncthreads();
     int before = 0, total = 0;
-#pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) {
+    for (int w = 0; w < nwarps; ++w) {
         before += w < warp ? warp_sum[w] : 0;
         total += warp_sum[w];
     }
@@ -203,21 +237,45 @@ __device__ __forceinline__ void epi_bar()
     asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
 }
 
+// 16 E4M3 codes (one 16-byte chunk) -> 16 bf16 values (two 16-byte
+// chunks), exactly: E4M3 -> f16 is exact, and so is f16 -> f32 -> bf16 for
+// values that came from E4M3 (at most 4 significant bits, exponents inside
+// bf16's range).
+__device__ __forceinline__ void widen_e4m3x16(const uint4 v, uint4 &lo, uint4 &hi)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const __nv_fp8x2_storage_t pair =
+            static_cast<__nv_fp8x2_storage_t>((w[i >> 1] >> (16 * (i & 1))) & 0xffffu);
+        const __half2 h = __half2(__nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3));
+        const __nv_bfloat162 b = __float22bfloat162_rn(__half22float2(h));
+        o[i] = *reinterpret_cast<const uint32_t *>(&b);
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 // GATHER: the B rows of a unit are token rows of x fetched by index
 // (srt_tok, four rows per TMA gather4) instead of consecutive rows of xs.
-template <bool GATED, bool GATHER>
-__global__ void __launch_bounds__(kThreads, 1)
+// W8: the A tiles arrive as E4M3 codes and are widened in shared memory.
+template <bool GATED, bool GATHER, bool W8>
+__global__ void __launch_bounds__(Cfg<W8>::kThreadsK, 1)
     k_ffn(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
           const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_out,
           const FfnArgs p)
 {
+    static_assert(!(GATHER && W8), "gathered rows come with bf16 weights only");
     constexpr int S = kStages;
     constexpr int UM = Kind<GATED>::kUnitM;
+    constexpr uint32_t SB = Cfg<W8>::kStageB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
-    uint16_t *stg = reinterpret_cast<uint16_t *>(smem + S * kStageBytes);
-    Ctrl<S> *ctl = reinterpret_cast<Ctrl<S> *>(smem + S * kStageBytes + kStgBytes);
+    uint8_t *conv = smem + S * SB;  // W8: widened A tiles, kConvSlots slots
+    uint16_t *stg = reinterpret_cast<uint16_t *>(smem + Cfg<W8>::kRingBytes);
+    Ctrl<S> *ctl = reinterpret_cast<Ctrl<S> *>(smem + Cfg<W8>::kRingBytes + kStgBytes);
     int *row_tok = reinterpret_cast<int *>(ctl + 1);  // [BN] tokens of the unit's rows
     float *row_w = reinterpret_cast<float *>(row_tok + BN);  // [BN] routing weights (down)
     int *chunk_start = row_tok + 2 * BN;
@@ -232,6 +290,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ctl->tmem_full[b], 1);
             mbar_init(&ctl->tmem_empty[b], kEpiThreads);
+        }
+        for (int c = 0; c < kConvSlots; ++c) {
+            mbar_init(&ctl->conv_full[c], kConvThreads);
+            mbar_init(&ctl->conv_empty[c], 1);
         }
         mbar_init(&ctl->mma_done, 1);
         ctl->abort_flag = 0;
@@ -287,7 +349,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 0; t < 2; ++t)
                     for (int h = 0; h < 2; ++h)
                         boxes += tile_base(m0, t) + 64 * h < p.M;
-                const uint32_t bytes = boxes * kABoxBytes + uint32_t(w.nrows) * uint32_t(BK * 2);
+                // W8: one E4M3 box of 128 features per A tile that starts
+                // inside M (features past M are zero-filled and still counted)
+                const uint32_t a_bytes =
+                    W8 ? (1u + uint32_t(tile_base(m0, 1) < p.M)) * kA8TileBytes
+                       : boxes * kABoxBytes;
+                const uint32_t bytes = a_bytes + uint32_t(w.nrows) * uint32_t(BK * 2);
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag)) {
                         ok = false;
@@ -296,20 +363,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint64_t *fb = &ctl->full[stage];
                     mbar_arrive_expect_tx(fb, bytes + stall_bytes);
                     stall_bytes = 0;
-                    uint8_t *sa = smem + stage * kStageBytes;
+                    uint8_t *sa = smem + stage * SB;
                     const int k0 = kb * BK;
 #pragma unroll
                     for (int t = 0; t < 2; ++t) {
                         const CUtensorMap *m = (GATED && t == 1) ? &map_a1 : &map_a0;
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int f0 = tile_base(m0, t) + 64 * h;
-                            if (f0 < p.M)
-                                tma_load_3d(sa + t * kATileBytes + h * kABoxBytes, m, fb, f0, k0,
+                        if (W8) {
+                            if (tile_base(m0, t) < p.M)
+                                tma_load_3d(sa + t * kA8TileBytes, m, fb, tile_base(m0, t), k0,
                                             w.e);
+                        } else {
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const int f0 = tile_base(m0, t) + 64 * h;
+                                if (f0 < p.M)
+                                    tma_load_3d(sa + t * kATileBytes + h * kABoxBytes, m, fb, f0,
+                                                k0, w.e);
+                            }
                         }
                     }
-                    uint8_t *sb = sa + 2 * kATileBytes;
+                    uint8_t *sb = sa + (W8 ? 2 * kA8TileBytes : 2 * kATileBytes);
                     if (GATHER) {
                         for (int j = 0; j < w.nrows; j += 4)
                             tma_gather4(sb + j * (BK * 2), &map_b, fb, k0, row_tok[j],
@@ -348,8 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ---- MMA issuer ----
         if (lane == 0) {
-            int stage = 0, abuf = 0;
-            uint32_t phase = 0, aphase = 0;
+            int stage = 0, abuf = 0, cslot = 0;
+            uint32_t phase = 0, aphase = 0, cphase = 0;
             bool ok = true;
             for (int64_t u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
                 const Unit w = map_unit(u, n_mt, chunk_start, p.E, p.offsets);
@@ -363,13 +436,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d0 = tmem_base + uint32_t(abuf) * kAccCols;
                 const uint32_t idesc = idesc_bf16_f32(BM, uint32_t(w.nrows), 1u, 0u);
                 for (int kb = 0; kb < nk; ++kb) {
-                    if (!mbar_wait(&ctl->full[stage], phase, abort_flag)) {
+                    if (!mbar_wait(&ctl->full[stage], phase, abort_flag) ||
+                        (W8 && !mbar_wait(&ctl->conv_full[cslot], cphase, abort_flag))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t sa = smem_u32(smem + stage * kStageBytes);
-                    const uint32_t sb = sa + 2 * kATileBytes;
+                    const uint32_t sst = smem_u32(smem + stage * SB);
+                    const uint32_t sa = W8 ? smem_u32(conv + cslot * kConvSlotBytes) : sst;
+                    const uint32_t sb = sst + (W8 ? 2 * kA8TileBytes : 2 * kATileBytes);
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                         // B: K-major rows of 128 B; the K step moves 32 B inside the row.
@@ -389,6 +464,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         stage = 0;
                         phase ^= 1u;
                     }
+                    if (W8) {
+                        tc_commit(&ctl->conv_empty[cslot]);
+                        if (++cslot == kConvSlots) {
+                            cslot = 0;
+                            cphase ^= 1u;
+                        }
+                    }
                 }
                 if (!ok)
                     break;
@@ -402,6 +484,64 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_drain(&ctl->mma_done, 0);
         }
         __syncwarp();
+    } else if (W8 && warp >= kThreads / 32) {
+        // ---- widening (W8): E4M3 A tiles of a stage -> bf16 tiles of a slot ----
+        const int ct = int(threadIdx.x) - kThreads;  // 0..kConvThreads-1
+        int stage = 0, cslot = 0;
+        uint32_t phase = 0, cphase = 0;
+        bool ok = true;
+        for (int64_t u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+            const Unit w = map_unit(u, n_mt, chunk_start, p.E, p.offsets);
+            const int nt = 1 + int(tile_base(w.mt * UM, 1) < p.M);  // A tiles loaded
+            for (int kb = 0; kb < nk; ++kb) {
+                if (!mbar_wait(&ctl->full[stage], phase, abort_flag) ||
+                    !mbar_wait(&ctl->conv_empty[cslot], cphase ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *src = smem + stage * SB;
+                uint8_t *dst = conv + cslot * kConvSlotBytes;
+                // a tile is 64 K rows x 8 chunks of 16 codes.  Chunk c of row
+                // r (features 16c..16c+15)
+                // becomes the 16-byte chunks 2(c&3) and 2(c&3)+1 of row r of
+                // 64-feature box c>>2, each placed at its index XOR (r mod 8),
+                // the 128-byte swizzle a TMA load of the bf16 box would apply.
+                // all of a thread's loads first, then the widening and stores:
+                // kPer independent chains instead of one after another
+                constexpr int kPer = 2 * 512 / kConvThreads;
+                uint4 v[kPer];
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) {
+                    const int g = ct + i * kConvThreads;
+                    if (g < 512 * nt)
+                        v[i] = *reinterpret_cast<const uint4 *>(src + (g >> 9) * kA8TileBytes +
+                                                                ((g >> 3) & 63) * 128 + (g & 7) * 16);
+                }
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) {
+                    const int g = ct + i * kConvThreads;
+                    if (g < 512 * nt) {
+                        const int t = g >> 9, r = (g >> 3) & 63, c = g & 7;
+                        uint4 lo, hi;
+                        widen_e4m3x16(v[i], lo, hi);
+                        uint8_t *row = dst + t * kATileBytes + (c >> 2) * kABoxBytes + r * 128;
+                        const int j0 = 2 * (c & 3);
+                        *reinterpret_cast<uint4 *>(row + ((j0 ^ (r & 7)) << 4)) = lo;
+                        *reinterpret_cast<uint4 *>(row + (((j0 + 1) ^ (r & 7)) << 4)) = hi;
+                    }
+                }
+                fence_proxy_async_smem();  // the widened tiles -> visible to the MMAs
+                mbar_arrive(&ctl->conv_full[cslot]);
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                if (++cslot == kConvSlots) {
+                    cslot = 0;
+                    cphase ^= 1u;
+                }
+            }
+        }
     } else {
         // ---- epilogue: TMEM -> registers -> shared (16 rows) -> TMA store ----
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
@@ -413,6 +553,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Unit w = map_unit(u, n_mt, chunk_start, p.E, p.offsets);
             const int m0 = w.mt * UM;
             const bool use1 = tile_base(m0, 1) < p.M;
+            // W8: the scales of this thread's output feature in both A tiles
+            float sc0 = 1.0f, sc1 = 1.0f;
+            if (W8) {
+                const int64_t eb = int64_t(w.e) * p.M;
+                const int fa = tile_base(m0, 0) + fq, fb = tile_base(m0, 1) + fq;
+                sc0 = fa < p.M ? p.scale0[eb + fa] : 0.0f;
+                sc1 = fb < p.M ? p.scale1[eb + fb] : 0.0f;
+            }
             // The four warps stop together or not at all: they meet at named
             // barriers below.  epi_stop is written before this barrier and read
             // after it; the next write can only come after the unit's chunk
@@ -438,15 +586,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (GATED) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const float g = __uint_as_float(a[j]);
-                        v0[j] = __fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(b[j]);
+                        const float g = W8 ? __uint_as_float(a[j]) * sc0 : __uint_as_float(a[j]);
+                        const float up = W8 ? __uint_as_float(b[j]) * sc1 : __uint_as_float(b[j]);
+                        v0[j] = __fdividef(g, 1.0f + __expf(-g)) * up;
                     }
                 } else {
                     const float *wr = row_w + c0;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        v0[j] = wr[j] * __uint_as_float(a[j]);
-                        v1[j] = use1 ? wr[j] * __uint_as_float(b[j]) : 0.0f;
+                        const float o0 = W8 ? __uint_as_float(a[j]) * sc0 : __uint_as_float(a[j]);
+                        const float o1 = W8 ? __uint_as_float(b[j]) * sc1 : __uint_as_float(b[j]);
+                        v0[j] = wr[j] * o0;
+                        v1[j] = use1 ? wr[j] * o1 : 0.0f;
                     }
                 }
                 // the bulk store that last read this staging buffer (two chunks
@@ -506,15 +657,18 @@ cudaError_t get_encoder()
     return g_encode ? cudaSuccess : cudaErrorNotSupported;
 }
 
-// bf16 tensor map (128-byte swizzle unless `plain`); dims innermost first.
+// bf16 (or, with `u8`, byte) tensor map, 128-byte swizzle unless `plain`;
+// dims innermost first.
 cudaError_t encode_bf16(CUtensorMap *m, const void *base, uint32_t rank, const cuuint64_t *dims,
-                        const cuuint64_t *strides_bytes, const cuuint32_t *box, bool plain = false)
+                        const cuuint64_t *strides_bytes, const cuuint32_t *box, bool plain = false,
+                        bool u8 = false)
 {
     cudaError_t err = get_encoder();
     if (err != cudaSuccess)
         return err;
     const cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base),
+    const CUresult r = g_encode(m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                rank, const_cast<void *>(base),
                                 dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                 plain ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -529,6 +683,16 @@ cudaError_t weight_map(CUtensorMap *m, const void *W, int E, int K, int M)
     const cuuint64_t strides[2] = {cuuint64_t(M) * 2, cuuint64_t(M) * K * 2};
     const cuuint32_t box[3] = {64, BK, 1};
     return encode_bf16(m, W, 3, dims, strides, box);
+}
+
+// E4M3 weight codes [E, K, M] (M contiguous): unswizzled boxes of 128
+// features x 64 K rows of one expert (rows of 128 bytes).
+cudaError_t weight_map_e4m3(CUtensorMap *m, const void *Wq, int E, int K, int M)
+{
+    const cuuint64_t dims[3] = {cuuint64_t(M), cuuint64_t(K), cuuint64_t(E)};
+    const cuuint64_t strides[2] = {cuuint64_t(M), cuuint64_t(M) * K};
+    const cuuint32_t box[3] = {BM, BK, 1};
+    return encode_bf16(m, Wq, 3, dims, strides, box, true, true);
 }
 
 // Rows [cap, K] (K contiguous): boxes of 16 rows x 64 K.
@@ -572,14 +736,15 @@ cudaError_t launch_ffn_gate_up(const void *xs, const void *Wg, const void *Wu,
         (err = rows_map(&mx, xs, cap, d)) != cudaSuccess ||
         (err = out_map(&mo, H, cap, f, Kind<true>::kUnitM)) != cudaSuccess)
         return err;
-    err = ensure_smem_limit(reinterpret_cast<const void *>(k_ffn<true, false>), kSlotGateUp,
-                            ffn_smem_bytes(MOE_MAX_EXPERTS));
+    auto kern = k_ffn<true, false, false>;
+    err = ensure_smem_limit(reinterpret_cast<const void *>(kern), kSlotGateUp,
+                            ffn_smem_bytes<false>(MOE_MAX_EXPERTS));
     if (err != cudaSuccess)
         return err;
     const FfnArgs a{offsets, nullptr, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f,
-                    stall_cta};
-    return launch_pdl(k_ffn<true, false>, dim3(device_sm_count()), dim3(kThreads),
-                      ffn_smem_bytes(E), stream, mg, mu, mx, mo, a);
+                    stall_cta, nullptr, nullptr};
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<false>(E),
+                      stream, mg, mu, mx, mo, a);
 }
 
 cudaError_t launch_ffn_gate_up_rows(const void *x, int T, const int32_t *srt_tok, const void *Wg,
@@ -593,13 +758,15 @@ cudaError_t launch_ffn_gate_up_rows(const void *x, int T, const int32_t *srt_tok
         (err = token_rows_map(&mx, x, T, d)) != cudaSuccess ||
         (err = out_map(&mo, H, cap, f, Kind<true>::kUnitM)) != cudaSuccess)
         return err;
-    err = ensure_smem_limit(reinterpret_cast<const void *>(k_ffn<true, true>), kSlotGateUpRows,
-                            ffn_smem_bytes(MOE_MAX_EXPERTS));
+    auto kern = k_ffn<true, true, false>;
+    err = ensure_smem_limit(reinterpret_cast<const void *>(kern), kSlotGateUpRows,
+                            ffn_smem_bytes<false>(MOE_MAX_EXPERTS));
     if (err != cudaSuccess)
         return err;
-    const FfnArgs a{offsets, srt_tok, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f, -1};
-    return launch_pdl(k_ffn<true, true>, dim3(device_sm_count()), dim3(kThreads),
-                      ffn_smem_bytes(E), stream, mg, mu, mx, mo, a);
+    const FfnArgs a{offsets, srt_tok, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f,
+                    -1, nullptr, nullptr};
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<false>(E),
+                      stream, mg, mu, mx, mo, a);
 }
 
 cudaError_t launch_ffn_down(const void *H, const void *Wd, const int32_t *offsets,
@@ -612,13 +779,59 @@ cudaError_t launch_ffn_down(const void *H, const void *Wd, const int32_t *offset
         (err = rows_map(&mh, H, cap, f)) != cudaSuccess ||
         (err = out_map(&mo, Ys, cap, d, Kind<false>::kUnitM)) != cudaSuccess)
         return err;
-    err = ensure_smem_limit(reinterpret_cast<const void *>(k_ffn<false, false>), kSlotDown,
-                            ffn_smem_bytes(MOE_MAX_EXPERTS));
+    auto kern = k_ffn<false, false, false>;
+    err = ensure_smem_limit(reinterpret_cast<const void *>(kern), kSlotDown,
+                            ffn_smem_bytes<false>(MOE_MAX_EXPERTS));
     if (err != cudaSuccess)
         return err;
-    const FfnArgs a{offsets, nullptr, srt_w, static_cast<uint16_t *>(Ys), status, cap, E, f, d, -1};
-    return launch_pdl(k_ffn<false, false>, dim3(device_sm_count()), dim3(kThreads),
-                      ffn_smem_bytes(E), stream, mw, mw, mh, mo, a);
+    const FfnArgs a{offsets, nullptr, srt_w, static_cast<uint16_t *>(Ys), status, cap, E, f, d,
+                    -1, nullptr, nullptr};
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<false>(E),
+                      stream, mw, mw, mh, mo, a);
+}
+
+cudaError_t launch_ffn_gate_up_e4m3(const void *xs, const uint8_t *Wg, const float *sg,
+                                    const uint8_t *Wu, const float *su, const int32_t *offsets,
+                                    int E, int d, int f, int64_t cap, void *H, uint32_t *status,
+                                    cudaStream_t stream)
+{
+    CUtensorMap mg, mu, mx, mo;
+    cudaError_t err;
+    if ((err = weight_map_e4m3(&mg, Wg, E, d, f)) != cudaSuccess ||
+        (err = weight_map_e4m3(&mu, Wu, E, d, f)) != cudaSuccess ||
+        (err = rows_map(&mx, xs, cap, d)) != cudaSuccess ||
+        (err = out_map(&mo, H, cap, f, Kind<true>::kUnitM)) != cudaSuccess)
+        return err;
+    auto kern = k_ffn<true, false, true>;
+    err = ensure_smem_limit(reinterpret_cast<const void *>(kern), kSlotGateUpE4m3,
+                            ffn_smem_bytes<true>(MOE_MAX_EXPERTS));
+    if (err != cudaSuccess)
+        return err;
+    const FfnArgs a{offsets, nullptr, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f,
+                    -1, sg, su};
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreadsW8), ffn_smem_bytes<true>(E),
+                      stream, mg, mu, mx, mo, a);
+}
+
+cudaError_t launch_ffn_down_e4m3(const void *H, const uint8_t *Wd, const float *sd,
+                                 const int32_t *offsets, const float *srt_w, int E, int d, int f,
+                                 int64_t cap, void *Ys, uint32_t *status, cudaStream_t stream)
+{
+    CUtensorMap mw, mh, mo;
+    cudaError_t err;
+    if ((err = weight_map_e4m3(&mw, Wd, E, f, d)) != cudaSuccess ||
+        (err = rows_map(&mh, H, cap, f)) != cudaSuccess ||
+        (err = out_map(&mo, Ys, cap, d, Kind<false>::kUnitM)) != cudaSuccess)
+        return err;
+    auto kern = k_ffn<false, false, true>;
+    err = ensure_smem_limit(reinterpret_cast<const void *>(kern), kSlotDownE4m3,
+                            ffn_smem_bytes<true>(MOE_MAX_EXPERTS));
+    if (err != cudaSuccess)
+        return err;
+    const FfnArgs a{offsets, nullptr, srt_w, static_cast<uint16_t *>(Ys), status, cap, E, f, d,
+                    -1, sd, sd};
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreadsW8), ffn_smem_bytes<true>(E),
+                      stream, mw, mw, mh, mo, a);
 }
 
 }  // namespace moe

@@ -68,6 +68,17 @@ cudaError_t launch_ffn_down(const void *H, const void *Wd, const int32_t *offset
                             const float *srt_w, int E, int d, int f, int64_t cap, void *Ys,
                             uint32_t *status, cudaStream_t stream);
 
+// E4M3 weights (codes [E, K, M]) with fp32 scales [E, M]; see quant.cu.
+cudaError_t launch_quantize_e4m3(const void *W, int E, int K, int M, uint8_t *q, float *scale,
+                                 cudaStream_t stream);
+cudaError_t launch_ffn_gate_up_e4m3(const void *xs, const uint8_t *Wg, const float *sg,
+                                    const uint8_t *Wu, const float *su, const int32_t *offsets,
+                                    int E, int d, int f, int64_t cap, void *H, uint32_t *status,
+                                    cudaStream_t stream);
+cudaError_t launch_ffn_down_e4m3(const void *H, const uint8_t *Wd, const float *sd,
+                                 const int32_t *offsets, const float *srt_w, int E, int d, int f,
+                                 int64_t cap, void *Ys, uint32_t *status, cudaStream_t stream);
+
 // ---- launch helpers (api.cu) -------------------------------------------------
 
 // Streaming multiprocessors of the current device (cached per device).
@@ -97,6 +108,15 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // Slots of ensure_smem_limit's per-device cache.
-enum SmemSlot { kSlotPlace = 0, kSlotHist, kSlotGateUp, kSlotGateUpRows, kSlotDown, kSlotCount };
+enum SmemSlot {
+    kSlotPlace = 0,
+    kSlotHist,
+    kSlotGateUp,
+    kSlotGateUpRows,
+    kSlotDown,
+    kSlotGateUpE4m3,
+    kSlotDownE4m3,
+    kSlotCount
+};
 
 }  // namespace moe

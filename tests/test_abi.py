@@ -129,15 +129,15 @@ def test_prefill_host_workspace(lib):
 def prefill_host_call(lib, n=2, ptrs=None, **kw):
     # host pointer arrays of stand-in addresses: only checked for NULL here
     arr = (C.c_void_p * max(n, 1))(*([FAKE] * max(n, 1)))
-    a = dict(x=arr, ids=arr, w=arr, y=arr, Wg=FAKE, Wu=FAKE, Wd=FAKE, T=8, d=64, E=4, k=2,
-             f=64, tm=16, ws=FAKE, ws_bytes=1 << 30)
+    a = dict(x=arr, ids=arr, w=arr, y=arr, Wg=FAKE, Wu=FAKE, Wd=FAKE, sg=None, su=None, sd=None,
+             T=8, d=64, E=4, k=2, f=64, tm=16, ws=FAKE, ws_bytes=1 << 30)
     a.update(ptrs or {})
     a.update(kw)
     cast = lambda v: C.cast(v, C.c_void_p) if isinstance(v, C.Array) else v
     return lib.moe_prefill_forward_host(n, cast(a["x"]), cast(a["ids"]), cast(a["w"]),
-                                        cast(a["y"]), a["Wg"], a["Wu"], a["Wd"], a["T"], a["d"],
-                                        a["E"], a["k"], a["f"], a["tm"], a["ws"], a["ws_bytes"],
-                                        None)
+                                        cast(a["y"]), a["Wg"], a["Wu"], a["Wd"], a["sg"],
+                                        a["su"], a["sd"], a["T"], a["d"], a["E"], a["k"], a["f"],
+                                        a["tm"], a["ws"], a["ws_bytes"], None)
 
 
 def test_prefill_host_argument_errors(lib):
@@ -152,9 +152,47 @@ def test_prefill_host_argument_errors(lib):
     assert prefill_host_call(lib, ws_bytes=1024) == B.MOE_ERR_WORKSPACE
     assert prefill_host_call(lib, ws=FAKE + 128) == B.MOE_ERR_ALIGN
     assert prefill_host_call(lib, Wg=FAKE + 8) == B.MOE_ERR_ALIGN
+    assert prefill_host_call(lib, sg=FAKE) == B.MOE_ERR_NULL      # E4M3 needs all three scales
     # nothing to do: returns before any CUDA call
     assert prefill_host_call(lib, n=0) == B.MOE_OK
     assert prefill_host_call(lib, T=0) == B.MOE_OK
+
+
+def test_e4m3_argument_errors(lib):
+    q = lib.moe_quantize_e4m3
+    assert q(FAKE, 0, 8, 64, FAKE, FAKE, None) == B.MOE_ERR_SHAPE
+    assert q(FAKE, 4, 0, 64, FAKE, FAKE, None) == B.MOE_ERR_SHAPE
+    assert q(None, 4, 8, 64, FAKE, FAKE, None) == B.MOE_ERR_NULL
+    assert q(FAKE, 4, 8, 64, FAKE, FAKE + 2, None) == B.MOE_ERR_ALIGN
+    gu = lib.moe_ffn_gate_up_e4m3
+    assert gu(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 96, 64, 100, FAKE, None, None) == B.MOE_ERR_SHAPE
+    assert gu(FAKE, FAKE, None, FAKE, FAKE, FAKE, 4, 64, 64, 100, FAKE, None, None) == B.MOE_ERR_NULL
+    assert gu(FAKE, FAKE + 8, FAKE, FAKE, FAKE, FAKE, 4, 64, 64, 100, FAKE, None, None) == B.MOE_ERR_ALIGN
+    assert gu(FAKE, FAKE, FAKE + 2, FAKE, FAKE, FAKE, 4, 64, 64, 100, FAKE, None, None) == B.MOE_ERR_ALIGN
+    assert gu(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 64, 0, FAKE, None, None) == B.MOE_OK
+    dn = lib.moe_ffn_down_e4m3
+    assert dn(FAKE, FAKE, None, FAKE, FAKE, 4, 64, 64, 100, FAKE, None, None) == B.MOE_ERR_NULL
+    assert dn(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 64, 0, FAKE, None, None) == B.MOE_OK
+    lf = lib.moe_layer_forward_e4m3
+    ws = 1 << 40
+    args = [FAKE] * 9 + [8, 64, 4, 2, 64, 16, FAKE, FAKE, ws, None]
+    bad = list(args); bad[4] = None                                    # su missing
+    assert lf(*bad) == B.MOE_ERR_NULL
+    bad = list(args); bad[1 + 1] = FAKE + 2                             # w misaligned
+    assert lf(*bad) == B.MOE_ERR_ALIGN
+    bad = list(args); bad[14] = 8                                       # tm
+    assert lf(*bad) == B.MOE_ERR_SHAPE
+
+
+def test_moe_layer_holds_either_weight_form():
+    import torch
+    t = lambda *shape: torch.empty(*shape, dtype=torch.bfloat16)
+    L = B.MoeLayer(t(2, 64, 128), t(2, 64, 128), t(2, 128, 64))
+    assert (L.E, L.d, L.f, L.e4m3) == (2, 64, 128, False) and L._ws is None
+    q = lambda *shape: (torch.empty(*shape, dtype=torch.uint8),
+                        torch.empty(shape[0], shape[2], dtype=torch.float32))
+    L8 = B.MoeLayer(q(2, 64, 128), q(2, 64, 128), q(2, 128, 64))
+    assert (L8.E, L8.d, L8.f, L8.e4m3) == (2, 64, 128, True) and L8._host_ws is None
 
 
 def test_status_strings(lib):
