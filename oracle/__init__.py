@@ -94,11 +94,14 @@ def _load():
             lib.oracle_layer_tokens_e4m3.restype = C.c_int
             lib.oracle_layer_tokens_e4m3.argtypes = [P, C.c_int, P, P, P, P, P, P, P, P,
                                                      C.c_int, C.c_int, C.c_int, C.c_int,
-                                                     C.c_int, P, C.c_int, C.c_int, C.c_int, P]
+                                                     C.c_int, P, C.c_int, C.c_int, C.c_int,
+                                                     C.c_int, P]
             lib.oracle_expert_rows_e4m3.restype = C.c_int
             lib.oracle_expert_rows_e4m3.argtypes = [P, C.c_int, C.c_int, C.c_int, P, C.c_int,
                                                     P, P, C.c_int, P, P, P, P, P, P, C.c_int,
-                                                    C.c_int, P, P]
+                                                    C.c_int, C.c_int, P, P]
+            lib.oracle_quantize_rows_e4m3.restype = None
+            lib.oracle_quantize_rows_e4m3.argtypes = [P, C.c_long, C.c_int, P, P]
             _lib = lib
     return _lib
 
@@ -179,10 +182,12 @@ def _weights(Wg, Wu, Wd):
 
 
 def layer(x, ids, w, Wg, Wu, Wd, x_dtype: str = "bf16", tokens=None,
-          mirror: bool = False, nthreads: int | None = None) -> np.ndarray:
+          mirror: bool = False, nthreads: int | None = None, act_e4m3: bool = False) -> np.ndarray:
     """Layer output y (fp64 [len(tokens), d]) for the listed tokens (all by
     default).  ``mirror`` returns the bf16-mirror reference instead.  The
-    weights are bf16 bit arrays or, all three, (E4M3 codes, scales) pairs."""
+    weights are bf16 bit arrays or, all three, (E4M3 codes, scales) pairs;
+    with E4M3 weights, ``act_e4m3`` gives gate/up the rows' E4M3 values
+    (``quantize_rows_e4m3``)."""
     x = _c(x, np.uint16)
     ids = _c(ids, np.int32)
     w = _c(w, np.float32)
@@ -196,16 +201,23 @@ def layer(x, ids, w, Wg, Wu, Wd, x_dtype: str = "bf16", tokens=None,
     y = np.zeros((max(len(tokens), 1), d), np.float64)
     if nthreads is None:
         nthreads = os.cpu_count() or 1
-    fn = _load().oracle_layer_tokens_e4m3 if q8 else _load().oracle_layer_tokens
-    rc = fn(_p(x), int(x_dtype == "f16"), _p(ids), _p(w), *[_p(a) for a in warrs],
-            T, d, E, k, f, _p(tokens), len(tokens), int(bool(mirror)), int(nthreads), _p(y))
+    assert q8 or not act_e4m3, "E4M3 activations come with E4M3 weights"
+    if q8:
+        rc = _load().oracle_layer_tokens_e4m3(
+            _p(x), int(x_dtype == "f16"), _p(ids), _p(w), *[_p(a) for a in warrs], T, d, E, k,
+            f, _p(tokens), len(tokens), int(bool(mirror)), int(bool(act_e4m3)), int(nthreads),
+            _p(y))
+    else:
+        rc = _load().oracle_layer_tokens(
+            _p(x), int(x_dtype == "f16"), _p(ids), _p(w), *[_p(a) for a in warrs], T, d, E, k,
+            f, _p(tokens), len(tokens), int(bool(mirror)), int(nthreads), _p(y))
     if rc != 0:
         raise OracleError(_ERR.get(rc, str(rc)))
     return y[:len(tokens)]
 
 
 def expert_rows(xs, rows, row_expert, row_w, Wg, Wu, Wd, x_dtype: str = "bf16",
-                mirror: bool = False, nthreads: int | None = None):
+                mirror: bool = False, nthreads: int | None = None, act_e4m3: bool = False):
     """For the listed rows of xs: h (fp64 [n, f]) and the weighted down
     projection ys = w * o (fp64 [n, d])."""
     xs = _c(xs, np.uint16)
@@ -219,8 +231,15 @@ def expert_rows(xs, rows, row_expert, row_w, Wg, Wu, Wd, x_dtype: str = "bf16",
     ys = np.zeros((max(n, 1), d), np.float64)
     if nthreads is None:
         nthreads = os.cpu_count() or 1
-    fn = _load().oracle_expert_rows_e4m3 if q8 else _load().oracle_expert_rows
-    rc = fn(_p(xs), int(x_dtype == "f16"), d, f, _p(rows), n, _p(row_expert), _p(row_w), E,
+    assert q8 or not act_e4m3, "E4M3 activations come with E4M3 weights"
+    if q8:
+        rc = _load().oracle_expert_rows_e4m3(
+            _p(xs), int(x_dtype == "f16"), d, f, _p(rows), n, _p(row_expert), _p(row_w), E,
+            *[_p(a) for a in warrs], int(bool(mirror)), int(bool(act_e4m3)), int(nthreads),
+            _p(h), _p(ys))
+    else:
+        rc = _load().oracle_expert_rows(
+            _p(xs), int(x_dtype == "f16"), d, f, _p(rows), n, _p(row_expert), _p(row_w), E,
             *[_p(a) for a in warrs], int(bool(mirror)), int(nthreads), _p(h), _p(ys))
     if rc != 0:
         raise OracleError(_ERR.get(rc, str(rc)))
@@ -273,3 +292,16 @@ def dequantize_e4m3(q, s) -> np.ndarray:
     table = np.array([e4m3_value(c) for c in range(256)], np.float64)
     q = np.asarray(q, np.uint8)
     return table[q] * np.asarray(s, np.float64)[:, None, :]
+
+
+def quantize_rows_e4m3(x):
+    """bf16 rows x [R, d] -> (E4M3 codes [R, d], exponents e [R]): each row
+    scaled by 2^-e, e the smallest integer with max|x| <= 448 * 2^e (0 for a
+    zero row), codes the nearest E4M3 values.  value(code) * 2^e is the row
+    gate/up sees with E4M3 activations."""
+    x = _c(x, np.uint16)
+    R, d = x.shape
+    q = np.empty((max(R, 1), d), np.uint8)
+    e = np.empty(max(R, 1), np.int32)
+    _load().oracle_quantize_rows_e4m3(_p(x), R, d, _p(q), _p(e))
+    return q[:R], e[:R]

@@ -170,6 +170,54 @@ void oracle_quantize_e4m3(const uint16_t *W, int E, int K, int M, uint8_t *q, fl
     }
 }
 
+/*
+ * E4M3 activations: one row x[0..d-1] (exact bf16 values) with a power-of-
+ * two scale 2^e, e the smallest integer with max |x| <= 448 * 2^e (e = 0
+ * for an all-zero row); codes are e4m3_encode(x * 2^-e), exact scaling.
+ * Writes the codes (if q) and returns e.
+ */
+static int quantize_row_e4m3(const double *x, int d, uint8_t *q)
+{
+    double amax = 0.0;
+    int c, e = 0;
+    for (c = 0; c < d; c++)
+        if (fabs(x[c]) > amax)
+            amax = fabs(x[c]);
+    if (amax > 0.0) {
+        e = ilogb(amax) - 8;             /* amax in [2^(e+8), 2^(e+9)) */
+        if (amax > ldexp(448.0, e))
+            e++;
+    }
+    if (q)
+        for (c = 0; c < d; c++)
+            q[c] = e4m3_encode((float)ldexp(x[c], -e));
+    return e;
+}
+
+/* The row replaced by its dequantized values value(code) * 2^e. */
+static void dequantize_row_e4m3(double *x, int d)
+{
+    int c, e = quantize_row_e4m3(x, d, NULL);
+    for (c = 0; c < d; c++)
+        x[c] = ldexp(e4m3_value(e4m3_encode((float)ldexp(x[c], -e))), e);
+}
+
+/* Rows of a bf16 matrix x [R][d]: codes [R][d] and exponents e [R]. */
+void oracle_quantize_rows_e4m3(const uint16_t *x, long R, int d, uint8_t *q, int32_t *e)
+{
+    long r;
+    int c;
+    double *row = (double *)malloc(sizeof(double) * (size_t)(d > 0 ? d : 1));
+    if (!row)
+        return;
+    for (r = 0; r < R; r++) {
+        for (c = 0; c < d; c++)
+            row[c] = bf16_value(x[r * (long)d + c]);
+        e[r] = quantize_row_e4m3(row, d, q + r * (long)d);
+    }
+    free(row);
+}
+
 /* ---- routing plan [P1 sec. 1 items 1-2, sec. 3; P4 Mechanism] ---------- */
 
 /*
@@ -306,12 +354,14 @@ static double wval(const wmat_t *W, long e, long r, long c)
 
 static void expert_job(const uint16_t *xrow, int x_is_f16, const wmat_t *Wg,
                        const wmat_t *Wu, const wmat_t *Wd, long e, int d, int f,
-                       int mirror, double *xv, double *g, double *u, double *h,
+                       int mirror, int a8, double *xv, double *g, double *u, double *h,
                        double *o)
 {
     int c, n, m;
     for (c = 0; c < d; c++)
         xv[c] = value16(xrow[c], x_is_f16);
+    if (a8) /* gate/up sees the row's E4M3 values (quantize_row_e4m3) */
+        dequantize_row_e4m3(xv, d);
     for (n = 0; n < f; n++) {
         g[n] = 0.0;
         u[n] = 0.0;
@@ -346,7 +396,7 @@ typedef struct {
     const job_t *jobs;
     long njobs;
     int tid, nthreads;
-    int x_is_f16, d, f, mirror;
+    int x_is_f16, d, f, mirror, a8;
     const wmat_t *Wg, *Wu, *Wd;
     int failed;
 } pass_t;
@@ -369,7 +419,7 @@ static void *pass_worker(void *arg)
     for (j = p->tid; j < p->njobs; j += p->nthreads) {
         const job_t *jb = &p->jobs[j];
         expert_job(jb->xrow, p->x_is_f16, p->Wg, p->Wu, p->Wd, jb->e, p->d, p->f,
-                   p->mirror, xv, g, u, jb->h ? jb->h : hbuf, jb->o);
+                   p->mirror, p->a8, xv, g, u, jb->h ? jb->h : hbuf, jb->o);
     }
     free(xv);
     return NULL;
@@ -377,7 +427,7 @@ static void *pass_worker(void *arg)
 
 /* Run the flat parallel pass over a job list on nthreads host threads. */
 static int run_pass(const job_t *jobs, long njobs, int x_is_f16, int d, int f,
-                    int mirror, const wmat_t *Wg, const wmat_t *Wu,
+                    int mirror, int a8, const wmat_t *Wg, const wmat_t *Wu,
                     const wmat_t *Wd, int nthreads)
 {
     pthread_t th[256];
@@ -399,6 +449,7 @@ static int run_pass(const job_t *jobs, long njobs, int x_is_f16, int d, int f,
         ps[t].d = d;
         ps[t].f = f;
         ps[t].mirror = mirror;
+        ps[t].a8 = a8;
         ps[t].Wg = Wg;
         ps[t].Wu = Wu;
         ps[t].Wd = Wd;
@@ -435,7 +486,7 @@ static int run_pass(const job_t *jobs, long njobs, int x_is_f16, int d, int f,
 static int layer_tokens(const uint16_t *x, int x_is_f16, const int32_t *ids,
                         const float *w, const wmat_t *Wg, const wmat_t *Wu,
                         const wmat_t *Wd, int T, int d, int E, int k, int f,
-                        const int32_t *tokens, int ntok, int mirror, int nthreads,
+                        const int32_t *tokens, int ntok, int mirror, int a8, int nthreads,
                         double *y)
 {
     long ti, j, nj = 0, m;
@@ -487,7 +538,7 @@ static int layer_tokens(const uint16_t *x, int x_is_f16, const int32_t *ids,
     }
 
     /* one flat pass over all jobs */
-    rc = run_pass(jobs, nj, x_is_f16, d, f, mirror, Wg, Wu, Wd, nthreads);
+    rc = run_pass(jobs, nj, x_is_f16, d, f, mirror, a8, Wg, Wu, Wd, nthreads);
 
     /* per-token combine in slot order */
     if (rc == ORC_OK) {
@@ -546,21 +597,22 @@ int oracle_layer_tokens(const uint16_t *x, int x_is_f16, const int32_t *ids,
 {
     wmat_t g = bf16_mat(Wg, d, f), u = bf16_mat(Wu, d, f), dn = bf16_mat(Wd, f, d);
     return layer_tokens(x, x_is_f16, ids, w, &g, &u, &dn, T, d, E, k, f, tokens, ntok,
-                        mirror, nthreads, y);
+                        mirror, 0, nthreads, y);
 }
 
 /* The same layer with E4M3 weights: Wg, Wu codes [E][d][f] with scales
- * [E][f], Wd codes [E][f][d] with scales [E][d]. */
+ * [E][f], Wd codes [E][f][d] with scales [E][d].  a8 != 0 also gives the
+ * gate/up projections each row's E4M3 values (quantize_row_e4m3). */
 int oracle_layer_tokens_e4m3(const uint16_t *x, int x_is_f16, const int32_t *ids,
                              const float *w, const uint8_t *Wg, const float *sg,
                              const uint8_t *Wu, const float *su, const uint8_t *Wd,
                              const float *sd, int T, int d, int E, int k, int f,
-                             const int32_t *tokens, int ntok, int mirror, int nthreads,
-                             double *y)
+                             const int32_t *tokens, int ntok, int mirror, int a8,
+                             int nthreads, double *y)
 {
     wmat_t g = e4m3_mat(Wg, sg, d, f), u = e4m3_mat(Wu, su, d, f), dn = e4m3_mat(Wd, sd, f, d);
     return layer_tokens(x, x_is_f16, ids, w, &g, &u, &dn, T, d, E, k, f, tokens, ntok,
-                        mirror, nthreads, y);
+                        mirror, a8, nthreads, y);
 }
 
 /* ---- stage-level views used to check one GPU stage at a time ------------ */
@@ -574,7 +626,7 @@ int oracle_layer_tokens_e4m3(const uint16_t *x, int x_is_f16, const int32_t *ids
 static int expert_rows(const uint16_t *xs, int x_is_f16, int d, int f,
                        const int64_t *rows, int nrows, const int32_t *row_expert,
                        const float *row_w, int E, const wmat_t *Wg,
-                       const wmat_t *Wu, const wmat_t *Wd, int mirror,
+                       const wmat_t *Wu, const wmat_t *Wd, int mirror, int a8,
                        int nthreads, double *h_out, double *ys_out)
 {
     long i, m;
@@ -592,7 +644,7 @@ static int expert_rows(const uint16_t *xs, int x_is_f16, int d, int f,
         jobs[i].h = h_out + i * (long)f;
         jobs[i].o = ys_out + i * (long)d;
     }
-    rc = run_pass(jobs, nrows, x_is_f16, d, f, mirror, Wg, Wu, Wd, nthreads);
+    rc = run_pass(jobs, nrows, x_is_f16, d, f, mirror, a8, Wg, Wu, Wd, nthreads);
     if (rc == ORC_OK) {
         for (i = 0; i < nrows; i++)
             for (m = 0; m < d; m++)
@@ -610,19 +662,19 @@ int oracle_expert_rows(const uint16_t *xs, int x_is_f16, int d, int f,
 {
     wmat_t g = bf16_mat(Wg, d, f), u = bf16_mat(Wu, d, f), dn = bf16_mat(Wd, f, d);
     return expert_rows(xs, x_is_f16, d, f, rows, nrows, row_expert, row_w, E, &g, &u, &dn,
-                       mirror, nthreads, h_out, ys_out);
+                       mirror, 0, nthreads, h_out, ys_out);
 }
 
 int oracle_expert_rows_e4m3(const uint16_t *xs, int x_is_f16, int d, int f,
                             const int64_t *rows, int nrows, const int32_t *row_expert,
                             const float *row_w, int E, const uint8_t *Wg, const float *sg,
                             const uint8_t *Wu, const float *su, const uint8_t *Wd,
-                            const float *sd, int mirror, int nthreads, double *h_out,
+                            const float *sd, int mirror, int a8, int nthreads, double *h_out,
                             double *ys_out)
 {
     wmat_t g = e4m3_mat(Wg, sg, d, f), u = e4m3_mat(Wu, su, d, f), dn = e4m3_mat(Wd, sd, f, d);
     return expert_rows(xs, x_is_f16, d, f, rows, nrows, row_expert, row_w, E, &g, &u, &dn,
-                       mirror, nthreads, h_out, ys_out);
+                       mirror, a8, nthreads, h_out, ys_out);
 }
 
 /*

@@ -150,3 +150,46 @@ def test_layer_e4m3_single_expert_dense_mlp():
     ref = (g / (1.0 + np.exp(-g)) * u) @ Wd
     y = oracle.layer(inp["x"], inp["ids"], inp["w"], *q)
     assert np.allclose(y, ref, rtol=1e-12, atol=1e-15)
+
+
+def test_row_quantize_scale_is_the_smallest_power_of_two():
+    rng = np.random.default_rng(7)
+    rows = [rng.standard_normal(40) * 10.0 ** p for p in (-30, -8, -2, 0, 1, 2, 3, 5, 30)]
+    rows += [np.zeros(40), np.full(40, 448.0), np.full(40, 449.0), np.full(40, 224.0),
+             np.array([448.0 * 2 ** 5] + [1.0] * 39)]
+    x = W.bf16_bits(np.array(rows, np.float32))
+    xv = W.bits_to_float(x, "bf16").astype(np.float64)
+    q, e = oracle.quantize_rows_e4m3(x)
+    for r in range(len(rows)):
+        amax = np.abs(xv[r]).max()
+        if amax == 0:
+            assert e[r] == 0 and np.all(q[r] & 0x7F == 0)
+            continue
+        assert amax <= 448.0 * 2.0 ** e[r]                 # fits
+        assert amax > 448.0 * 2.0 ** (e[r] - 1)            # and is the smallest that does
+        scaled = (xv[r] * 2.0 ** -int(e[r])).astype(np.float32)
+        assert np.array_equal(q[r], torch_encode(scaled))  # nearest codes, ties to even
+
+
+@pytest.mark.parametrize("mirror", [False, True])
+def test_layer_e4m3_activations_equal_layer_on_dequantized_rows(mirror):
+    # gate/up on E4M3 activations == the same layer fed the rows' dequantized
+    # values (exact in bf16), so the activation step is pinned through the
+    # already pinned layer
+    T, d, E, k, f = 10, 64, 3, 2, 32
+    inp = W.make_layer(T, d, E, k, f, seed=11)
+    qw = tuple(oracle.quantize_e4m3(inp[n]) for n in ("Wg", "Wu", "Wd"))
+    q, e = oracle.quantize_rows_e4m3(inp["x"])
+    deq = np.array([[oracle.e4m3_value(c) for c in row] for row in q]) * (2.0 ** e)[:, None]
+    xd = W.bf16_bits(deq.astype(np.float32))
+    assert np.array_equal(W.bits_to_float(xd, "bf16").astype(np.float64), deq)
+    y8 = oracle.layer(inp["x"], inp["ids"], inp["w"], *qw, mirror=mirror, act_e4m3=True)
+    yd = oracle.layer(xd, inp["ids"], inp["w"], *qw, mirror=mirror)
+    assert np.array_equal(y8, yd)
+    assert not np.array_equal(y8, oracle.layer(inp["x"], inp["ids"], inp["w"], *qw, mirror=mirror))
+    rows = np.arange(T, dtype=np.int64)
+    re = (np.arange(T) % E).astype(np.int32)
+    rw = np.ones(T, np.float32)
+    h8, _ = oracle.expert_rows(inp["x"], rows, re, rw, *qw, act_e4m3=True)
+    hd, _ = oracle.expert_rows(xd, rows, re, rw, *qw)
+    assert np.array_equal(h8, hd)

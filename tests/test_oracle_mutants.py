@@ -37,6 +37,10 @@ MUTANTS = {
     "scale_per_expert": ("return e4m3_value(W->q8[i]) * (double)W->scale[e * W->cols + c];",
                          "return e4m3_value(W->q8[i]) * (double)W->scale[e * W->cols];"),
     "scale_divisor": ("s = amax / 448.0f;", "s = amax / 256.0f;"),
+    "row_scale_not_minimal": ("        if (amax > ldexp(448.0, e))\n            e++;",
+                              "        if (amax >= ldexp(224.0, e))\n            e++;"),
+    "row_scale_ignored": ("        x[c] = ldexp(e4m3_value(e4m3_encode((float)ldexp(x[c], -e))), e);",
+                          "        x[c] = e4m3_value(e4m3_encode((float)ldexp(x[c], -e)));"),
     "quantize_amax_axis": ("float a = (float)fabs(bf16_value(W[(e * K + k) * M + m]));",
                            "float a = (float)fabs(bf16_value(W[(e * K + m % K) * M + k % M]));"),
 }
