@@ -315,11 +315,12 @@ MOE_API int moe_layer_forward(const void *x, const int32_t *ids, const float *w,
  * bf16 in shared memory (exact) and apply the scale in their epilogue.
  *
  * moe_quantize_e4m3 -- W bf16 [E, K, M] (M = output features, contiguous)
- * -> q uint8 [E, K, M], scale fp32 [E, M].  W must be finite.  A one-time
- * preparation (two passes over W), not part of the layer.
+ * -> q uint8 [E, K, M] (kmajor = 0) or [E, M, K] (kmajor = 1, K and M
+ * multiples of 64; the layout moe_ffn_gate_up_f8 reads), scale fp32
+ * [E, M].  W must be finite.  A one-time preparation, not part of the layer.
  */
 MOE_API int moe_quantize_e4m3(const void *W, int E, int K, int M, uint8_t *q, float *scale,
-                              moe_stream_t stream);
+                              int kmajor, moe_stream_t stream);
 
 /* moe_ffn_gate_up / moe_ffn_down with E4M3 weights: Wg, Wu uint8 [E, d, f]
  * with scales sg, su fp32 [E, f]; Wd uint8 [E, f, d] with scales sd fp32
@@ -333,6 +334,30 @@ MOE_API int moe_ffn_down_e4m3(const void *H, const uint8_t *Wd, const float *sd,
                               const int32_t *offsets, const float *srt_w, int E, int d, int f,
                               int64_t cap, void *Ys, uint32_t *status, moe_stream_t stream);
 
+/*
+ * E4M3 activations for the gate/up projection, so that it runs on 8-bit
+ * operands (tcgen05.mma.kind::f8f6f4) with no widening.  Each routed row
+ * gets a power-of-two scale 2^e, e the smallest integer with
+ * max |row| <= 448 * 2^e (0 for a zero or pad row); its codes are the
+ * nearest E4M3 values of row * 2^-e (exact scaling, ties to even).
+ *
+ * moe_gather_e4m3 -- moe_gather with E4M3 rows: xs8 uint8 [cap, d] and
+ * xexp int32 [cap] (the e of each row) for rows < R_pad.  d a multiple of
+ * 16; x, xs8 16-byte aligned.
+ *
+ * moe_ffn_gate_up_f8 -- H[r] = bf16(silu(g) * u) with g = 2^xexp[r] *
+ * sg[e] * (codes of row r . Wg codes), fp32 accumulation, likewise u: Wg, Wu
+ * K-major E4M3 codes [E, f, d] (moe_quantize_e4m3 with kmajor = 1), scales
+ * [E, f].  d a multiple of 128.
+ */
+MOE_API int moe_gather_e4m3(const void *x, int T, int d, const int32_t *srt_tok,
+                            const int32_t *offsets, int E, int64_t cap, uint8_t *xs8,
+                            int32_t *xexp, moe_stream_t stream);
+MOE_API int moe_ffn_gate_up_f8(const uint8_t *xs8, const int32_t *xexp, const uint8_t *Wg,
+                               const float *sg, const uint8_t *Wu, const float *su,
+                               const int32_t *offsets, int E, int d, int f, int64_t cap, void *H,
+                               uint32_t *status, moe_stream_t stream);
+
 /* moe_layer_forward with E4M3 weights (as above); same workspace
  * (moe_workspace_bytes) and outputs. */
 MOE_API int moe_layer_forward_e4m3(const void *x, const int32_t *ids, const float *w,
@@ -340,6 +365,17 @@ MOE_API int moe_layer_forward_e4m3(const void *x, const int32_t *ids, const floa
                                    const float *su, const uint8_t *Wd, const float *sd, int T,
                                    int d, int E, int k, int f, int tm, void *y, void *ws,
                                    size_t ws_bytes, moe_stream_t stream);
+
+/* moe_layer_forward_f8 -- the layer with moe_gather_e4m3 and
+ * moe_ffn_gate_up_f8 (Wg, Wu K-major codes [E, f, d]) in place of the
+ * gather and gate/up; down as in moe_layer_forward_e4m3 (Wd codes
+ * [E, f, d]).  d a multiple of 128; same workspace (the E4M3 rows and their
+ * exponents sit in its xs field). */
+MOE_API int moe_layer_forward_f8(const void *x, const int32_t *ids, const float *w,
+                                 const uint8_t *Wg, const float *sg, const uint8_t *Wu,
+                                 const float *su, const uint8_t *Wd, const float *sd, int T,
+                                 int d, int E, int k, int f, int tm, void *y, void *ws,
+                                 size_t ws_bytes, moe_stream_t stream);
 
 /*
  * moe_prefill_forward_host -- moe_layer_forward over n_chunks prefill
@@ -359,6 +395,7 @@ MOE_API int moe_layer_forward_e4m3(const void *x, const int32_t *ids, const floa
  *                moe_layer_forward (T is the size of every chunk)
  * in   sg, su, sd  NULL for bf16 weights; with E4M3 weights (codes in Wg,
  *                Wu, Wd) their scales, as in moe_layer_forward_e4m3
+ * in   act_e4m3  0, or 1 to run each chunk as moe_layer_forward_f8
  * ws            moe_prefill_host_workspace_bytes(...) device bytes, 256-byte
  *               aligned: the layer's workspace (moe_workspace_bytes, at offset
  *               0, so moe_read_status works on it) then the staging buffers
@@ -376,8 +413,9 @@ MOE_API int moe_prefill_forward_host(int n_chunks, const void *const *x_h,
                                      const int32_t *const *ids_h, const float *const *w_h,
                                      void *const *y_h, const void *Wg, const void *Wu,
                                      const void *Wd, const float *sg, const float *su,
-                                     const float *sd, int T, int d, int E, int k, int f, int tm,
-                                     void *ws, size_t ws_bytes, moe_stream_t stream);
+                                     const float *sd, int act_e4m3, int T, int d, int E, int k,
+                                     int f, int tm, void *ws, size_t ws_bytes,
+                                     moe_stream_t stream);
 
 /*
  * moe_read_status -- copy the status word at ws (a plan or layer workspace)

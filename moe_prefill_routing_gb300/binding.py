@@ -60,11 +60,21 @@ _SIGS = {
     "moe_prefill_host_workspace_bytes": (C.c_size_t, [C.c_int] * 6),
     "moe_prefill_forward_host": (C.c_int, [C.c_int, C.c_void_p, C.c_void_p, C.c_void_p,
                                            C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
-                                           C.c_void_p, C.c_void_p, C.c_void_p,
+                                           C.c_void_p, C.c_void_p, C.c_void_p, C.c_int,
                                            C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
                                            C.c_void_p, C.c_size_t, C.c_void_p]),
     "moe_quantize_e4m3": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p,
-                                    C.c_void_p, C.c_void_p]),
+                                    C.c_void_p, C.c_int, C.c_void_p]),
+    "moe_gather_e4m3": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_int,
+                                  C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p]),
+    "moe_ffn_gate_up_f8": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                     C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int,
+                                     C.c_int, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p]),
+    "moe_layer_forward_f8": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                       C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                       C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int,
+                                       C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_size_t,
+                                       C.c_void_p]),
     "moe_ffn_gate_up_e4m3": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                        C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                        C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p]),
@@ -329,7 +339,8 @@ def _host_ptrs(ts, name):
     return (C.c_void_p * max(len(ts), 1))(*[t.data_ptr() for t in ts])
 
 
-def prefill_forward_host(x_hs, ids_hs, w_hs, y_hs, Wg, Wu, Wd, tm: int, ws=None):
+def prefill_forward_host(x_hs, ids_hs, w_hs, y_hs, Wg, Wu, Wd, tm: int, ws=None,
+                         act_e4m3: bool = False):
     """moe_prefill_forward_host over len(x_hs) chunks: host (preferably
     pinned) x [T, d] bf16, ids/w [T, k] in; host y [T, d] bf16 out.  The
     weights are bf16 tensors or, all three, (E4M3 codes, scales) pairs.
@@ -338,7 +349,7 @@ def prefill_forward_host(x_hs, ids_hs, w_hs, y_hs, Wg, Wu, Wd, tm: int, ws=None)
     if not (len(ids_hs) == len(w_hs) == len(y_hs) == n):
         raise ValueError("one ids, w and y per chunk")
     (Wg, Wu, Wd), scales = _split_weights(Wg, Wu, Wd)
-    E, d, f = Wg.shape
+    E, f, d = Wd.shape
     T, k = (ids_hs[0].shape if n else (0, 1))
     dev = Wg.device
     nbytes = prefill_host_workspace_bytes(T, d, E, k, f, tm)
@@ -349,7 +360,8 @@ def prefill_forward_host(x_hs, ids_hs, w_hs, y_hs, Wg, Wu, Wd, tm: int, ws=None)
     with torch.cuda.device(dev):
         rc = lib().moe_prefill_forward_host(n, *[C.cast(a, C.c_void_p) for a in arrays],
                                             _ptr(Wg), _ptr(Wu), _ptr(Wd),
-                                            *[_ptr(t) for t in scales], T, d, E, k, f, tm,
+                                            *[_ptr(t) for t in scales], int(act_e4m3), T, d, E,
+                                            k, f, tm,
                                             _ptr(ws), ws.numel(), _stream(dev))
     _check("moe_prefill_forward_host", rc)
     return y_hs
@@ -363,16 +375,46 @@ def _split_weights(Wg, Wu, Wd):
     return (Wg, Wu, Wd), (None, None, None)
 
 
-def quantize_e4m3(W):
-    """moe_quantize_e4m3: bf16 W [E, K, M] -> (uint8 codes [E, K, M], fp32
-    scales [E, M]), the pair the *_e4m3 calls and MoeLayer take."""
+def quantize_e4m3(W, kmajor: bool = False):
+    """moe_quantize_e4m3: bf16 W [E, K, M] -> (uint8 codes [E, K, M], or
+    [E, M, K] with kmajor, fp32 scales [E, M]), the pair the *_e4m3 / *_f8
+    calls and MoeLayer take."""
     E, K, M = W.shape
-    q = torch.empty((E, K, M), dtype=torch.uint8, device=W.device)
+    q = torch.empty((E, M, K) if kmajor else (E, K, M), dtype=torch.uint8, device=W.device)
     s = torch.empty((E, M), dtype=torch.float32, device=W.device)
     with torch.cuda.device(W.device):
-        rc = lib().moe_quantize_e4m3(_ptr(W), E, K, M, _ptr(q), _ptr(s), _stream(W.device))
+        rc = lib().moe_quantize_e4m3(_ptr(W), E, K, M, _ptr(q), _ptr(s), int(kmajor),
+                                     _stream(W.device))
     _check("moe_quantize_e4m3", rc)
     return q, s
+
+
+def gather_e4m3(x, srt_tok, offsets, E: int, cap: int, xs8=None, xexp=None):
+    """moe_gather_e4m3: (uint8 codes [cap, d], int32 row exponents [cap])."""
+    T, d = x.shape
+    if xs8 is None:
+        xs8 = torch.empty((max(cap, 1), d), dtype=torch.uint8, device=x.device)
+    if xexp is None:
+        xexp = torch.empty(max(cap, 1), dtype=torch.int32, device=x.device)
+    with torch.cuda.device(x.device):
+        rc = lib().moe_gather_e4m3(_ptr(x), T, d, _ptr(srt_tok), _ptr(offsets), E, cap,
+                                   _ptr(xs8), _ptr(xexp), _stream(x.device))
+    _check("moe_gather_e4m3", rc)
+    return xs8, xexp
+
+
+def ffn_gate_up_f8(xs8, xexp, Wg, Wu, offsets, cap: int, H=None, status=None):
+    """moe_ffn_gate_up_f8 with K-major (codes, scales) pairs Wg, Wu [E, f, d]."""
+    (qg, sg), (qu, su) = Wg, Wu
+    E, f, d = qg.shape
+    if H is None:
+        H = torch.empty((max(cap, 1), f), dtype=torch.bfloat16, device=xs8.device)
+    with torch.cuda.device(xs8.device):
+        rc = lib().moe_ffn_gate_up_f8(_ptr(xs8), _ptr(xexp), _ptr(qg), _ptr(sg), _ptr(qu),
+                                      _ptr(su), _ptr(offsets), E, d, f, cap, _ptr(H),
+                                      _ptr(status), _stream(xs8.device))
+    _check("moe_ffn_gate_up_f8", rc)
+    return H
 
 
 def ffn_gate_up_e4m3(xs, Wg, Wu, offsets, cap: int, H=None, status=None):
@@ -400,22 +442,24 @@ def ffn_down_e4m3(H, Wd, offsets, srt_w, cap: int, Ys=None, status=None):
     return Ys
 
 
-def layer_forward_e4m3(x, ids, w, Wg, Wu, Wd, tm: int, y=None, ws=None):
-    """moe_layer_forward_e4m3 with (codes, scales) weight pairs."""
+def layer_forward_e4m3(x, ids, w, Wg, Wu, Wd, tm: int, y=None, ws=None, act_e4m3: bool = False):
+    """moe_layer_forward_e4m3 with (codes, scales) weight pairs, or with
+    act_e4m3 moe_layer_forward_f8 (Wg, Wu codes K-major)."""
     T, d = x.shape
     k = ids.shape[1]
     (qg, sg), (qu, su), (qd, sd) = Wg, Wu, Wd
-    E, _, f = qg.shape
+    E, f, _ = qd.shape
     dev = x.device
     if y is None:
         y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
     if ws is None:
         ws = torch.empty(workspace_bytes(T, d, E, k, f, tm), dtype=torch.uint8, device=dev)
+    name = "moe_layer_forward_f8" if act_e4m3 else "moe_layer_forward_e4m3"
     with torch.cuda.device(dev):
-        rc = lib().moe_layer_forward_e4m3(_ptr(x), _ptr(ids), _ptr(w), _ptr(qg), _ptr(sg),
-                                          _ptr(qu), _ptr(su), _ptr(qd), _ptr(sd), T, d, E, k, f,
-                                          tm, _ptr(y), _ptr(ws), ws.numel(), _stream(dev))
-    _check("moe_layer_forward_e4m3", rc)
+        rc = getattr(lib(), name)(_ptr(x), _ptr(ids), _ptr(w), _ptr(qg), _ptr(sg), _ptr(qu),
+                                  _ptr(su), _ptr(qd), _ptr(sd), T, d, E, k, f, tm, _ptr(y),
+                                  _ptr(ws), ws.numel(), _stream(dev))
+    _check(name, rc)
     return y
 
 
@@ -453,19 +497,25 @@ class MoeLayer:
     copied back on the library's copy streams, overlapped with the layer,
     which runs on the current stream."""
 
-    def __init__(self, Wg, Wu, Wd, tm: int = 16):
+    def __init__(self, Wg, Wu, Wd, tm: int = 16, act_e4m3: bool = False):
         self.Wg, self.Wu, self.Wd, self.tm = Wg, Wu, Wd, tm
         self.e4m3 = isinstance(Wg, tuple)
-        codes = Wg[0] if self.e4m3 else Wg
-        self.E, self.d, self.f = codes.shape
-        self.device = codes.device
+        self.act_e4m3 = bool(act_e4m3)
+        if self.act_e4m3 and not self.e4m3:
+            raise ValueError("E4M3 activations come with E4M3 weights")
+        wd = Wd[0] if self.e4m3 else Wd   # [E, f, d] in every form
+        self.E, self.f, self.d = wd.shape
+        self.device = wd.device
         self._ws = None
         self._host_ws = None
 
     @classmethod
-    def quantized(cls, Wg, Wu, Wd, tm: int = 16):
-        """The same layer with its bf16 weights quantized to E4M3 on the device."""
-        return cls(quantize_e4m3(Wg), quantize_e4m3(Wu), quantize_e4m3(Wd), tm=tm)
+    def quantized(cls, Wg, Wu, Wd, tm: int = 16, act_e4m3: bool = False):
+        """The same layer with its bf16 weights quantized to E4M3 on the device;
+        with act_e4m3 the gate/up projection also runs on E4M3 rows (its
+        weight codes K-major)."""
+        return cls(quantize_e4m3(Wg, kmajor=act_e4m3), quantize_e4m3(Wu, kmajor=act_e4m3),
+                   quantize_e4m3(Wd), tm=tm, act_e4m3=act_e4m3)
 
     def workspace(self, T: int, k: int):
         n = workspace_bytes(T, self.d, self.E, k, self.f, self.tm)
@@ -475,9 +525,11 @@ class MoeLayer:
 
     def forward(self, x, ids, w, y=None):
         T = x.shape[0]
-        fn = layer_forward_e4m3 if self.e4m3 else layer_forward
-        return fn(x, ids, w, self.Wg, self.Wu, self.Wd, self.tm, y=y,
-                  ws=self.workspace(T, ids.shape[1]))
+        ws = self.workspace(T, ids.shape[1])
+        if self.e4m3:
+            return layer_forward_e4m3(x, ids, w, self.Wg, self.Wu, self.Wd, self.tm, y=y, ws=ws,
+                                      act_e4m3=self.act_e4m3)
+        return layer_forward(x, ids, w, self.Wg, self.Wu, self.Wd, self.tm, y=y, ws=ws)
 
     def forward_host(self, x_h, ids_h, w_h, y_h):
         """Host (pinned) x, ids, w in; host y out, through the C ABI's host
@@ -494,4 +546,4 @@ class MoeLayer:
         if self._host_ws is None or self._host_ws.numel() < n:
             self._host_ws = torch.empty(n, dtype=torch.uint8, device=self.device)
         return prefill_forward_host(x_hs, ids_hs, w_hs, y_hs, self.Wg, self.Wu, self.Wd, self.tm,
-                                    ws=self._host_ws)
+                                    ws=self._host_ws, act_e4m3=self.act_e4m3)

@@ -270,10 +270,12 @@ int moe_workspace_layout(int T, int d, int E, int k, int f, int tm, size_t *out)
     return layout(T, d, E, k, f, tm, out);
 }
 
-// The expert weights of a layer: bf16, or E4M3 codes with per-feature scales.
+// The expert weights of a layer: bf16, or E4M3 codes with per-feature scales
+// (act_e4m3: Wg, Wu K-major and the gate/up rows in E4M3 too).
 struct LayerWeights {
     const void *Wg, *Wu, *Wd;
     const float *sg, *su, *sd;  // all null for bf16
+    bool act_e4m3;
 };
 
 static int layer_forward(const void *x, const int32_t *ids, const float *w,
@@ -282,7 +284,7 @@ static int layer_forward(const void *x, const int32_t *ids, const float *w,
 {
     const bool e4m3 = W.sg != nullptr;
     if (!base_sizes_ok(T, k, E) || tm < 16 || tm > MOE_MAX_TM || tm % 16 != 0 || d <= 0 ||
-        f <= 0 || d % 64 != 0 || f % 64 != 0)
+        f <= 0 || d % 64 != 0 || f % 64 != 0 || (W.act_e4m3 && d % 128 != 0))
         return MOE_ERR_SHAPE;
     if (!W.Wg || !W.Wu || !W.Wd || !ws || (T > 0 && (!x || !ids || !w || !y)) ||
         (e4m3 && (!W.su || !W.sd)))
@@ -314,13 +316,20 @@ static int layer_forward(const void *x, const int32_t *ids, const float *w,
         ids, w, T, k, E, tm, offsets, reinterpret_cast<int32_t *>(b + L[MOE_WS_COUNTS]), srt_tok,
         srt_w, pos, reinterpret_cast<int32_t *>(b + L[MOE_WS_TILE_EXPERT]), cap, status,
         reinterpret_cast<int32_t *>(b + L[MOE_WS_BCNT]), s);
+    // E4M3 rows share the xs region: codes [cap, d], then the row exponents
+    uint8_t *xs8 = static_cast<uint8_t *>(xs);
+    int32_t *xexp = reinterpret_cast<int32_t *>(xs8 + ((size_t(cap) * d + 255) & ~size_t(255)));
     if (e == cudaSuccess)
-        e = moe::launch_gather(x, T, d, srt_tok, offsets, E, cap, xs, s);
+        e = W.act_e4m3 ? moe::launch_gather_e4m3(x, T, d, srt_tok, offsets, E, cap, xs8, xexp, s)
+                       : moe::launch_gather(x, T, d, srt_tok, offsets, E, cap, xs, s);
+    const uint8_t *qg = static_cast<const uint8_t *>(W.Wg), *qu = static_cast<const uint8_t *>(W.Wu);
     if (e == cudaSuccess)
-        e = e4m3 ? moe::launch_ffn_gate_up_e4m3(xs, static_cast<const uint8_t *>(W.Wg), W.sg,
-                                                static_cast<const uint8_t *>(W.Wu), W.su, offsets,
-                                                E, d, f, cap, H, status, s)
-                 : moe::launch_ffn_gate_up(xs, W.Wg, W.Wu, offsets, E, d, f, cap, H, status, s);
+        e = W.act_e4m3 ? moe::launch_ffn_gate_up_native(xs8, xexp, qg, W.sg, qu, W.su, offsets, E,
+                                                        d, f, cap, H, status, s)
+            : e4m3     ? moe::launch_ffn_gate_up_e4m3(xs, qg, W.sg, qu, W.su, offsets, E, d, f, cap,
+                                                      H, status, s)
+                       : moe::launch_ffn_gate_up(xs, W.Wg, W.Wu, offsets, E, d, f, cap, H, status,
+                                                 s);
     if (e == cudaSuccess)
         e = e4m3 ? moe::launch_ffn_down_e4m3(H, static_cast<const uint8_t *>(W.Wd), W.sd, offsets,
                                              srt_w, E, d, f, cap, Ys, status, s)
@@ -334,7 +343,7 @@ int moe_layer_forward(const void *x, const int32_t *ids, const float *w, const v
                       const void *Wu, const void *Wd, int T, int d, int E, int k, int f, int tm,
                       void *y, void *ws, size_t ws_bytes, moe_stream_t stream)
 {
-    const LayerWeights W{Wg, Wu, Wd, nullptr, nullptr, nullptr};
+    const LayerWeights W{Wg, Wu, Wd, nullptr, nullptr, nullptr, false};
     return layer_forward(x, ids, w, W, T, d, E, k, f, tm, y, ws, ws_bytes, stream);
 }
 
@@ -345,20 +354,69 @@ int moe_layer_forward_e4m3(const void *x, const int32_t *ids, const float *w, co
 {
     if (!sg)
         return MOE_ERR_NULL;
-    const LayerWeights W{Wg, Wu, Wd, sg, su, sd};
+    const LayerWeights W{Wg, Wu, Wd, sg, su, sd, false};
     return layer_forward(x, ids, w, W, T, d, E, k, f, tm, y, ws, ws_bytes, stream);
 }
 
-int moe_quantize_e4m3(const void *W, int E, int K, int M, uint8_t *q, float *scale,
+int moe_layer_forward_f8(const void *x, const int32_t *ids, const float *w, const uint8_t *Wg,
+                         const float *sg, const uint8_t *Wu, const float *su, const uint8_t *Wd,
+                         const float *sd, int T, int d, int E, int k, int f, int tm, void *y,
+                         void *ws, size_t ws_bytes, moe_stream_t stream)
+{
+    if (!sg)
+        return MOE_ERR_NULL;
+    const LayerWeights W{Wg, Wu, Wd, sg, su, sd, true};
+    return layer_forward(x, ids, w, W, T, d, E, k, f, tm, y, ws, ws_bytes, stream);
+}
+
+int moe_quantize_e4m3(const void *W, int E, int K, int M, uint8_t *q, float *scale, int kmajor,
                       moe_stream_t stream)
 {
-    if (E < 1 || E > MOE_MAX_EXPERTS || K < 1 || M < 1)
+    if (E < 1 || E > MOE_MAX_EXPERTS || K < 1 || M < 1 || (kmajor && (K % 64 || M % 64)))
         return MOE_ERR_SHAPE;
     if (!W || !q || !scale)
         return MOE_ERR_NULL;
     if (!aligned(W, 2) || !aligned(scale, 4))
         return MOE_ERR_ALIGN;
-    return cuda_rc(moe::launch_quantize_e4m3(W, E, K, M, q, scale, as_stream(stream)));
+    return cuda_rc(moe::launch_quantize_e4m3(W, E, K, M, q, scale, kmajor != 0,
+                                             as_stream(stream)));
+}
+
+int moe_gather_e4m3(const void *x, int T, int d, const int32_t *srt_tok, const int32_t *offsets,
+                    int E, int64_t cap, uint8_t *xs8, int32_t *xexp, moe_stream_t stream)
+{
+    if (T < 0 || d <= 0 || d % 16 != 0 || E < 1 || E > MOE_MAX_EXPERTS)
+        return MOE_ERR_SHAPE;
+    if (cap < 0 || cap > INT_MAX)
+        return MOE_ERR_CAPACITY;
+    if (!srt_tok || !offsets || !xs8 || !xexp || (T > 0 && !x))
+        return MOE_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(xs8, 16) || !aligned(xexp, 4) || !aligned(srt_tok, 4) ||
+        !aligned(offsets, 4))
+        return MOE_ERR_ALIGN;
+    if (cap == 0)
+        return MOE_OK;
+    return cuda_rc(moe::launch_gather_e4m3(x, T, d, srt_tok, offsets, E, cap, xs8, xexp,
+                                           as_stream(stream)));
+}
+
+int moe_ffn_gate_up_f8(const uint8_t *xs8, const int32_t *xexp, const uint8_t *Wg,
+                       const float *sg, const uint8_t *Wu, const float *su,
+                       const int32_t *offsets, int E, int d, int f, int64_t cap, void *H,
+                       uint32_t *status, moe_stream_t stream)
+{
+    int rc = ffn_checks(xs8, Wg, Wu, offsets, E, d, f, cap, H);
+    if (rc == MOE_OK && d % 128 != 0)
+        rc = MOE_ERR_SHAPE;
+    if (rc == MOE_OK && (!sg || !su || !xexp))
+        rc = MOE_ERR_NULL;
+    if (rc == MOE_OK &&
+        (!aligned(sg, 4) || !aligned(su, 4) || !aligned(xexp, 4) || !aligned(status, 4)))
+        rc = MOE_ERR_ALIGN;
+    if (rc != MOE_OK || cap == 0)
+        return rc;
+    return cuda_rc(moe::launch_ffn_gate_up_native(xs8, xexp, Wg, sg, Wu, su, offsets, E, d, f, cap,
+                                                  H, status, as_stream(stream)));
 }
 
 int moe_ffn_gate_up_e4m3(const void *xs, const uint8_t *Wg, const float *sg, const uint8_t *Wu,

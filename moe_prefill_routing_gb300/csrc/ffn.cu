@@ -31,13 +31,20 @@
 // warp 1 issues tcgen05.mma into one of two TMEM accumulators, warps 2-5
 // read the accumulator with tcgen05.ld, apply the epilogue, stage 16 rows of
 // bf16 in shared memory, and one thread writes them out with a TMA store.
-// W8: the weights are E4M3 codes with a per-(expert, output feature) scale
+// Weight modes (WM): bf16 weights and activations; kWiden: E4M3 weights,
+// bf16 activations; kNative: E4M3 weights and E4M3 activations for gate/up.
+// kWiden: the weights are E4M3 codes with a per-(expert, output feature) scale
 // (see quant.cu).  TMA brings the 8-bit tiles into the stage ring (half the
 // bytes of bf16), eight more warps (6-13) widen them to bf16 -- exactly: every
 // E4M3 value is a bf16 value -- into a second ring laid out as the bf16
 // tiles would be (MN-major, 128-byte swizzle), and the epilogue multiplies
 // each accumulator row (one output feature) by its scale.  The MMAs are the
 // same bf16 MMAs.
+// kNative (gate/up): the weight codes are stored K-major [E, f, d] and the
+// routed rows are E4M3 codes with a power-of-two scale per row (rows.cu);
+// both go straight to tcgen05.mma.kind::f8f6f4, K = 128 per stage in the
+// same 128-byte rows, and the epilogue multiplies by feature scale times
+// row scale.
 // Every output element is written by one CTA with a fixed K order: results
 // are deterministic.  Every wait is bounded (2 s); on a timeout the CTA
 // stops, lets its copies and MMAs land, frees TMEM and sets
@@ -87,12 +94,16 @@ constexpr uint32_t kStageBytesW8 = 2 * kA8TileBytes + kBTileBytes;
 constexpr int kConvSlots = 2;
 constexpr uint32_t kConvSlotBytes = 2 * kATileBytes;
 
-template <bool W8>
+enum WeightMode : int { kBf16 = 0, kWiden = 1, kNative = 2 };
+
+template <int WM>
 struct Cfg {
-    static constexpr int kThreadsK = W8 ? kThreadsW8 : kThreads;
-    static constexpr uint32_t kStageB = W8 ? kStageBytesW8 : kStageBytes;
+    static constexpr bool kW8 = WM == kWiden;
+    static constexpr int kThreadsK = kW8 ? kThreadsW8 : kThreads;
+    static constexpr uint32_t kStageB = kW8 ? kStageBytesW8 : kStageBytes;
     static constexpr uint32_t kRingBytes =
-        kStages * kStageB + (W8 ? kConvSlots * kConvSlotBytes : 0u);
+        kStages * kStageB + (kW8 ? kConvSlots * kConvSlotBytes : 0u);
+    static constexpr int kKStep = WM == kNative ? 128 : BK;  // K elements per stage
 };
 
 // GATED: gate/up (A tiles = Wg and Wu over the same 128 features, output H).
@@ -129,18 +140,20 @@ struct FfnArgs {
     int M;  // output features: f (gate/up) or d (down)
     int stall_cta;  // self-test only: this CTA's first stage waits for 16 bytes
                     // that never come; -1 in every normal launch
-    const float *scale0;  // W8: scales [E, M] of A tile 0's weight (Wg or Wd)
-    const float *scale1;  // W8: scales [E, M] of A tile 1's weight (Wu or Wd)
+    const float *scale0;  // E4M3: scales [E, M] of A tile 0's weight (Wg or Wd)
+    const float *scale1;  // E4M3: scales [E, M] of A tile 1's weight (Wu or Wd)
+    const int32_t *row_exp;  // kNative: each row's scale exponent (row scale 2^e)
 };
 
-template <bool W8>
+template <int WM>
 constexpr size_t ffn_smem_bytes(int E)
 {
-    return 1024 + size_t(Cfg<W8>::kRingBytes) + kStgBytes + sizeof(Ctrl<kStages>) +
+    return 1024 + size_t(Cfg<WM>::kRingBytes) + kStgBytes + sizeof(Ctrl<kStages>) +
            2 * BN * sizeof(int) + size_t(E + 1) * sizeof(int);
 }
-static_assert(ffn_smem_bytes<true>(MOE_MAX_EXPERTS) <= 227 * 1024, "shared memory per CTA");
-static_assert(ffn_smem_bytes<false>(MOE_MAX_EXPERTS) <= 227 * 1024, "shared memory per CTA");
+static_assert(ffn_smem_bytes<kBf16>(MOE_MAX_EXPERTS) <= 227 * 1024, "shared memory per CTA");
+static_assert(ffn_smem_bytes<kWiden>(MOE_MAX_EXPERTS) <= 227 * 1024, "shared memory per CTA");
+static_assert(ffn_smem_bytes<kNative>(MOE_MAX_EXPERTS) <= 227 * 1024, "shared memory per CTA");
 
 // Bounded wait that ignores the abort flag (used while stopping).
 __device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity)
@@ -259,23 +272,25 @@ __device__ __forceinline__ void widen_e4m3x16(const uint4 v, uint4 &lo, uint4 &h
 
 // GATHER: the B rows of a unit are token rows of x fetched by index
 // (srt_tok, four rows per TMA gather4) instead of consecutive rows of xs.
-// W8: the A tiles arrive as E4M3 codes and are widened in shared memory.
-template <bool GATED, bool GATHER, bool W8>
-__global__ void __launch_bounds__(Cfg<W8>::kThreadsK, 1)
+// WM: weight mode (kBf16, kWiden, kNative), see the top of this file.
+template <bool GATED, bool GATHER, int WM>
+__global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
     k_ffn(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
           const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_out,
           const FfnArgs p)
 {
-    static_assert(!(GATHER && W8), "gathered rows come with bf16 weights only");
+    constexpr bool W8 = WM == kWiden, A8 = WM == kNative, SCALED = WM != kBf16;
+    static_assert(!(GATHER && SCALED), "gathered rows come with bf16 weights only");
+    static_assert(!A8 || GATED, "E4M3 activations feed the gate/up projection only");
     constexpr int S = kStages;
     constexpr int UM = Kind<GATED>::kUnitM;
-    constexpr uint32_t SB = Cfg<W8>::kStageB;
+    constexpr uint32_t SB = Cfg<WM>::kStageB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
-    uint8_t *conv = smem + S * SB;  // W8: widened A tiles, kConvSlots slots
-    uint16_t *stg = reinterpret_cast<uint16_t *>(smem + Cfg<W8>::kRingBytes);
-    Ctrl<S> *ctl = reinterpret_cast<Ctrl<S> *>(smem + Cfg<W8>::kRingBytes + kStgBytes);
+    uint8_t *conv = smem + S * SB;  // kWiden: widened A tiles, kConvSlots slots
+    uint16_t *stg = reinterpret_cast<uint16_t *>(smem + Cfg<WM>::kRingBytes);
+    Ctrl<S> *ctl = reinterpret_cast<Ctrl<S> *>(smem + Cfg<WM>::kRingBytes + kStgBytes);
     int *row_tok = reinterpret_cast<int *>(ctl + 1);  // [BN] tokens of the unit's rows
     float *row_w = reinterpret_cast<float *>(row_tok + BN);  // [BN] routing weights (down)
     int *chunk_start = row_tok + 2 * BN;
@@ -323,7 +338,7 @@ __global__ void __launch_bounds__(Cfg<W8>::kThreadsK, 1)
     const int total_chunks =
         build_chunk_table(p.offsets, p.E, p.cap, chunk_start, ctl->warp_sum, p.status);
     const int n_mt = (p.M + UM - 1) / UM;
-    const int nk = p.K / BK;
+    const int nk = p.K / Cfg<WM>::kKStep;
     const int64_t total_units = int64_t(total_chunks) * n_mt;
 
     // first feature of A tile t of a unit starting at feature m0
@@ -353,7 +368,8 @@ __global__ void __launch_bounds__(Cfg<W8>::kThreadsK, 1)
                 // inside M (features past M are zero-filled and still counted)
                 const uint32_t a_bytes =
                     W8 ? (1u + uint32_t(tile_base(m0, 1) < p.M)) * kA8TileBytes
-                       : boxes * kABoxBytes;
+                    : A8 ? 2u * kATileBytes  // 128 features x 128 K codes per tile
+                         : boxes * kABoxBytes;
                 const uint32_t bytes = a_bytes + uint32_t(w.nrows) * uint32_t(BK * 2);
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag)) {
@@ -364,7 +380,7 @@ __global__ void __launch_bounds__(Cfg<W8>::kThreadsK, 1)
                     mbar_arrive_expect_tx(fb, bytes + stall_bytes);
                     stall_bytes = 0;
                     uint8_t *sa = smem + stage * SB;
-                    const int k0 = kb * BK;
+                    const int k0 = kb * Cfg<WM>::kKStep;
 #pragma unroll
                     for (int t = 0; t < 2; ++t) {
                         const CUtensorMap *m = (GATED && t == 1) ? &map_a1 : &map_a0;
@@ -372,6 +388,9 @@ __global__ void __launch_bounds__(Cfg<W8>::kThreadsK, 1)
                             if (tile_base(m0, t) < p.M)
                                 tma_load_3d(sa + t * kA8TileBytes, m, fb, tile_base(m0, t), k0,
                                             w.e);
+                        } else if (A8) {
+                            // K-major codes [E, M, K]: coordinates (k, feature, expert)
+                            tma_load_3d(sa + t * kATileBytes, m, fb, k0, tile_base(m0, t), w.e);
                         } else {
 #pragma unroll
                             for (int h = 0; h < 2; ++h) {
@@ -434,7 +453,8 @@ __global__ void __launch_bounds__(Cfg<W8>::kThreadsK, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d0 = tmem_base + uint32_t(abuf) * kAccCols;
-                const uint32_t idesc = idesc_bf16_f32(BM, uint32_t(w.nrows), 1u, 0u);
+                const uint32_t idesc = A8 ? idesc_e4m3_f32(BM, uint32_t(w.nrows))
+                                          : idesc_bf16_f32(BM, uint32_t(w.nrows), 1u, 0u);
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait(&ctl->full[stage], phase, abort_flag) ||
                         (W8 && !mbar_wait(&ctl->conv_full[cslot], cphase, abort_flag))) {
@@ -445,19 +465,33 @@ __global__ void __launch_bounds__(Cfg<W8>::kThreadsK, 1)
                     const uint32_t sst = smem_u32(smem + stage * SB);
                     const uint32_t sa = W8 ? smem_u32(conv + cslot * kConvSlotBytes) : sst;
                     const uint32_t sb = sst + (W8 ? 2 * kA8TileBytes : 2 * kATileBytes);
+                    if (A8) {
+                        // both operands K-major 128-byte rows; K = 32 codes (32 bytes)
+                        // per instruction, four per stage
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        // B: K-major rows of 128 B; the K step moves 32 B inside the row.
-                        const uint64_t bdesc = smem_desc_sw128(sb + kk * UMMA_K * 2, 16, 1024);
-                        // A: MN-major, one 128-byte row per K index; the K step moves 16 rows.
-                        const uint32_t acc = (kb | kk) != 0;
-                        tc_mma_f16(d0, smem_desc_sw128(sa + kk * UMMA_K * 128, kABoxBytes, 1024),
-                                   bdesc, idesc, acc);
-                        if (use1)
-                            tc_mma_f16(d0 + BN,
-                                       smem_desc_sw128(sa + kATileBytes + kk * UMMA_K * 128,
-                                                       kABoxBytes, 1024),
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t bdesc = smem_desc_sw128(sb + kk * 32, 16, 1024);
+                            const uint32_t acc = (kb | kk) != 0;
+                            tc_mma_f8(d0, smem_desc_sw128(sa + kk * 32, 16, 1024), bdesc, idesc,
+                                      acc);
+                            tc_mma_f8(d0 + BN, smem_desc_sw128(sa + kATileBytes + kk * 32, 16, 1024),
+                                      bdesc, idesc, acc);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                            // B: K-major rows of 128 B; the K step moves 32 B inside the row.
+                            const uint64_t bdesc = smem_desc_sw128(sb + kk * UMMA_K * 2, 16, 1024);
+                            // A: MN-major, one 128-byte row per K index; the K step moves 16 rows.
+                            const uint32_t acc = (kb | kk) != 0;
+                            tc_mma_f16(d0, smem_desc_sw128(sa + kk * UMMA_K * 128, kABoxBytes, 1024),
                                        bdesc, idesc, acc);
+                            if (use1)
+                                tc_mma_f16(d0 + BN,
+                                           smem_desc_sw128(sa + kATileBytes + kk * UMMA_K * 128,
+                                                           kABoxBytes, 1024),
+                                           bdesc, idesc, acc);
+                        }
                     }
                     tc_commit(&ctl->empty[stage]);  // frees the stage once these MMAs finish
                     if (++stage == S) {
@@ -555,7 +589,7 @@ __global__ void __launch_bounds__(Cfg<W8>::kThreadsK, 1)
             const bool use1 = tile_base(m0, 1) < p.M;
             // W8: the scales of this thread's output feature in both A tiles
             float sc0 = 1.0f, sc1 = 1.0f;
-            if (W8) {
+            if (SCALED) {
                 const int64_t eb = int64_t(w.e) * p.M;
                 const int fa = tile_base(m0, 0) + fq, fb = tile_base(m0, 1) + fq;
                 sc0 = fa < p.M ? p.scale0[eb + fa] : 0.0f;
@@ -567,6 +601,8 @@ __global__ void __launch_bounds__(Cfg<W8>::kThreadsK, 1)
             // barriers, which every thread reaches after its read.
             if (!GATED && et < w.nrows)  // read by every thread of the unit's chunks
                 row_w[et] = p.srt_w[w.row0 + et];
+            if (A8 && et < w.nrows)  // the rows' scales 2^e
+                row_w[et] = ldexpf(1.0f, p.row_exp[w.row0 + et]);
             if (!mbar_wait(&ctl->tmem_full[abuf], aphase, abort_flag))
                 *reinterpret_cast<volatile int *>(&ctl->epi_stop) = 1;
             epi_bar();
@@ -584,18 +620,23 @@ __global__ void __launch_bounds__(Cfg<W8>::kThreadsK, 1)
                 tmem_ld_wait();
                 float v0[16], v1[16];
                 if (GATED) {
+                    const float *rs = row_w + c0;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const float g = W8 ? __uint_as_float(a[j]) * sc0 : __uint_as_float(a[j]);
-                        const float up = W8 ? __uint_as_float(b[j]) * sc1 : __uint_as_float(b[j]);
+                        const float s0 = A8 ? sc0 * rs[j] : sc0, s1 = A8 ? sc1 * rs[j] : sc1;
+                        const float g = SCALED ? __uint_as_float(a[j]) * s0 : __uint_as_float(a[j]);
+                        const float up =
+                            SCALED ? __uint_as_float(b[j]) * s1 : __uint_as_float(b[j]);
                         v0[j] = __fdividef(g, 1.0f + __expf(-g)) * up;
                     }
                 } else {
                     const float *wr = row_w + c0;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const float o0 = W8 ? __uint_as_float(a[j]) * sc0 : __uint_as_float(a[j]);
-                        const float o1 = W8 ? __uint_as_float(b[j]) * sc1 : __uint_as_float(b[j]);
+                        const float o0 =
+                            SCALED ? __uint_as_float(a[j]) * sc0 : __uint_as_float(a[j]);
+                        const float o1 =
+                            SCALED ? __uint_as_float(b[j]) * sc1 : __uint_as_float(b[j]);
                         v0[j] = wr[j] * o0;
                         v1[j] = use1 ? wr[j] * o1 : 0.0f;
                     }
@@ -695,6 +736,25 @@ cudaError_t weight_map_e4m3(CUtensorMap *m, const void *Wq, int E, int K, int M)
     return encode_bf16(m, Wq, 3, dims, strides, box, true, true);
 }
 
+// K-major E4M3 weight codes [E, M, K] (K contiguous): 128-byte-swizzled
+// boxes of 128 K x 128 features of one expert.
+cudaError_t weight_map_e4m3_kmajor(CUtensorMap *m, const void *Wq, int E, int K, int M)
+{
+    const cuuint64_t dims[3] = {cuuint64_t(K), cuuint64_t(M), cuuint64_t(E)};
+    const cuuint64_t strides[2] = {cuuint64_t(K), cuuint64_t(K) * M};
+    const cuuint32_t box[3] = {128, BM, 1};
+    return encode_bf16(m, Wq, 3, dims, strides, box, false, true);
+}
+
+// E4M3 rows [cap, K] (K contiguous): boxes of 16 rows x 128 K codes.
+cudaError_t rows_map_e4m3(CUtensorMap *m, const void *X, int64_t cap, int K)
+{
+    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(cap)};
+    const cuuint64_t strides[1] = {cuuint64_t(K)};
+    const cuuint32_t box[2] = {128, kBoxRows};
+    return encode_bf16(m, X, 2, dims, strides, box, false, true);
+}
+
 // Rows [cap, K] (K contiguous): boxes of 16 rows x 64 K.
 cudaError_t rows_map(CUtensorMap *m, const void *X, int64_t cap, int K)
 {
@@ -736,14 +796,14 @@ cudaError_t launch_ffn_gate_up(const void *xs, const void *Wg, const void *Wu,
         (err = rows_map(&mx, xs, cap, d)) != cudaSuccess ||
         (err = out_map(&mo, H, cap, f, Kind<true>::kUnitM)) != cudaSuccess)
         return err;
-    auto kern = k_ffn<true, false, false>;
+    auto kern = k_ffn<true, false, kBf16>;
     err = ensure_smem_limit(reinterpret_cast<const void *>(kern), kSlotGateUp,
-                            ffn_smem_bytes<false>(MOE_MAX_EXPERTS));
+                            ffn_smem_bytes<kBf16>(MOE_MAX_EXPERTS));
     if (err != cudaSuccess)
         return err;
     const FfnArgs a{offsets, nullptr, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f,
-                    stall_cta, nullptr, nullptr};
-    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<false>(E),
+                    stall_cta, nullptr, nullptr, nullptr};
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<kBf16>(E),
                       stream, mg, mu, mx, mo, a);
 }
 
@@ -758,14 +818,14 @@ cudaError_t launch_ffn_gate_up_rows(const void *x, int T, const int32_t *srt_tok
         (err = token_rows_map(&mx, x, T, d)) != cudaSuccess ||
         (err = out_map(&mo, H, cap, f, Kind<true>::kUnitM)) != cudaSuccess)
         return err;
-    auto kern = k_ffn<true, true, false>;
+    auto kern = k_ffn<true, true, kBf16>;
     err = ensure_smem_limit(reinterpret_cast<const void *>(kern), kSlotGateUpRows,
-                            ffn_smem_bytes<false>(MOE_MAX_EXPERTS));
+                            ffn_smem_bytes<kBf16>(MOE_MAX_EXPERTS));
     if (err != cudaSuccess)
         return err;
     const FfnArgs a{offsets, srt_tok, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f,
-                    -1, nullptr, nullptr};
-    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<false>(E),
+                    -1, nullptr, nullptr, nullptr};
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<kBf16>(E),
                       stream, mg, mu, mx, mo, a);
 }
 
@@ -779,14 +839,14 @@ cudaError_t launch_ffn_down(const void *H, const void *Wd, const int32_t *offset
         (err = rows_map(&mh, H, cap, f)) != cudaSuccess ||
         (err = out_map(&mo, Ys, cap, d, Kind<false>::kUnitM)) != cudaSuccess)
         return err;
-    auto kern = k_ffn<false, false, false>;
+    auto kern = k_ffn<false, false, kBf16>;
     err = ensure_smem_limit(reinterpret_cast<const void *>(kern), kSlotDown,
-                            ffn_smem_bytes<false>(MOE_MAX_EXPERTS));
+                            ffn_smem_bytes<kBf16>(MOE_MAX_EXPERTS));
     if (err != cudaSuccess)
         return err;
     const FfnArgs a{offsets, nullptr, srt_w, static_cast<uint16_t *>(Ys), status, cap, E, f, d,
-                    -1, nullptr, nullptr};
-    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<false>(E),
+                    -1, nullptr, nullptr, nullptr};
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<kBf16>(E),
                       stream, mw, mw, mh, mo, a);
 }
 
@@ -802,14 +862,37 @@ cudaError_t launch_ffn_gate_up_e4m3(const void *xs, const uint8_t *Wg, const flo
         (err = rows_map(&mx, xs, cap, d)) != cudaSuccess ||
         (err = out_map(&mo, H, cap, f, Kind<true>::kUnitM)) != cudaSuccess)
         return err;
-    auto kern = k_ffn<true, false, true>;
+    auto kern = k_ffn<true, false, kWiden>;
     err = ensure_smem_limit(reinterpret_cast<const void *>(kern), kSlotGateUpE4m3,
-                            ffn_smem_bytes<true>(MOE_MAX_EXPERTS));
+                            ffn_smem_bytes<kWiden>(MOE_MAX_EXPERTS));
     if (err != cudaSuccess)
         return err;
     const FfnArgs a{offsets, nullptr, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f,
-                    -1, sg, su};
-    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreadsW8), ffn_smem_bytes<true>(E),
+                    -1, sg, su, nullptr};
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreadsW8), ffn_smem_bytes<kWiden>(E),
+                      stream, mg, mu, mx, mo, a);
+}
+
+cudaError_t launch_ffn_gate_up_native(const uint8_t *xs8, const int32_t *xexp, const uint8_t *Wg,
+                                      const float *sg, const uint8_t *Wu, const float *su,
+                                      const int32_t *offsets, int E, int d, int f, int64_t cap,
+                                      void *H, uint32_t *status, cudaStream_t stream)
+{
+    CUtensorMap mg, mu, mx, mo;
+    cudaError_t err;
+    if ((err = weight_map_e4m3_kmajor(&mg, Wg, E, d, f)) != cudaSuccess ||
+        (err = weight_map_e4m3_kmajor(&mu, Wu, E, d, f)) != cudaSuccess ||
+        (err = rows_map_e4m3(&mx, xs8, cap, d)) != cudaSuccess ||
+        (err = out_map(&mo, H, cap, f, Kind<true>::kUnitM)) != cudaSuccess)
+        return err;
+    auto kern = k_ffn<true, false, kNative>;
+    err = ensure_smem_limit(reinterpret_cast<const void *>(kern), kSlotGateUpNative,
+                            ffn_smem_bytes<kNative>(MOE_MAX_EXPERTS));
+    if (err != cudaSuccess)
+        return err;
+    const FfnArgs a{offsets, nullptr, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f,
+                    -1, sg, su, xexp};
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<kNative>(E),
                       stream, mg, mu, mx, mo, a);
 }
 
@@ -823,14 +906,14 @@ cudaError_t launch_ffn_down_e4m3(const void *H, const uint8_t *Wd, const float *
         (err = rows_map(&mh, H, cap, f)) != cudaSuccess ||
         (err = out_map(&mo, Ys, cap, d, Kind<false>::kUnitM)) != cudaSuccess)
         return err;
-    auto kern = k_ffn<false, false, true>;
+    auto kern = k_ffn<false, false, kWiden>;
     err = ensure_smem_limit(reinterpret_cast<const void *>(kern), kSlotDownE4m3,
-                            ffn_smem_bytes<true>(MOE_MAX_EXPERTS));
+                            ffn_smem_bytes<kWiden>(MOE_MAX_EXPERTS));
     if (err != cudaSuccess)
         return err;
     const FfnArgs a{offsets, nullptr, srt_w, static_cast<uint16_t *>(Ys), status, cap, E, f, d,
-                    -1, sd, sd};
-    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreadsW8), ffn_smem_bytes<true>(E),
+                    -1, sd, sd, nullptr};
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreadsW8), ffn_smem_bytes<kWiden>(E),
                       stream, mw, mw, mh, mo, a);
 }
 

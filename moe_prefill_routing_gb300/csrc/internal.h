@@ -68,13 +68,25 @@ cudaError_t launch_ffn_down(const void *H, const void *Wd, const int32_t *offset
                             const float *srt_w, int E, int d, int f, int64_t cap, void *Ys,
                             uint32_t *status, cudaStream_t stream);
 
+// E4M3 rows for the gate/up GEMM on E4M3 operands (codes [cap, d], row
+// exponents [cap]); see rows.cu.
+cudaError_t launch_gather_e4m3(const void *x, int T, int d, const int32_t *srt_tok,
+                               const int32_t *offsets, int E, int64_t cap, uint8_t *xs8,
+                               int32_t *xexp, cudaStream_t stream);
+
 // E4M3 weights (codes [E, K, M]) with fp32 scales [E, M]; see quant.cu.
 cudaError_t launch_quantize_e4m3(const void *W, int E, int K, int M, uint8_t *q, float *scale,
-                                 cudaStream_t stream);
+                                 bool kmajor, cudaStream_t stream);
 cudaError_t launch_ffn_gate_up_e4m3(const void *xs, const uint8_t *Wg, const float *sg,
                                     const uint8_t *Wu, const float *su, const int32_t *offsets,
                                     int E, int d, int f, int64_t cap, void *H, uint32_t *status,
                                     cudaStream_t stream);
+// gate/up on E4M3 rows (xs8 [cap, d], row exponents xexp) and K-major E4M3
+// weight codes Wg, Wu [E, f, d] with scales [E, f].
+cudaError_t launch_ffn_gate_up_native(const uint8_t *xs8, const int32_t *xexp, const uint8_t *Wg,
+                                      const float *sg, const uint8_t *Wu, const float *su,
+                                      const int32_t *offsets, int E, int d, int f, int64_t cap,
+                                      void *H, uint32_t *status, cudaStream_t stream);
 cudaError_t launch_ffn_down_e4m3(const void *H, const uint8_t *Wd, const float *sd,
                                  const int32_t *offsets, const float *srt_w, int E, int d, int f,
                                  int64_t cap, void *Ys, uint32_t *status, cudaStream_t stream);
@@ -116,6 +128,7 @@ enum SmemSlot {
     kSlotDown,
     kSlotGateUpE4m3,
     kSlotDownE4m3,
+    kSlotGateUpNative,
     kSlotCount
 };
 

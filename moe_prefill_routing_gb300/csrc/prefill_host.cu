@@ -115,18 +115,18 @@ size_t moe_prefill_host_workspace_bytes(int T, int d, int E, int k, int f, int t
 int moe_prefill_forward_host(int n_chunks, const void *const *x_h, const int32_t *const *ids_h,
                              const float *const *w_h, void *const *y_h, const void *Wg,
                              const void *Wu, const void *Wd, const float *sg, const float *su,
-                             const float *sd, int T, int d, int E, int k, int f, int tm,
-                             void *ws, size_t ws_bytes, moe_stream_t stream)
+                             const float *sd, int act_e4m3, int T, int d, int E, int k, int f,
+                             int tm, void *ws, size_t ws_bytes, moe_stream_t stream)
 {
     if (n_chunks < 0)
         return MOE_ERR_SHAPE;
     moe::HostLayout L;
     // the shape rules of moe_layer_forward, checked before anything is enqueued
     if (tm < 16 || tm % 16 != 0 || d <= 0 || f <= 0 || d % 64 != 0 || f % 64 != 0 ||
-        !moe::host_layout(T, d, E, k, f, tm, L))
+        (act_e4m3 && d % 128 != 0) || !moe::host_layout(T, d, E, k, f, tm, L))
         return MOE_ERR_SHAPE;
     if (!Wg || !Wu || !Wd || !ws || (n_chunks > 0 && (!x_h || !ids_h || !w_h || !y_h)) ||
-        (sg && (!su || !sd)))
+        (sg && (!su || !sd)) || (act_e4m3 && !sg))
         return MOE_ERR_NULL;
     for (int c = 0; T > 0 && c < n_chunks; ++c)
         if (!x_h[c] || !ids_h[c] || !w_h[c] || !y_h[c])
@@ -183,13 +183,15 @@ int moe_prefill_forward_host(int n_chunks, const void *const *x_h, const int32_t
             e = cudaStreamWaitEvent(s, back[b], 0);
         if (e != cudaSuccess)
             break;
+        const uint8_t *qg = static_cast<const uint8_t *>(Wg), *qu = static_cast<const uint8_t *>(Wu),
+                      *qd = static_cast<const uint8_t *>(Wd);
         const int rc =
-            sg ? moe_layer_forward_e4m3(x, ids, w, static_cast<const uint8_t *>(Wg), sg,
-                                        static_cast<const uint8_t *>(Wu), su,
-                                        static_cast<const uint8_t *>(Wd), sd, T, d, E, k, f, tm, y,
-                                        layer_ws, L.layer, stream)
-               : moe_layer_forward(x, ids, w, Wg, Wu, Wd, T, d, E, k, f, tm, y, layer_ws, L.layer,
-                                   stream);
+            act_e4m3 ? moe_layer_forward_f8(x, ids, w, qg, sg, qu, su, qd, sd, T, d, E, k, f, tm,
+                                            y, layer_ws, L.layer, stream)
+            : sg     ? moe_layer_forward_e4m3(x, ids, w, qg, sg, qu, su, qd, sd, T, d, E, k, f, tm,
+                                              y, layer_ws, L.layer, stream)
+                     : moe_layer_forward(x, ids, w, Wg, Wu, Wd, T, d, E, k, f, tm, y, layer_ws,
+                                         L.layer, stream);
         if (rc != MOE_OK)
             return rc;
         e = cudaEventRecord(out[b], s);

@@ -292,6 +292,21 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// Same with 8-bit (or 6-/4-bit) operands: A and B formats in the instruction
+// descriptor, K = 32 elements per instruction.
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // 32 lanes x 16 consecutive 32-bit columns: thread i of the warp receives
 // lane (quadrant base + i), columns [col, col+16).
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16])
@@ -345,6 +360,13 @@ __host__ __device__ __forceinline__ constexpr uint32_t idesc_bf16_f32(uint32_t M
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn_major << 15) | (b_mn_major << 16) |
            ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// Instruction descriptor of tcgen05.mma.kind::f8f6f4 with E4M3 A and B
+// (format code 0 in bits 7-9 and 10-12), both K-major, fp32 accumulator.
+__host__ __device__ __forceinline__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N)
+{
+    return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 }  // namespace moe

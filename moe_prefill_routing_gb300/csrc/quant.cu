@@ -22,13 +22,13 @@ namespace moe {
 namespace {
 
 constexpr int kQuantThreads = 256;
+constexpr int kTile = 64;  // K-major codes: 64 x 64 tiles transposed through shared memory
 
-// One thread per output feature m of one expert: a pass over K for the
-// largest magnitude, then a pass writing the codes.  Adjacent threads take
-// adjacent features, so every row access of a warp is contiguous.
+// One thread per output feature m of one expert: the largest magnitude
+// over K, then the scale.  Adjacent threads take adjacent features, so
+// every row access of a warp is contiguous.
 __global__ void __launch_bounds__(kQuantThreads)
-    k_quantize_e4m3(const __nv_bfloat16 *__restrict__ W, int K, int M, uint8_t *__restrict__ q,
-                    float *__restrict__ scale)
+    k_quant_scales(const __nv_bfloat16 *__restrict__ W, int K, int M, float *__restrict__ scale)
 {
     const int m = blockIdx.x * kQuantThreads + threadIdx.x;
     const int64_t e = blockIdx.y;
@@ -38,25 +38,63 @@ __global__ void __launch_bounds__(kQuantThreads)
     float amax = 0.0f;
     for (int k = 0; k < K; ++k)
         amax = fmaxf(amax, fabsf(__bfloat162float(col[int64_t(k) * M])));
-    float s = __fdiv_rn(amax, 448.0f);
-    if (s == 0.0f)
-        s = 1.0f;
-    scale[e * M + m] = s;
-    uint8_t *qc = q + e * K * int64_t(M) + m;
-    for (int k = 0; k < K; ++k) {
-        const float v = __fdiv_rn(__bfloat162float(col[int64_t(k) * M]), s);
-        qc[int64_t(k) * M] = __nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+    const float s = __fdiv_rn(amax, 448.0f);
+    scale[e * M + m] = s == 0.0f ? 1.0f : s;
+}
+
+__device__ __forceinline__ uint8_t e4m3_code(__nv_bfloat16 w, float s)
+{
+    return __nv_cvt_float_to_fp8(__fdiv_rn(__bfloat162float(w), s), __NV_SATFINITE, __NV_E4M3);
+}
+
+// Codes in the weights' own layout [E, K, M].
+__global__ void __launch_bounds__(kQuantThreads)
+    k_quant_codes_mn(const __nv_bfloat16 *__restrict__ W, int K, int M,
+                     const float *__restrict__ scale, uint8_t *__restrict__ q)
+{
+    const int m = blockIdx.x * kQuantThreads + threadIdx.x;
+    const int64_t e = blockIdx.y;
+    if (m >= M)
+        return;
+    const float s = scale[e * M + m];
+    const int64_t base = e * K * int64_t(M) + m;
+    for (int k = 0; k < K; ++k)
+        q[base + int64_t(k) * M] = e4m3_code(W[base + int64_t(k) * M], s);
+}
+
+// Codes transposed to [E, M, K] (K contiguous): block (m-tile, k-tile, e)
+// reads a 64 x 64 tile along M, writes it along K.
+__global__ void __launch_bounds__(kQuantThreads)
+    k_quant_codes_km(const __nv_bfloat16 *__restrict__ W, int K, int M,
+                     const float *__restrict__ scale, uint8_t *__restrict__ q)
+{
+    __shared__ uint8_t tile[kTile][kTile + 4];
+    const int m0 = blockIdx.x * kTile, k0 = blockIdx.y * kTile;
+    const int64_t e = blockIdx.z;
+    const int tx = threadIdx.x & (kTile - 1), ty = threadIdx.x / kTile;  // 64 x 4
+    const float s = scale[e * M + m0 + tx];
+    for (int r = ty; r < kTile; r += kQuantThreads / kTile) {
+        const int64_t i = (e * K + k0 + r) * int64_t(M) + m0 + tx;
+        tile[tx][r] = e4m3_code(W[i], s);
     }
+    __syncthreads();
+    for (int r = ty; r < kTile; r += kQuantThreads / kTile)
+        q[(e * M + m0 + r) * int64_t(K) + k0 + tx] = tile[r][tx];
 }
 
 }  // namespace
 
 cudaError_t launch_quantize_e4m3(const void *W, int E, int K, int M, uint8_t *q, float *scale,
-                                 cudaStream_t stream)
+                                 bool kmajor, cudaStream_t stream)
 {
+    const __nv_bfloat16 *w = static_cast<const __nv_bfloat16 *>(W);
     const dim3 grid(unsigned((M + kQuantThreads - 1) / kQuantThreads), unsigned(E));
-    k_quantize_e4m3<<<grid, kQuantThreads, 0, stream>>>(
-        static_cast<const __nv_bfloat16 *>(W), K, M, q, scale);
+    k_quant_scales<<<grid, kQuantThreads, 0, stream>>>(w, K, M, scale);
+    if (kmajor)
+        k_quant_codes_km<<<dim3(unsigned(M / kTile), unsigned(K / kTile), unsigned(E)),
+                           kQuantThreads, 0, stream>>>(w, K, M, scale, q);
+    else
+        k_quant_codes_mn<<<grid, kQuantThreads, 0, stream>>>(w, K, M, scale, q);
     return cudaGetLastError();
 }
 

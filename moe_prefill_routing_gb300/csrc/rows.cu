@@ -14,6 +14,7 @@
 #include "ptx.cuh"
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 namespace moe {
 namespace {
@@ -57,6 +58,73 @@ __global__ void __launch_bounds__(kRowThreads)
             for (int c = lane; c < dvec; c += 32)
                 dst[c] = z;
         }
+    }
+    pdl_launch_dependents();
+}
+
+// The gather with E4M3 rows for the gate/up GEMM on E4M3 operands: each
+// row's codes are its bf16 values times 2^-e, e the smallest integer with
+// max |row| <= 448 * 2^e (0 for zero rows and -1 rows), to the nearest E4M3
+// value; xexp[r] = e.  Power-of-two scaling is exact, so this is one
+// multiply and one conversion per value.  Two passes over the source row
+// (the largest magnitude, then the codes); the second pass reads it from L1.
+__global__ void __launch_bounds__(kRowThreads)
+    k_gather_e4m3(const uint4 *__restrict__ x, int T, int dvec,
+                  const int32_t *__restrict__ srt_tok, const int32_t *__restrict__ offsets,
+                  int E, int64_t cap, uint2 *__restrict__ xs8, int32_t *__restrict__ xexp)
+{
+    pdl_wait();
+    const int64_t R = min(int64_t(offsets[E]), cap);
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = int64_t(gridDim.x) * kRowWarps;
+    for (int64_t r = int64_t(blockIdx.x) * kRowWarps + (threadIdx.x >> 5); r < R; r += nw) {
+        const int t = srt_tok[r];
+        uint2 *dst = xs8 + r * dvec;
+        if (t < 0 || t >= T) {
+            for (int c = lane; c < dvec; c += 32)
+                dst[c] = make_uint2(0u, 0u);
+            if (lane == 0)
+                xexp[r] = 0;
+            continue;
+        }
+        const uint4 *src = x + int64_t(t) * dvec;
+        uint32_t amax_bits = 0;  // bf16 magnitudes order like their bit patterns
+        for (int c = lane; c < dvec; c += 32) {
+            const uint4 v = ldg_nc(src + c);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                amax_bits = max(amax_bits, max(w[i] & 0x7fffu, (w[i] >> 16) & 0x7fffu));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            amax_bits = max(amax_bits, __shfl_xor_sync(0xffffffffu, amax_bits, o));
+        const float amax = __uint_as_float(amax_bits << 16);
+        int e = 0;
+        if (amax > 0.0f) {
+            e = ilogbf(amax) - 8;  // amax in [448 * 2^(e-1), 2 * 448 * 2^e)
+            if (amax > ldexpf(448.0f, e))
+                ++e;
+        }
+        const bool plain = e >= -127 && e <= 126;  // 2^-e a normal fp32
+        const float mul = plain ? __uint_as_float(uint32_t(127 - e) << 23) : 0.0f;
+        for (int c = lane; c < dvec; c += 32) {
+            const uint4 v = ldg_nc(src + c);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t out[2] = {0u, 0u};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float a = __uint_as_float(w[i] << 16), b = __uint_as_float(w[i] & 0xffff0000u);
+                a = plain ? a * mul : ldexpf(a, -e);
+                b = plain ? b * mul : ldexpf(b, -e);
+                const uint32_t pair =
+                    __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+                out[i >> 1] |= pair << (16 * (i & 1));
+            }
+            dst[c] = make_uint2(out[0], out[1]);
+        }
+        if (lane == 0)
+            xexp[r] = e;
     }
     pdl_launch_dependents();
 }
@@ -141,6 +209,19 @@ cudaError_t launch_gather(const void *x, int T, int d, const int32_t *srt_tok,
     return launch_pdl(k_gather, dim3(grid), dim3(kRowThreads), 0, stream,
                       static_cast<const uint4 *>(x), T, dvec, srt_tok, offsets, E, cap,
                       static_cast<uint4 *>(xs));
+}
+
+cudaError_t launch_gather_e4m3(const void *x, int T, int d, const int32_t *srt_tok,
+                               const int32_t *offsets, int E, int64_t cap, uint8_t *xs8,
+                               int32_t *xexp, cudaStream_t stream)
+{
+    const int dvec = d / 8;
+    const int64_t want = (cap + kRowWarps - 1) / kRowWarps;
+    const int64_t cap_grid = int64_t(device_sm_count()) * kCtasPerSm;
+    const int grid = int(want < 1 ? 1 : (want < cap_grid ? want : cap_grid));
+    return launch_pdl(k_gather_e4m3, dim3(grid), dim3(kRowThreads), 0, stream,
+                      static_cast<const uint4 *>(x), T, dvec, srt_tok, offsets, E, cap,
+                      reinterpret_cast<uint2 *>(xs8), xexp);
 }
 
 cudaError_t launch_combine(const void *Ys, const int32_t *pos, int T, int k, int d, void *y,

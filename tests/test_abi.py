@@ -130,14 +130,14 @@ def prefill_host_call(lib, n=2, ptrs=None, **kw):
     # host pointer arrays of stand-in addresses: only checked for NULL here
     arr = (C.c_void_p * max(n, 1))(*([FAKE] * max(n, 1)))
     a = dict(x=arr, ids=arr, w=arr, y=arr, Wg=FAKE, Wu=FAKE, Wd=FAKE, sg=None, su=None, sd=None,
-             T=8, d=64, E=4, k=2, f=64, tm=16, ws=FAKE, ws_bytes=1 << 30)
+             act=0, T=8, d=64, E=4, k=2, f=64, tm=16, ws=FAKE, ws_bytes=1 << 30)
     a.update(ptrs or {})
     a.update(kw)
     cast = lambda v: C.cast(v, C.c_void_p) if isinstance(v, C.Array) else v
     return lib.moe_prefill_forward_host(n, cast(a["x"]), cast(a["ids"]), cast(a["w"]),
                                         cast(a["y"]), a["Wg"], a["Wu"], a["Wd"], a["sg"],
-                                        a["su"], a["sd"], a["T"], a["d"], a["E"], a["k"], a["f"],
-                                        a["tm"], a["ws"], a["ws_bytes"], None)
+                                        a["su"], a["sd"], a["act"], a["T"], a["d"], a["E"], a["k"],
+                                        a["f"], a["tm"], a["ws"], a["ws_bytes"], None)
 
 
 def test_prefill_host_argument_errors(lib):
@@ -153,6 +153,8 @@ def test_prefill_host_argument_errors(lib):
     assert prefill_host_call(lib, ws=FAKE + 128) == B.MOE_ERR_ALIGN
     assert prefill_host_call(lib, Wg=FAKE + 8) == B.MOE_ERR_ALIGN
     assert prefill_host_call(lib, sg=FAKE) == B.MOE_ERR_NULL      # E4M3 needs all three scales
+    assert prefill_host_call(lib, act=1, d=128) == B.MOE_ERR_NULL  # E4M3 rows need E4M3 weights
+    assert prefill_host_call(lib, act=1, sg=FAKE, su=FAKE, sd=FAKE) == B.MOE_ERR_SHAPE  # d % 128
     # nothing to do: returns before any CUDA call
     assert prefill_host_call(lib, n=0) == B.MOE_OK
     assert prefill_host_call(lib, T=0) == B.MOE_OK
@@ -160,10 +162,20 @@ def test_prefill_host_argument_errors(lib):
 
 def test_e4m3_argument_errors(lib):
     q = lib.moe_quantize_e4m3
-    assert q(FAKE, 0, 8, 64, FAKE, FAKE, None) == B.MOE_ERR_SHAPE
-    assert q(FAKE, 4, 0, 64, FAKE, FAKE, None) == B.MOE_ERR_SHAPE
-    assert q(None, 4, 8, 64, FAKE, FAKE, None) == B.MOE_ERR_NULL
-    assert q(FAKE, 4, 8, 64, FAKE, FAKE + 2, None) == B.MOE_ERR_ALIGN
+    assert q(FAKE, 0, 8, 64, FAKE, FAKE, 0, None) == B.MOE_ERR_SHAPE
+    assert q(FAKE, 4, 0, 64, FAKE, FAKE, 0, None) == B.MOE_ERR_SHAPE
+    assert q(FAKE, 4, 96, 64, FAKE, FAKE, 1, None) == B.MOE_ERR_SHAPE    # K-major: K % 64
+    assert q(None, 4, 8, 64, FAKE, FAKE, 0, None) == B.MOE_ERR_NULL
+    assert q(FAKE, 4, 8, 64, FAKE, FAKE + 2, 0, None) == B.MOE_ERR_ALIGN
+    g8 = lib.moe_gather_e4m3
+    assert g8(FAKE, 8, 72, FAKE, FAKE, 4, 100, FAKE, FAKE, None) == B.MOE_ERR_SHAPE  # d % 16
+    assert g8(FAKE, 8, 64, FAKE, FAKE, 4, 100, FAKE, None, None) == B.MOE_ERR_NULL
+    assert g8(FAKE, 8, 64, FAKE, FAKE, 4, 100, FAKE + 8, FAKE, None) == B.MOE_ERR_ALIGN
+    assert g8(FAKE, 8, 64, FAKE, FAKE, 4, 0, FAKE, FAKE, None) == B.MOE_OK
+    gf = lib.moe_ffn_gate_up_f8
+    assert gf(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 64, 100, FAKE, None, None) == B.MOE_ERR_SHAPE
+    assert gf(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 128, 64, 100, FAKE, None, None) == B.MOE_ERR_NULL
+    assert gf(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 128, 64, 0, FAKE, None, None) == B.MOE_OK
     gu = lib.moe_ffn_gate_up_e4m3
     assert gu(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 96, 64, 100, FAKE, None, None) == B.MOE_ERR_SHAPE
     assert gu(FAKE, FAKE, None, FAKE, FAKE, FAKE, 4, 64, 64, 100, FAKE, None, None) == B.MOE_ERR_NULL
@@ -173,6 +185,8 @@ def test_e4m3_argument_errors(lib):
     dn = lib.moe_ffn_down_e4m3
     assert dn(FAKE, FAKE, None, FAKE, FAKE, 4, 64, 64, 100, FAKE, None, None) == B.MOE_ERR_NULL
     assert dn(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 64, 0, FAKE, None, None) == B.MOE_OK
+    lf8 = lib.moe_layer_forward_f8
+    assert lf8(*([FAKE] * 9 + [8, 64, 4, 2, 64, 16, FAKE, FAKE, 1 << 40, None])) == B.MOE_ERR_SHAPE
     lf = lib.moe_layer_forward_e4m3
     ws = 1 << 40
     args = [FAKE] * 9 + [8, 64, 4, 2, 64, 16, FAKE, FAKE, ws, None]
@@ -193,6 +207,11 @@ def test_moe_layer_holds_either_weight_form():
                         torch.empty(shape[0], shape[2], dtype=torch.float32))
     L8 = B.MoeLayer(q(2, 64, 128), q(2, 64, 128), q(2, 128, 64))
     assert (L8.E, L8.d, L8.f, L8.e4m3) == (2, 64, 128, True) and L8._host_ws is None
+    # E4M3 rows: gate/up codes K-major [E, f, d]
+    Lf = B.MoeLayer(q(2, 128, 64), q(2, 128, 64), q(2, 128, 64), act_e4m3=True)
+    assert (Lf.E, Lf.d, Lf.f, Lf.act_e4m3) == (2, 64, 128, True)
+    with pytest.raises(ValueError):
+        B.MoeLayer(t(2, 64, 128), t(2, 64, 128), t(2, 128, 64), act_e4m3=True)
 
 
 def test_status_strings(lib):

@@ -205,3 +205,142 @@ def test_e4m3_layer_host_chunks():
         ref = oracle.layer(inp["x"], inp["ids"], inp["w"], *qw)
         ok, err, bound = layer_tolerance(host_f(ys[c]), ref)
         assert ok, (c, err, bound)
+
+
+# ---- E4M3 activations: gate/up on 8-bit operands (tcgen05 kind::f8f6f4) ----
+
+def kmajor(qs):
+    q, s = qs
+    return np.ascontiguousarray(q.transpose(0, 2, 1)), s
+
+
+def test_quantize_kmajor_matches_oracle_transposed():
+    rng = np.random.default_rng(3)
+    Wf = (rng.standard_normal((3, 192, 320)) * 0.05).astype(np.float32)
+    bits = W.bf16_bits(Wf)
+    q, s = B.quantize_e4m3(dev16(bits), kmajor=True)
+    torch.cuda.synchronize()
+    qo, so = oracle.quantize_e4m3(bits)
+    assert np.array_equal(s.cpu().numpy(), so)
+    assert np.array_equal(q.cpu().numpy(), kmajor((qo, so))[0])
+
+
+def test_gather_e4m3_matches_oracle_rows():
+    T, d, E, k = 300, 256, 7, 3
+    inp = W.make_layer(T, d, E, k, 64, seed=21, skip_frac=0.1, weights=False)
+    xf = W.bits_to_float(inp["x"], "bf16").astype(np.float32)
+    xf[5] *= 1e6                                               # exponents far from 0
+    xf[9] *= 1e-6
+    xf[11] = 0.0                                               # zero row: e = 0
+    xf[13, :] = 448.0                                          # exactly at the top code
+    x = W.bf16_bits(xf)
+    p = oracle.plan(inp["ids"], inp["w"], E, 16)
+    cap = B.capacity(T, k, E, 16)
+    xs8, xexp = B.gather_e4m3(dev16(x), dev(to_cap(p["srt_tok"], cap, fill=-1)),
+                              dev(p["offsets"]), E, cap)
+    torch.cuda.synchronize()
+    R = p["R_pad"]
+    q = xs8.cpu().numpy()[:R]
+    e = xexp.cpu().numpy()[:R]
+    xs = oracle.gather(x, p["srt_tok"])
+    qo, eo = oracle.quantize_rows_e4m3(xs)
+    assert np.array_equal(e, eo)
+    assert np.array_equal(q, qo)
+    pad = p["srt_tok"] < 0
+    assert np.all(q[pad] == 0) and np.all(e[pad] == 0)
+
+
+def run_f8_gate_up(inp, E, d, f, tm, qw, nsample=None, seed=0):
+    p, xs, real, row_e = staged(inp, E, tm)
+    T, k = inp["ids"].shape
+    cap = B.capacity(T, k, E, tm)
+    offsets = dev(p["offsets"])
+    x8, xe = B.gather_e4m3(dev16(inp["x"]), dev(to_cap(p["srt_tok"], cap, fill=-1)), offsets, E,
+                           cap)
+    H = B.ffn_gate_up_f8(x8, xe, q_dev(kmajor(qw[0])), q_dev(kmajor(qw[1])), offsets, cap)
+    rows = real
+    if nsample is not None and len(real) > nsample:
+        rows = np.unique(np.random.default_rng(seed).choice(real, nsample, replace=False))
+    h_ref, _ = oracle.expert_rows(xs, rows, row_e[rows], p["srt_w"][rows], *qw, act_e4m3=True)
+    Hh = host16(H)
+    ok, err, bound = layer_tolerance(W.bits_to_float(Hh[rows], "bf16").astype(np.float64), h_ref)
+    assert ok, f"gate/up f8: max err {err} > {bound}"
+    assert np.all(Hh[np.nonzero(p["srt_tok"] < 0)[0]] == 0)
+
+
+@pytest.mark.parametrize("T,d,E,k,f,tm", [
+    (40, 128, 3, 2, 64, 16),     # one K stage; half the 128-feature box outside f
+    (257, 256, 6, 4, 704, 16),   # f = 5.5 x 128
+    (300, 384, 2, 1, 256, 32),   # experts with several chunks
+    (64, 128, 40, 2, 128, 16),   # many small experts
+])
+def test_f8_gate_up_all_rows(T, d, E, k, f, tm):
+    inp = W.make_layer(T, d, E, k, f, tm=tm, seed=T + d)
+    run_f8_gate_up(inp, E, d, f, tm, quantized(inp))
+
+
+@pytest.mark.parametrize("cfg", [3, 5])
+def test_f8_gate_up_workloads_sampled_rows(cfg):
+    wl = W.workload(cfg)
+    inp = inputs(cfg)
+    qw = []
+    for n in ("Wg", "Wu", "Wd"):
+        q, s = B.quantize_e4m3(dev16(inp[n]))
+        qw.append((q.cpu().numpy(), s.cpu().numpy()))
+    run_f8_gate_up(inp, wl.E, wl.d, wl.f, wl.tm, tuple(qw), nsample=40, seed=cfg)
+
+
+def test_f8_layer_tiny_full_output():
+    wl = W.workload(1)
+    inp = inputs(1)
+    qw = quantized(inp)
+    layer = B.MoeLayer(q_dev(kmajor(qw[0])), q_dev(kmajor(qw[1])), q_dev(qw[2]), tm=wl.tm,
+                       act_e4m3=True)
+    y = layer.forward(dev16(inp["x"]), dev(inp["ids"]), dev(inp["w"]))
+    torch.cuda.synchronize()
+    assert B.read_status(layer._ws) == 0
+    ref = oracle.layer(inp["x"], inp["ids"], inp["w"], *qw, act_e4m3=True)
+    ok, err, bound = layer_tolerance(host_f(y), ref)
+    assert ok, (err, bound)
+
+
+@pytest.mark.parametrize("cfg", [3, 5])
+def test_f8_layer_workloads_sampled_tokens(cfg):
+    wl = W.workload(cfg)
+    inp = inputs(cfg)
+    Wb = [dev16(inp[n]) for n in ("Wg", "Wu", "Wd")]
+    layer = B.MoeLayer.quantized(*Wb, tm=wl.tm, act_e4m3=True)
+    del Wb
+    y = layer.forward(dev16(inp["x"]), dev(inp["ids"]), dev(inp["w"]))
+    torch.cuda.synchronize()
+    assert B.read_status(layer._ws) == 0
+    # the oracle takes the gate/up codes in the weights' own layout
+    tr = lambda qs: (np.ascontiguousarray(qs[0].cpu().numpy().transpose(0, 2, 1)),
+                     qs[1].cpu().numpy())
+    qw = (tr(layer.Wg), tr(layer.Wu), (layer.Wd[0].cpu().numpy(), layer.Wd[1].cpu().numpy()))
+    toks = sample_tokens(inp["ids"], 24, seed=cfg)
+    ref = oracle.layer(inp["x"], inp["ids"], inp["w"], *qw, tokens=toks, act_e4m3=True)
+    ok, err, bound = layer_tolerance(host_f(y)[toks], ref)
+    assert ok, (err, bound)
+    y2 = layer.forward(dev16(inp["x"]), dev(inp["ids"]), dev(inp["w"]))
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
+def test_f8_layer_host_chunks():
+    T, d, E, k, f, tm = 200, 256, 8, 4, 192, 16
+    chunks = [W.make_layer(T, d, E, k, f, tm=tm, seed=80 + c) for c in range(3)]
+    qw = quantized(chunks[0])
+    layer = B.MoeLayer(q_dev(kmajor(qw[0])), q_dev(kmajor(qw[1])), q_dev(qw[2]), tm=tm,
+                       act_e4m3=True)
+    xs = [torch.from_numpy(c["x"].view(np.int16)).view(torch.bfloat16).pin_memory() for c in chunks]
+    ids = [torch.from_numpy(c["ids"]).pin_memory() for c in chunks]
+    ws = [torch.from_numpy(c["w"]).pin_memory() for c in chunks]
+    ys = [torch.empty((T, d), dtype=torch.bfloat16).pin_memory() for _ in chunks]
+    layer.forward_host_chunks(xs, ids, ws, ys)
+    torch.cuda.synchronize()
+    for c, inp in enumerate(chunks):
+        ref_dev = layer.forward(dev16(inp["x"]), dev(inp["ids"]), dev(inp["w"])).cpu()
+        assert torch.equal(ys[c].view(torch.int16), ref_dev.view(torch.int16))
+        ref = oracle.layer(inp["x"], inp["ids"], inp["w"], *qw, act_e4m3=True)
+        ok, err, bound = layer_tolerance(host_f(ys[c]), ref)
+        assert ok, (c, err, bound)
