@@ -355,7 +355,7 @@ static double wval(const wmat_t *W, long e, long r, long c)
 static void expert_job(const uint16_t *xrow, int x_is_f16, const wmat_t *Wg,
                        const wmat_t *Wu, const wmat_t *Wd, long e, int d, int f,
                        int mirror, int a8, double *xv, double *g, double *u, double *h,
-                       double *o)
+                       double *hq, double *o)
 {
     int c, n, m;
     for (c = 0; c < d; c++)
@@ -376,12 +376,15 @@ static void expert_job(const uint16_t *xrow, int x_is_f16, const wmat_t *Wg,
         h[n] = g[n] / (1.0 + exp(-g[n])) * u[n];
         if (mirror)
             h[n] = to_bf16(h[n]);
+        hq[n] = h[n];
     }
+    if (a8) /* ... and the down projection sees h's E4M3 values (h itself is kept) */
+        dequantize_row_e4m3(hq, f);
     for (m = 0; m < d; m++)
         o[m] = 0.0;
     for (n = 0; n < f; n++)
         for (m = 0; m < d; m++)
-            o[m] += h[n] * wval(Wd, e, n, m);
+            o[m] += hq[n] * wval(Wd, e, n, m);
 }
 
 /* A job: one routed row, its expert, and where its results go. */
@@ -405,8 +408,8 @@ static void *pass_worker(void *arg)
 {
     pass_t *p = (pass_t *)arg;
     long d = p->d, f = p->f, j;
-    double *xv = (double *)malloc(sizeof(double) * (size_t)(d + 3 * f));
-    double *g, *u, *hbuf;
+    double *xv = (double *)malloc(sizeof(double) * (size_t)(d + 4 * f));
+    double *g, *u, *hbuf, *hq;
     if (!xv) {
         p->failed = 1;
         return NULL;
@@ -414,12 +417,13 @@ static void *pass_worker(void *arg)
     g = xv + d;
     u = g + f;
     hbuf = u + f;
+    hq = hbuf + f;
     /* jobs are independent; each thread takes every nthreads-th job, so the
      * arithmetic of a job does not depend on the thread count */
     for (j = p->tid; j < p->njobs; j += p->nthreads) {
         const job_t *jb = &p->jobs[j];
         expert_job(jb->xrow, p->x_is_f16, p->Wg, p->Wu, p->Wd, jb->e, p->d, p->f,
-                   p->mirror, p->a8, xv, g, u, jb->h ? jb->h : hbuf, jb->o);
+                   p->mirror, p->a8, xv, g, u, jb->h ? jb->h : hbuf, hq, jb->o);
     }
     free(xv);
     return NULL;
@@ -601,8 +605,10 @@ int oracle_layer_tokens(const uint16_t *x, int x_is_f16, const int32_t *ids,
 }
 
 /* The same layer with E4M3 weights: Wg, Wu codes [E][d][f] with scales
- * [E][f], Wd codes [E][f][d] with scales [E][d].  a8 != 0 also gives the
- * gate/up projections each row's E4M3 values (quantize_row_e4m3). */
+ * [E][f], Wd codes [E][f][d] with scales [E][d].  a8 != 0 also gives both
+ * projections E4M3 inputs: gate/up each row's E4M3 values and down the
+ * E4M3 values of h (after the bf16 rounding in the mirror), each quantized
+ * per row by quantize_row_e4m3. */
 int oracle_layer_tokens_e4m3(const uint16_t *x, int x_is_f16, const int32_t *ids,
                              const float *w, const uint8_t *Wg, const float *sg,
                              const uint8_t *Wu, const float *su, const uint8_t *Wd,

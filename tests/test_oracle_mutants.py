@@ -41,6 +41,7 @@ MUTANTS = {
                               "        if (amax >= ldexp(224.0, e))\n            e++;"),
     "row_scale_ignored": ("        x[c] = ldexp(e4m3_value(e4m3_encode((float)ldexp(x[c], -e))), e);",
                           "        x[c] = e4m3_value(e4m3_encode((float)ldexp(x[c], -e)));"),
+    "down_input_not_quantized": ("        dequantize_row_e4m3(hq, f);", "        (void)hq;"),
     "quantize_amax_axis": ("float a = (float)fabs(bf16_value(W[(e * K + k) * M + m]));",
                            "float a = (float)fabs(bf16_value(W[(e * K + m % K) * M + k % M]));"),
 }
