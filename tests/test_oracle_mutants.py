@@ -17,8 +17,8 @@ MUTANTS = {
                         "h[n] = u[n] / (1.0 + exp(-u[n])) * g[n];"),
     "sigmoid_sign": ("h[n] = g[n] / (1.0 + exp(-g[n])) * u[n];",
                      "h[n] = g[n] / (1.0 + exp(g[n])) * u[n];"),
-    "down_transposed": ("o[m] += h[n] * wval(Wd, e, n, m);",
-                        "o[m] += h[n] * wval(Wd, e, ((long)m * f + n) / d, ((long)m * f + n) % d);"),
+    "down_transposed": ("o[m] += hq[n] * wval(Wd, e, n, m);",
+                        "o[m] += hq[n] * wval(Wd, e, ((long)m * f + n) / d, ((long)m * f + n) % d);"),
     "weight_dropped": ("yt[m] += wt * jobs[jb].o[m];", "yt[m] += jobs[jb].o[m];"),
     "no_padding": ("offsets[e + 1] = (int32_t)(offsets[e] + tiles * tm);",
                    "offsets[e + 1] = (int32_t)(offsets[e] + counts[e]);"),
