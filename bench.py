@@ -145,11 +145,13 @@ class ClockSampler:
                 "window": "timed region" if inwin else "whole run"}
 
 
-def algorithmic(wl, ids, wbytes=2):
+def algorithmic(wl, ids, wbytes=2, abytes=2):
     """Algorithmic work of one layer from the routing itself: active experts,
     real and padded rows, and the bytes / flops each stage must move.
     ``wbytes`` is the size of one weight element (2 bf16, 1 E4M3, which also
-    reads one fp32 scale per expert and output feature)."""
+    reads one fp32 scale per expert and output feature); ``abytes`` the size
+    of one element of the GEMMs' row operands (2 bf16, 1 E4M3 rows of x and
+    H, which also carry one int32 exponent per row)."""
     flat = ids.ravel()
     counts = np.bincount(flat[flat >= 0], minlength=wl.E)
     active = int((counts > 0).sum())
@@ -157,10 +159,15 @@ def algorithmic(wl, ids, wbytes=2):
     R_pad = int((-(-counts // wl.tm) * wl.tm).sum())
     d, f = wl.d, wl.f
     sc = 4 if wbytes == 1 else 0  # E4M3 scales
-    gate_up = active * 2 * (d * f * wbytes + f * sc) + R_pad * d * 2 + R_pad * f * 2
+    ex = 4 if abytes == 1 else 0  # E4M3 row exponents
+    gate_up = (active * 2 * (d * f * wbytes + f * sc) + R_pad * (d * abytes + ex) +
+               R_pad * f * 2)
     gate_up_flops = 4 * d * f * R
-    down = active * (f * d * wbytes + d * sc) + R_pad * f * 2 + R_pad * d * 2 + R_pad * 4
-    gather = wl.T * d * 2 + R_pad * d * 2 + R_pad * 4
+    down = (active * (f * d * wbytes + d * sc) + R_pad * (f * abytes + ex) + R_pad * d * 2 +
+            R_pad * 4)
+    if abytes == 1:  # the pass that turns H into E4M3 rows
+        down += R_pad * f * 2 + R_pad * (f + ex)
+    gather = wl.T * d * 2 + R_pad * (d * abytes + ex) + R_pad * 4
     combine = R * d * 2 + wl.T * d * 2 + R * 4
     plan = 8 * wl.T * wl.k + 4 * wl.T * wl.k + 8 * R_pad + 8 * (wl.E + 1)
     return dict(active=active, R=R, R_pad=R_pad, gate_up=gate_up, gate_up_flops=gate_up_flops,
@@ -210,14 +217,15 @@ def run_native(args, rank, world, local):
     chunk = replicas.chunk_of_rank(rank, world) % wl.n_chunks
     log(f"[rank {rank}] generating {wl.name} (chunk {chunk}) ...")
     inp = W.make_inputs(wl, seed=0, chunk=chunk)
-    e4m3 = args.weights == "e4m3"
-    alg = algorithmic(wl, inp["ids"], wbytes=1 if e4m3 else 2)
+    f8 = args.weights == "f8"
+    e4m3 = args.weights == "e4m3" or f8
+    alg = algorithmic(wl, inp["ids"], wbytes=1 if e4m3 else 2, abytes=1 if f8 else 2)
     x, ids, w = d16(inp["x"], dev), torch.from_numpy(inp["ids"]).to(dev), torch.from_numpy(inp["w"]).to(dev)
     Wg, Wu, Wd = (d16(inp[n], dev) for n in ("Wg", "Wu", "Wd"))
     if e4m3:
         # the experts' weights as E4M3 codes + per-feature scales (quantized
         # once on the device, before anything is timed)
-        layer = B.MoeLayer.quantized(Wg, Wu, Wd, tm=wl.tm)
+        layer = B.MoeLayer.quantized(Wg, Wu, Wd, tm=wl.tm, act_e4m3=f8)
         Wg, Wu, Wd = layer.Wg, layer.Wu, layer.Wd
         torch.cuda.synchronize(dev)
     else:
@@ -266,14 +274,28 @@ def run_native(args, rank, world, local):
     Ys = torch.empty((cap, wl.d), dtype=torch.bfloat16, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     stages = ("plan", "gather", "gate_up", "down", "combine")
-    calls = (lambda: B.plan(ids, w, wl.E, wl.tm, cap=cap, out=o),
-             lambda: B.gather(x, o["srt_tok"], o["offsets"], wl.E, cap, xs=xs),
-             (lambda: B.ffn_gate_up_e4m3(xs, Wg, Wu, o["offsets"], cap, H=H, status=st)) if e4m3
-             else (lambda: B.ffn_gate_up(xs, Wg, Wu, o["offsets"], cap, H=H, status=st)),
-             (lambda: B.ffn_down_e4m3(H, Wd, o["offsets"], o["srt_w"], cap, Ys=Ys, status=st))
-             if e4m3 else (lambda: B.ffn_down(H, Wd, o["offsets"], o["srt_w"], cap, Ys=Ys,
-                                               status=st)),
-             lambda: B.combine(Ys, o["pos"], y=y))
+    if f8:
+        x8, xe = B.gather_e4m3(x, o["srt_tok"], o["offsets"], wl.E, cap)
+        H8, he = B.rows_e4m3(H, o["offsets"], wl.E, cap)
+
+        def down_f8():
+            B.rows_e4m3(H, o["offsets"], wl.E, cap, H8, he)
+            B.ffn_down_f8(H8, he, Wd, o["offsets"], o["srt_w"], cap, Ys=Ys, status=st)
+
+        calls = (lambda: B.plan(ids, w, wl.E, wl.tm, cap=cap, out=o),
+                 lambda: B.gather_e4m3(x, o["srt_tok"], o["offsets"], wl.E, cap, x8, xe),
+                 lambda: B.ffn_gate_up_f8(x8, xe, Wg, Wu, o["offsets"], cap, H=H, status=st),
+                 down_f8,
+                 lambda: B.combine(Ys, o["pos"], y=y))
+    else:
+        calls = (lambda: B.plan(ids, w, wl.E, wl.tm, cap=cap, out=o),
+                 lambda: B.gather(x, o["srt_tok"], o["offsets"], wl.E, cap, xs=xs),
+                 (lambda: B.ffn_gate_up_e4m3(xs, Wg, Wu, o["offsets"], cap, H=H, status=st)) if e4m3
+                 else (lambda: B.ffn_gate_up(xs, Wg, Wu, o["offsets"], cap, H=H, status=st)),
+                 (lambda: B.ffn_down_e4m3(H, Wd, o["offsets"], o["srt_w"], cap, Ys=Ys, status=st))
+                 if e4m3 else (lambda: B.ffn_down(H, Wd, o["offsets"], o["srt_w"], cap, Ys=Ys,
+                                                   status=st)),
+                 lambda: B.combine(Ys, o["pos"], y=y))
     K2 = max(3, min(args.steps, 200))
     per = {s: [] for s in stages}
     for i in range(K2 + 3):
@@ -338,6 +360,9 @@ def run_native(args, rank, world, local):
     if rank != 0:
         return
     hbm, tflops, peak_src = peaks()
+    if f8:  # dense fp8 tensor peak: the measured bf16 figure x the nominal 2x ratio
+        tflops *= 2.0
+        peak_src += " (fp8 = 2 x bf16)"
     t_gu = stage_mean_us["gate_up"] * 1e-6
     # the bound is whichever of the two floors is longer for this kernel
     tensor_bound = alg["gate_up_flops"] / (tflops * 1e12) > alg["gate_up"] / (hbm * 1e9)
@@ -351,13 +376,16 @@ def run_native(args, rank, world, local):
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(ms),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16 (E4M3 weights widened to bf16)" if e4m3 else "bf16",
+        "dtype": ("e4m3 x e4m3 -> f32 (weights and activations)" if f8 else
+                  "bf16 (E4M3 weights widened to bf16)" if e4m3 else "bf16"),
         "data": "synthetic (seeded: x~N(0,1), W~N(0,0.02) bf16, " + ROUTING[wl.routing] + ")",
         "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k, "f": wl.f,
                    "tm": wl.tm, "routing": ROUTING[wl.routing],
                    "active_experts": alg["active"], "R_pad": alg["R_pad"],
                    "weights": ("E4M3 codes + fp32 scale per expert and output feature" if e4m3
                                else "bf16"),
+                   "activations": ("E4M3 rows of x and H, power-of-two scale per row" if f8
+                                   else "bf16"),
                    "l2": "flushed before every timed step (256 MiB write)",
                    "parallelism": "replicas (one independent layer per GPU)"},
         "plan_us_per_layer": plan_graph_us,
@@ -365,8 +393,10 @@ def run_native(args, rank, world, local):
         "plan_us_cold": stage_us["plan"],
         "stages_us": stage_us,
         "layer_hbm_gbs": layer_gbs,
-        "roofline": {"kernel": ("k_ffn<gate/up, E4M3 weights> (widened to bf16 in shared memory; "
-                               "tcgen05 grouped GEMM + SwiGLU)") if e4m3
+        "roofline": {"kernel": ("k_ffn<gate/up, E4M3 operands> (tcgen05.mma.kind::f8f6f4 "
+                               "grouped GEMM + SwiGLU)") if f8
+                     else ("k_ffn<gate/up, E4M3 weights> (widened to bf16 in shared memory; "
+                           "tcgen05 grouped GEMM + SwiGLU)") if e4m3
                      else "k_ffn<gate/up> (tcgen05 grouped GEMM + SwiGLU)",
                      "bound": "tensor" if tensor_bound else "hbm",
                      "achieved": achieved, "peak": peak, "unit": unit,
@@ -382,7 +412,7 @@ def run_native(args, rank, world, local):
                 "l2": "not flushed: every step streams the active expert weights "
                       f"({alg['weights'] / 1e9:.2f} GB > 129 MB L2)"},
         "clocks": clk,
-        "gpu_launches": KERNELS_PER_LAYER * args.steps,
+        "gpu_launches": (KERNELS_PER_LAYER + int(f8)) * args.steps,
     }
     if world == 1 and not args.no_cpu_baseline and not e4m3:
         nth = os.cpu_count() or 1
@@ -437,9 +467,10 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--weights", choices=("bf16", "e4m3"), default="bf16",
-                    help="expert weights: bf16 (the default measurement) or E4M3 codes with "
-                         "per-feature scales")
+    ap.add_argument("--weights", choices=("bf16", "e4m3", "f8"), default="bf16",
+                    help="expert weights: bf16 (the default measurement), E4M3 codes with "
+                         "per-feature scales (bf16 activations), or f8: E4M3 weights and E4M3 "
+                         "activations (both projections on 8-bit operands)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -348,7 +348,15 @@ MOE_API int moe_ffn_down_e4m3(const void *H, const uint8_t *Wd, const float *sd,
  * moe_ffn_gate_up_f8 -- H[r] = bf16(silu(g) * u) with g = 2^xexp[r] *
  * sg[e] * (codes of row r . Wg codes), fp32 accumulation, likewise u: Wg, Wu
  * K-major E4M3 codes [E, f, d] (moe_quantize_e4m3 with kmajor = 1), scales
- * [E, f].  d a multiple of 128.
+ * [E, f].
+ *
+ * moe_rows_e4m3 -- the same per-row quantization of H [cap, f] bf16 itself
+ * (rows < offsets[E]): H8 uint8 [cap, f], hexp int32 [cap].  f a multiple
+ * of 16.
+ *
+ * moe_ffn_down_f8 -- Ys[r] = bf16(srt_w[r] * 2^hexp[r] * sd[e] * (codes of
+ * H row r . Wd codes)), fp32 accumulation: Wd K-major E4M3 codes [E, d, f]
+ * (moe_quantize_e4m3 of Wd [E, f, d] with kmajor = 1), scales sd [E, d].
  */
 MOE_API int moe_gather_e4m3(const void *x, int T, int d, const int32_t *srt_tok,
                             const int32_t *offsets, int E, int64_t cap, uint8_t *xs8,
@@ -357,6 +365,12 @@ MOE_API int moe_ffn_gate_up_f8(const uint8_t *xs8, const int32_t *xexp, const ui
                                const float *sg, const uint8_t *Wu, const float *su,
                                const int32_t *offsets, int E, int d, int f, int64_t cap, void *H,
                                uint32_t *status, moe_stream_t stream);
+MOE_API int moe_rows_e4m3(const void *H, int f, const int32_t *offsets, int E, int64_t cap,
+                          uint8_t *H8, int32_t *hexp, moe_stream_t stream);
+MOE_API int moe_ffn_down_f8(const uint8_t *H8, const int32_t *hexp, const uint8_t *Wd,
+                            const float *sd, const int32_t *offsets, const float *srt_w, int E,
+                            int d, int f, int64_t cap, void *Ys, uint32_t *status,
+                            moe_stream_t stream);
 
 /* moe_layer_forward with E4M3 weights (as above); same workspace
  * (moe_workspace_bytes) and outputs. */
@@ -366,11 +380,11 @@ MOE_API int moe_layer_forward_e4m3(const void *x, const int32_t *ids, const floa
                                    int d, int E, int k, int f, int tm, void *y, void *ws,
                                    size_t ws_bytes, moe_stream_t stream);
 
-/* moe_layer_forward_f8 -- the layer with moe_gather_e4m3 and
- * moe_ffn_gate_up_f8 (Wg, Wu K-major codes [E, f, d]) in place of the
- * gather and gate/up; down as in moe_layer_forward_e4m3 (Wd codes
- * [E, f, d]).  d a multiple of 128; same workspace (the E4M3 rows and their
- * exponents sit in its xs field). */
+/* moe_layer_forward_f8 -- the layer with both projections on 8-bit
+ * operands: moe_gather_e4m3 -> moe_ffn_gate_up_f8 (Wg, Wu K-major codes
+ * [E, f, d]) -> moe_rows_e4m3 -> moe_ffn_down_f8 (Wd K-major codes
+ * [E, d, f]) -> moe_combine.  Same workspace (the E4M3 rows and their
+ * exponents, first of x then of H, sit in its xs field). */
 MOE_API int moe_layer_forward_f8(const void *x, const int32_t *ids, const float *w,
                                  const uint8_t *Wg, const float *sg, const uint8_t *Wu,
                                  const float *su, const uint8_t *Wd, const float *sd, int T,

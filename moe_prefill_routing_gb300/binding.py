@@ -70,6 +70,11 @@ _SIGS = {
     "moe_ffn_gate_up_f8": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                      C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int,
                                      C.c_int, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p]),
+    "moe_rows_e4m3": (C.c_int, [C.c_void_p, C.c_int, C.c_void_p, C.c_int, C.c_int64, C.c_void_p,
+                                C.c_void_p, C.c_void_p]),
+    "moe_ffn_down_f8": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                  C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int64, C.c_void_p,
+                                  C.c_void_p, C.c_void_p]),
     "moe_layer_forward_f8": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                        C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                        C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int,
@@ -349,7 +354,7 @@ def prefill_forward_host(x_hs, ids_hs, w_hs, y_hs, Wg, Wu, Wd, tm: int, ws=None,
     if not (len(ids_hs) == len(w_hs) == len(y_hs) == n):
         raise ValueError("one ids, w and y per chunk")
     (Wg, Wu, Wd), scales = _split_weights(Wg, Wu, Wd)
-    E, f, d = Wd.shape
+    E, f, d = Wg.shape if act_e4m3 else Wd.shape
     T, k = (ids_hs[0].shape if n else (0, 1))
     dev = Wg.device
     nbytes = prefill_host_workspace_bytes(T, d, E, k, f, tm)
@@ -417,6 +422,35 @@ def ffn_gate_up_f8(xs8, xexp, Wg, Wu, offsets, cap: int, H=None, status=None):
     return H
 
 
+def rows_e4m3(H, offsets, E: int, cap: int, H8=None, hexp=None):
+    """moe_rows_e4m3: the rows of H [cap, f] as (uint8 codes [cap, f], int32
+    exponents [cap])."""
+    f = H.shape[1]
+    if H8 is None:
+        H8 = torch.empty((max(cap, 1), f), dtype=torch.uint8, device=H.device)
+    if hexp is None:
+        hexp = torch.empty(max(cap, 1), dtype=torch.int32, device=H.device)
+    with torch.cuda.device(H.device):
+        rc = lib().moe_rows_e4m3(_ptr(H), f, _ptr(offsets), E, cap, _ptr(H8), _ptr(hexp),
+                                 _stream(H.device))
+    _check("moe_rows_e4m3", rc)
+    return H8, hexp
+
+
+def ffn_down_f8(H8, hexp, Wd, offsets, srt_w, cap: int, Ys=None, status=None):
+    """moe_ffn_down_f8 with the K-major (codes, scales) pair Wd [E, d, f]."""
+    qd, sd = Wd
+    E, d, f = qd.shape
+    if Ys is None:
+        Ys = torch.empty((max(cap, 1), d), dtype=torch.bfloat16, device=H8.device)
+    with torch.cuda.device(H8.device):
+        rc = lib().moe_ffn_down_f8(_ptr(H8), _ptr(hexp), _ptr(qd), _ptr(sd), _ptr(offsets),
+                                   _ptr(srt_w), E, d, f, cap, _ptr(Ys), _ptr(status),
+                                   _stream(H8.device))
+    _check("moe_ffn_down_f8", rc)
+    return Ys
+
+
 def ffn_gate_up_e4m3(xs, Wg, Wu, offsets, cap: int, H=None, status=None):
     (qg, sg), (qu, su) = Wg, Wu
     E, d, f = qg.shape
@@ -444,11 +478,11 @@ def ffn_down_e4m3(H, Wd, offsets, srt_w, cap: int, Ys=None, status=None):
 
 def layer_forward_e4m3(x, ids, w, Wg, Wu, Wd, tm: int, y=None, ws=None, act_e4m3: bool = False):
     """moe_layer_forward_e4m3 with (codes, scales) weight pairs, or with
-    act_e4m3 moe_layer_forward_f8 (Wg, Wu codes K-major)."""
+    act_e4m3 moe_layer_forward_f8 (all three codes K-major)."""
     T, d = x.shape
     k = ids.shape[1]
     (qg, sg), (qu, su), (qd, sd) = Wg, Wu, Wd
-    E, f, _ = qd.shape
+    E, f = qg.shape[0], sg.shape[1]
     dev = x.device
     if y is None:
         y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
@@ -503,9 +537,10 @@ class MoeLayer:
         self.act_e4m3 = bool(act_e4m3)
         if self.act_e4m3 and not self.e4m3:
             raise ValueError("E4M3 activations come with E4M3 weights")
-        wd = Wd[0] if self.e4m3 else Wd   # [E, f, d] in every form
-        self.E, self.f, self.d = wd.shape
-        self.device = wd.device
+        # Wd is [E, f, d] except with E4M3 rows, where Wg is (K-major)
+        ref = Wg[0] if self.act_e4m3 else (Wd[0] if self.e4m3 else Wd)
+        self.E, self.f, self.d = ref.shape
+        self.device = ref.device
         self._ws = None
         self._host_ws = None
 
@@ -515,7 +550,7 @@ class MoeLayer:
         with act_e4m3 the gate/up projection also runs on E4M3 rows (its
         weight codes K-major)."""
         return cls(quantize_e4m3(Wg, kmajor=act_e4m3), quantize_e4m3(Wu, kmajor=act_e4m3),
-                   quantize_e4m3(Wd), tm=tm, act_e4m3=act_e4m3)
+                   quantize_e4m3(Wd, kmajor=act_e4m3), tm=tm, act_e4m3=act_e4m3)
 
     def workspace(self, T: int, k: int):
         n = workspace_bytes(T, self.d, self.E, k, self.f, self.tm)

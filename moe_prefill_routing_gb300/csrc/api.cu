@@ -95,7 +95,9 @@ int layout(int T, int d, int E, int k, int f, int tm, size_t *out)
         size_t(cap) * 4,                                 // srt_w
         size_t(n) * 4,                                   // pos
         size_t(cap / tm + 1) * 4,                        // tile_expert
-        size_t(cap) * d * 2,                             // xs
+        // xs; with E4M3 activations it holds the E4M3 rows and their
+        // exponents, later those of H
+        std::max(size_t(cap) * d * 2, align256(size_t(cap) * f) + size_t(cap) * 4),
         size_t(cap) * f * 2,                             // H
         size_t(cap) * d * 2,                             // Ys
     };
@@ -284,7 +286,7 @@ static int layer_forward(const void *x, const int32_t *ids, const float *w,
 {
     const bool e4m3 = W.sg != nullptr;
     if (!base_sizes_ok(T, k, E) || tm < 16 || tm > MOE_MAX_TM || tm % 16 != 0 || d <= 0 ||
-        f <= 0 || d % 64 != 0 || f % 64 != 0 || (W.act_e4m3 && d % 128 != 0))
+        f <= 0 || d % 64 != 0 || f % 64 != 0)
         return MOE_ERR_SHAPE;
     if (!W.Wg || !W.Wu || !W.Wd || !ws || (T > 0 && (!x || !ids || !w || !y)) ||
         (e4m3 && (!W.su || !W.sd)))
@@ -330,10 +332,20 @@ static int layer_forward(const void *x, const int32_t *ids, const float *w,
                                                       H, status, s)
                        : moe::launch_ffn_gate_up(xs, W.Wg, W.Wu, offsets, E, d, f, cap, H, status,
                                                  s);
+    // E4M3 activations: H's rows become E4M3 rows in the xs field (free once
+    // gate/up has run), then down runs on them
+    uint8_t *h8 = xs8;
+    int32_t *hexp = reinterpret_cast<int32_t *>(h8 + ((size_t(cap) * f + 255) & ~size_t(255)));
+    if (e == cudaSuccess && W.act_e4m3)
+        e = moe::launch_rows_e4m3(H, f, offsets, E, cap, h8, hexp, s);
+    const uint8_t *qd = static_cast<const uint8_t *>(W.Wd);
     if (e == cudaSuccess)
-        e = e4m3 ? moe::launch_ffn_down_e4m3(H, static_cast<const uint8_t *>(W.Wd), W.sd, offsets,
-                                             srt_w, E, d, f, cap, Ys, status, s)
-                 : moe::launch_ffn_down(H, W.Wd, offsets, srt_w, E, d, f, cap, Ys, status, s);
+        e = W.act_e4m3 ? moe::launch_ffn_down_native(h8, hexp, qd, W.sd, offsets, srt_w, E, d, f,
+                                                     cap, Ys, status, s)
+            : e4m3     ? moe::launch_ffn_down_e4m3(H, qd, W.sd, offsets, srt_w, E, d, f, cap, Ys,
+                                                   status, s)
+                       : moe::launch_ffn_down(H, W.Wd, offsets, srt_w, E, d, f, cap, Ys, status,
+                                              s);
     if (e == cudaSuccess)
         e = moe::launch_combine(Ys, pos, T, k, d, y, s);
     return cuda_rc(e);
@@ -406,8 +418,6 @@ int moe_ffn_gate_up_f8(const uint8_t *xs8, const int32_t *xexp, const uint8_t *W
                        uint32_t *status, moe_stream_t stream)
 {
     int rc = ffn_checks(xs8, Wg, Wu, offsets, E, d, f, cap, H);
-    if (rc == MOE_OK && d % 128 != 0)
-        rc = MOE_ERR_SHAPE;
     if (rc == MOE_OK && (!sg || !su || !xexp))
         rc = MOE_ERR_NULL;
     if (rc == MOE_OK &&
@@ -417,6 +427,37 @@ int moe_ffn_gate_up_f8(const uint8_t *xs8, const int32_t *xexp, const uint8_t *W
         return rc;
     return cuda_rc(moe::launch_ffn_gate_up_native(xs8, xexp, Wg, sg, Wu, su, offsets, E, d, f, cap,
                                                   H, status, as_stream(stream)));
+}
+
+int moe_rows_e4m3(const void *H, int f, const int32_t *offsets, int E, int64_t cap, uint8_t *H8,
+                  int32_t *hexp, moe_stream_t stream)
+{
+    if (f <= 0 || f % 16 != 0 || E < 1 || E > MOE_MAX_EXPERTS)
+        return MOE_ERR_SHAPE;
+    if (cap < 0 || cap > INT_MAX)
+        return MOE_ERR_CAPACITY;
+    if (!H || !offsets || !H8 || !hexp)
+        return MOE_ERR_NULL;
+    if (!aligned(H, 16) || !aligned(H8, 16) || !aligned(hexp, 4) || !aligned(offsets, 4))
+        return MOE_ERR_ALIGN;
+    if (cap == 0)
+        return MOE_OK;
+    return cuda_rc(moe::launch_rows_e4m3(H, f, offsets, E, cap, H8, hexp, as_stream(stream)));
+}
+
+int moe_ffn_down_f8(const uint8_t *H8, const int32_t *hexp, const uint8_t *Wd, const float *sd,
+                    const int32_t *offsets, const float *srt_w, int E, int d, int f, int64_t cap,
+                    void *Ys, uint32_t *status, moe_stream_t stream)
+{
+    int rc = ffn_checks(H8, Wd, srt_w, offsets, E, d, f, cap, Ys);
+    if (rc == MOE_OK && (!sd || !hexp))
+        rc = MOE_ERR_NULL;
+    if (rc == MOE_OK && (!aligned(sd, 4) || !aligned(hexp, 4) || !aligned(status, 4)))
+        rc = MOE_ERR_ALIGN;
+    if (rc != MOE_OK || cap == 0)
+        return rc;
+    return cuda_rc(moe::launch_ffn_down_native(H8, hexp, Wd, sd, offsets, srt_w, E, d, f, cap, Ys,
+                                               status, as_stream(stream)));
 }
 
 int moe_ffn_gate_up_e4m3(const void *xs, const uint8_t *Wg, const float *sg, const uint8_t *Wu,

@@ -40,10 +40,12 @@
 // tiles would be (MN-major, 128-byte swizzle), and the epilogue multiplies
 // each accumulator row (one output feature) by its scale.  The MMAs are the
 // same bf16 MMAs.
-// kNative (gate/up): the weight codes are stored K-major [E, f, d] and the
-// routed rows are E4M3 codes with a power-of-two scale per row (rows.cu);
-// both go straight to tcgen05.mma.kind::f8f6f4, K = 128 per stage in the
-// same 128-byte rows, and the epilogue multiplies by feature scale times
+// kNative: the weight codes are stored K-major ([E, f, d] for gate/up,
+// [E, d, f] for down) and the rows (routed x rows, or H rows for down) are
+// E4M3 codes with a power-of-two scale per row (rows.cu); both go straight
+// to tcgen05.mma.kind::f8f6f4, K = 128 per stage in the same 128-byte rows
+// (a K that is not a multiple of 128 ends in a stage whose upper half the
+// TMA fills with zeros), and the epilogue multiplies by feature scale times
 // row scale.
 // Every output element is written by one CTA with a fixed K order: results
 // are deterministic.  Every wait is bounded (2 s); on a timeout the CTA
@@ -281,7 +283,6 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
 {
     constexpr bool W8 = WM == kWiden, A8 = WM == kNative, SCALED = WM != kBf16;
     static_assert(!(GATHER && SCALED), "gathered rows come with bf16 weights only");
-    static_assert(!A8 || GATED, "E4M3 activations feed the gate/up projection only");
     constexpr int S = kStages;
     constexpr int UM = Kind<GATED>::kUnitM;
     constexpr uint32_t SB = Cfg<WM>::kStageB;
@@ -293,6 +294,8 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
     Ctrl<S> *ctl = reinterpret_cast<Ctrl<S> *>(smem + Cfg<WM>::kRingBytes + kStgBytes);
     int *row_tok = reinterpret_cast<int *>(ctl + 1);  // [BN] tokens of the unit's rows
     float *row_w = reinterpret_cast<float *>(row_tok + BN);  // [BN] routing weights (down)
+    // kNative: the unit's row scales (gate/up has no routing weights to stage)
+    float *row_s = GATED ? row_w : reinterpret_cast<float *>(row_tok);
     int *chunk_start = row_tok + 2 * BN;
     const int warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
@@ -338,7 +341,7 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
     const int total_chunks =
         build_chunk_table(p.offsets, p.E, p.cap, chunk_start, ctl->warp_sum, p.status);
     const int n_mt = (p.M + UM - 1) / UM;
-    const int nk = p.K / Cfg<WM>::kKStep;
+    const int nk = (p.K + Cfg<WM>::kKStep - 1) / Cfg<WM>::kKStep;
     const int64_t total_units = int64_t(total_chunks) * n_mt;
 
     // first feature of A tile t of a unit starting at feature m0
@@ -368,7 +371,7 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                 // inside M (features past M are zero-filled and still counted)
                 const uint32_t a_bytes =
                     W8 ? (1u + uint32_t(tile_base(m0, 1) < p.M)) * kA8TileBytes
-                    : A8 ? 2u * kATileBytes  // 128 features x 128 K codes per tile
+                    : A8 ? (1u + uint32_t(tile_base(m0, 1) < p.M)) * kATileBytes  // 128 x 128 codes
                          : boxes * kABoxBytes;
                 const uint32_t bytes = a_bytes + uint32_t(w.nrows) * uint32_t(BK * 2);
                 for (int kb = 0; kb < nk; ++kb) {
@@ -390,7 +393,9 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                                             w.e);
                         } else if (A8) {
                             // K-major codes [E, M, K]: coordinates (k, feature, expert)
-                            tma_load_3d(sa + t * kATileBytes, m, fb, k0, tile_base(m0, t), w.e);
+                            if (tile_base(m0, t) < p.M)
+                                tma_load_3d(sa + t * kATileBytes, m, fb, k0, tile_base(m0, t),
+                                            w.e);
                         } else {
 #pragma unroll
                             for (int h = 0; h < 2; ++h) {
@@ -474,8 +479,10 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                             const uint32_t acc = (kb | kk) != 0;
                             tc_mma_f8(d0, smem_desc_sw128(sa + kk * 32, 16, 1024), bdesc, idesc,
                                       acc);
-                            tc_mma_f8(d0 + BN, smem_desc_sw128(sa + kATileBytes + kk * 32, 16, 1024),
-                                      bdesc, idesc, acc);
+                            if (use1)
+                                tc_mma_f8(d0 + BN,
+                                          smem_desc_sw128(sa + kATileBytes + kk * 32, 16, 1024),
+                                          bdesc, idesc, acc);
                         }
                     } else {
 #pragma unroll
@@ -602,7 +609,7 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
             if (!GATED && et < w.nrows)  // read by every thread of the unit's chunks
                 row_w[et] = p.srt_w[w.row0 + et];
             if (A8 && et < w.nrows)  // the rows' scales 2^e
-                row_w[et] = ldexpf(1.0f, p.row_exp[w.row0 + et]);
+                row_s[et] = ldexpf(1.0f, p.row_exp[w.row0 + et]);
             if (!mbar_wait(&ctl->tmem_full[abuf], aphase, abort_flag))
                 *reinterpret_cast<volatile int *>(&ctl->epi_stop) = 1;
             epi_bar();
@@ -619,8 +626,8 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                     tmem_ld_32x32b_x16(t0 + BN + uint32_t(c0), b);
                 tmem_ld_wait();
                 float v0[16], v1[16];
+                const float *rs = row_s + c0;
                 if (GATED) {
-                    const float *rs = row_w + c0;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const float s0 = A8 ? sc0 * rs[j] : sc0, s1 = A8 ? sc1 * rs[j] : sc1;
@@ -633,10 +640,9 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                     const float *wr = row_w + c0;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const float o0 =
-                            SCALED ? __uint_as_float(a[j]) * sc0 : __uint_as_float(a[j]);
-                        const float o1 =
-                            SCALED ? __uint_as_float(b[j]) * sc1 : __uint_as_float(b[j]);
+                        const float s0 = A8 ? sc0 * rs[j] : sc0, s1 = A8 ? sc1 * rs[j] : sc1;
+                        const float o0 = SCALED ? __uint_as_float(a[j]) * s0 : __uint_as_float(a[j]);
+                        const float o1 = SCALED ? __uint_as_float(b[j]) * s1 : __uint_as_float(b[j]);
                         v0[j] = wr[j] * o0;
                         v1[j] = use1 ? wr[j] * o1 : 0.0f;
                     }
@@ -894,6 +900,28 @@ cudaError_t launch_ffn_gate_up_native(const uint8_t *xs8, const int32_t *xexp, c
                     -1, sg, su, xexp};
     return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<kNative>(E),
                       stream, mg, mu, mx, mo, a);
+}
+
+cudaError_t launch_ffn_down_native(const uint8_t *H8, const int32_t *hexp, const uint8_t *Wd,
+                                   const float *sd, const int32_t *offsets, const float *srt_w,
+                                   int E, int d, int f, int64_t cap, void *Ys, uint32_t *status,
+                                   cudaStream_t stream)
+{
+    CUtensorMap mw, mh, mo;
+    cudaError_t err;
+    if ((err = weight_map_e4m3_kmajor(&mw, Wd, E, f, d)) != cudaSuccess ||
+        (err = rows_map_e4m3(&mh, H8, cap, f)) != cudaSuccess ||
+        (err = out_map(&mo, Ys, cap, d, Kind<false>::kUnitM)) != cudaSuccess)
+        return err;
+    auto kern = k_ffn<false, false, kNative>;
+    err = ensure_smem_limit(reinterpret_cast<const void *>(kern), kSlotDownNative,
+                            ffn_smem_bytes<kNative>(MOE_MAX_EXPERTS));
+    if (err != cudaSuccess)
+        return err;
+    const FfnArgs a{offsets, nullptr, srt_w, static_cast<uint16_t *>(Ys), status, cap, E, f, d,
+                    -1, sd, sd, hexp};
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<kNative>(E),
+                      stream, mw, mw, mh, mo, a);
 }
 
 cudaError_t launch_ffn_down_e4m3(const void *H, const uint8_t *Wd, const float *sd,

@@ -74,6 +74,10 @@ cudaError_t launch_gather_e4m3(const void *x, int T, int d, const int32_t *srt_t
                                const int32_t *offsets, int E, int64_t cap, uint8_t *xs8,
                                int32_t *xexp, cudaStream_t stream);
 
+// E4M3 rows of H [cap, f] itself (rows < offsets[E]).
+cudaError_t launch_rows_e4m3(const void *H, int f, const int32_t *offsets, int E, int64_t cap,
+                             uint8_t *H8, int32_t *hexp, cudaStream_t stream);
+
 // E4M3 weights (codes [E, K, M]) with fp32 scales [E, M]; see quant.cu.
 cudaError_t launch_quantize_e4m3(const void *W, int E, int K, int M, uint8_t *q, float *scale,
                                  bool kmajor, cudaStream_t stream);
@@ -87,6 +91,12 @@ cudaError_t launch_ffn_gate_up_native(const uint8_t *xs8, const int32_t *xexp, c
                                       const float *sg, const uint8_t *Wu, const float *su,
                                       const int32_t *offsets, int E, int d, int f, int64_t cap,
                                       void *H, uint32_t *status, cudaStream_t stream);
+// down on E4M3 rows of H (H8 [cap, f], exponents hexp) and K-major E4M3
+// codes Wd [E, d, f] with scales [E, d].
+cudaError_t launch_ffn_down_native(const uint8_t *H8, const int32_t *hexp, const uint8_t *Wd,
+                                   const float *sd, const int32_t *offsets, const float *srt_w,
+                                   int E, int d, int f, int64_t cap, void *Ys, uint32_t *status,
+                                   cudaStream_t stream);
 cudaError_t launch_ffn_down_e4m3(const void *H, const uint8_t *Wd, const float *sd,
                                  const int32_t *offsets, const float *srt_w, int E, int d, int f,
                                  int64_t cap, void *Ys, uint32_t *status, cudaStream_t stream);
@@ -129,6 +139,7 @@ enum SmemSlot {
     kSlotGateUpE4m3,
     kSlotDownE4m3,
     kSlotGateUpNative,
+    kSlotDownNative,
     kSlotCount
 };
 

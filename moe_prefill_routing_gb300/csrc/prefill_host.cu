@@ -123,7 +123,7 @@ int moe_prefill_forward_host(int n_chunks, const void *const *x_h, const int32_t
     moe::HostLayout L;
     // the shape rules of moe_layer_forward, checked before anything is enqueued
     if (tm < 16 || tm % 16 != 0 || d <= 0 || f <= 0 || d % 64 != 0 || f % 64 != 0 ||
-        (act_e4m3 && d % 128 != 0) || !moe::host_layout(T, d, E, k, f, tm, L))
+        !moe::host_layout(T, d, E, k, f, tm, L))
         return MOE_ERR_SHAPE;
     if (!Wg || !Wu || !Wd || !ws || (n_chunks > 0 && (!x_h || !ids_h || !w_h || !y_h)) ||
         (sg && (!su || !sd)) || (act_e4m3 && !sg))

@@ -68,6 +68,8 @@ __global__ void __launch_bounds__(kRowThreads)
 // value; xexp[r] = e.  Power-of-two scaling is exact, so this is one
 // multiply and one conversion per value.  Two passes over the source row
 // (the largest magnitude, then the codes); the second pass reads it from L1.
+// With srt_tok = null, row r is x[r] itself (the rows of H for the down
+// projection on E4M3 operands).
 __global__ void __launch_bounds__(kRowThreads)
     k_gather_e4m3(const uint4 *__restrict__ x, int T, int dvec,
                   const int32_t *__restrict__ srt_tok, const int32_t *__restrict__ offsets,
@@ -78,7 +80,7 @@ __global__ void __launch_bounds__(kRowThreads)
     const int lane = threadIdx.x & 31;
     const int64_t nw = int64_t(gridDim.x) * kRowWarps;
     for (int64_t r = int64_t(blockIdx.x) * kRowWarps + (threadIdx.x >> 5); r < R; r += nw) {
-        const int t = srt_tok[r];
+        const int t = srt_tok ? srt_tok[r] : int(r);
         uint2 *dst = xs8 + r * dvec;
         if (t < 0 || t >= T) {
             for (int c = lane; c < dvec; c += 32)
@@ -222,6 +224,19 @@ cudaError_t launch_gather_e4m3(const void *x, int T, int d, const int32_t *srt_t
     return launch_pdl(k_gather_e4m3, dim3(grid), dim3(kRowThreads), 0, stream,
                       static_cast<const uint4 *>(x), T, dvec, srt_tok, offsets, E, cap,
                       reinterpret_cast<uint2 *>(xs8), xexp);
+}
+
+cudaError_t launch_rows_e4m3(const void *H, int f, const int32_t *offsets, int E, int64_t cap,
+                             uint8_t *H8, int32_t *hexp, cudaStream_t stream)
+{
+    const int dvec = f / 8;
+    const int64_t want = (cap + kRowWarps - 1) / kRowWarps;
+    const int64_t cap_grid = int64_t(device_sm_count()) * kCtasPerSm;
+    const int grid = int(want < 1 ? 1 : (want < cap_grid ? want : cap_grid));
+    return launch_pdl(k_gather_e4m3, dim3(grid), dim3(kRowThreads), 0, stream,
+                      static_cast<const uint4 *>(H), int(cap), dvec,
+                      static_cast<const int32_t *>(nullptr), offsets, E, cap,
+                      reinterpret_cast<uint2 *>(H8), hexp);
 }
 
 cudaError_t launch_combine(const void *Ys, const int32_t *pos, int T, int k, int d, void *y,

@@ -376,9 +376,12 @@ static void expert_job(const uint16_t *xrow, int x_is_f16, const wmat_t *Wg,
         h[n] = g[n] / (1.0 + exp(-g[n])) * u[n];
         if (mirror)
             h[n] = to_bf16(h[n]);
-        hq[n] = h[n];
+        /* with E4M3 activations h's codes are decided from h as stored, in
+         * bf16 (the same precision on both sides: one bf16 step can move a
+         * value across an E4M3 midpoint, a whole E4M3 step) */
+        hq[n] = a8 ? to_bf16(h[n]) : h[n];
     }
-    if (a8) /* ... and the down projection sees h's E4M3 values (h itself is kept) */
+    if (a8) /* ... and the down projection sees those E4M3 values (h itself is kept) */
         dequantize_row_e4m3(hq, f);
     for (m = 0; m < d; m++)
         o[m] = 0.0;
@@ -607,8 +610,8 @@ int oracle_layer_tokens(const uint16_t *x, int x_is_f16, const int32_t *ids,
 /* The same layer with E4M3 weights: Wg, Wu codes [E][d][f] with scales
  * [E][f], Wd codes [E][f][d] with scales [E][d].  a8 != 0 also gives both
  * projections E4M3 inputs: gate/up each row's E4M3 values and down the
- * E4M3 values of h (after the bf16 rounding in the mirror), each quantized
- * per row by quantize_row_e4m3. */
+ * E4M3 values of h rounded to bf16 (how h is stored), each quantized per row
+ * by quantize_row_e4m3. */
 int oracle_layer_tokens_e4m3(const uint16_t *x, int x_is_f16, const int32_t *ids,
                              const float *w, const uint8_t *Wg, const float *sg,
                              const uint8_t *Wu, const float *su, const uint8_t *Wd,

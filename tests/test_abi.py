@@ -154,7 +154,7 @@ def test_prefill_host_argument_errors(lib):
     assert prefill_host_call(lib, Wg=FAKE + 8) == B.MOE_ERR_ALIGN
     assert prefill_host_call(lib, sg=FAKE) == B.MOE_ERR_NULL      # E4M3 needs all three scales
     assert prefill_host_call(lib, act=1, d=128) == B.MOE_ERR_NULL  # E4M3 rows need E4M3 weights
-    assert prefill_host_call(lib, act=1, sg=FAKE, su=FAKE, sd=FAKE) == B.MOE_ERR_SHAPE  # d % 128
+    assert prefill_host_call(lib, act=1, sg=FAKE, su=FAKE, sd=FAKE, d=96) == B.MOE_ERR_SHAPE
     # nothing to do: returns before any CUDA call
     assert prefill_host_call(lib, n=0) == B.MOE_OK
     assert prefill_host_call(lib, T=0) == B.MOE_OK
@@ -173,8 +173,15 @@ def test_e4m3_argument_errors(lib):
     assert g8(FAKE, 8, 64, FAKE, FAKE, 4, 100, FAKE + 8, FAKE, None) == B.MOE_ERR_ALIGN
     assert g8(FAKE, 8, 64, FAKE, FAKE, 4, 0, FAKE, FAKE, None) == B.MOE_OK
     gf = lib.moe_ffn_gate_up_f8
-    assert gf(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 64, 100, FAKE, None, None) == B.MOE_ERR_SHAPE
+    assert gf(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 96, 64, 100, FAKE, None, None) == B.MOE_ERR_SHAPE
     assert gf(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 128, 64, 100, FAKE, None, None) == B.MOE_ERR_NULL
+    r8 = lib.moe_rows_e4m3
+    assert r8(FAKE, 24, FAKE, 4, 100, FAKE, FAKE, None) == B.MOE_ERR_SHAPE
+    assert r8(FAKE, 64, FAKE, 4, 100, FAKE, None, None) == B.MOE_ERR_NULL
+    assert r8(FAKE, 64, FAKE, 4, 0, FAKE, FAKE, None) == B.MOE_OK
+    df = lib.moe_ffn_down_f8
+    assert df(FAKE, None, FAKE, FAKE, FAKE, FAKE, 4, 64, 64, 100, FAKE, None, None) == B.MOE_ERR_NULL
+    assert df(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 64, 0, FAKE, None, None) == B.MOE_OK
     assert gf(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 128, 64, 0, FAKE, None, None) == B.MOE_OK
     gu = lib.moe_ffn_gate_up_e4m3
     assert gu(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 96, 64, 100, FAKE, None, None) == B.MOE_ERR_SHAPE
@@ -186,7 +193,7 @@ def test_e4m3_argument_errors(lib):
     assert dn(FAKE, FAKE, None, FAKE, FAKE, 4, 64, 64, 100, FAKE, None, None) == B.MOE_ERR_NULL
     assert dn(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 64, 0, FAKE, None, None) == B.MOE_OK
     lf8 = lib.moe_layer_forward_f8
-    assert lf8(*([FAKE] * 9 + [8, 64, 4, 2, 64, 16, FAKE, FAKE, 1 << 40, None])) == B.MOE_ERR_SHAPE
+    assert lf8(*([FAKE] * 9 + [8, 96, 4, 2, 64, 16, FAKE, FAKE, 1 << 40, None])) == B.MOE_ERR_SHAPE
     lf = lib.moe_layer_forward_e4m3
     ws = 1 << 40
     args = [FAKE] * 9 + [8, 64, 4, 2, 64, 16, FAKE, FAKE, ws, None]

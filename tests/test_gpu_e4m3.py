@@ -290,12 +290,53 @@ def test_f8_gate_up_workloads_sampled_rows(cfg):
     run_f8_gate_up(inp, wl.E, wl.d, wl.f, wl.tm, tuple(qw), nsample=40, seed=cfg)
 
 
+def test_rows_e4m3_matches_oracle():
+    rng = np.random.default_rng(31)
+    cap, f = 200, 192
+    Hf = (rng.standard_normal((cap, f)) * 3.0).astype(np.float32)
+    Hf[7] *= 1e-9
+    Hf[8] = 0.0
+    H = W.bf16_bits(Hf)
+    R = 160                                                    # rows past offsets[E] untouched
+    offsets = np.array([0, 64, 64, 160], np.int32)
+    H8 = torch.full((cap, f), 0x55, dtype=torch.uint8, device="cuda")
+    hexp = torch.full((cap,), 99, dtype=torch.int32, device="cuda")
+    B.rows_e4m3(dev16(H), dev(offsets), 3, cap, H8, hexp)
+    torch.cuda.synchronize()
+    qo, eo = oracle.quantize_rows_e4m3(H[:R])
+    assert np.array_equal(H8.cpu().numpy()[:R], qo) and np.array_equal(hexp.cpu().numpy()[:R], eo)
+    assert np.all(H8.cpu().numpy()[R:] == 0x55) and np.all(hexp.cpu().numpy()[R:] == 99)
+
+
+@pytest.mark.parametrize("T,d,E,k,f,tm", [
+    (40, 128, 3, 2, 64, 16),     # one K stage, half of it past f (zero-filled)
+    (100, 192, 5, 3, 704, 16),   # d = 1.5 x 128: down's second feature tile half outside
+    (300, 256, 2, 1, 384, 32),   # experts with several chunks
+])
+def test_f8_down_all_rows(T, d, E, k, f, tm):
+    # down on E4M3 H rows: the oracle's mirror h (bf16) quantized per row by
+    # the oracle feeds the GPU, against the oracle's E4M3-activation mirror
+    inp = W.make_layer(T, d, E, k, f, tm=tm, seed=T + f + 7)
+    qw = quantized(inp)
+    p, xs, real, row_e = staged(inp, E, tm)
+    cap = B.capacity(T, k, E, tm)
+    hm, ysm = oracle.expert_rows(xs, real, row_e[real], p["srt_w"][real], *qw, mirror=True,
+                                 act_e4m3=True)
+    Hin = np.zeros((cap, f), np.uint16)
+    Hin[real] = W.bf16_bits(hm.astype(np.float32))
+    q8, e8 = oracle.quantize_rows_e4m3(Hin)
+    Ys = host16(B.ffn_down_f8(dev(q8), dev(e8), q_dev(kmajor(qw[2])), dev(p["offsets"]),
+                              dev(to_cap(p["srt_w"], cap)), cap))
+    ok, err, bound = layer_tolerance(W.bits_to_float(Ys[real], "bf16").astype(np.float64), ysm)
+    assert ok, f"down f8: max err {err} > {bound}"
+    assert np.all(Ys[np.nonzero(p["srt_tok"] < 0)[0]] == 0)
+
+
 def test_f8_layer_tiny_full_output():
     wl = W.workload(1)
     inp = inputs(1)
     qw = quantized(inp)
-    layer = B.MoeLayer(q_dev(kmajor(qw[0])), q_dev(kmajor(qw[1])), q_dev(qw[2]), tm=wl.tm,
-                       act_e4m3=True)
+    layer = B.MoeLayer(*[q_dev(kmajor(w)) for w in qw], tm=wl.tm, act_e4m3=True)
     y = layer.forward(dev16(inp["x"]), dev(inp["ids"]), dev(inp["w"]))
     torch.cuda.synchronize()
     assert B.read_status(layer._ws) == 0
@@ -317,7 +358,7 @@ def test_f8_layer_workloads_sampled_tokens(cfg):
     # the oracle takes the gate/up codes in the weights' own layout
     tr = lambda qs: (np.ascontiguousarray(qs[0].cpu().numpy().transpose(0, 2, 1)),
                      qs[1].cpu().numpy())
-    qw = (tr(layer.Wg), tr(layer.Wu), (layer.Wd[0].cpu().numpy(), layer.Wd[1].cpu().numpy()))
+    qw = (tr(layer.Wg), tr(layer.Wu), tr(layer.Wd))
     toks = sample_tokens(inp["ids"], 24, seed=cfg)
     ref = oracle.layer(inp["x"], inp["ids"], inp["w"], *qw, tokens=toks, act_e4m3=True)
     ok, err, bound = layer_tolerance(host_f(y)[toks], ref)
@@ -330,8 +371,7 @@ def test_f8_layer_host_chunks():
     T, d, E, k, f, tm = 200, 256, 8, 4, 192, 16
     chunks = [W.make_layer(T, d, E, k, f, tm=tm, seed=80 + c) for c in range(3)]
     qw = quantized(chunks[0])
-    layer = B.MoeLayer(q_dev(kmajor(qw[0])), q_dev(kmajor(qw[1])), q_dev(qw[2]), tm=tm,
-                       act_e4m3=True)
+    layer = B.MoeLayer(*[q_dev(kmajor(w)) for w in qw], tm=tm, act_e4m3=True)
     xs = [torch.from_numpy(c["x"].view(np.int16)).view(torch.bfloat16).pin_memory() for c in chunks]
     ids = [torch.from_numpy(c["ids"]).pin_memory() for c in chunks]
     ws = [torch.from_numpy(c["w"]).pin_memory() for c in chunks]

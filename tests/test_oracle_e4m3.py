@@ -203,10 +203,12 @@ def test_layer_e4m3_activations_dense_reference(mirror):
     xq = rows_e4m3_torch(x)
     g, u = xq @ Wg, xq @ Wu
     h = g / (1.0 + np.exp(-g)) * u
+    # h's codes are decided from h as stored, in bf16 (h -> fp32 -> bf16 is
+    # the oracle's rounding for these magnitudes)
+    hb = W.bits_to_float(W.bf16_bits(h.astype(np.float32)), "bf16").astype(np.float64)
     if mirror:
-        h = W.bits_to_float(W.bf16_bits(h.astype(np.float32)), "bf16").astype(np.float64)
-        # (h -> fp32 -> bf16 equals the oracle's rounding for these magnitudes)
-    ref = rows_e4m3_torch(h) @ Wd
+        h = hb
+    ref = rows_e4m3_torch(hb) @ Wd
     y = oracle.layer(inp["x"], inp["ids"], inp["w"], *qw, act_e4m3=True, mirror=False)
     if not mirror:
         assert np.allclose(y, ref, rtol=1e-12, atol=1e-15)

@@ -42,6 +42,7 @@ MUTANTS = {
     "row_scale_ignored": ("        x[c] = ldexp(e4m3_value(e4m3_encode((float)ldexp(x[c], -e))), e);",
                           "        x[c] = e4m3_value(e4m3_encode((float)ldexp(x[c], -e)));"),
     "down_input_not_quantized": ("        dequantize_row_e4m3(hq, f);", "        (void)hq;"),
+    "down_codes_from_fp64_h": ("        hq[n] = a8 ? to_bf16(h[n]) : h[n];", "        hq[n] = h[n];"),
     "quantize_amax_axis": ("float a = (float)fabs(bf16_value(W[(e * K + k) * M + m]));",
                            "float a = (float)fabs(bf16_value(W[(e * K + m % K) * M + k % M]));"),
 }
