@@ -55,6 +55,7 @@ ROUTING = {"topk": "top-k of N(0,1) logits", "topk_bias": "top-k of N(0,1) logit
 KERNELS_PER_LAYER = 5
 FLUSH_BYTES = 256 << 20
 PROFILE = os.path.join(ROOT, "profiles", "ffn_gate_up_layer_t2048_d2560_e512_k10_f512.md")
+PROFILE_F8 = os.path.join(ROOT, "profiles", "ffn_gate_up_f8_layer_t2048_d2560_e512_k10_f512.md")
 FFN_SRC = os.path.join(ROOT, "moe_prefill_routing_gb300", "csrc", "ffn.cu")
 FALLBACK_HBM_GBS = 6800.0
 
@@ -78,12 +79,12 @@ def peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def profile_traffic():
+def profile_traffic(path=PROFILE):
     """dram bytes per launch of the gate/up kernel from the committed ncu
     summary, or None when the kernel source changed since the capture."""
-    if not os.path.exists(PROFILE):
+    if not os.path.exists(path):
         return None
-    txt = open(PROFILE).read()
+    txt = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", txt)
     h = re.search(r"ffn_cu_sha256:\s*([0-9a-f]{64})", txt)
     if not m or not h:
@@ -370,7 +371,7 @@ def run_native(args, rank, world, local):
         achieved, peak, unit = alg["gate_up_flops"] / t_gu / 1e12, tflops, "TFLOP/s"
     else:
         achieved, peak, unit = alg["gate_up"] / t_gu / 1e9, hbm, "GB/s"
-    traffic = profile_traffic()
+    traffic = profile_traffic(PROFILE_F8 if f8 else PROFILE)
     layer_gbs = alg["layer"] / (sum(ms) / len(ms) / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
@@ -403,7 +404,8 @@ def run_native(args, rank, world, local):
                      "frac": achieved / peak, "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": alg["gate_up"],
                      "algorithmic_flops_per_launch": alg["gate_up_flops"],
-                     "traffic": traffic if args.workload == WORKLOAD and not e4m3 else None},
+                     "traffic": (traffic if args.workload == WORKLOAD and (f8 or not e4m3)
+                                 else None)},
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_total / K3, "steps": K3,
                 "api": "moe_prefill_forward_host (host buffers; copies overlap the layer)",

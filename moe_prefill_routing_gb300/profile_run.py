@@ -6,7 +6,10 @@
 Generates the named workload (optionally with fewer experts, routing redrawn
 for that expert count, so that the device holds a few GB at most), runs the
 whole layer once through the stage entry points, then runs the chosen stage
-``--iters`` more times.  Every stage call goes through the C ABI.
+``--iters`` more times.  Every stage call goes through the C ABI.  With
+``--weights f8`` the gather, gate/up and down stages are the E4M3-operand
+ones (weights quantized on the device first; down includes the pass that
+makes H's rows E4M3).
 """
 from __future__ import annotations
 
@@ -30,6 +33,7 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=0, help="override T (0: the workload's)")
     ap.add_argument("--stage", choices=STAGES, default="gate_up")
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--weights", choices=("bf16", "f8"), default="bf16")
     a = ap.parse_args(argv)
     wl = W.workload(a.workload)
     if a.experts:
@@ -49,10 +53,15 @@ def main(argv=None):
     cap = B.capacity(wl.T, wl.k, wl.E, wl.tm)
     o = B.plan(ids, w, wl.E, wl.tm, cap=cap)
     xs = B.gather(x, o["srt_tok"], o["offsets"], wl.E, cap)
+    f8 = a.weights == "f8"
     if not plan_only:
         Wg, Wu, Wd = (d16(inp[n]) for n in ("Wg", "Wu", "Wd"))
         H, Ys = B.expert_ffn(xs, Wg, Wu, Wd, o["offsets"], o["srt_w"], cap)
         y = B.combine(Ys, o["pos"])
+        if f8:
+            Wg, Wu, Wd = (B.quantize_e4m3(t, kmajor=True) for t in (Wg, Wu, Wd))
+            x8, xe = B.gather_e4m3(x, o["srt_tok"], o["offsets"], wl.E, cap)
+            H8, he = B.rows_e4m3(H, o["offsets"], wl.E, cap)
     calls = {
         "plan": lambda: B.plan(ids, w, wl.E, wl.tm, cap=cap, out=o),
         "gather": lambda: B.gather(x, o["srt_tok"], o["offsets"], wl.E, cap, xs=xs),
@@ -61,6 +70,19 @@ def main(argv=None):
         "combine": lambda: B.combine(Ys, o["pos"], y=y),
         "layer": lambda: B.layer_forward(x, ids, w, Wg, Wu, Wd, wl.tm, y=y),
     }
+    if f8 and not plan_only:
+
+        def down_f8():
+            B.rows_e4m3(H, o["offsets"], wl.E, cap, H8, he)
+            B.ffn_down_f8(H8, he, Wd, o["offsets"], o["srt_w"], cap, Ys=Ys)
+
+        calls.update({
+            "gather": lambda: B.gather_e4m3(x, o["srt_tok"], o["offsets"], wl.E, cap, x8, xe),
+            "gate_up": lambda: B.ffn_gate_up_f8(x8, xe, Wg, Wu, o["offsets"], cap, H=H),
+            "down": down_f8,
+            "layer": lambda: B.layer_forward_e4m3(x, ids, w, Wg, Wu, Wd, wl.tm, y=y,
+                                                  act_e4m3=True),
+        })
     for _ in range(a.iters):
         calls[a.stage]()
     torch.cuda.synchronize(dev)
