@@ -384,3 +384,23 @@ def test_f8_layer_host_chunks():
         ref = oracle.layer(inp["x"], inp["ids"], inp["w"], *qw, act_e4m3=True)
         ok, err, bound = layer_tolerance(host_f(ys[c]), ref)
         assert ok, (c, err, bound)
+
+
+@pytest.mark.parametrize("T,d,E,k,f,tm,skip", [
+    (300, 128, 4096, 4, 64, 16, 0.0),    # E at its limit: the largest chunk table
+    (9000, 128, 64, 8, 128, 16, 0.05),   # T*k above 16 x 4096: the three-kernel plan
+    (123, 192, 9, 3, 192, 16, 0.2),      # ragged tiles, skipped slots, d = 1.5 x 128
+])
+def test_f8_and_e4m3_layers_at_the_limits(T, d, E, k, f, tm, skip):
+    inp = W.make_layer(T, d, E, k, f, tm=tm, seed=5 * T + E, skip_frac=skip)
+    qw = quantized(inp)
+    x, ids, w = dev16(inp["x"]), dev(inp["ids"]), dev(inp["w"])
+    for act in (False, True):
+        weights = [q_dev(kmajor(q)) if act else q_dev(q) for q in qw]
+        layer = B.MoeLayer(*weights, tm=tm, act_e4m3=act)
+        y = layer.forward(x, ids, w)
+        torch.cuda.synchronize()
+        assert B.read_status(layer._ws) == 0
+        ref = oracle.layer(inp["x"], inp["ids"], inp["w"], *qw, act_e4m3=act)
+        ok, err, bound = layer_tolerance(host_f(y), ref)
+        assert ok, (act, err, bound)
