@@ -358,6 +358,30 @@ def run_native(args, rank, world, local):
     h2d = x_h.numel() * 2 + ids_h.numel() * 4 + w_h.numel() * 4
     d2h = y_h.numel() * 2
 
+    # alongside the bf16 measurement: the same layer with E4M3 weights and E4M3
+    # activations (both GEMMs on tcgen05 kind::f8f6f4), timed the same way;
+    # a different arithmetic, so reported beside the headline, not as it
+    fp8 = None
+    if not e4m3 and not args.no_fp8:
+        layer8 = B.MoeLayer.quantized(Wg, Wu, Wd, tm=wl.tm, act_e4m3=True)
+        for i in range(args.warmup):
+            flush.fill_(i & 0xFF)
+            layer8.forward(x, ids, w, y=y)
+        torch.cuda.synchronize(dev)
+        if B.read_status(layer8._ws) != 0:
+            raise RuntimeError("device status set in the E4M3 layer")
+        ms8 = timed(lambda: layer8.forward(x, ids, w, y=y), args.steps)
+        total8 = replicas.max_over_ranks(sum(ms8), world, dev)
+        alg8 = algorithmic(wl, inp["ids"], wbytes=1, abytes=1)
+        fp8 = {"value": args.steps * rows * world / (total8 / 1e3), "unit": "rows/s",
+               "ms_per_step": statistics.mean(ms8), "steps": args.steps,
+               "arithmetic": "E4M3 weights (fp32 scale per expert and output feature) and "
+                             "E4M3 rows of x and H (power-of-two scale per row); fp32 "
+                             "accumulation; bf16 H, Ys, y",
+               "layer_hbm_gbs": alg8["layer"] / (statistics.mean(ms8) / 1e3) / 1e9,
+               "gpu_launches": (KERNELS_PER_LAYER + 1) * args.steps}
+        del layer8
+
     if rank != 0:
         return
     hbm, tflops, peak_src = peaks()
@@ -414,6 +438,7 @@ def run_native(args, rank, world, local):
                 "l2": "not flushed: every step streams the active expert weights "
                       f"({alg['weights'] / 1e9:.2f} GB > 129 MB L2)"},
         "clocks": clk,
+        "fp8_layer": fp8,
         "gpu_launches": (KERNELS_PER_LAYER + int(f8)) * args.steps,
     }
     if world == 1 and not args.no_cpu_baseline and not e4m3:
@@ -469,6 +494,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true",
+                    help="skip the E4M3 layer measured beside the bf16 one")
     ap.add_argument("--weights", choices=("bf16", "e4m3", "f8"), default="bf16",
                     help="expert weights: bf16 (the default measurement), E4M3 codes with "
                          "per-feature scales (bf16 activations), or f8: E4M3 weights and E4M3 "

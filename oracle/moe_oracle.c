@@ -344,12 +344,24 @@ typedef struct {
     long rows, cols;     /* per expert */
 } wmat_t;
 
+/* e4m3_value of every code, filled once (same values, looked up) */
+static double e4m3_table[256];
+static pthread_once_t e4m3_once = PTHREAD_ONCE_INIT;
+
+static void e4m3_fill(void)
+{
+    int c;
+    for (c = 0; c < 256; c++)
+        e4m3_table[c] = e4m3_value((uint8_t)c);
+}
+
+/* Weight [e][r][c] of W, as a value. */
 static double wval(const wmat_t *W, long e, long r, long c)
 {
     long i = (e * W->rows + r) * W->cols + c;
     if (W->b16)
         return bf16_value(W->b16[i]);
-    return e4m3_value(W->q8[i]) * (double)W->scale[e * W->cols + c];
+    return e4m3_table[W->q8[i]] * (double)W->scale[e * W->cols + c];
 }
 
 static void expert_job(const uint16_t *xrow, int x_is_f16, const wmat_t *Wg,
@@ -367,6 +379,15 @@ static void expert_job(const uint16_t *xrow, int x_is_f16, const wmat_t *Wg,
         u[n] = 0.0;
     }
     for (c = 0; c < d; c++) {
+        if (Wg->b16 && Wu->b16) { /* the same sums, with the rows addressed once */
+            const uint16_t *wg = Wg->b16 + (e * Wg->rows + c) * (long)f;
+            const uint16_t *wu = Wu->b16 + (e * Wu->rows + c) * (long)f;
+            for (n = 0; n < f; n++) {
+                g[n] += xv[c] * bf16_value(wg[n]);
+                u[n] += xv[c] * bf16_value(wu[n]);
+            }
+            continue;
+        }
         for (n = 0; n < f; n++) {
             g[n] += xv[c] * wval(Wg, e, c, n);
             u[n] += xv[c] * wval(Wu, e, c, n);
@@ -385,9 +406,16 @@ static void expert_job(const uint16_t *xrow, int x_is_f16, const wmat_t *Wg,
         dequantize_row_e4m3(hq, f);
     for (m = 0; m < d; m++)
         o[m] = 0.0;
-    for (n = 0; n < f; n++)
+    for (n = 0; n < f; n++) {
+        if (Wd->b16) {
+            const uint16_t *wd = Wd->b16 + (e * Wd->rows + n) * (long)d;
+            for (m = 0; m < d; m++)
+                o[m] += hq[n] * bf16_value(wd[m]);
+            continue;
+        }
         for (m = 0; m < d; m++)
             o[m] += hq[n] * wval(Wd, e, n, m);
+    }
 }
 
 /* A job: one routed row, its expert, and where its results go. */
@@ -441,6 +469,7 @@ static int run_pass(const job_t *jobs, long njobs, int x_is_f16, int d, int f,
     pass_t ps[256];
     int started[256];
     int t, failed = 0;
+    pthread_once(&e4m3_once, e4m3_fill);
     if (nthreads < 1)
         nthreads = 1;
     if (nthreads > 256)

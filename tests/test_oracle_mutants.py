@@ -17,8 +17,8 @@ MUTANTS = {
                         "h[n] = u[n] / (1.0 + exp(-u[n])) * g[n];"),
     "sigmoid_sign": ("h[n] = g[n] / (1.0 + exp(-g[n])) * u[n];",
                      "h[n] = g[n] / (1.0 + exp(g[n])) * u[n];"),
-    "down_transposed": ("o[m] += hq[n] * wval(Wd, e, n, m);",
-                        "o[m] += hq[n] * wval(Wd, e, ((long)m * f + n) / d, ((long)m * f + n) % d);"),
+    "down_transposed": ("                o[m] += hq[n] * bf16_value(wd[m]);",
+                        "                o[m] += hq[n] * bf16_value(Wd->b16[e * (long)f * d + (long)m * f + n]);"),
     "weight_dropped": ("yt[m] += wt * jobs[jb].o[m];", "yt[m] += jobs[jb].o[m];"),
     "no_padding": ("offsets[e + 1] = (int32_t)(offsets[e] + tiles * tm);",
                    "offsets[e + 1] = (int32_t)(offsets[e] + counts[e]);"),
@@ -34,8 +34,8 @@ MUTANTS = {
     "e4m3_ties_up": ("best = ((c - 1) & 1) == 0 ? c - 1 : c;", "best = c;"),
     "e4m3_no_saturation": ("    if (a >= 448.0)\n        return (uint8_t)(sign | 0x7e);",
                            "    if (a > 464.0)\n        return (uint8_t)(sign | 0x7e);"),
-    "scale_per_expert": ("return e4m3_value(W->q8[i]) * (double)W->scale[e * W->cols + c];",
-                         "return e4m3_value(W->q8[i]) * (double)W->scale[e * W->cols];"),
+    "scale_per_expert": ("return e4m3_table[W->q8[i]] * (double)W->scale[e * W->cols + c];",
+                         "return e4m3_table[W->q8[i]] * (double)W->scale[e * W->cols];"),
     "scale_divisor": ("s = amax / 448.0f;", "s = amax / 256.0f;"),
     "row_scale_not_minimal": ("        if (amax > ldexp(448.0, e))\n            e++;",
                               "        if (amax >= ldexp(224.0, e))\n            e++;"),
