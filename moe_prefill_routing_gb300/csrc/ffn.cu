@@ -22,17 +22,18 @@
 // rows are K-major B tiles.  Both use 128-byte swizzled shared memory.
 //
 // Work unit = (expert chunk of <= 128 rows, 128 (gate/up) or 256 (down)
-// output features), numbered
-// chunk-major so that the tiles of one chunk (same activation rows) and the
-// chunks of one big expert (same weight tile) run close together in time
-// and share L2.  Each CTA (one per SM) walks units u = blockIdx.x + i*grid.
+// output features), numbered chunk-major so that the tiles of one chunk
+// (same activation rows) and the chunks of one big expert (same weight
+// tile) run close together in time and share L2.  Each CTA (one per SM)
+// walks units u = blockIdx.x + i*grid.
 //
 // Warp roles: warp 0 issues TMA copies into a ring of shared-memory stages,
 // warp 1 issues tcgen05.mma into one of two TMEM accumulators, warps 2-5
 // read the accumulator with tcgen05.ld, apply the epilogue, stage 16 rows of
 // bf16 in shared memory, and one thread writes them out with a TMA store.
-// Weight modes (WM): bf16 weights and activations; kWiden: E4M3 weights,
-// bf16 activations; kNative: E4M3 weights and E4M3 activations for gate/up.
+//
+// Weight modes (WM): kBf16: bf16 weights and rows; kWiden: E4M3 weights,
+// bf16 rows; kNative: E4M3 weights and E4M3 rows.
 // kWiden: the weights are E4M3 codes with a per-(expert, output feature) scale
 // (see quant.cu).  TMA brings the 8-bit tiles into the stage ring (half the
 // bytes of bf16), eight more warps (6-13) widen them to bf16 -- exactly: every
@@ -88,9 +89,11 @@ constexpr uint32_t kAccCols = 2 * BN;                            // two accumula
 constexpr uint32_t kTmemCols = 2 * kAccCols;                     // double-buffered
 constexpr int kStageRows = 16;                                   // rows per epilogue chunk
 constexpr uint32_t kStgBytes = 2 * kStageRows * 256 * 2;         // two chunks of <= 256 features
-// W8: a stage holds two E4M3 tiles (128 features x 64 K, 1 byte each, rows
-// of 128 bytes unswizzled) and the B tile; two more slots hold the widened
-// bf16 A tiles.  Shared memory in stages is the same 192 KB either way.
+// kWiden: a stage holds two E4M3 tiles (128 features x 64 K, 1 byte each,
+// rows of 128 bytes unswizzled) and the B tile; two more slots hold the
+// widened bf16 A tiles.  Shared memory in stages is the same 192 KB either
+// way.  (kNative stages have the bf16 layout's sizes: two 128 x 128-byte A
+// tiles and one B tile.)
 constexpr uint32_t kA8TileBytes = BM * BK;                       // 8 KB
 constexpr uint32_t kStageBytesW8 = 2 * kA8TileBytes + kBTileBytes;
 constexpr int kConvSlots = 2;
@@ -121,8 +124,8 @@ struct Ctrl {
     uint64_t empty[S];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
-    uint64_t conv_full[kConvSlots];   // W8: widened A tiles ready (kConvThreads arrivals)
-    uint64_t conv_empty[kConvSlots];  // W8: the MMAs are done with a slot
+    uint64_t conv_full[kConvSlots];   // kWiden: widened A tiles ready (kConvThreads arrivals)
+    uint64_t conv_empty[kConvSlots];  // kWiden: the MMAs are done with a slot
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -367,7 +370,7 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                 for (int t = 0; t < 2; ++t)
                     for (int h = 0; h < 2; ++h)
                         boxes += tile_base(m0, t) + 64 * h < p.M;
-                // W8: one E4M3 box of 128 features per A tile that starts
+                // kWiden: one E4M3 box of 128 features per A tile that starts
                 // inside M (features past M are zero-filled and still counted)
                 const uint32_t a_bytes =
                     W8 ? (1u + uint32_t(tile_base(m0, 1) < p.M)) * kA8TileBytes
@@ -594,7 +597,7 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
             const Unit w = map_unit(u, n_mt, chunk_start, p.E, p.offsets);
             const int m0 = w.mt * UM;
             const bool use1 = tile_base(m0, 1) < p.M;
-            // W8: the scales of this thread's output feature in both A tiles
+            // E4M3 weights: the scales of this thread's output feature in both A tiles
             float sc0 = 1.0f, sc1 = 1.0f;
             if (SCALED) {
                 const int64_t eb = int64_t(w.e) * p.M;
