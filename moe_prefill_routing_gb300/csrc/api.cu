@@ -321,8 +321,15 @@ static int layer_forward(const void *x, const int32_t *ids, const float *w,
     // E4M3 rows share the xs region: codes [cap, d], then the row exponents
     uint8_t *xs8 = static_cast<uint8_t *>(xs);
     int32_t *xexp = reinterpret_cast<int32_t *>(xs8 + ((size_t(cap) * d + 255) & ~size_t(255)));
+    // with E4M3 rows each token is quantized once, into the Ys field (free
+    // until down runs), and its codes are then gathered as bytes
+    uint8_t *tok8 = static_cast<uint8_t *>(Ys);
+    int32_t *texp = reinterpret_cast<int32_t *>(tok8 + ((size_t(T) * d + 255) & ~size_t(255)));
+    if (e == cudaSuccess && W.act_e4m3)
+        e = moe::launch_quant_tokens_e4m3(x, T, d, tok8, texp, s);
     if (e == cudaSuccess)
-        e = W.act_e4m3 ? moe::launch_gather_e4m3(x, T, d, srt_tok, offsets, E, cap, xs8, xexp, s)
+        e = W.act_e4m3 ? moe::launch_gather_codes(tok8, texp, T, d, srt_tok, offsets, E, cap, xs8,
+                                                  xexp, s)
                        : moe::launch_gather(x, T, d, srt_tok, offsets, E, cap, xs, s);
     const uint8_t *qg = static_cast<const uint8_t *>(W.Wg), *qu = static_cast<const uint8_t *>(W.Wu);
     if (e == cudaSuccess)

@@ -74,6 +74,15 @@ cudaError_t launch_gather_e4m3(const void *x, int T, int d, const int32_t *srt_t
                                const int32_t *offsets, int E, int64_t cap, uint8_t *xs8,
                                int32_t *xexp, cudaStream_t stream);
 
+// The same quantization of the T token rows of x once (x8 [T, d], texp [T]),
+// then the routed rows gathered as bytes with their exponents: equal to
+// launch_gather_e4m3, without quantizing a token once per slot.
+cudaError_t launch_quant_tokens_e4m3(const void *x, int T, int d, uint8_t *x8, int32_t *texp,
+                                     cudaStream_t stream);
+cudaError_t launch_gather_codes(const uint8_t *x8, const int32_t *texp, int T, int d,
+                                const int32_t *srt_tok, const int32_t *offsets, int E,
+                                int64_t cap, uint8_t *xs8, int32_t *xexp, cudaStream_t stream);
+
 // E4M3 rows of H [cap, f] itself (rows < offsets[E]).
 cudaError_t launch_rows_e4m3(const void *H, int f, const int32_t *offsets, int E, int64_t cap,
                              uint8_t *H8, int32_t *hexp, cudaStream_t stream);

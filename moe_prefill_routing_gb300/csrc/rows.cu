@@ -29,9 +29,12 @@ __device__ __forceinline__ uint4 ldg_nc(const uint4 *p)
 }
 
 // xs[r] = x[srt_tok[r]] for r < R_pad (= offsets[E]); zero rows where srt_tok = -1.
+// With side_out, also side_out[r] = side_in[srt_tok[r]] (0 for -1 rows): the
+// per-token exponents that go with E4M3 token rows.
 __global__ void __launch_bounds__(kRowThreads)
     k_gather(const uint4 *__restrict__ x, int T, int dvec, const int32_t *__restrict__ srt_tok,
-             const int32_t *__restrict__ offsets, int E, int64_t cap, uint4 *__restrict__ xs)
+             const int32_t *__restrict__ offsets, int E, int64_t cap, uint4 *__restrict__ xs,
+             const int32_t *__restrict__ side_in, int32_t *__restrict__ side_out)
 {
     pdl_wait();
     const int64_t R = min(int64_t(offsets[E]), cap);
@@ -40,6 +43,8 @@ __global__ void __launch_bounds__(kRowThreads)
     for (int64_t r = int64_t(blockIdx.x) * kRowWarps + (threadIdx.x >> 5); r < R; r += nw) {
         const int t = srt_tok[r];
         uint4 *dst = xs + r * dvec;
+        if (side_out && lane == 0)
+            side_out[r] = t >= 0 && t < T ? side_in[t] : 0;
         if (t >= 0 && t < T) {
             const uint4 *src = x + int64_t(t) * dvec;
             int c = lane;
@@ -70,13 +75,15 @@ __global__ void __launch_bounds__(kRowThreads)
 // (the largest magnitude, then the codes); the second pass reads it from L1.
 // With srt_tok = null, row r is x[r] itself (the rows of H for the down
 // projection on E4M3 operands).
+// nrows >= 0 fixes the row count instead of offsets[E] (the token rows of x).
 __global__ void __launch_bounds__(kRowThreads)
     k_gather_e4m3(const uint4 *__restrict__ x, int T, int dvec,
                   const int32_t *__restrict__ srt_tok, const int32_t *__restrict__ offsets,
-                  int E, int64_t cap, uint2 *__restrict__ xs8, int32_t *__restrict__ xexp)
+                  int E, int64_t cap, uint2 *__restrict__ xs8, int32_t *__restrict__ xexp,
+                  int64_t nrows)
 {
     pdl_wait();
-    const int64_t R = min(int64_t(offsets[E]), cap);
+    const int64_t R = nrows >= 0 ? nrows : min(int64_t(offsets[E]), cap);
     const int lane = threadIdx.x & 31;
     const int64_t nw = int64_t(gridDim.x) * kRowWarps;
     for (int64_t r = int64_t(blockIdx.x) * kRowWarps + (threadIdx.x >> 5); r < R; r += nw) {
@@ -210,7 +217,33 @@ cudaError_t launch_gather(const void *x, int T, int d, const int32_t *srt_tok,
     const int grid = int(want < 1 ? 1 : (want < cap_grid ? want : cap_grid));
     return launch_pdl(k_gather, dim3(grid), dim3(kRowThreads), 0, stream,
                       static_cast<const uint4 *>(x), T, dvec, srt_tok, offsets, E, cap,
-                      static_cast<uint4 *>(xs));
+                      static_cast<uint4 *>(xs), static_cast<const int32_t *>(nullptr),
+                      static_cast<int32_t *>(nullptr));
+}
+
+cudaError_t launch_quant_tokens_e4m3(const void *x, int T, int d, uint8_t *x8, int32_t *texp,
+                                     cudaStream_t stream)
+{
+    const int64_t want = (int64_t(T) + kRowWarps - 1) / kRowWarps;
+    const int64_t cap_grid = int64_t(device_sm_count()) * kCtasPerSm;
+    const int grid = int(want < 1 ? 1 : (want < cap_grid ? want : cap_grid));
+    return launch_pdl(k_gather_e4m3, dim3(grid), dim3(kRowThreads), 0, stream,
+                      static_cast<const uint4 *>(x), T, d / 8,
+                      static_cast<const int32_t *>(nullptr), static_cast<const int32_t *>(nullptr),
+                      0, int64_t(T), reinterpret_cast<uint2 *>(x8), texp, int64_t(T));
+}
+
+cudaError_t launch_gather_codes(const uint8_t *x8, const int32_t *texp, int T, int d,
+                                const int32_t *srt_tok, const int32_t *offsets, int E,
+                                int64_t cap, uint8_t *xs8, int32_t *xexp, cudaStream_t stream)
+{
+    const int dvec = d / 16;
+    const int64_t want = (cap + kRowWarps - 1) / kRowWarps;
+    const int64_t cap_grid = int64_t(device_sm_count()) * kCtasPerSm;
+    const int grid = int(want < 1 ? 1 : (want < cap_grid ? want : cap_grid));
+    return launch_pdl(k_gather, dim3(grid), dim3(kRowThreads), 0, stream,
+                      reinterpret_cast<const uint4 *>(x8), T, dvec, srt_tok, offsets, E, cap,
+                      reinterpret_cast<uint4 *>(xs8), texp, xexp);
 }
 
 cudaError_t launch_gather_e4m3(const void *x, int T, int d, const int32_t *srt_tok,
@@ -223,7 +256,7 @@ cudaError_t launch_gather_e4m3(const void *x, int T, int d, const int32_t *srt_t
     const int grid = int(want < 1 ? 1 : (want < cap_grid ? want : cap_grid));
     return launch_pdl(k_gather_e4m3, dim3(grid), dim3(kRowThreads), 0, stream,
                       static_cast<const uint4 *>(x), T, dvec, srt_tok, offsets, E, cap,
-                      reinterpret_cast<uint2 *>(xs8), xexp);
+                      reinterpret_cast<uint2 *>(xs8), xexp, int64_t(-1));
 }
 
 cudaError_t launch_rows_e4m3(const void *H, int f, const int32_t *offsets, int E, int64_t cap,
@@ -236,7 +269,7 @@ cudaError_t launch_rows_e4m3(const void *H, int f, const int32_t *offsets, int E
     return launch_pdl(k_gather_e4m3, dim3(grid), dim3(kRowThreads), 0, stream,
                       static_cast<const uint4 *>(H), int(cap), dvec,
                       static_cast<const int32_t *>(nullptr), offsets, E, cap,
-                      reinterpret_cast<uint2 *>(H8), hexp);
+                      reinterpret_cast<uint2 *>(H8), hexp, int64_t(-1));
 }
 
 cudaError_t launch_combine(const void *Ys, const int32_t *pos, int T, int k, int d, void *y,

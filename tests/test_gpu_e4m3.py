@@ -404,3 +404,24 @@ def test_f8_and_e4m3_layers_at_the_limits(T, d, E, k, f, tm, skip):
         ref = oracle.layer(inp["x"], inp["ids"], inp["w"], *qw, act_e4m3=act)
         ok, err, bound = layer_tolerance(host_f(y), ref)
         assert ok, (act, err, bound)
+
+
+@pytest.mark.parametrize("cfg", [1, 3])
+def test_f8_layer_equals_its_stages_bitwise(cfg):
+    # the layer quantizes each token once and gathers its codes; the stage
+    # calls quantize each routed row: the same codes, so the same bits
+    wl = W.workload(cfg)
+    inp = inputs(cfg)
+    layer = B.MoeLayer.quantized(*[dev16(inp[n]) for n in ("Wg", "Wu", "Wd")], tm=wl.tm,
+                                 act_e4m3=True)
+    x, ids, w = dev16(inp["x"]), dev(inp["ids"]), dev(inp["w"])
+    y = layer.forward(x, ids, w)
+    cap = B.capacity(wl.T, wl.k, wl.E, wl.tm)
+    o = B.plan(ids, w, wl.E, wl.tm, cap=cap)
+    x8, xe = B.gather_e4m3(x, o["srt_tok"], o["offsets"], wl.E, cap)
+    H = B.ffn_gate_up_f8(x8, xe, layer.Wg, layer.Wu, o["offsets"], cap)
+    H8, he = B.rows_e4m3(H, o["offsets"], wl.E, cap)
+    Ys = B.ffn_down_f8(H8, he, layer.Wd, o["offsets"], o["srt_w"], cap)
+    y2 = B.combine(Ys, o["pos"])
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
