@@ -382,6 +382,40 @@ def run_native(args, rank, world, local):
                "gpu_launches": (KERNELS_PER_LAYER + 1) * args.steps}
         del layer8
 
+    # the plan alone on large inputs, where its HBM traffic is what bounds it:
+    # T*k = 1M and 10M entries, E = 512, ids uniform over the experts (drawn on
+    # the device from a seeded generator), L2 flushed before each call
+    sweep = None
+    if not args.no_plan_sweep:
+        sweep = []
+        hbm_peak = peaks()[0]
+        for n in (1 << 20, 10 << 20):
+            kk, EE, tmm = 10, 512, 16
+            TT = n // kk
+            gen = torch.Generator(device=dev).manual_seed(1234 + n)
+            ids_s = torch.randint(0, EE, (TT, kk), generator=gen, device=dev, dtype=torch.int32)
+            w_s = torch.rand((TT, kk), generator=gen, device=dev)
+            cap_s = B.capacity(TT, kk, EE, tmm)
+            o_s = B.plan(ids_s, w_s, EE, tmm, cap=cap_s)
+            ts = []
+            for i in range(13):
+                flush.fill_(i & 0xFF)
+                a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a_ev.record(stream)
+                B.plan(ids_s, w_s, EE, tmm, cap=cap_s, out=o_s)
+                b_ev.record(stream)
+                torch.cuda.synchronize(dev)
+                if i >= 3:
+                    ts.append(a_ev.elapsed_time(b_ev) * 1e3)
+            r_pad = int(o_s["offsets"][-1])
+            # read ids and w, write pos, srt_tok and srt_w, the offsets and counts
+            byts = 8 * n + 4 * n + 8 * r_pad + 8 * (EE + 1)
+            us = statistics.median(ts)
+            sweep.append({"entries": n, "T": TT, "k": kk, "E": EE, "tm": tmm, "us": us,
+                          "algorithmic_bytes": byts, "hbm_gbs": byts / us / 1e3,
+                          "frac": byts / us / 1e3 / hbm_peak})
+            del ids_s, w_s, o_s
+
     if rank != 0:
         return
     hbm, tflops, peak_src = peaks()
@@ -416,6 +450,7 @@ def run_native(args, rank, world, local):
         "plan_us_per_layer": plan_graph_us,
         "plan_us_per_layer_method": "48 moe_plan calls per CUDA graph replay, mean per call",
         "plan_us_cold": stage_us["plan"],
+        "plan_sweep": sweep,
         "stages_us": stage_us,
         "layer_hbm_gbs": layer_gbs,
         "roofline": {"kernel": ("k_ffn<gate/up, E4M3 operands> (tcgen05.mma.kind::f8f6f4 "
@@ -494,6 +529,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-plan-sweep", action="store_true",
+                    help="skip the plan timed alone at 1M and 10M entries")
     ap.add_argument("--no-fp8", action="store_true",
                     help="skip the E4M3 layer measured beside the bf16 one")
     ap.add_argument("--weights", choices=("bf16", "e4m3", "f8"), default="bf16",

@@ -158,10 +158,9 @@ MOE_API int moe_plan(const int32_t *ids, const float *w, int T, int k, int E, in
  * Arguments are those of moe_plan, without ws / ws_bytes and with
  *   status   uint32* device word that receives the MOE_STATUS_* bits of this
  *            call (reset by the call), or NULL to leave them in the library.
- * Limit: (plan blocks rounded up to a multiple of 4) x E <=
- * MOE_PLAN_NOALLOC_MAX_COUNTS, where the plan uses ceil(T*k / 512) blocks
- * (at most 256): any T with E <= 1024, or T*k <= 32768 with E = 4096.
- * Larger sizes return MOE_ERR_WORKSPACE.
+ * Limit: ceil(T*k / 4096) x E <= MOE_PLAN_NOALLOC_MAX_COUNTS (one row of
+ * E counts per block of 4096 entries): T*k up to 2M entries with E = 512,
+ * up to 262144 with E = 4096.  Larger sizes return MOE_ERR_WORKSPACE.
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any

@@ -88,7 +88,7 @@ int layout(int T, int d, int E, int k, int f, int tm, size_t *out)
     const int64_t n = int64_t(T) * k;
     const size_t sizes[MOE_WS_TOTAL] = {
         256,                                             // status word
-        size_t(moe::plan_count_stride(n)) * E * 4,       // per-block expert counts / bases
+        size_t(moe::plan_count_rows(n)) * E * 4,       // per-block expert counts / bases
         size_t(E + 1) * 4,                               // offsets
         size_t(E) * 4,                                   // counts
         size_t(cap) * 4,                                 // srt_tok
@@ -126,7 +126,7 @@ size_t moe_plan_workspace_bytes(int T, int k, int E)
 {
     if (!base_sizes_ok(T, k, E))
         return 0;
-    return 256 + align256(size_t(moe::plan_count_stride(int64_t(T) * k)) * E * 4);
+    return 256 + align256(size_t(moe::plan_count_rows(int64_t(T) * k)) * E * 4);
 }
 
 int moe_plan(const int32_t *ids, const float *w, int T, int k, int E, int tm, int32_t *offsets,

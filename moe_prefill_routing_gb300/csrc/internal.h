@@ -10,31 +10,19 @@ namespace moe {
 
 // ---- routing plan (plan.cu) ------------------------------------------------
 
-// Flat entries per histogram / place block.  Grows past 512 only when
-// T*k > 512 * kPlanMaxBlocks, so the single-CTA scan reads at most
-// kPlanMaxBlocks * E counts.
-constexpr int kPlanBlockMin = 512;
-constexpr int kPlanMaxBlocks = 256;
-
-inline int64_t plan_block_entries(int64_t n)
-{
-    if (n <= int64_t(kPlanBlockMin) * kPlanMaxBlocks)
-        return kPlanBlockMin;
-    int64_t b = (n + kPlanMaxBlocks - 1) / kPlanMaxBlocks;
-    return (b + kPlanBlockMin - 1) / kPlanBlockMin * kPlanBlockMin;
-}
+// Flat entries per block of the multi-kernel plan (inputs above the
+// one-launch cluster plan): 8 warps x 16 steps x 32 entries.
+constexpr int kPlanBlockEntries = 4096;
 
 inline int plan_num_blocks(int64_t n)
 {
-    const int64_t b = plan_block_entries(n);
-    return static_cast<int>((n + b - 1) / b);
+    return static_cast<int>((n + kPlanBlockEntries - 1) / kPlanBlockEntries);
 }
 
-// The per-block counts are stored expert-major, one row of this many int32
-// per expert (the block count rounded up to 4, so rows load as int4).
-inline int plan_count_stride(int64_t n)
+// The per-block expert counts: one row of E int32 per block.
+inline int64_t plan_count_rows(int64_t n)
 {
-    return (plan_num_blocks(n) + 3) / 4 * 4;
+    return plan_num_blocks(n);
 }
 
 cudaError_t launch_plan(const int32_t *ids, const float *w, int T, int k, int E, int tm,

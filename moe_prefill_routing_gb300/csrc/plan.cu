@@ -1,30 +1,35 @@
-// Routing plan: per-block expert histogram with in-block ranks -> single-CTA
-// padded scan with the tail-row fill -> parallel place.
+// Routing plan: per-expert counts, an exclusive scan padded to tm with the
+// tail rows filled, and a stable place.
 //
 // "Round 4 Track C: Prefill MoE Plan (mm_clear + mm_hist + mm_scan + mm_place)
 // & Epilogue / Gather Audit", section 1:
-//  - item 1: the histogram writes every (block, expert) count, so nothing has
-//    to be cleared; the scan, which already knows each expert's first row,
-//    count and padded size, writes the -1 tail rows itself;
+//  - item 1: every (block, expert) count is written, so nothing has to be
+//    cleared; the scan, which knows each expert's first row, count and
+//    padded size, writes the -1 tail rows itself;
 //  - item 2: the rank of an entry among the earlier entries of its block
-//    with the same expert is found without a serial per-thread loop.  Here
-//    the histogram kernel finds it while counting: inside a warp,
-//    __match_any_sync groups the lanes holding the same expert and popc of
-//    the lower peers is the rank; across the block's warps, each warp's
-//    per-expert count (shared memory, one byte per expert per warp) is added
-//    for the warps before it.  No counter can overflow and nothing depends
-//    on top-k.  The place kernel is then a parallel scatter: row = block
-//    base of the expert + rank.
-//  - item 3: one CTA for the whole histogram+scan was slower than a multi-CTA
-//    histogram plus a one-CTA scan, because one CTA cannot use the whole GPU.
-//    On GB300 the launch and completion gaps between three small kernels
-//    cost more than the work, so chunks of up to 64K entries run the whole
-//    plan in ONE launch of a thread-block cluster (16 CTAs
-//    where the GPU can place them, else 8; 256 threads each): each CTA counts
-//    and ranks its share of the entries, then, through distributed shared
-//    memory and hardware cluster barriers, each CTA scans a share of the
-//    experts and hands every CTA the first row of each expert for its share
-//    of entries.  Larger inputs use the three kernels below.
+//    with the same expert is found without a serial per-thread loop: each
+//    warp walks a contiguous range 32 entries at a time with a running count
+//    per expert in shared memory, __match_any_sync grouping the lanes that
+//    hold the same expert and popc of the lower peers giving the rank inside
+//    a step; the warps' counts, prefixed over the warps, place each warp's
+//    range after the earlier ones.  No counter can overflow and nothing
+//    depends on top-k;
+//  - item 3: one CTA for the whole histogram+scan was slower than a
+//    multi-CTA histogram plus a one-CTA scan, because one CTA cannot use the
+//    whole GPU.  On GB300 the launch and completion gaps between small
+//    kernels cost more than the work, so chunks of up to 64K entries run the
+//    whole plan in ONE launch of a thread-block cluster (16 CTAs where the
+//    GPU can place them, else 8; 256 threads each): each CTA counts and
+//    ranks its share, then, through distributed shared memory and hardware
+//    cluster barriers, each CTA scans a share of the experts and hands every
+//    CTA the first row of each expert for its share of entries.
+// Larger inputs, where the plan is bound by its HBM traffic, run four
+// kernels over blocks of 4096 entries, chained with programmatic dependent
+// launch: count (each block's count per expert), column scan (per expert,
+// the rows of the earlier blocks), expert scan (offsets, tail rows, tile
+// table), place (the ranks walked again, in registers, and the scatter).
+// The ranks are recomputed rather than stored between the passes, so the
+// entries are read twice and pos, srt_tok and srt_w written once.
 #include "../../include/moe_prefill.h"
 #include "internal.h"
 #include "ptx.cuh"
@@ -34,115 +39,164 @@
 namespace moe {
 namespace {
 
-constexpr int kHistThreads = 512;   // 16 warps: one 512-entry sub-block per pass
-constexpr int kHistWarps = kHistThreads / 32;
-constexpr int kScanThreads = 1024;
-constexpr int kPlaceThreads = 256;
 constexpr uint32_t kFull = 0xffffffffu;
-constexpr int kRankSkipped = -1;  // id -1
-constexpr int kRankBadId = -2;    // id outside [-1, E)
 
-// Block b of B flat entries.  For each entry: pos[i] = its rank among the
-// earlier entries of the block with the same expert (or -1 / -2 for a
-// skipped / bad id).  For each expert: bcnt[e][b] = the block's count.
-// The block is walked in sub-blocks of 512 entries, one per thread, so
-// ranks keep flat order: earlier sub-blocks (carry), then earlier warps of
-// this sub-block (per-warp counts), then lower lanes (match_any peers).
-__global__ void __launch_bounds__(kHistThreads)
-    k_hist(const int32_t *__restrict__ ids, int64_t n, int E, int64_t B, int stride,
-           int32_t *__restrict__ bcnt, int32_t *__restrict__ pos)
+// ---- multi-kernel plan for large inputs ------------------------------------------
+
+constexpr int kPThreads = 256;  // 8 warps, each walking 16 steps of 32 entries
+constexpr int kPWarps = kPThreads / 32;
+constexpr int kPSteps = 16;
+static_assert(kPWarps * kPSteps * 32 == kPlanBlockEntries, "entries per block");
+constexpr int kColThreads = 1024;  // column scan: 32 warps x 32 experts
+constexpr int kScanThreads = 1024;
+
+// 16 * E bytes of per-warp 16-bit counters: E vectors of 16 bytes.
+__device__ __forceinline__ void zero_warp_counts(uint16_t *cntw, int E)
 {
-    extern __shared__ __align__(16) uint8_t hist_smem[];
-    uint8_t *cnt = hist_smem;                                  // [16 warps][E] counts
-    int *carry = reinterpret_cast<int *>(hist_smem + kHistWarps * E);  // [E]
-    pdl_launch_dependents();
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const uint32_t lane = tid & 31, lt = lanemask_lt();
-    for (int e = tid; e < E; e += kHistThreads)
-        carry[e] = 0;
-    pdl_wait();
+    for (int v = threadIdx.x; v < E; v += kPThreads)
+        reinterpret_cast<uint4 *>(cntw)[v] = make_uint4(0u, 0u, 0u, 0u);
+}
 
-    const int64_t start = int64_t(blockIdx.x) * B;
-    const int64_t end = min(n, start + B);
-    for (int64_t s0 = start; s0 < end; s0 += kHistThreads) {
-        for (int v = tid; v < E; v += kHistThreads)  // 16*E bytes = E vectors of 16
-            reinterpret_cast<uint4 *>(cnt)[v] = make_uint4(0u, 0u, 0u, 0u);
-        __syncthreads();
-        const int64_t i = s0 + tid;
-        const int id = i < end ? ids[i] : -1;
-        const bool ok = id >= 0 && id < E;
-        const uint32_t key = ok ? uint32_t(id) : (0x80000000u | lane);
-        const uint32_t peers = __match_any_sync(kFull, key);
-        if (ok && lane == uint32_t(__ffs(peers) - 1))
-            cnt[warp * E + id] = uint8_t(__popc(peers));
-        __syncthreads();
-        if (i < end) {
-            int r = id == -1 ? kRankSkipped : kRankBadId;
-            if (ok) {
-                r = carry[id] + __popc(peers & lt);
-                for (int w2 = 0; w2 < warp; ++w2)
-                    r += cnt[w2 * E + id];
-            }
-            pos[i] = r;
-        }
-        __syncthreads();
-        for (int e = tid; e < E; e += kHistThreads) {
-            int c = 0;
+// Walk this warp's range [lo, hi) (at most kPSteps * 32 entries): running
+// counts per expert in mycnt, and each entry's rank among the earlier
+// entries of the range with the same expert (-1 for an id outside [0, E)).
+// The lanes holding the same expert come from __match_any_sync, or (BALLOT)
+// from one ballot per bit of the expert id plus one for validity; measured,
+// the first is faster in the one-launch cluster plan, the second in the
+// place kernel of large inputs.
+template <bool BALLOT>
+__device__ __forceinline__ void warp_walk(const int (&id)[kPSteps], int64_t lo, int64_t hi, int E,
+                                          uint16_t *mycnt, int (*rank)[kPSteps])
+{
+    const uint32_t lane = threadIdx.x & 31, lt = lanemask_lt();
+    const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;  // bits of the largest id
 #pragma unroll
-            for (int w2 = 0; w2 < kHistWarps; ++w2)
-                c += cnt[w2 * E + e];
-            carry[e] += c;
+    for (int s = 0; s < kPSteps; ++s) {
+        if (lo + s * 32 < hi) {  // the same for the whole warp
+            const bool ok = lo + s * 32 + lane < hi && id[s] >= 0 && id[s] < E;
+            uint32_t peers;
+            if (BALLOT) {
+                const uint32_t vb = __ballot_sync(kFull, ok);  // every lane, then select
+                peers = ok ? vb : (1u << lane);
+                for (int bit = 0; bit < nbits; ++bit) {
+                    const bool set = (uint32_t(id[s]) >> bit) & 1u;
+                    const uint32_t bb = __ballot_sync(kFull, set);
+                    peers &= set ? bb : ~bb;
+                }
+            } else {
+                peers = __match_any_sync(kFull, ok ? uint32_t(id[s]) : (0x80000000u | lane));
+            }
+            const int leader = __ffs(peers) - 1;
+            int first = 0;
+            if (ok && lane == uint32_t(leader)) {
+                first = mycnt[id[s]];
+                mycnt[id[s]] = uint16_t(first + __popc(peers));
+            }
+            if (rank) {
+                first = __shfl_sync(kFull, first, leader);
+                (*rank)[s] = ok ? first + __popc(peers & lt) : -1;
+            }
+            __syncwarp();
         }
-        __syncthreads();
     }
-    for (int e = tid; e < E; e += kHistThreads)
-        bcnt[int64_t(e) * stride + blockIdx.x] = carry[e];
 }
 
-__device__ __forceinline__ int take(int b, int nblk, int v)
+// Count: bcnt[b][e] = entries of block b (kPlanBlockEntries flat entries)
+// routed to expert e.  Only the totals matter here, so shared-memory atomics
+// count (the order of the adds does not change a sum of ones).
+__global__ void __launch_bounds__(kPThreads)
+    k_count(const int32_t *__restrict__ ids, int64_t n, int E, int32_t *__restrict__ bcnt)
 {
-    return b < nblk ? v : 0;
+    extern __shared__ __align__(16) uint8_t psm[];
+    int *cnt = reinterpret_cast<int *>(psm);  // [E]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_launch_dependents();
+    for (int e = threadIdx.x; e < E; e += kPThreads)
+        cnt[e] = 0;
+    pdl_wait();
+    const int64_t lo = int64_t(blockIdx.x) * kPlanBlockEntries + warp * kPSteps * 32;
+    const int64_t hi = min(n, lo + kPSteps * 32);
+    int id[kPSteps];
+#pragma unroll
+    for (int s = 0; s < kPSteps; ++s) {
+        const int64_t i = lo + s * 32 + lane;
+        id[s] = i < hi ? ids[i] : -1;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int s = 0; s < kPSteps; ++s)
+        if (lo + s * 32 + lane < hi && id[s] >= 0 && id[s] < E)
+            atomicAdd(&cnt[id[s]], 1);
+    __syncthreads();
+    int32_t *row = bcnt + int64_t(blockIdx.x) * E;
+    for (int e = threadIdx.x; e < E; e += kPThreads)
+        row[e] = cnt[e];
 }
 
-// One CTA.  For each expert (ascending id): c_e = sum of its block counts,
-// padded size P_e = ceil(c_e / tm) * tm, offsets[e] = exclusive scan of P_e.
-// Each expert's row of block counts (int4 loads) is replaced in place by
-// block bases (first row of the expert's entries of that block); the tail
-// rows [offsets[e] + c_e, offsets[e] + P_e) get srt_tok = -1, srt_w = +0,
-// and the tile table gets the expert's tiles.  Resets the status word.
+// Column scan: for 32 experts per CTA, bcnt[b][e] <- entries of expert e in
+// blocks < b, and counts[e] = the total.  Warp w sums a contiguous segment
+// of blocks, the segment sums are prefixed in shared memory, and each warp
+// rewrites its segment.  Rows are read 32 experts (128 bytes) at a time.
+__global__ void __launch_bounds__(kColThreads)
+    k_colscan(int32_t *__restrict__ bcnt, int nblk, int E, int32_t *__restrict__ counts)
+{
+    __shared__ int seg_sum[kColThreads / 32][32];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * 32 + lane;
+    const bool valid = e < E;
+    const int seg = (nblk + kColThreads / 32 - 1) / (kColThreads / 32);
+    const int b0 = min(nblk, warp * seg), b1 = min(nblk, b0 + seg);
+    int sum = 0;
+    if (valid) {
+#pragma unroll 8
+        for (int b = b0; b < b1; ++b)
+            sum += bcnt[int64_t(b) * E + e];
+    }
+    seg_sum[warp][lane] = sum;
+    __syncthreads();
+    int run = 0, total = 0;
+    for (int w2 = 0; w2 < kColThreads / 32; ++w2) {
+        run += w2 < warp ? seg_sum[w2][lane] : 0;
+        total += seg_sum[w2][lane];
+    }
+    if (valid) {
+#pragma unroll 8
+        for (int b = b0; b < b1; ++b) {
+            const int64_t i = int64_t(b) * E + e;
+            const int v = bcnt[i];
+            bcnt[i] = run;
+            run += v;
+        }
+        if (warp == 0)
+            counts[e] = total;
+    }
+}
+
+// Expert scan (one CTA): offsets[e] = sum over e' < e of counts[e'] rounded
+// up to tm, offsets[E] = R_pad; the tail rows [offsets[e] + counts[e],
+// offsets[e + 1]) get srt_tok = -1 and srt_w = +0; with fill_tiles (no place
+// kernel follows, i.e. no entries) tile_expert[t] = e for the tiles of e.
+// Resets the status word (the place adds bad-id bits after).
 __global__ void __launch_bounds__(kScanThreads)
-    k_scan_pad(int32_t *__restrict__ bcnt, int nblk, int stride, int E, int tm, int64_t cap,
-               int32_t *__restrict__ offsets, int32_t *__restrict__ counts,
-               int32_t *__restrict__ srt_tok, float *__restrict__ srt_w,
-               int32_t *__restrict__ tile_expert, uint32_t *__restrict__ status)
+    k_scan_experts(const int32_t *__restrict__ counts, int E, int tm, int64_t cap,
+                   int32_t *__restrict__ offsets, int32_t *__restrict__ srt_tok,
+                   float *__restrict__ srt_w, int32_t *__restrict__ tile_expert,
+                   uint32_t *__restrict__ status, bool fill_tiles)
 {
     __shared__ int warp_incl[kScanThreads / 32];
     pdl_launch_dependents();
     pdl_wait();
-
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int64_t n_tiles_cap = cap / tm;
-    const int nq = stride / 4;
     int64_t carry = 0;  // padded rows of the experts before this slice
-
     for (int base = 0; base < E; base += kScanThreads) {
         const int e = base + tid;
-        int4 *row = reinterpret_cast<int4 *>(bcnt + int64_t(min(e, E - 1)) * stride);
-        int c = 0;
-        if (e < E) {
-#pragma unroll 8
-            for (int q = 0; q < nq; ++q) {
-                const int4 v = row[q];
-                const int b = 4 * q;
-                c += take(b, nblk, v.x) + take(b + 1, nblk, v.y) + take(b + 2, nblk, v.z) +
-                     take(b + 3, nblk, v.w);
-            }
-        }
-        const int P = e < E ? (c + tm - 1) / tm * tm : 0;
-
-        // block-wide exclusive scan of P (warp shuffles, then warp totals)
-        int v = P;
+        const int c = e < E ? counts[e] : 0;
+        const int P = (c + tm - 1) / tm * tm;
+        int v = P;  // block-wide exclusive scan: warp shuffles, then warp totals
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int t = __shfl_up_sync(kFull, v, o);
@@ -166,32 +220,15 @@ __global__ void __launch_bounds__(kScanThreads)
         const int64_t off = carry + (v - P) + (warp > 0 ? warp_incl[warp - 1] : 0);
         const int slice_total = warp_incl[kScanThreads / 32 - 1];
         __syncthreads();  // warp_incl is reused by the next slice
-
         if (e < E) {
             offsets[e] = int32_t(off);
-            counts[e] = c;
-            int run = int(off);
-#pragma unroll 8
-            for (int q = 0; q < nq; ++q) {
-                const int4 cv = row[q];
-                const int b = 4 * q;
-                int4 o;
-                o.x = run;
-                run += take(b, nblk, cv.x);
-                o.y = run;
-                run += take(b + 1, nblk, cv.y);
-                o.z = run;
-                run += take(b + 2, nblk, cv.z);
-                o.w = run;
-                run += take(b + 3, nblk, cv.w);
-                row[q] = o;
-            }
             for (int64_t r = off + c; r < off + P && r < cap; ++r) {
                 srt_tok[r] = -1;
                 srt_w[r] = 0.0f;
             }
-            for (int64_t t = off / tm; t < (off + P) / tm && t < n_tiles_cap; ++t)
-                tile_expert[t] = e;
+            if (fill_tiles)
+                for (int64_t t = off / tm; t < (off + P) / tm && t < n_tiles_cap; ++t)
+                    tile_expert[t] = e;
         }
         carry += slice_total;
     }
@@ -201,35 +238,148 @@ __global__ void __launch_bounds__(kScanThreads)
     }
 }
 
-// One thread per flat entry: row = base[e][block] + rank (left in pos by
-// k_hist); pos[i] = row, srt_tok[row] = token, srt_w[row] = weight (bit copy).
-__global__ void __launch_bounds__(kPlaceThreads)
-    k_place(const int32_t *__restrict__ ids, const float *__restrict__ w, int64_t n, int k,
-            int64_t B, int stride, int64_t cap, const int32_t *__restrict__ bbase,
-            int32_t *__restrict__ pos, int32_t *__restrict__ srt_tok, float *__restrict__ srt_w,
-            uint32_t *__restrict__ status)
+// Place: block b walks its entries again (same ranges, same ranks), prefixes
+// the warps' counts per expert, and gives each entry row = offsets[e] +
+// (rows of e in earlier blocks) + (its rank among the block's entries of e).
+// A block's entries of one expert fill consecutive rows, so they are first
+// sorted by expert in shared memory and then written out run after run:
+// neighbouring lanes write neighbouring rows of srt_tok and srt_w (pos keeps
+// flat order).  The kernel also fills the tile table: tile t belongs to the
+// expert whose rows hold row t * tm.
+constexpr size_t place_smem_bytes(int E)
 {
+    return size_t(kPWarps) * E * sizeof(uint16_t) + size_t(3 * E + 2) * sizeof(int) +
+           size_t(kPlanBlockEntries) * (2 * sizeof(int) + sizeof(uint16_t));
+}
+
+__global__ void __launch_bounds__(kPThreads)
+    k_place_blocks(const int32_t *__restrict__ ids, const float *__restrict__ w, int64_t n,
+                   int k, int E, int tm, int64_t cap, const int32_t *__restrict__ offsets,
+                   const int32_t *__restrict__ bcnt, int32_t *__restrict__ pos,
+                   int32_t *__restrict__ srt_tok, float *__restrict__ srt_w,
+                   int32_t *__restrict__ tile_expert, uint32_t *__restrict__ status)
+{
+    extern __shared__ __align__(16) uint8_t psm[];
+    uint16_t *cntw = reinterpret_cast<uint16_t *>(psm);                            // [8][E]
+    int *rowbase = reinterpret_cast<int *>(psm + kPWarps * E * sizeof(uint16_t));  // [E]
+    int *loc = rowbase + E;               // [E + 1] block-local first slot of each expert
+    int *s_tok = loc + E + 1;             // [4096] the block's entries sorted by expert
+    float *s_w = reinterpret_cast<float *>(s_tok + kPlanBlockEntries);
+    int *s_off = reinterpret_cast<int *>(s_w + kPlanBlockEntries);  // [E + 1] offsets
+    uint16_t *s_e = reinterpret_cast<uint16_t *>(s_off + E + 1);
+    __shared__ int warp_tot[kPWarps];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_launch_dependents();
+    zero_warp_counts(cntw, E);
+    // everything is read after the wait: this launch may begin before the
+    // count kernel's own wait for whatever wrote the ids has ended
     pdl_wait();
+    const int64_t lo = int64_t(blockIdx.x) * kPlanBlockEntries + warp * kPSteps * 32;
+    const int64_t hi = min(n, lo + kPSteps * 32);
+    int id[kPSteps], rank[kPSteps];
+    float wv[kPSteps];
+#pragma unroll
+    for (int s = 0; s < kPSteps; ++s) {
+        const int64_t i = lo + s * 32 + lane;
+        id[s] = i < hi ? ids[i] : -1;
+        wv[s] = i < hi ? w[i] : 0.0f;
+    }
+    __syncthreads();
+    warp_walk<true>(id, lo, hi, E, cntw + warp * E, &rank);
+    __syncthreads();
+    // per expert: warp counts -> prefix over warps, the block's total, and
+    // an exclusive scan of the totals over the experts (contiguous runs of J
+    // experts per thread, then warp shuffles and warp totals)
+    const int32_t *brow = bcnt + int64_t(blockIdx.x) * E;
+    const int J = (E + kPThreads - 1) / kPThreads;
+    const int e0 = min(E, tid * J), e1 = min(E, e0 + J);
+    int tsum = 0;
+    for (int e = e0; e < e1; ++e) {
+        int run = 0;
+#pragma unroll
+        for (int w2 = 0; w2 < kPWarps; ++w2) {
+            const int t = cntw[w2 * E + e];
+            cntw[w2 * E + e] = uint16_t(run);
+            run += t;
+        }
+        loc[e] = run;  // the block's count for now
+        tsum += run;
+        s_off[e] = offsets[e];
+        rowbase[e] = s_off[e] + brow[e];
+    }
+    if (tid == 0)
+        s_off[E] = offsets[E];
+    int v = tsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(kFull, v, o);
+        if (lane >= o)
+            v += t;
+    }
+    if (lane == 31)
+        warp_tot[warp] = v;
+    __syncthreads();
+    int slot0 = v - tsum, total = 0;
+#pragma unroll
+    for (int w2 = 0; w2 < kPWarps; ++w2) {
+        slot0 += w2 < warp ? warp_tot[w2] : 0;
+        total += warp_tot[w2];
+    }
+    for (int e = e0; e < e1; ++e) {
+        const int c = loc[e];
+        loc[e] = slot0;
+        slot0 += c;
+    }
+    if (tid == 0)
+        loc[E] = total;
+    __syncthreads();
+    // each entry: its rank in the block, pos in flat order, its sorted slot
+    const uint16_t *mycnt = cntw + warp * E;
     bool bad = false;
-    const int64_t nthreads = int64_t(gridDim.x) * blockDim.x;
-    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += nthreads) {
-        const int r = pos[i];
-        if (r >= 0) {
-            const int e = ids[i];
-            const int row = bbase[int64_t(e) * stride + i / B] + r;
-            pos[i] = row;
-            if (row < cap) {
-                srt_tok[row] = int32_t(i / k);
-                srt_w[row] = w[i];
+#pragma unroll
+    for (int s = 0; s < kPSteps; ++s) {
+        const int64_t i = lo + s * 32 + lane;
+        if (i < hi) {
+            if (rank[s] >= 0) {
+                const int r = mycnt[id[s]] + rank[s];
+                pos[i] = rowbase[id[s]] + r;
+                const int slot = loc[id[s]] + r;
+                s_tok[slot] = int32_t(i / k);
+                s_w[slot] = wv[s];
+                s_e[slot] = uint16_t(id[s]);
+            } else {
+                pos[i] = -1;
+                bad |= id[s] != -1;
             }
-        } else if (r == kRankBadId) {
-            bad = true;
-            pos[i] = -1;
         }
     }
-    if (__any_sync(kFull, bad) && (threadIdx.x & 31) == 0)
+    if (__any_sync(kFull, bad) && lane == 0)
         atomicOr(status, MOE_STATUS_BAD_ID);
+    __syncthreads();
+    for (int j = tid; j < total; j += kPThreads) {
+        const int e = s_e[j];
+        const int row = rowbase[e] + (j - loc[e]);
+        if (row < cap) {
+            srt_tok[row] = s_tok[j];
+            srt_w[row] = s_w[j];
+        }
+    }
+    // tile table, spread over the grid
+    const int64_t R = min(int64_t(s_off[E]), cap);
+    const int64_t ntiles = R / tm;
+    for (int64_t t = int64_t(blockIdx.x) * kPThreads + tid; t < ntiles;
+         t += int64_t(gridDim.x) * kPThreads) {
+        const int64_t r = t * tm;
+        int l = 0, h = E - 1;  // the last e with offsets[e] <= r
+        while (l < h) {
+            const int mid = (l + h + 1) >> 1;
+            if (s_off[mid] <= r)
+                l = mid;
+            else
+                h = mid - 1;
+        }
+        tile_expert[t] = l;
+    }
 }
 
 // ---- one-launch plan for a thread-block cluster --------------------------------
@@ -239,6 +389,7 @@ constexpr int kCWarps = kCThreads / 32;
 constexpr int kCSteps = 16;  // 32-entry steps per warp, held in registers
 constexpr int kClusterMax = 16;
 constexpr int kCEntriesPerCta = kCWarps * kCSteps * 32;  // 4096
+static_assert(kCSteps == kPSteps, "the cluster plan walks with warp_walk");
 
 constexpr size_t cluster_smem_bytes(int E)
 {
@@ -296,25 +447,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
     }
     __syncthreads();  // counters zeroed
     uint16_t *mycnt = cntw + warp * E;
-#pragma unroll
-    for (int s = 0; s < kCSteps; ++s) {
-        if (w_lo + s * 32 < w_hi) {  // the same for the whole warp
-            const int id = my_id[s];
-            const bool ok = w_lo + s * 32 + lane < w_hi && id >= 0 && id < E;
-            const uint32_t key = ok ? uint32_t(id) : (0x80000000u | lane);
-            const uint32_t peers = __match_any_sync(kFull, key);
-            const int leader = __ffs(peers) - 1;
-            int first = 0;
-            if (ok && lane == uint32_t(leader)) {
-                first = mycnt[id];
-                mycnt[id] = uint16_t(first + __popc(peers));
-            }
-            first = __shfl_sync(kFull, first, leader);
-            if (ok)
-                my_rank[s] = first + __popc(peers & lt);
-            __syncwarp();
-        }
-    }
+    warp_walk<false>(my_id, w_lo, w_hi, E, mycnt, &my_rank);
     __syncthreads();
     for (int e = tid; e < E; e += kCThreads) {  // warp counts -> prefix over warps
         int run = 0;
@@ -513,30 +646,36 @@ cudaError_t launch_plan(const int32_t *ids, const float *w, int T, int k, int E,
         return cudaLaunchKernelEx(&cfg, k_plan_cluster, ids, w, n, k, E, tm, cap, chunk, offsets,
                                   counts, srt_tok, srt_w, pos, tile_expert, status);
     }
-    const int64_t B = plan_block_entries(n);
     const int nblk = plan_num_blocks(n);
-    const int stride = plan_count_stride(n);
+    const size_t cnt_smem = size_t(E) * sizeof(int);
+    const size_t place_smem = place_smem_bytes(E);
+    const size_t max_place_smem = place_smem_bytes(MOE_MAX_EXPERTS);
     cudaError_t err;
     if (nblk > 0) {
-        const size_t hist_smem = size_t(E) * (kHistWarps + sizeof(int));
-        err = ensure_smem_limit(reinterpret_cast<const void *>(k_hist), kSlotHist,
-                                size_t(MOE_MAX_EXPERTS) * (kHistWarps + sizeof(int)));
+        err = ensure_smem_limit(reinterpret_cast<const void *>(k_place_blocks), kSlotPlace,
+                                    max_place_smem);
+        if (err == cudaSuccess)
+            err = launch_pdl(k_count, dim3(nblk), dim3(kPThreads), cnt_smem, stream, ids, n, E,
+                             bcnt);
+        if (err == cudaSuccess)
+            err = launch_pdl(k_colscan, dim3((E + 31) / 32), dim3(kColThreads), 0, stream, bcnt,
+                             nblk, E, counts);
         if (err != cudaSuccess)
             return err;
-        err = launch_pdl(k_hist, dim3(nblk), dim3(kHistThreads), hist_smem, stream, ids, n, E, B,
-                         stride, bcnt, pos);
+    } else {
+        err = cudaMemsetAsync(counts, 0, size_t(E) * sizeof(int32_t), stream);
         if (err != cudaSuccess)
             return err;
     }
-    err = launch_pdl(k_scan_pad, dim3(1), dim3(kScanThreads), 0, stream, bcnt, nblk, stride, E,
-                     tm, cap, offsets, counts, srt_tok, srt_w, tile_expert, status);
+    err = launch_pdl(k_scan_experts, dim3(1), dim3(kScanThreads), 0, stream,
+                     static_cast<const int32_t *>(counts), E, tm, cap, offsets, srt_tok, srt_w,
+                     tile_expert, status, nblk == 0);
     if (err != cudaSuccess || nblk == 0)
         return err;
-    const int64_t want = (n + kPlaceThreads - 1) / kPlaceThreads;
-    const int64_t most = int64_t(device_sm_count()) * 8;
-    return launch_pdl(k_place, dim3(unsigned(want < most ? want : most)), dim3(kPlaceThreads), 0,
-                      stream, ids, w, n, k, B, stride, cap, (const int32_t *)bcnt, pos, srt_tok,
-                      srt_w, status);
+    return launch_pdl(k_place_blocks, dim3(nblk), dim3(kPThreads), place_smem, stream, ids, w, n,
+                      k, E, tm, cap, static_cast<const int32_t *>(offsets),
+                      static_cast<const int32_t *>(bcnt), pos, srt_tok, srt_w, tile_expert,
+                      status);
 }
 
 }  // namespace moe

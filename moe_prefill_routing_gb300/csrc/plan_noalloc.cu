@@ -65,7 +65,7 @@ extern "C" int moe_plan_noalloc(const int32_t *ids, const float *w, int T, int k
         return MOE_ERR_NULL;
     if (cap < moe_capacity(T, k, E, tm) || cap > INT_MAX)
         return MOE_ERR_CAPACITY;
-    if (int64_t(moe::plan_count_stride(int64_t(T) * k)) * E > MOE_PLAN_NOALLOC_MAX_COUNTS)
+    if (int64_t(moe::plan_count_rows(int64_t(T) * k)) * E > MOE_PLAN_NOALLOC_MAX_COUNTS)
         return MOE_ERR_WORKSPACE;
     if (!aligned4(ids) || !aligned4(w) || !aligned4(offsets) || !aligned4(counts) ||
         !aligned4(srt_tok) || !aligned4(srt_w) || !aligned4(pos) || !aligned4(tile_expert) ||

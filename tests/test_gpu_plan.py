@@ -127,7 +127,7 @@ def test_plan_one_launch_limit(T, k, E):
 
 
 def test_plan_large_block_path():
-    # T*k above 512 * 256 entries: blocks of more than 512 entries
+    # T*k = 140002 entries: 35 blocks of 4096, the last one ragged
     ids, w = W.make_routing(70001, 256, 2, "topk", seed=3)
     check(ids, w, 256, 16)
 
@@ -167,3 +167,27 @@ def test_plan_repeatable():
     b, _ = gpu_plan(inp["ids"], inp["w"], 512, 16)
     for n in a:
         assert np.array_equal(a[n], b[n])
+
+
+def test_plan_ten_million_entries_bit_exact():
+    # the size of the plan sweep the benchmark times: 10M entries (k = 10,
+    # E = 512), three-kernel plan, against the oracle's counting sort
+    T, k, E, tm = 1 << 20, 10, 512, 16
+    rng = np.random.default_rng(10)
+    ids = rng.integers(0, E, size=(T, k), dtype=np.int32)
+    ids[rng.random(ids.shape) < 0.01] = -1
+    w = rng.standard_normal((T, k)).astype(np.float32)
+    check(ids, w, E, tm)
+
+
+@pytest.mark.parametrize("tm", [1, 16, 128, 1024])
+def test_plan_multi_kernel_empty_experts_and_tiles(tm):
+    # above the one-launch size, with most experts empty (runs of equal
+    # offsets for the tile table's search), a few skipped slots and bad ids
+    T, k, E = 20000, 4, 700
+    rng = np.random.default_rng(tm)
+    used = rng.choice(E, size=90, replace=False)
+    ids = rng.choice(used, size=(T, k)).astype(np.int32)
+    ids[rng.random(ids.shape) < 0.05] = -1
+    w = rng.standard_normal(ids.shape).astype(np.float32)
+    check(ids, w, E, tm)

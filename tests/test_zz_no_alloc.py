@@ -62,8 +62,8 @@ def test_noalloc_plan_equals_moe_plan_two_calls_in_a_row():
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
-    # 256 blocks x 4096 experts is above MOE_PLAN_NOALLOC_MAX_COUNTS
-    T, k, E, tm = 16384, 10, 4096, 16
+    # 74 blocks of 4096 entries x 4096 experts is above MOE_PLAN_NOALLOC_MAX_COUNTS
+    T, k, E, tm = 30000, 10, 4096, 16
     ids = torch.zeros((T, k), dtype=torch.int32, device="cuda")
     w = torch.zeros((T, k), dtype=torch.float32, device="cuda")
     with pytest.raises(B.MoeError) as e:
