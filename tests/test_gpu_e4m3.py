@@ -388,7 +388,7 @@ def test_f8_layer_host_chunks():
 
 @pytest.mark.parametrize("T,d,E,k,f,tm,skip", [
     (300, 128, 4096, 4, 64, 16, 0.0),    # E at its limit: the largest chunk table
-    (9000, 128, 64, 8, 128, 16, 0.05),   # T*k above 16 x 4096: the three-kernel plan
+    (9000, 128, 64, 8, 128, 16, 0.05),   # T*k above 16 x 4096: the multi-kernel plan
     (123, 192, 9, 3, 192, 16, 0.2),      # ragged tiles, skipped slots, d = 1.5 x 128
 ])
 def test_f8_and_e4m3_layers_at_the_limits(T, d, E, k, f, tm, skip):

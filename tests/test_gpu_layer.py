@@ -70,7 +70,7 @@ def test_layer_tiny_full_output():
     (200, 128, 70, 4, 704, 16, 0.1),     # f = 5.5 x 128
     (1, 128, 8, 8, 64, 16, 0.0),         # one token
     (300, 128, 4096, 4, 64, 16, 0.0),    # E at its limit: largest GEMM shared-memory table
-    (9000, 64, 64, 8, 64, 16, 0.05),     # T*k above 16 x 4096: the three-kernel plan
+    (9000, 64, 64, 8, 64, 16, 0.05),     # T*k above 16 x 4096: the multi-kernel plan
 ])
 def test_layer_shapes_full_output(T, d, E, k, f, tm, skip):
     inp = W.make_layer(T, d, E, k, f, tm=tm, seed=3 * T + E, skip_frac=skip)

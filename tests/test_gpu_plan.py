@@ -121,7 +121,7 @@ def test_plan_many_empty_experts_and_skips():
 @pytest.mark.parametrize("T,k,E", [(8192, 8, 128), (8193, 8, 128), (4096, 8, 4096), (4097, 8, 4096)])
 def test_plan_one_launch_limit(T, k, E):
     # up to 16 x 4096 entries the plan runs as one cluster launch, above it as
-    # three kernels; both sides of the limit must match the oracle
+    # the multi-kernel plan; both sides of the limit must match the oracle
     ids, w = W.make_routing(T, E, k, "topk", seed=T)
     check(ids, w, E, 16)
 
@@ -171,7 +171,7 @@ def test_plan_repeatable():
 
 def test_plan_ten_million_entries_bit_exact():
     # the size of the plan sweep the benchmark times: 10M entries (k = 10,
-    # E = 512), three-kernel plan, against the oracle's counting sort
+    # E = 512), multi-kernel plan, against the oracle's counting sort
     T, k, E, tm = 1 << 20, 10, 512, 16
     rng = np.random.default_rng(10)
     ids = rng.integers(0, E, size=(T, k), dtype=np.int32)
