@@ -108,7 +108,8 @@ MOE_API int64_t moe_capacity(int T, int k, int E, int tm);
 
 /*
  * Device workspace of moe_plan, in bytes: a 256-byte header holding the
- * status word (uint32 at offset 0) followed by the per-block expert counts.
+ * status word (uint32 at offset 0) followed by the per-block and per-group
+ * expert counts of the multi-kernel plan.
  */
 MOE_API size_t moe_plan_workspace_bytes(int T, int k, int E);
 
@@ -158,9 +159,10 @@ MOE_API int moe_plan(const int32_t *ids, const float *w, int T, int k, int E, in
  * Arguments are those of moe_plan, without ws / ws_bytes and with
  *   status   uint32* device word that receives the MOE_STATUS_* bits of this
  *            call (reset by the call), or NULL to leave them in the library.
- * Limit: ceil(T*k / 4096) x E <= MOE_PLAN_NOALLOC_MAX_COUNTS (one row of
- * E counts per block of 4096 entries): T*k up to 2M entries with E = 512,
- * up to 262144 with E = 4096.  Larger sizes return MOE_ERR_WORKSPACE.
+ * Limit: (B + ceil(B / 128)) x E <= MOE_PLAN_NOALLOC_MAX_COUNTS with
+ * B = ceil(T*k / 4096) (one row of E counts per block of 4096 entries and
+ * one per group of 128 blocks): T*k up to 2M entries with E = 512, up to
+ * 262144 with E = 4096.  Larger sizes return MOE_ERR_WORKSPACE.
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any
@@ -170,7 +172,7 @@ MOE_API int moe_plan(const int32_t *ids, const float *w, int T, int k, int E, in
  * the GPU (on different streams without ordering) race on it and must not
  * be issued.
  */
-#define MOE_PLAN_NOALLOC_MAX_COUNTS 262144
+#define MOE_PLAN_NOALLOC_MAX_COUNTS 266240
 #define MOE_PLAN_NOALLOC_SCRATCH_BYTES (256 + 4 * MOE_PLAN_NOALLOC_MAX_COUNTS)
 MOE_API int moe_plan_noalloc(const int32_t *ids, const float *w, int T, int k, int E, int tm,
                              int32_t *offsets, int32_t *counts, int32_t *srt_tok, float *srt_w,

@@ -19,10 +19,22 @@ inline int plan_num_blocks(int64_t n)
     return static_cast<int>((n + kPlanBlockEntries - 1) / kPlanBlockEntries);
 }
 
-// The per-block expert counts: one row of E int32 per block.
+// The column scan over blocks runs in groups of this many blocks; the
+// expert scan then adds the groups' totals.
+constexpr int kPlanGroupBlocks = 128;
+
+inline int plan_num_groups(int nblk)
+{
+    return (nblk + kPlanGroupBlocks - 1) / kPlanGroupBlocks;
+}
+
+// The multi-kernel plan's scratch: one row of E int32 per block (its
+// counts, then the rows of its group's earlier blocks), then one per group
+// (the group's totals, then the rows of the earlier groups).
 inline int64_t plan_count_rows(int64_t n)
 {
-    return plan_num_blocks(n);
+    const int nblk = plan_num_blocks(n);
+    return int64_t(nblk) + plan_num_groups(nblk);
 }
 
 cudaError_t launch_plan(const int32_t *ids, const float *w, int T, int k, int E, int tm,
@@ -129,6 +141,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // Slots of ensure_smem_limit's per-device cache.
 enum SmemSlot {
     kSlotPlace = 0,
+    kSlotPlaceOr,
     kSlotHist,
     kSlotGateUp,
     kSlotGateUpRows,

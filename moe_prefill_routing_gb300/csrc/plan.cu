@@ -26,8 +26,10 @@
 // Larger inputs, where the plan is bound by its HBM traffic, run four
 // kernels over blocks of 4096 entries, chained with programmatic dependent
 // launch: count (each block's count per expert), column scan (per expert,
-// the rows of the earlier blocks), expert scan (offsets, tail rows, tile
-// table), place (the ranks walked again, in registers, and the scatter).
+// the rows of the earlier blocks of the same group of 128 blocks, and each
+// group's total), expert scan (the groups' totals prefixed, offsets, tail
+// rows), place (the ranks walked again, in registers, the scatter and the
+// tile table).
 // The ranks are recomputed rather than stored between the passes, so the
 // entries are read twice and pos, srt_tok and srt_w written once.
 #include "../../include/moe_prefill.h"
@@ -60,32 +62,18 @@ __device__ __forceinline__ void zero_warp_counts(uint16_t *cntw, int E)
 // Walk this warp's range [lo, hi) (at most kPSteps * 32 entries): running
 // counts per expert in mycnt, and each entry's rank among the earlier
 // entries of the range with the same expert (-1 for an id outside [0, E)).
-// The lanes holding the same expert come from __match_any_sync, or (BALLOT)
-// from one ballot per bit of the expert id plus one for validity; measured,
-// the first is faster in the one-launch cluster plan, the second in the
-// place kernel of large inputs.
-template <bool BALLOT>
+// The lanes holding the same expert come from __match_any_sync (measured
+// faster than one ballot per id bit in the one-launch cluster plan).
 __device__ __forceinline__ void warp_walk(const int (&id)[kPSteps], int64_t lo, int64_t hi, int E,
                                           uint16_t *mycnt, int (*rank)[kPSteps])
 {
     const uint32_t lane = threadIdx.x & 31, lt = lanemask_lt();
-    const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;  // bits of the largest id
 #pragma unroll
     for (int s = 0; s < kPSteps; ++s) {
         if (lo + s * 32 < hi) {  // the same for the whole warp
             const bool ok = lo + s * 32 + lane < hi && id[s] >= 0 && id[s] < E;
-            uint32_t peers;
-            if (BALLOT) {
-                const uint32_t vb = __ballot_sync(kFull, ok);  // every lane, then select
-                peers = ok ? vb : (1u << lane);
-                for (int bit = 0; bit < nbits; ++bit) {
-                    const bool set = (uint32_t(id[s]) >> bit) & 1u;
-                    const uint32_t bb = __ballot_sync(kFull, set);
-                    peers &= set ? bb : ~bb;
-                }
-            } else {
-                peers = __match_any_sync(kFull, ok ? uint32_t(id[s]) : (0x80000000u | lane));
-            }
+            const uint32_t peers =
+                __match_any_sync(kFull, ok ? uint32_t(id[s]) : (0x80000000u | lane));
             const int leader = __ffs(peers) - 1;
             int first = 0;
             if (ok && lane == uint32_t(leader)) {
@@ -133,12 +121,14 @@ __global__ void __launch_bounds__(kPThreads)
         row[e] = cnt[e];
 }
 
-// Column scan: for 32 experts per CTA, bcnt[b][e] <- entries of expert e in
-// blocks < b, and counts[e] = the total.  Warp w sums a contiguous segment
-// of blocks, the segment sums are prefixed in shared memory, and each warp
-// rewrites its segment.  Rows are read 32 experts (128 bytes) at a time.
+// Column scan, per group of kPlanGroupBlocks blocks and 32 experts per CTA
+// (grid: expert slices x groups): bcnt[b][e] <- entries of expert e in the
+// group's blocks before b, and gsum[g][e] = the group's total.  Warp w sums
+// a contiguous segment of the group's blocks, the segment sums are prefixed
+// in shared memory, and each warp rewrites its segment.  Rows are read 32
+// experts (128 bytes) at a time.
 __global__ void __launch_bounds__(kColThreads)
-    k_colscan(int32_t *__restrict__ bcnt, int nblk, int E, int32_t *__restrict__ counts)
+    k_colscan(int32_t *__restrict__ bcnt, int nblk, int E, int32_t *__restrict__ gsum)
 {
     __shared__ int seg_sum[kColThreads / 32][32];
     pdl_launch_dependents();
@@ -146,11 +136,13 @@ __global__ void __launch_bounds__(kColThreads)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * 32 + lane;
     const bool valid = e < E;
-    const int seg = (nblk + kColThreads / 32 - 1) / (kColThreads / 32);
-    const int b0 = min(nblk, warp * seg), b1 = min(nblk, b0 + seg);
+    const int g0 = blockIdx.y * kPlanGroupBlocks;
+    const int gn = min(nblk - g0, kPlanGroupBlocks);
+    const int seg = (gn + kColThreads / 32 - 1) / (kColThreads / 32);
+    const int b0 = g0 + min(gn, warp * seg), b1 = g0 + min(gn, (warp + 1) * seg);
     int sum = 0;
     if (valid) {
-#pragma unroll 8
+#pragma unroll 4
         for (int b = b0; b < b1; ++b)
             sum += bcnt[int64_t(b) * E + e];
     }
@@ -162,7 +154,7 @@ __global__ void __launch_bounds__(kColThreads)
         total += seg_sum[w2][lane];
     }
     if (valid) {
-#pragma unroll 8
+#pragma unroll 4
         for (int b = b0; b < b1; ++b) {
             const int64_t i = int64_t(b) * E + e;
             const int v = bcnt[i];
@@ -170,20 +162,23 @@ __global__ void __launch_bounds__(kColThreads)
             run += v;
         }
         if (warp == 0)
-            counts[e] = total;
+            gsum[int64_t(blockIdx.y) * E + e] = total;
     }
 }
 
-// Expert scan (one CTA): offsets[e] = sum over e' < e of counts[e'] rounded
-// up to tm, offsets[E] = R_pad; the tail rows [offsets[e] + counts[e],
-// offsets[e + 1]) get srt_tok = -1 and srt_w = +0; with fill_tiles (no place
-// kernel follows, i.e. no entries) tile_expert[t] = e for the tiles of e.
-// Resets the status word (the place adds bad-id bits after).
+// Expert scan (one CTA): counts[e] = the sum of the groups' totals, each
+// total replaced by the rows of e in the earlier groups; offsets[e] = sum
+// over e' < e of counts[e'] rounded up to tm, offsets[E] = R_pad; the tail
+// rows [offsets[e] + counts[e], offsets[e + 1]) get srt_tok = -1 and srt_w =
+// +0; with fill_tiles (no place kernel follows, i.e. no entries)
+// tile_expert[t] = e for the tiles of e.  Resets the status word (the place
+// adds bad-id bits after).
 __global__ void __launch_bounds__(kScanThreads)
-    k_scan_experts(const int32_t *__restrict__ counts, int E, int tm, int64_t cap,
-                   int32_t *__restrict__ offsets, int32_t *__restrict__ srt_tok,
-                   float *__restrict__ srt_w, int32_t *__restrict__ tile_expert,
-                   uint32_t *__restrict__ status, bool fill_tiles)
+    k_scan_experts(int32_t *__restrict__ gsum, int ngroups, int32_t *__restrict__ counts, int E,
+                   int tm, int64_t cap, int32_t *__restrict__ offsets,
+                   int32_t *__restrict__ srt_tok, float *__restrict__ srt_w,
+                   int32_t *__restrict__ tile_expert, uint32_t *__restrict__ status,
+                   bool fill_tiles)
 {
     __shared__ int warp_incl[kScanThreads / 32];
     pdl_launch_dependents();
@@ -194,7 +189,17 @@ __global__ void __launch_bounds__(kScanThreads)
     int64_t carry = 0;  // padded rows of the experts before this slice
     for (int base = 0; base < E; base += kScanThreads) {
         const int e = base + tid;
-        const int c = e < E ? counts[e] : 0;
+        int c = 0;
+        if (e < E) {
+#pragma unroll 4
+            for (int g = 0; g < ngroups; ++g) {
+                const int64_t i = int64_t(g) * E + e;
+                const int t = gsum[i];
+                gsum[i] = c;
+                c += t;
+            }
+            counts[e] = c;
+        }
         const int P = (c + tm - 1) / tm * tm;
         int v = P;  // block-wide exclusive scan: warp shuffles, then warp totals
 #pragma unroll
@@ -238,59 +243,161 @@ __global__ void __launch_bounds__(kScanThreads)
     }
 }
 
+// Division of a flat index (< 2^31) by k through one multiply-high, the
+// method of Granlund and Montgomery, "Division by Invariant Integers using
+// Multiplication" (PLDI 1994), section 4: with l = ceil(log2 k) and
+// m = floor(2^32 (2^l - k) / k) + 1, n / k = (t + ((n - t) >> min(l, 1)))
+// >> max(l - 1, 0) for t = mulhi(m, n), exact for every 32-bit n.
+struct DivK {
+    uint32_t m;
+    int s1, s2;
+};
+
+DivK make_divk(uint32_t k)
+{
+    int l = 0;
+    while ((uint64_t(1) << l) < k)
+        ++l;
+    const uint64_t m = ((uint64_t(1) << 32) * ((uint64_t(1) << l) - k)) / k + 1;
+    return DivK{uint32_t(m), l < 1 ? l : 1, l > 1 ? l - 1 : 0};
+}
+
+__device__ __forceinline__ uint32_t div_k(uint32_t n, DivK d)
+{
+    const uint32_t t = __umulhi(d.m, n);
+    return (t + ((n - t) >> d.s1)) >> d.s2;
+}
+
+// The place kernel finds the lanes of a step that hold the same expert in
+// one of two ways.  With E <= kOrWalkMaxE each warp keeps a 32-bit word per
+// expert in shared memory: every lane ORs its bit into its expert's word and
+// reads back the whole set (one shared atomic and one load per step).  Above
+// that the per-warp words would not fit, and one ballot per bit of the id
+// (plus one for validity) intersects the lanes bit by bit.
+constexpr int kOrWalkMaxE = 1024;
+constexpr int kMaxIdBits = 12;  // ids < MOE_MAX_EXPERTS = 4096
+static_assert(MOE_MAX_EXPERTS <= (1 << kMaxIdBits), "id bits");
+
 // Place: block b walks its entries again (same ranges, same ranks), prefixes
 // the warps' counts per expert, and gives each entry row = offsets[e] +
 // (rows of e in earlier blocks) + (its rank among the block's entries of e).
-// A block's entries of one expert fill consecutive rows, so they are first
-// sorted by expert in shared memory and then written out run after run:
-// neighbouring lanes write neighbouring rows of srt_tok and srt_w (pos keeps
-// flat order).  The kernel also fills the tile table: tile t belongs to the
-// expert whose rows hold row t * tm.
-constexpr size_t place_smem_bytes(int E)
+// A block's entries of one expert fill consecutive rows, so their rows,
+// weights and block-local indices are first put in shared memory in expert
+// order and then written out run after run: neighbouring lanes write
+// neighbouring rows of srt_tok and srt_w (pos keeps flat order).  The kernel
+// also fills the tile table: tile t belongs to the expert whose rows hold
+// row t * tm.
+constexpr size_t place_smem_bytes(int E, bool or_walk)
 {
-    return size_t(kPWarps) * E * sizeof(uint16_t) + size_t(3 * E + 2) * sizeof(int) +
-           size_t(kPlanBlockEntries) * (2 * sizeof(int) + sizeof(uint16_t));
+    return size_t(kPWarps) * E * (sizeof(uint16_t) + (or_walk ? sizeof(uint32_t) : 0)) +
+           size_t(3 * E + 2) * sizeof(int) +
+           size_t(kPlanBlockEntries) * (sizeof(int) + sizeof(float) + sizeof(uint16_t));
 }
 
-__global__ void __launch_bounds__(kPThreads)
+// Rank of each entry of this warp's range [lo, hi) among the earlier entries
+// of the range with the same expert, with running counts per expert in
+// mycnt (and, with OR_WALK, the per-expert lane words in mypm, zero between
+// steps).  v holds the ids on entry and, on exit, (rank << 16 | id) for a
+// valid id, -1 otherwise; bad is set for an id outside [0, E) other than -1.
+template <bool OR_WALK>
+__device__ __forceinline__ void place_walk(int (&v)[kPSteps], int64_t lo, int64_t hi, int E,
+                                           uint16_t *mycnt, uint32_t *mypm, bool &bad)
+{
+    const uint32_t lane = threadIdx.x & 31, lt = lanemask_lt();
+    const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;
+#pragma unroll
+    for (int s = 0; s < kPSteps; ++s) {
+        if (lo + s * 32 < hi) {  // the same for the whole warp
+            const bool in = lo + s * 32 + lane < hi;
+            const int e = v[s];
+            const bool ok = in && e >= 0 && e < E;
+            bad |= in && !ok && e != -1;
+            uint32_t peers;
+            if (OR_WALK) {
+                if (ok)
+                    atomicOr(&mypm[e], 1u << lane);
+                __syncwarp();
+                peers = ok ? mypm[e] : (1u << lane);
+            } else {
+                const uint32_t vb = __ballot_sync(kFull, ok);
+                peers = ok ? vb : (1u << lane);
+#pragma unroll
+                for (int bit = 0; bit < kMaxIdBits; ++bit) {
+                    if (bit < nbits) {  // the same for the whole warp
+                        const bool set = (uint32_t(e) >> bit) & 1u;
+                        const uint32_t bb = __ballot_sync(kFull, set);
+                        peers &= set ? bb : ~bb;
+                    }
+                }
+            }
+            // every lane reads its expert's running count (lanes of one
+            // expert read the same word), then the lowest of them moves it on
+            const int first = ok ? int(mycnt[e]) : 0;
+            __syncwarp();
+            if (ok && lane == uint32_t(__ffs(peers) - 1)) {
+                mycnt[e] = uint16_t(first + __popc(peers));
+                if (OR_WALK)
+                    mypm[e] = 0u;
+            }
+            v[s] = ok ? ((first + __popc(peers & lt)) << 16) | e : -1;
+            __syncwarp();
+        } else {
+            v[s] = -1;
+        }
+    }
+}
+
+// 80 registers a thread: three CTAs of 256 threads per SM.
+template <bool OR_WALK>
+__global__ void __launch_bounds__(kPThreads, 3)
     k_place_blocks(const int32_t *__restrict__ ids, const float *__restrict__ w, int64_t n,
-                   int k, int E, int tm, int64_t cap, const int32_t *__restrict__ offsets,
-                   const int32_t *__restrict__ bcnt, int32_t *__restrict__ pos,
+                   DivK kd, int E, int tm, int64_t cap, const int32_t *__restrict__ offsets,
+                   const int32_t *__restrict__ bcnt, int nblk, int32_t *__restrict__ pos,
                    int32_t *__restrict__ srt_tok, float *__restrict__ srt_w,
                    int32_t *__restrict__ tile_expert, uint32_t *__restrict__ status)
 {
     extern __shared__ __align__(16) uint8_t psm[];
-    uint16_t *cntw = reinterpret_cast<uint16_t *>(psm);                            // [8][E]
-    int *rowbase = reinterpret_cast<int *>(psm + kPWarps * E * sizeof(uint16_t));  // [E]
-    int *loc = rowbase + E;               // [E + 1] block-local first slot of each expert
-    int *s_tok = loc + E + 1;             // [4096] the block's entries sorted by expert
-    float *s_w = reinterpret_cast<float *>(s_tok + kPlanBlockEntries);
-    int *s_off = reinterpret_cast<int *>(s_w + kPlanBlockEntries);  // [E + 1] offsets
-    uint16_t *s_e = reinterpret_cast<uint16_t *>(s_off + E + 1);
+    uint16_t *cntw = reinterpret_cast<uint16_t *>(psm);  // [8][E]
+    uint32_t *pm = reinterpret_cast<uint32_t *>(psm + kPWarps * E * sizeof(uint16_t));  // [8][E]
+    int *rowbase = reinterpret_cast<int *>(
+        psm + kPWarps * E * (sizeof(uint16_t) + (OR_WALK ? sizeof(uint32_t) : 0)));  // [E]
+    int *loc = rowbase + E;      // [E + 1] block-local first slot of each expert
+    int *s_off = loc + E + 1;    // [E + 1] offsets
+    int *s_row = s_off + E + 1;  // [4096] the block's entries in expert order: row,
+    float *s_w = reinterpret_cast<float *>(s_row + kPlanBlockEntries);       // weight,
+    uint16_t *s_li = reinterpret_cast<uint16_t *>(s_w + kPlanBlockEntries);  // local index
     __shared__ int warp_tot[kPWarps];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_launch_dependents();
     zero_warp_counts(cntw, E);
+    if (OR_WALK)
+        for (int v = tid; v < 2 * E; v += kPThreads)
+            reinterpret_cast<uint4 *>(pm)[v] = make_uint4(0u, 0u, 0u, 0u);
     // everything is read after the wait: this launch may begin before the
     // count kernel's own wait for whatever wrote the ids has ended
     pdl_wait();
-    const int64_t lo = int64_t(blockIdx.x) * kPlanBlockEntries + warp * kPSteps * 32;
+    const int64_t blk_lo = int64_t(blockIdx.x) * kPlanBlockEntries;
+    const int64_t lo = blk_lo + warp * kPSteps * 32;
     const int64_t hi = min(n, lo + kPSteps * 32);
-    int id[kPSteps], rank[kPSteps];
+    int v[kPSteps];
     float wv[kPSteps];
 #pragma unroll
     for (int s = 0; s < kPSteps; ++s) {
         const int64_t i = lo + s * 32 + lane;
-        id[s] = i < hi ? ids[i] : -1;
+        v[s] = i < hi ? ids[i] : -1;
         wv[s] = i < hi ? w[i] : 0.0f;
     }
     __syncthreads();
-    warp_walk<true>(id, lo, hi, E, cntw + warp * E, &rank);
+    bool bad = false;
+    place_walk<OR_WALK>(v, lo, hi, E, cntw + warp * E, pm + warp * E, bad);
+    if (__any_sync(kFull, bad) && lane == 0)
+        atomicOr(status, MOE_STATUS_BAD_ID);
     __syncthreads();
     // per expert: warp counts -> prefix over warps, the block's total, and
     // an exclusive scan of the totals over the experts (contiguous runs of J
     // experts per thread, then warp shuffles and warp totals)
     const int32_t *brow = bcnt + int64_t(blockIdx.x) * E;
+    const int32_t *grow = bcnt + (int64_t(nblk) + blockIdx.x / kPlanGroupBlocks) * E;
     const int J = (E + kPThreads - 1) / kPThreads;
     const int e0 = min(E, tid * J), e1 = min(E, e0 + J);
     int tsum = 0;
@@ -305,21 +412,21 @@ __global__ void __launch_bounds__(kPThreads)
         loc[e] = run;  // the block's count for now
         tsum += run;
         s_off[e] = offsets[e];
-        rowbase[e] = s_off[e] + brow[e];
+        rowbase[e] = s_off[e] + grow[e] + brow[e];
     }
     if (tid == 0)
         s_off[E] = offsets[E];
-    int v = tsum;
+    int sc = tsum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(kFull, v, o);
+        const int t = __shfl_up_sync(kFull, sc, o);
         if (lane >= o)
-            v += t;
+            sc += t;
     }
     if (lane == 31)
-        warp_tot[warp] = v;
+        warp_tot[warp] = sc;
     __syncthreads();
-    int slot0 = v - tsum, total = 0;
+    int slot0 = sc - tsum, total = 0;
 #pragma unroll
     for (int w2 = 0; w2 < kPWarps; ++w2) {
         slot0 += w2 < warp ? warp_tot[w2] : 0;
@@ -330,37 +437,32 @@ __global__ void __launch_bounds__(kPThreads)
         loc[e] = slot0;
         slot0 += c;
     }
-    if (tid == 0)
-        loc[E] = total;
     __syncthreads();
     // each entry: its rank in the block, pos in flat order, its sorted slot
     const uint16_t *mycnt = cntw + warp * E;
-    bool bad = false;
 #pragma unroll
     for (int s = 0; s < kPSteps; ++s) {
         const int64_t i = lo + s * 32 + lane;
         if (i < hi) {
-            if (rank[s] >= 0) {
-                const int r = mycnt[id[s]] + rank[s];
-                pos[i] = rowbase[id[s]] + r;
-                const int slot = loc[id[s]] + r;
-                s_tok[slot] = int32_t(i / k);
+            const int p = v[s];
+            if (p >= 0) {
+                const int e = p & 0xffff, r = mycnt[e] + (p >> 16);
+                const int row = rowbase[e] + r;
+                pos[i] = row;
+                const int slot = loc[e] + r;
+                s_row[slot] = row;
                 s_w[slot] = wv[s];
-                s_e[slot] = uint16_t(id[s]);
+                s_li[slot] = uint16_t(i - blk_lo);
             } else {
                 pos[i] = -1;
-                bad |= id[s] != -1;
             }
         }
     }
-    if (__any_sync(kFull, bad) && lane == 0)
-        atomicOr(status, MOE_STATUS_BAD_ID);
     __syncthreads();
     for (int j = tid; j < total; j += kPThreads) {
-        const int e = s_e[j];
-        const int row = rowbase[e] + (j - loc[e]);
+        const int row = s_row[j];
         if (row < cap) {
-            srt_tok[row] = s_tok[j];
+            srt_tok[row] = int32_t(div_k(uint32_t(blk_lo + s_li[j]), kd));
             srt_w[row] = s_w[j];
         }
     }
@@ -447,7 +549,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
     }
     __syncthreads();  // counters zeroed
     uint16_t *mycnt = cntw + warp * E;
-    warp_walk<false>(my_id, w_lo, w_hi, E, mycnt, &my_rank);
+    warp_walk(my_id, w_lo, w_hi, E, mycnt, &my_rank);
     __syncthreads();
     for (int e = tid; e < E; e += kCThreads) {  // warp counts -> prefix over warps
         int run = 0;
@@ -647,35 +749,36 @@ cudaError_t launch_plan(const int32_t *ids, const float *w, int T, int k, int E,
                                   counts, srt_tok, srt_w, pos, tile_expert, status);
     }
     const int nblk = plan_num_blocks(n);
+    const int ngroups = plan_num_groups(nblk);
+    int32_t *gsum = bcnt + int64_t(nblk) * E;  // [ngroups][E] after the blocks' rows
     const size_t cnt_smem = size_t(E) * sizeof(int);
-    const size_t place_smem = place_smem_bytes(E);
-    const size_t max_place_smem = place_smem_bytes(MOE_MAX_EXPERTS);
+    const bool or_walk = E <= kOrWalkMaxE;
+    const void *place_fn = or_walk ? reinterpret_cast<const void *>(k_place_blocks<true>)
+                                   : reinterpret_cast<const void *>(k_place_blocks<false>);
+    // the opt-in size covers every E this instantiation takes
+    const size_t max_place_smem = or_walk ? place_smem_bytes(kOrWalkMaxE, true)
+                                          : place_smem_bytes(MOE_MAX_EXPERTS, false);
     cudaError_t err;
     if (nblk > 0) {
-        err = ensure_smem_limit(reinterpret_cast<const void *>(k_place_blocks), kSlotPlace,
-                                    max_place_smem);
+        err = ensure_smem_limit(place_fn, or_walk ? kSlotPlaceOr : kSlotPlace, max_place_smem);
         if (err == cudaSuccess)
             err = launch_pdl(k_count, dim3(nblk), dim3(kPThreads), cnt_smem, stream, ids, n, E,
                              bcnt);
         if (err == cudaSuccess)
-            err = launch_pdl(k_colscan, dim3((E + 31) / 32), dim3(kColThreads), 0, stream, bcnt,
-                             nblk, E, counts);
-        if (err != cudaSuccess)
-            return err;
-    } else {
-        err = cudaMemsetAsync(counts, 0, size_t(E) * sizeof(int32_t), stream);
+            err = launch_pdl(k_colscan, dim3((E + 31) / 32, ngroups), dim3(kColThreads), 0, stream,
+                             bcnt, nblk, E, gsum);
         if (err != cudaSuccess)
             return err;
     }
-    err = launch_pdl(k_scan_experts, dim3(1), dim3(kScanThreads), 0, stream,
-                     static_cast<const int32_t *>(counts), E, tm, cap, offsets, srt_tok, srt_w,
-                     tile_expert, status, nblk == 0);
+    err = launch_pdl(k_scan_experts, dim3(1), dim3(kScanThreads), 0, stream, gsum, ngroups,
+                     counts, E, tm, cap, offsets, srt_tok, srt_w, tile_expert, status, nblk == 0);
     if (err != cudaSuccess || nblk == 0)
         return err;
-    return launch_pdl(k_place_blocks, dim3(nblk), dim3(kPThreads), place_smem, stream, ids, w, n,
-                      k, E, tm, cap, static_cast<const int32_t *>(offsets),
-                      static_cast<const int32_t *>(bcnt), pos, srt_tok, srt_w, tile_expert,
-                      status);
+    return launch_pdl(or_walk ? k_place_blocks<true> : k_place_blocks<false>, dim3(nblk),
+                      dim3(kPThreads), place_smem_bytes(E, or_walk), stream, ids, w, n,
+                      make_divk(uint32_t(k)), E, tm, cap, static_cast<const int32_t *>(offsets),
+                      static_cast<const int32_t *>(bcnt), nblk, pos, srt_tok, srt_w,
+                      tile_expert, status);
 }
 
 }  // namespace moe
