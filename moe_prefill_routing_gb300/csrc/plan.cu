@@ -59,36 +59,6 @@ __device__ __forceinline__ void zero_warp_counts(uint16_t *cntw, int E)
         reinterpret_cast<uint4 *>(cntw)[v] = make_uint4(0u, 0u, 0u, 0u);
 }
 
-// Walk this warp's range [lo, hi) (at most kPSteps * 32 entries): running
-// counts per expert in mycnt, and each entry's rank among the earlier
-// entries of the range with the same expert (-1 for an id outside [0, E)).
-// The lanes holding the same expert come from __match_any_sync (measured
-// faster than one ballot per id bit in the one-launch cluster plan).
-__device__ __forceinline__ void warp_walk(const int (&id)[kPSteps], int64_t lo, int64_t hi, int E,
-                                          uint16_t *mycnt, int (*rank)[kPSteps])
-{
-    const uint32_t lane = threadIdx.x & 31, lt = lanemask_lt();
-#pragma unroll
-    for (int s = 0; s < kPSteps; ++s) {
-        if (lo + s * 32 < hi) {  // the same for the whole warp
-            const bool ok = lo + s * 32 + lane < hi && id[s] >= 0 && id[s] < E;
-            const uint32_t peers =
-                __match_any_sync(kFull, ok ? uint32_t(id[s]) : (0x80000000u | lane));
-            const int leader = __ffs(peers) - 1;
-            int first = 0;
-            if (ok && lane == uint32_t(leader)) {
-                first = mycnt[id[s]];
-                mycnt[id[s]] = uint16_t(first + __popc(peers));
-            }
-            if (rank) {
-                first = __shfl_sync(kFull, first, leader);
-                (*rank)[s] = ok ? first + __popc(peers & lt) : -1;
-            }
-            __syncwarp();
-        }
-    }
-}
-
 // Count: bcnt[b][e] = entries of block b (kPlanBlockEntries flat entries)
 // routed to expert e.  Only the totals matter here, so shared-memory atomics
 // count (the order of the adds does not change a sum of ones).
@@ -268,12 +238,16 @@ __device__ __forceinline__ uint32_t div_k(uint32_t n, DivK d)
     return (t + ((n - t) >> d.s1)) >> d.s2;
 }
 
-// The place kernel finds the lanes of a step that hold the same expert in
-// one of two ways.  With E <= kOrWalkMaxE each warp keeps a 32-bit word per
-// expert in shared memory: every lane ORs its bit into its expert's word and
-// reads back the whole set (one shared atomic and one load per step).  Above
-// that the per-warp words would not fit, and one ballot per bit of the id
-// (plus one for validity) intersects the lanes bit by bit.
+// A warp walks its range 32 entries (one step) at a time; the lanes of a
+// step that hold the same expert are found in one of three ways.  kWalkOr
+// (E <= kOrWalkMaxE): each warp keeps a 32-bit word per expert in shared
+// memory, every lane ORs its bit into its expert's word and reads back the
+// whole set (one shared atomic and one load per step).  Above that the
+// per-warp words would not fit: kWalkBallot intersects one ballot per bit of
+// the id (plus one for validity), kWalkMatch uses __match_any_sync; measured,
+// the first is faster in the place kernel of large inputs, the second in the
+// one-launch cluster plan.
+constexpr int kWalkOr = 0, kWalkBallot = 1, kWalkMatch = 2;
 constexpr int kOrWalkMaxE = 1024;
 constexpr int kMaxIdBits = 12;  // ids < MOE_MAX_EXPERTS = 4096
 static_assert(MOE_MAX_EXPERTS <= (1 << kMaxIdBits), "id bits");
@@ -294,14 +268,15 @@ constexpr size_t place_smem_bytes(int E, bool or_walk)
            size_t(kPlanBlockEntries) * (sizeof(int) + sizeof(float) + sizeof(uint16_t));
 }
 
-// Rank of each entry of this warp's range [lo, hi) among the earlier entries
-// of the range with the same expert, with running counts per expert in
-// mycnt (and, with OR_WALK, the per-expert lane words in mypm, zero between
-// steps).  v holds the ids on entry and, on exit, (rank << 16 | id) for a
-// valid id, -1 otherwise; bad is set for an id outside [0, E) other than -1.
-template <bool OR_WALK>
-__device__ __forceinline__ void place_walk(int (&v)[kPSteps], int64_t lo, int64_t hi, int E,
-                                           uint16_t *mycnt, uint32_t *mypm, bool &bad)
+// Rank of each entry of this warp's range [lo, hi) (at most kPSteps * 32
+// entries) among the earlier entries of the range with the same expert, with
+// running counts per expert in mycnt (and, for kWalkOr, the per-expert lane
+// words in mypm, zero between steps).  v holds the ids on entry and, on
+// exit, (rank << 16 | id) for a valid id, -1 otherwise; bad is set for an id
+// outside [0, E) other than -1.
+template <int WALK>
+__device__ __forceinline__ void warp_walk(int (&v)[kPSteps], int64_t lo, int64_t hi, int E,
+                                          uint16_t *mycnt, uint32_t *mypm, bool &bad)
 {
     const uint32_t lane = threadIdx.x & 31, lt = lanemask_lt();
     const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;
@@ -313,11 +288,13 @@ __device__ __forceinline__ void place_walk(int (&v)[kPSteps], int64_t lo, int64_
             const bool ok = in && e >= 0 && e < E;
             bad |= in && !ok && e != -1;
             uint32_t peers;
-            if (OR_WALK) {
+            if (WALK == kWalkOr) {
                 if (ok)
                     atomicOr(&mypm[e], 1u << lane);
                 __syncwarp();
                 peers = ok ? mypm[e] : (1u << lane);
+            } else if (WALK == kWalkMatch) {
+                peers = __match_any_sync(kFull, ok ? uint32_t(e) : (0x80000000u | lane));
             } else {
                 const uint32_t vb = __ballot_sync(kFull, ok);
                 peers = ok ? vb : (1u << lane);
@@ -336,7 +313,7 @@ __device__ __forceinline__ void place_walk(int (&v)[kPSteps], int64_t lo, int64_
             __syncwarp();
             if (ok && lane == uint32_t(__ffs(peers) - 1)) {
                 mycnt[e] = uint16_t(first + __popc(peers));
-                if (OR_WALK)
+                if (WALK == kWalkOr)
                     mypm[e] = 0u;
             }
             v[s] = ok ? ((first + __popc(peers & lt)) << 16) | e : -1;
@@ -389,7 +366,8 @@ __global__ void __launch_bounds__(kPThreads, 3)
     }
     __syncthreads();
     bool bad = false;
-    place_walk<OR_WALK>(v, lo, hi, E, cntw + warp * E, pm + warp * E, bad);
+    warp_walk<OR_WALK ? kWalkOr : kWalkBallot>(v, lo, hi, E, cntw + warp * E, pm + warp * E,
+                                               bad);
     if (__any_sync(kFull, bad) && lane == 0)
         atomicOr(status, MOE_STATUS_BAD_ID);
     __syncthreads();
@@ -493,33 +471,36 @@ constexpr int kClusterMax = 16;
 constexpr int kCEntriesPerCta = kCWarps * kCSteps * 32;  // 4096
 static_assert(kCSteps == kPSteps, "the cluster plan walks with warp_walk");
 
-constexpr size_t cluster_smem_bytes(int E)
+constexpr size_t cluster_smem_bytes(int E, bool or_walk)
 {
-    return size_t(kCWarps) * E * sizeof(uint16_t) + 2 * sizeof(int) * size_t(E) +
-           (kClusterMax + kCWarps) * sizeof(int);
+    return size_t(kCWarps) * E * (sizeof(uint16_t) + (or_walk ? sizeof(uint32_t) : 0)) +
+           2 * sizeof(int) * size_t(E) + (kClusterMax + kCWarps) * sizeof(int);
 }
 
 // CTA c of the cluster owns flat entries [c*chunk, (c+1)*chunk), split into
 // eight contiguous warp ranges, and experts [c*epc, (c+1)*epc).
 // Phase 1: each warp walks its range 32 entries at a time with a running
-// count per expert (match_any peers share one update), which gives each
-// entry its rank in the warp range; an in-place prefix of the eight warp
-// counts per expert turns that into the rank in the CTA range and leaves the
-// CTA's count per expert.  Phase 2 (owners, over distributed shared memory):
+// count per expert (the lanes of one expert share one update), which gives
+// each entry its rank in the warp range; an in-place prefix of the eight
+// warp counts per expert turns that into the rank in the CTA range and
+// leaves the CTA's count per expert.  Phase 2 (owners, over distributed shared memory):
 // the expert's count over all CTAs, its padded size, its first row by a scan
 // over the owned experts plus the totals of the CTAs before, the tail fill,
 // the tile table, and for every CTA the first row of the expert's entries in
 // that CTA.  Phase 3: row = that first row + rank.
+template <bool OR_WALK>
 __global__ void __launch_bounds__(kCThreads, 1)
-    k_plan_cluster(const int32_t *__restrict__ ids, const float *__restrict__ w, int64_t n, int k,
-                   int E, int tm, int64_t cap, int64_t chunk, int32_t *__restrict__ offsets,
+    k_plan_cluster(const int32_t *__restrict__ ids, const float *__restrict__ w, int64_t n,
+                   DivK kd, int E, int tm, int64_t cap, int64_t chunk, int32_t *__restrict__ offsets,
                    int32_t *__restrict__ counts, int32_t *__restrict__ srt_tok,
                    float *__restrict__ srt_w, int32_t *__restrict__ pos,
                    int32_t *__restrict__ tile_expert, uint32_t *__restrict__ status)
 {
     extern __shared__ __align__(16) uint8_t csm[];
     uint16_t *cntw = reinterpret_cast<uint16_t *>(csm);                   // [8 warps][E]
-    int *carry = reinterpret_cast<int *>(csm + kCWarps * E * sizeof(uint16_t));  // [E]
+    uint32_t *pm = reinterpret_cast<uint32_t *>(csm + kCWarps * E * sizeof(uint16_t));  // [8][E]
+    int *carry = reinterpret_cast<int *>(
+        csm + kCWarps * E * (sizeof(uint16_t) + (OR_WALK ? sizeof(uint32_t) : 0)));  // [E]
     int *rowbase = carry + E;                                             // [E]
     int *tot = rowbase + E;                                               // [16]
     int *warp_tot = tot + kClusterMax;                                    // [8]
@@ -528,7 +509,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
     const int C = int(cluster_nctarank()), c = int(cluster_ctarank());
 
     pdl_launch_dependents();
-    for (int v = tid; v < E; v += kCThreads)  // 16*E bytes = E vectors of 16
+    for (int v = tid; v < (OR_WALK ? 3 : 1) * E; v += kCThreads)  // 16 (48) * E bytes
         reinterpret_cast<uint4 *>(cntw)[v] = make_uint4(0u, 0u, 0u, 0u);
     pdl_wait();
     if (c == 0 && tid == 0)
@@ -540,16 +521,18 @@ __global__ void __launch_bounds__(kCThreads, 1)
     const int64_t wchunk = (chunk + kCWarps - 1) / kCWarps;
     const int64_t w_lo = min(cta_hi, cta_lo + warp * wchunk);
     const int64_t w_hi = min(cta_hi, w_lo + wchunk);
-    int my_id[kCSteps], my_rank[kCSteps];
+    int ent[kCSteps];  // ids, then (rank << 16 | id) or -1
+    float wv[kCSteps];
 #pragma unroll
     for (int s = 0; s < kCSteps; ++s) {
         const int64_t i = w_lo + s * 32 + lane;
-        my_id[s] = i < w_hi ? ids[i] : -1;
-        my_rank[s] = -1;
+        ent[s] = i < w_hi ? ids[i] : -1;
+        wv[s] = i < w_hi ? w[i] : 0.0f;
     }
     __syncthreads();  // counters zeroed
     uint16_t *mycnt = cntw + warp * E;
-    warp_walk(my_id, w_lo, w_hi, E, mycnt, &my_rank);
+    bool bad = false;  // reported after the cluster barriers (CTA 0 resets the status)
+    warp_walk<OR_WALK ? kWalkOr : kWalkMatch>(ent, w_lo, w_hi, E, mycnt, pm + warp * E, bad);
     __syncthreads();
     for (int e = tid; e < E; e += kCThreads) {  // warp counts -> prefix over warps
         int run = 0;
@@ -564,8 +547,8 @@ __global__ void __launch_bounds__(kCThreads, 1)
     __syncthreads();
 #pragma unroll
     for (int s = 0; s < kCSteps; ++s)
-        if (my_rank[s] >= 0)
-            my_rank[s] += mycnt[my_id[s]];
+        if (ent[s] >= 0)
+            ent[s] += int(mycnt[ent[s] & 0xffff]) << 16;
     cluster_sync();  // every CTA's counts are final
 
     // ---- phase 2: owners scan their experts ------------------------------------
@@ -650,22 +633,20 @@ __global__ void __launch_bounds__(kCThreads, 1)
     cluster_sync();  // every CTA holds the first row of each expert's entries
 
     // ---- phase 3: place ----------------------------------------------------------
-    bool bad = false;
 #pragma unroll
     for (int s = 0; s < kCSteps; ++s) {
         const int64_t i = w_lo + s * 32 + lane;
         if (i < w_hi) {
-            const int id = my_id[s];
-            if (my_rank[s] >= 0) {
-                const int row = rowbase[id] + my_rank[s];
+            const int p = ent[s];
+            if (p >= 0) {
+                const int row = rowbase[p & 0xffff] + (p >> 16);
                 pos[i] = row;
                 if (row < cap) {
-                    srt_tok[row] = int32_t(i / k);
-                    srt_w[row] = w[i];
+                    srt_tok[row] = int32_t(div_k(uint32_t(i), kd));
+                    srt_w[row] = wv[s];
                 }
             } else {
                 pos[i] = -1;
-                bad |= id != -1;
             }
         }
     }
@@ -685,9 +666,18 @@ int plan_cluster_size()
         return v > 0 ? v : 0;
     int chosen = -1;
     bool refused = false;
-    const void *fn = reinterpret_cast<const void *>(k_plan_cluster);
-    const size_t smem = cluster_smem_bytes(MOE_MAX_EXPERTS);
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+    // both instantiations get their opt-in sizes; the larger one decides
+    const void *fn_or = reinterpret_cast<const void *>(k_plan_cluster<true>);
+    const void *fn = reinterpret_cast<const void *>(k_plan_cluster<false>);
+    const size_t smem_or = cluster_smem_bytes(kOrWalkMaxE, true);
+    const size_t smem = cluster_smem_bytes(MOE_MAX_EXPERTS, false);
+    static_assert(cluster_smem_bytes(kOrWalkMaxE, true) <= cluster_smem_bytes(MOE_MAX_EXPERTS, false),
+                  "the occupancy check below covers both instantiations");
+    if (cudaFuncSetAttribute(fn_or, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_or)) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(fn_or, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
             cudaSuccess ||
         cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
             cudaSuccess) {
@@ -730,10 +720,11 @@ cudaError_t launch_plan(const int32_t *ids, const float *w, int T, int k, int E,
     const int64_t n = int64_t(T) * k;
     const int C = n > 0 ? plan_cluster_size() : 0;
     if (C > 0 && n <= int64_t(C) * kCEntriesPerCta && E <= C * 2 * kCThreads) {
+        const bool or_walk = E <= kOrWalkMaxE;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(C);
         cfg.blockDim = dim3(kCThreads);
-        cfg.dynamicSmemBytes = cluster_smem_bytes(E);
+        cfg.dynamicSmemBytes = cluster_smem_bytes(E, or_walk);
         cfg.stream = stream;
         cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -745,7 +736,8 @@ cudaError_t launch_plan(const int32_t *ids, const float *w, int T, int k, int E,
         cfg.attrs = attr;
         cfg.numAttrs = 2;
         const int64_t chunk = (n + C - 1) / C;
-        return cudaLaunchKernelEx(&cfg, k_plan_cluster, ids, w, n, k, E, tm, cap, chunk, offsets,
+        return cudaLaunchKernelEx(&cfg, or_walk ? k_plan_cluster<true> : k_plan_cluster<false>,
+                                  ids, w, n, make_divk(uint32_t(k)), E, tm, cap, chunk, offsets,
                                   counts, srt_tok, srt_w, pos, tile_expert, status);
     }
     const int nblk = plan_num_blocks(n);
