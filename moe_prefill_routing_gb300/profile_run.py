@@ -9,7 +9,9 @@ whole layer once through the stage entry points, then runs the chosen stage
 ``--iters`` more times.  Every stage call goes through the C ABI.  With
 ``--weights f8`` the gather, gate/up and down stages are the E4M3-operand
 ones (weights quantized on the device first; down includes the pass that
-makes H's rows E4M3).
+makes H's rows E4M3).  ``--plan-entries N`` runs the plan alone on N flat
+entries (k = 10, E = 512, tm = 16, ids uniform over the experts and drawn
+on the device, as in the bench's plan sweep).
 """
 from __future__ import annotations
 
@@ -34,7 +36,11 @@ def main(argv=None):
     ap.add_argument("--stage", choices=STAGES, default="gate_up")
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--weights", choices=("bf16", "f8"), default="bf16")
+    ap.add_argument("--plan-entries", type=int, default=0,
+                    help="run only the plan on this many uniform entries")
     a = ap.parse_args(argv)
+    if a.plan_entries:
+        return plan_only_run(a.plan_entries, a.iters)
     wl = W.workload(a.workload)
     if a.experts:
         wl = dataclasses.replace(wl, E=a.experts, name=f"{wl.name}_E{a.experts}")
@@ -90,6 +96,22 @@ def main(argv=None):
     counts = np.bincount(flat[flat >= 0], minlength=wl.E)
     print(f"{wl.name}: stage {a.stage} x{a.iters}; active experts {(counts > 0).sum()}, "
           f"R_pad {int((-(-counts // wl.tm) * wl.tm).sum())}", file=sys.stderr)
+
+
+def plan_only_run(n: int, iters: int):
+    k, E, tm = 10, 512, 16
+    T = n // k
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev).manual_seed(1234 + n)
+    ids = torch.randint(0, E, (T, k), generator=gen, device=dev, dtype=torch.int32)
+    w = torch.rand((T, k), generator=gen, device=dev)
+    cap = B.capacity(T, k, E, tm)
+    o = B.plan(ids, w, E, tm, cap=cap)
+    for _ in range(iters):
+        B.plan(ids, w, E, tm, cap=cap, out=o)
+    torch.cuda.synchronize(dev)
+    print(f"plan of {T * k} uniform entries (E={E}, k={k}) x{iters + 1}; "
+          f"R_pad {int(o['offsets'][-1])}", file=sys.stderr)
 
 
 if __name__ == "__main__":
