@@ -159,9 +159,9 @@ MOE_API int moe_plan(const int32_t *ids, const float *w, int T, int k, int E, in
  * Arguments are those of moe_plan, without ws / ws_bytes and with
  *   status   uint32* device word that receives the MOE_STATUS_* bits of this
  *            call (reset by the call), or NULL to leave them in the library.
- * Limit: (B + ceil(B / 128)) x E <= MOE_PLAN_NOALLOC_MAX_COUNTS with
+ * Limit: (B + ceil(B / 256)) x E <= MOE_PLAN_NOALLOC_MAX_COUNTS with
  * B = ceil(T*k / 4096) (one row of E counts per block of 4096 entries and
- * one per group of 128 blocks): T*k up to 2M entries with E = 512, up to
+ * one per group of 256 blocks): T*k up to 2M entries with E = 512, up to
  * 262144 with E = 4096.  Larger sizes return MOE_ERR_WORKSPACE.
  *
  * The first call on a device looks up the array's device address (once per

@@ -21,7 +21,7 @@ inline int plan_num_blocks(int64_t n)
 
 // The column scan over blocks runs in groups of this many blocks; the
 // expert scan then adds the groups' totals.
-constexpr int kPlanGroupBlocks = 128;
+constexpr int kPlanGroupBlocks = 256;
 
 inline int plan_num_groups(int nblk)
 {

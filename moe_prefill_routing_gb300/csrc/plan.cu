@@ -26,7 +26,7 @@
 // Larger inputs, where the plan is bound by its HBM traffic, run four
 // kernels over blocks of 4096 entries, chained with programmatic dependent
 // launch: count (each block's count per expert), column scan (per expert,
-// the rows of the earlier blocks of the same group of 128 blocks, and each
+// the rows of the earlier blocks of the same group of 256 blocks, and each
 // group's total), expert scan (the groups' totals prefixed, offsets, tail
 // rows), place (the ranks walked again, in registers, the scatter and the
 // tile table).
@@ -61,9 +61,14 @@ __device__ __forceinline__ void zero_warp_counts(uint16_t *cntw, int E)
 
 // Count: bcnt[b][e] = entries of block b (kPlanBlockEntries flat entries)
 // routed to expert e.  Only the totals matter here, so shared-memory atomics
-// count (the order of the adds does not change a sum of ones).
+// count (the order of the adds does not change a sum of ones).  A CTA counts
+// blocks blockIdx.x, + gridDim.x, ...; the next block's ids are loaded while
+// the current block's counts are written out.
+constexpr int kCountCtasPerSm = 8;
+
 __global__ void __launch_bounds__(kPThreads)
-    k_count(const int32_t *__restrict__ ids, int64_t n, int E, int32_t *__restrict__ bcnt)
+    k_count(const int32_t *__restrict__ ids, int64_t n, int nblk, int E,
+            int32_t *__restrict__ bcnt)
 {
     extern __shared__ __align__(16) uint8_t psm[];
     int *cnt = reinterpret_cast<int *>(psm);  // [E]
@@ -72,23 +77,32 @@ __global__ void __launch_bounds__(kPThreads)
     for (int e = threadIdx.x; e < E; e += kPThreads)
         cnt[e] = 0;
     pdl_wait();
-    const int64_t lo = int64_t(blockIdx.x) * kPlanBlockEntries + warp * kPSteps * 32;
-    const int64_t hi = min(n, lo + kPSteps * 32);
     int id[kPSteps];
+    auto load = [&](int b) {
+        const int64_t lo = int64_t(b) * kPlanBlockEntries + warp * kPSteps * 32;
+        const int64_t hi = min(n, lo + kPSteps * 32);
 #pragma unroll
-    for (int s = 0; s < kPSteps; ++s) {
-        const int64_t i = lo + s * 32 + lane;
-        id[s] = i < hi ? ids[i] : -1;
+        for (int s = 0; s < kPSteps; ++s) {
+            const int64_t i = lo + s * 32 + lane;
+            id[s] = i < hi ? ids[i] : -1;
+        }
+    };
+    load(blockIdx.x);
+    for (int b = blockIdx.x; b < nblk; b += gridDim.x) {
+        __syncthreads();  // counters zero
+#pragma unroll
+        for (int s = 0; s < kPSteps; ++s)  // out-of-range entries were loaded as -1
+            if (id[s] >= 0 && id[s] < E)
+                atomicAdd(&cnt[id[s]], 1);
+        if (b + int(gridDim.x) < nblk)
+            load(b + gridDim.x);
+        __syncthreads();
+        int32_t *row = bcnt + int64_t(b) * E;
+        for (int e = threadIdx.x; e < E; e += kPThreads) {
+            row[e] = cnt[e];
+            cnt[e] = 0;
+        }
     }
-    __syncthreads();
-#pragma unroll
-    for (int s = 0; s < kPSteps; ++s)
-        if (lo + s * 32 + lane < hi && id[s] >= 0 && id[s] < E)
-            atomicAdd(&cnt[id[s]], 1);
-    __syncthreads();
-    int32_t *row = bcnt + int64_t(blockIdx.x) * E;
-    for (int e = threadIdx.x; e < E; e += kPThreads)
-        row[e] = cnt[e];
 }
 
 // Column scan, per group of kPlanGroupBlocks blocks and 32 experts per CTA
@@ -112,7 +126,7 @@ __global__ void __launch_bounds__(kColThreads)
     const int b0 = g0 + min(gn, warp * seg), b1 = g0 + min(gn, (warp + 1) * seg);
     int sum = 0;
     if (valid) {
-#pragma unroll 4
+#pragma unroll 8
         for (int b = b0; b < b1; ++b)
             sum += bcnt[int64_t(b) * E + e];
     }
@@ -124,7 +138,7 @@ __global__ void __launch_bounds__(kColThreads)
         total += seg_sum[w2][lane];
     }
     if (valid) {
-#pragma unroll 4
+#pragma unroll 8
         for (int b = b0; b < b1; ++b) {
             const int64_t i = int64_t(b) * E + e;
             const int v = bcnt[i];
@@ -161,12 +175,17 @@ __global__ void __launch_bounds__(kScanThreads)
         const int e = base + tid;
         int c = 0;
         if (e < E) {
-#pragma unroll 4
-            for (int g = 0; g < ngroups; ++g) {
-                const int64_t i = int64_t(g) * E + e;
-                const int t = gsum[i];
-                gsum[i] = c;
-                c += t;
+            for (int g0 = 0; g0 < ngroups; g0 += 16) {  // 16 loads in flight, then the stores
+                int t[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    t[u] = g0 + u < ngroups ? gsum[int64_t(g0 + u) * E + e] : 0;
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    if (g0 + u < ngroups)
+                        gsum[int64_t(g0 + u) * E + e] = c;
+                    c += t[u];
+                }
             }
             counts[e] = c;
         }
@@ -754,8 +773,8 @@ cudaError_t launch_plan(const int32_t *ids, const float *w, int T, int k, int E,
     if (nblk > 0) {
         err = ensure_smem_limit(place_fn, or_walk ? kSlotPlaceOr : kSlotPlace, max_place_smem);
         if (err == cudaSuccess)
-            err = launch_pdl(k_count, dim3(nblk), dim3(kPThreads), cnt_smem, stream, ids, n, E,
-                             bcnt);
+            err = launch_pdl(k_count, dim3(std::min(nblk, device_sm_count() * kCountCtasPerSm)),
+                             dim3(kPThreads), cnt_smem, stream, ids, n, nblk, E, bcnt);
         if (err == cudaSuccess)
             err = launch_pdl(k_colscan, dim3((E + 31) / 32, ngroups), dim3(kColThreads), 0, stream,
                              bcnt, nblk, E, gsum);
