@@ -191,3 +191,34 @@ def test_plan_multi_kernel_empty_experts_and_tiles(tm):
     ids[rng.random(ids.shape) < 0.05] = -1
     w = rng.standard_normal(ids.shape).astype(np.float32)
     check(ids, w, E, tm)
+
+
+@pytest.mark.parametrize("n_entries", [256 * 4096, 256 * 4096 + 100, 512 * 4096])
+def test_plan_column_scan_group_boundaries(n_entries):
+    # the column scan prefixes block counts inside groups of 256 blocks of
+    # 4096 entries and the expert scan adds the groups' totals: exactly one
+    # full group, one full group plus a ragged block, two full groups
+    # (k = 4, E = 1000: the shared-memory OR walk; E = 2000: the ballot walk)
+    k = 4
+    T = n_entries // k
+    for E in (1000, 2000):
+        rng = np.random.default_rng(n_entries + E)
+        ids = rng.integers(0, E, size=(T, k), dtype=np.int32)
+        ids[rng.random(ids.shape) < 0.02] = -1
+        w = rng.standard_normal((T, k)).astype(np.float32)
+        check(ids, w, E, 16)
+
+
+@pytest.mark.parametrize("E", [1024, 1025])
+@pytest.mark.parametrize("T", [1000, 20000])
+def test_plan_walk_switch(E, T):
+    # up to 1024 experts the lanes of one expert are found through per-warp
+    # words in shared memory, above that by ballots (multi-kernel plan) or
+    # __match_any_sync (one-launch plan); T = 1000 runs the one-launch plan,
+    # T = 20000 the multi-kernel plan (k = 8)
+    rng = np.random.default_rng(E * 7 + T)
+    ids = rng.integers(0, E, size=(T, 8), dtype=np.int32)
+    ids[:, 0] = E - 1  # the largest id in every token
+    ids[rng.random(ids.shape) < 0.05] = -1
+    w = rng.standard_normal(ids.shape).astype(np.float32)
+    check(ids, w, E, 16)
