@@ -9,11 +9,12 @@
 //  - item 2: the rank of an entry among the earlier entries of its block
 //    with the same expert is found without a serial per-thread loop: each
 //    warp walks a contiguous range 32 entries at a time with a running count
-//    per expert in shared memory, __match_any_sync grouping the lanes that
-//    hold the same expert and popc of the lower peers giving the rank inside
-//    a step; the warps' counts, prefixed over the warps, place each warp's
-//    range after the earlier ones.  No counter can overflow and nothing
-//    depends on top-k;
+//    per expert in shared memory; the lanes that hold the same expert are
+//    grouped (through per-warp lane words in shared memory, ballots or
+//    __match_any_sync, see warp_walk) and popc of the lower peers gives the
+//    rank inside a step; the warps' counts, prefixed over the warps, place
+//    each warp's range after the earlier ones.  No counter can overflow and
+//    nothing depends on top-k;
 //  - item 3: one CTA for the whole histogram+scan was slower than a
 //    multi-CTA histogram plus a one-CTA scan, because one CTA cannot use the
 //    whole GPU.  On GB300 the launch and completion gaps between small
