@@ -1,5 +1,5 @@
 """Shared helpers of the tests: cached seeded inputs, host/device moves and
-the layer tolerance of the spec bar."""
+the layer tolerance (max|y - ref| <= 1e-2 * max|ref| + 1e-3)."""
 import functools
 
 import numpy as np
