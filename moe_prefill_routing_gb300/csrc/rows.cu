@@ -1,7 +1,8 @@
 // Row kernels: the gather of token rows into expert-sorted order and the
 // slot-ordered combine.  Both are HBM-bound copies/reductions of whole
 // 16-byte-aligned rows, so they move 128-bit vectors with every lane of a
-// warp on consecutive vectors of one row; grids are a multiple of the SM
+// warp on consecutive vectors of one row (the combine stages its slot rows
+// in shared memory with cp.async first); grids are a multiple of the SM
 // count and loop over rows.
 //
 // Gather: "Round 4 Track C: Prefill MoE Plan ... & Epilogue / Gather Audit",
@@ -16,9 +17,12 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include <atomic>
+
 namespace moe {
 namespace {
 
+constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kRowWarps = 8;
 constexpr int kRowThreads = kRowWarps * 32;
 constexpr int kCtasPerSm = 8;
@@ -160,49 +164,125 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float *acc)
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// One warp per (token, 512-column segment): y[t] = sum_{j=0..k-1} Ys[pos[t,j]],
-// fp32 from zero in slot order, one bf16 rounding.
-constexpr int kSegVec = 64;  // 16-byte vectors per warp segment (2 per lane)
 
-__global__ void __launch_bounds__(kRowThreads)
+
+// Combine with the slot rows staged in shared memory: one warp per (token,
+// 512-byte segment), each lane on one 16-byte column; the segment's slot
+// rows are copied in groups of kCombSlots with cp.async (16 bytes a lane,
+// no registers held while they travel), double-buffered so that the next
+// group (of this task or the warp's next task) is in flight while this one
+// is added.  Each lane reads back only what it copied itself.  Sum order:
+// slot 0, 1, ..., k - 1 in fp32 from zero, one bf16 rounding.
+constexpr int kCombWarps = 4;
+constexpr int kCombSlots = 4;
+constexpr int kCombSmem = kCombWarps * 2 * kCombSlots * 32 * 16;
+
+__device__ __forceinline__ void cp_async16(const void *sdst, const void *gsrc)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(sdst))),
+                 "l"(gsrc)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(kCombWarps * 32)
     k_combine(const uint4 *__restrict__ Ys, const int32_t *__restrict__ pos, int T, int k,
               int dvec, uint4 *__restrict__ y)
 {
+    extern __shared__ __align__(16) uint4 csm[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint4 *buf = csm + warp * (2 * kCombSlots * 32);  // [2][kCombSlots][32]
     pdl_wait();
-    const int lane = threadIdx.x & 31;
-    const int nseg = (dvec + kSegVec - 1) / kSegVec;
+    const int nseg = (dvec + 31) / 32;
+    const int ngrp = (k + kCombSlots - 1) / kCombSlots;
     const int64_t ntask = int64_t(T) * nseg;
-    const int64_t nw = int64_t(gridDim.x) * kRowWarps;
-    for (int64_t task = int64_t(blockIdx.x) * kRowWarps + (threadIdx.x >> 5); task < ntask;
-         task += nw) {
-        const int64_t t = task / nseg;
-        const int seg = int(task - t * nseg);
-        const int c0 = seg * kSegVec + lane, c1 = c0 + 32;
-        float acc[16];
+    const int64_t nw = int64_t(gridDim.x) * kCombWarps;
+    int64_t task = int64_t(blockIdx.x) * kCombWarps + warp;
+    // copy group gg of task tk into buffer b; returns the mask of its non-skipped slots
+    auto issue = [&](int64_t tk, int gg, int b) -> uint32_t {
+        const int64_t t = tk / nseg;
+        const int c = int(tk - t * nseg) * 32 + lane;
+        const int j0 = gg * kCombSlots;
+        const int jn = min(kCombSlots, k - j0);
+        const int pl = lane < jn ? pos[t * k + j0 + lane] : -1;
+        uint32_t m = 0;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            acc[i] = 0.0f;
-        const int32_t *pt = pos + t * k;
-        for (int j = 0; j < k; ++j) {
-            const int p = pt[j];
-            if (p < 0)
-                continue;
-            const uint4 *row = Ys + int64_t(p) * dvec;
-            if (c1 < dvec) {
-                const uint4 a = ldg_nc(row + c0), b = ldg_nc(row + c1);
-                add_bf16x8(acc, a);
-                add_bf16x8(acc + 8, b);
-            } else if (c0 < dvec) {
-                add_bf16x8(acc, ldg_nc(row + c0));
+        for (int s = 0; s < kCombSlots; ++s) {
+            const int p = __shfl_sync(kFull, pl, s);
+            if (s < jn && p >= 0) {
+                m |= 1u << s;
+                if (c < dvec)
+                    cp_async16(buf + (b * kCombSlots + s) * 32 + lane, Ys + int64_t(p) * dvec + c);
             }
         }
-        uint4 *out = y + t * dvec;
-        if (c0 < dvec)
-            out[c0] = pack_bf16x8(acc);
-        if (c1 < dvec)
-            out[c1] = pack_bf16x8(acc + 8);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        return m;
+    };
+    if (task < ntask) {
+        int g = 0, b = 0;
+        uint32_t mcur = issue(task, 0, 0);
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            acc[i] = 0.0f;
+        while (true) {
+            int64_t ntk = task;
+            int ng = g + 1;
+            if (ng == ngrp) {
+                ng = 0;
+                ntk = task + nw;
+            }
+            const bool more = ntk < ntask;
+            uint32_t mnext = 0;
+            if (more) {
+                mnext = issue(ntk, ng, b ^ 1);
+                asm volatile("cp.async.wait_group 1;" ::: "memory");
+            } else {
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
+            }
+#pragma unroll
+            for (int s = 0; s < kCombSlots; ++s)
+                if ((mcur >> s) & 1u)
+                    add_bf16x8(acc, buf[(b * kCombSlots + s) * 32 + lane]);
+            if (g == ngrp - 1) {
+                const int64_t t = task / nseg;
+                const int c = int(task - t * nseg) * 32 + lane;
+                if (c < dvec)
+                    y[t * dvec + c] = pack_bf16x8(acc);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    acc[i] = 0.0f;
+            }
+            if (!more)
+                break;
+            task = ntk;
+            g = ng;
+            b ^= 1;
+            mcur = mnext;
+        }
     }
     pdl_launch_dependents();
+}
+
+// Resident combine CTAs per SM on this device (registers decide), once per device.
+int combine_ctas_per_sm()
+{
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 1;
+    const int v = cached[dev].load(std::memory_order_relaxed);
+    if (v > 0)
+        return v;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_combine, kCombWarps * 32, kCombSmem) !=
+            cudaSuccess ||
+        n <= 0) {
+        cudaGetLastError();  // a failed query is not the caller's error
+        n = 1;
+    }
+    cached[dev].store(n, std::memory_order_relaxed);
+    return n;
 }
 
 }  // namespace
@@ -276,11 +356,11 @@ cudaError_t launch_combine(const void *Ys, const int32_t *pos, int T, int k, int
                            cudaStream_t stream)
 {
     const int dvec = d / 8;
-    const int64_t ntask = int64_t(T) * ((dvec + kSegVec - 1) / kSegVec);
-    const int64_t want = (ntask + kRowWarps - 1) / kRowWarps;
-    const int64_t cap_grid = int64_t(device_sm_count()) * kCtasPerSm;
+    const int64_t ntask = int64_t(T) * ((dvec + 31) / 32);
+    const int64_t want = (ntask + kCombWarps - 1) / kCombWarps;
+    const int64_t cap_grid = int64_t(device_sm_count()) * combine_ctas_per_sm();
     const int grid = int(want < 1 ? 1 : (want < cap_grid ? want : cap_grid));
-    return launch_pdl(k_combine, dim3(grid), dim3(kRowThreads), 0, stream,
+    return launch_pdl(k_combine, dim3(grid), dim3(kCombWarps * 32), size_t(kCombSmem), stream,
                       static_cast<const uint4 *>(Ys), pos, T, k, dvec, static_cast<uint4 *>(y));
 }
 
