@@ -93,3 +93,31 @@ def test_combine_order_is_slot_order():
     assert np.all(got == 0.0)
     got = B.combine(dev16(Ys), dev(np.array([[0, 2, 1]], np.int32))).float().cpu().numpy()
     assert np.all(got == 1.0)
+
+
+def test_combine_order_across_slot_groups():
+    # the combine copies slot rows in groups of four; the sum still runs in
+    # slot order across the groups: 2^24 (slot 0) + 1 (slot 4) -> 2^24 (tie
+    # to even), then - 2^24 (slot 8) -> 0; any other order gives 1
+    d = 8
+    rows = np.array([[2.0 ** 24] * d, [1.0] * d, [-(2.0 ** 24)] * d, [0.0] * d], np.float32)
+    Ys = W.bf16_bits(rows)
+    pos = np.array([[0, 3, 3, 3, 1, 3, -1, 3, 2]], np.int32)
+    got = B.combine(dev16(Ys), dev(pos)).float().cpu().numpy()
+    assert np.all(got == 0.0)
+    pos = np.array([[0, 3, 3, 3, 2, 3, -1, 3, 1]], np.int32)
+    got = B.combine(dev16(Ys), dev(pos)).float().cpu().numpy()
+    assert np.all(got == 1.0)
+
+
+def test_combine_many_slots_several_segments():
+    # k = 37 (ten groups of slots, more slots than lanes), d = 808: three
+    # full 256-column segments and a ragged one of 40 columns
+    T, k, d = 50, 37, 808
+    rng = np.random.default_rng(12)
+    Ys = W.bf16_bits(rng.standard_normal((600, d)).astype(np.float32))
+    pos = rng.integers(0, 600, size=(T, k)).astype(np.int32)
+    pos[rng.random((T, k)) < 0.2] = -1
+    got = B.combine(dev16(Ys), dev(pos)).float().cpu().numpy().astype(np.float64)
+    ref = oracle.combine(Ys, pos)
+    assert np.all(np.abs(got - ref) <= combine_bound(Ys, pos, ref))
