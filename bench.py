@@ -14,7 +14,9 @@ Printed: ONE JSON line with rows/s (T*k routed rows per layer), the plan's
 microseconds per layer, per-stage times, the roofline of the dominant kernel
 (the gate/up GEMM), the end-to-end rows/s through host buffers, SM clocks
 sampled during the timed region, and the CPU oracle timed on a bounded
-sample on this host's cores.
+sample on this host's cores.  Beside them: the plan alone on 1M and 10M
+entries (plan_sweep), the plan + gather configuration with fp16 rows
+(plan_gather), and the same layer on 8-bit operands (fp8_layer).
 
 ``--impl reference`` times the CPU oracle itself (the only reference this
 method has) on bounded samples of the same workload.
@@ -416,6 +418,51 @@ def run_native(args, rank, world, local):
                           "frac": byts / us / 1e3 / hbm_peak})
             del ids_s, w_s, o_s
 
+    # the plan + gather configuration (no expert FFN): T=2048, E=512, top-10,
+    # d=2560 fp16 rows gathered into expert order; each step = one moe_plan
+    # and one moe_gather on inputs resident in HBM, L2 flushed before it
+    plan_gather = None
+    if not args.no_plan_gather:
+        wl2 = W.workload(2)
+        inp2 = W.make_inputs(wl2, seed=0, weights=False)
+        x2 = torch.from_numpy(np.ascontiguousarray(inp2["x"]).view(np.int16)).to(dev).view(
+            torch.float16)
+        ids2 = torch.from_numpy(inp2["ids"]).to(dev)
+        w2 = torch.from_numpy(inp2["w"]).to(dev)
+        cap2 = B.capacity(wl2.T, wl2.k, wl2.E, wl2.tm)
+        o2 = B.plan(ids2, w2, wl2.E, wl2.tm, cap=cap2)
+        xs2 = B.gather(x2, o2["srt_tok"], o2["offsets"], wl2.E, cap2)
+
+        def plan_step():
+            B.plan(ids2, w2, wl2.E, wl2.tm, cap=cap2, out=o2)
+
+        def gather_step():
+            B.gather(x2, o2["srt_tok"], o2["offsets"], wl2.E, cap2, xs=xs2)
+
+        def both():
+            plan_step()
+            gather_step()
+
+        for i in range(args.warmup):
+            flush.fill_(i & 0xFF)
+            both()
+        torch.cuda.synchronize(dev)
+        K2 = min(args.steps, 200)
+        ms2 = timed(both, K2)
+        g_ms = timed(gather_step, K2)
+        r_pad2 = int(o2["offsets"][-1])
+        g_us = statistics.mean(g_ms) * 1e3
+        # bytes the gather must move across HBM at least once: x read once (its
+        # rows are read k times, from L2 after the first), xs written, srt_tok
+        g_bytes = wl2.T * wl2.d * 2 + r_pad2 * wl2.d * 2 + 4 * r_pad2
+        plan_gather = {"workload": wl2.name, "x_dtype": "f16",
+                       "value": wl2.T * wl2.k / (statistics.mean(ms2) / 1e3), "unit": "rows/s",
+                       "ms_per_step": statistics.mean(ms2), "steps": K2, "R_pad": r_pad2,
+                       "gather_us": g_us, "gather_hbm_bytes": g_bytes,
+                       "gather_hbm_gbs": g_bytes / g_us / 1e3,
+                       "gather_frac": g_bytes / g_us / 1e3 / peaks()[0]}
+        del x2, ids2, w2, o2, xs2
+
     if rank != 0:
         return
     hbm, tflops, peak_src = peaks()
@@ -451,6 +498,7 @@ def run_native(args, rank, world, local):
         "plan_us_per_layer_method": "48 moe_plan calls per CUDA graph replay, mean per call",
         "plan_us_cold": stage_us["plan"],
         "plan_sweep": sweep,
+        "plan_gather": plan_gather,
         "stages_us": stage_us,
         "layer_hbm_gbs": layer_gbs,
         "roofline": {"kernel": ("k_ffn<gate/up, E4M3 operands> (tcgen05.mma.kind::f8f6f4 "
@@ -531,6 +579,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-plan-sweep", action="store_true",
                     help="skip the plan timed alone at 1M and 10M entries")
+    ap.add_argument("--no-plan-gather", action="store_true",
+                    help="skip the plan + gather configuration (T=2048, E=512, fp16 rows)")
     ap.add_argument("--no-fp8", action="store_true",
                     help="skip the E4M3 layer measured beside the bf16 one")
     ap.add_argument("--weights", choices=("bf16", "e4m3", "f8"), default="bf16",
