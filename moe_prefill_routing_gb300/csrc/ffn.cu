@@ -593,26 +593,88 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
         const int et = int(threadIdx.x) - 64;  // 0..127; thread 0 issues the stores
         int abuf = 0;
         uint32_t aphase = 0, chunk = 0;
-        for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
-            const Unit w = map_unit(u, n_mt, chunk_start, p.E, p.offsets);
+        // What a unit's epilogue reads from global memory is loaded ahead in
+        // registers: the offsets bounding its expert two units ahead, then
+        // (from those) its rows' routing weights and exponents and its
+        // features' scales one unit ahead, so no load's latency falls
+        // between one unit's stores and the next unit's TMEM reads.
+        struct Ahead {  // unit index split and the expert's offsets (in flight)
+            int c, mt, e, oa, ob;
+        };
+        struct Vals {  // per-thread values of a unit (in flight)
+            float rw, s0, s1;
+            int rx;
+        };
+        auto ahead_of = [&](int64_t uu) {
+            Ahead a;
+            a.c = int(uu / n_mt);
+            a.mt = int(uu - int64_t(a.c) * n_mt);
+            int lo = 0, hi = p.E - 1;  // the expert e with chunk_start[e] <= c < chunk_start[e+1]
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (chunk_start[mid] <= a.c)
+                    lo = mid;
+                else
+                    hi = mid - 1;
+            }
+            a.e = lo;
+            a.oa = p.offsets[lo];
+            a.ob = p.offsets[lo + 1];
+            return a;
+        };
+        auto unit_of = [&](const Ahead &a) {
+            Unit r;
+            r.mt = a.mt;
+            r.e = a.e;
+            r.row0 = a.oa + (a.c - chunk_start[a.e]) * BN;
+            r.nrows = min(BN, a.ob - r.row0);
+            return r;
+        };
+        auto vals_of = [&](const Unit &uw) {
+            Vals v{1.0f, 1.0f, 1.0f, 0};
+            if (!GATED && et < uw.nrows)  // the rows' routing weights
+                v.rw = p.srt_w[uw.row0 + et];
+            if (A8 && et < uw.nrows)  // the rows' scale exponents
+                v.rx = p.row_exp[uw.row0 + et];
+            if (SCALED) {  // E4M3 weights: this thread's output feature in both A tiles
+                const int64_t eb = int64_t(uw.e) * p.M;
+                const int um0 = uw.mt * UM;
+                const int fa = tile_base(um0, 0) + fq, fb = tile_base(um0, 1) + fq;
+                v.s0 = fa < p.M ? p.scale0[eb + fa] : 0.0f;
+                v.s1 = fb < p.M ? p.scale1[eb + fb] : 0.0f;
+            }
+            return v;
+        };
+        const int64_t ustep = gridDim.x;
+        Unit wnext{};
+        Vals vnext{1.0f, 1.0f, 1.0f, 0};
+        Ahead anext{};
+        if (int64_t(blockIdx.x) < total_units) {
+            wnext = unit_of(ahead_of(blockIdx.x));
+            vnext = vals_of(wnext);
+        }
+        if (int64_t(blockIdx.x) + ustep < total_units)
+            anext = ahead_of(int64_t(blockIdx.x) + ustep);
+        for (int64_t u = blockIdx.x; u < total_units; u += ustep) {
+            const Unit w = wnext;
+            const Vals vals = vnext;
+            if (u + ustep < total_units) {  // its offsets were loaded one unit ago
+                wnext = unit_of(anext);
+                vnext = vals_of(wnext);
+            }
+            if (u + 2 * ustep < total_units)
+                anext = ahead_of(u + 2 * ustep);
             const int m0 = w.mt * UM;
             const bool use1 = tile_base(m0, 1) < p.M;
-            // E4M3 weights: the scales of this thread's output feature in both A tiles
-            float sc0 = 1.0f, sc1 = 1.0f;
-            if (SCALED) {
-                const int64_t eb = int64_t(w.e) * p.M;
-                const int fa = tile_base(m0, 0) + fq, fb = tile_base(m0, 1) + fq;
-                sc0 = fa < p.M ? p.scale0[eb + fa] : 0.0f;
-                sc1 = fb < p.M ? p.scale1[eb + fb] : 0.0f;
-            }
+            const float sc0 = vals.s0, sc1 = vals.s1;
             // The four warps stop together or not at all: they meet at named
             // barriers below.  epi_stop is written before this barrier and read
             // after it; the next write can only come after the unit's chunk
             // barriers, which every thread reaches after its read.
             if (!GATED && et < w.nrows)  // read by every thread of the unit's chunks
-                row_w[et] = p.srt_w[w.row0 + et];
+                row_w[et] = vals.rw;
             if (A8 && et < w.nrows)  // the rows' scales 2^e
-                row_s[et] = ldexpf(1.0f, p.row_exp[w.row0 + et]);
+                row_s[et] = ldexpf(1.0f, vals.rx);
             if (!mbar_wait(&ctl->tmem_full[abuf], aphase, abort_flag))
                 *reinterpret_cast<volatile int *>(&ctl->epi_stop) = 1;
             epi_bar();
