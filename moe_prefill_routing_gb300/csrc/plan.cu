@@ -272,8 +272,9 @@ constexpr int kOrWalkMaxE = 1024;
 constexpr int kMaxIdBits = 12;  // ids < MOE_MAX_EXPERTS = 4096
 static_assert(MOE_MAX_EXPERTS <= (1 << kMaxIdBits), "id bits");
 
-// Place: block b walks its entries again (same ranges, same ranks), prefixes
-// the warps' counts per expert, and gives each entry row = offsets[e] +
+// Place (each CTA loops over blocks, the grid being the CTAs the GPU holds
+// at once): block b walks its entries again (same ranges, same ranks),
+// prefixes the warps' counts per expert, and gives each entry row = offsets[e] +
 // (rows of e in earlier blocks) + (its rank among the block's entries of e).
 // A block's entries of one expert fill consecutive rows, so their rows,
 // weights and block-local indices are first put in shared memory in expert
@@ -373,95 +374,112 @@ __global__ void __launch_bounds__(kPThreads, 3)
     // everything is read after the wait: this launch may begin before the
     // count kernel's own wait for whatever wrote the ids has ended
     pdl_wait();
-    const int64_t blk_lo = int64_t(blockIdx.x) * kPlanBlockEntries;
-    const int64_t lo = blk_lo + warp * kPSteps * 32;
-    const int64_t hi = min(n, lo + kPSteps * 32);
     int v[kPSteps];
     float wv[kPSteps];
+    auto load_ids = [&](int bb) {
+        const int64_t blo = int64_t(bb) * kPlanBlockEntries + warp * kPSteps * 32;
+        const int64_t bhi = min(n, blo + kPSteps * 32);
 #pragma unroll
-    for (int s = 0; s < kPSteps; ++s) {
-        const int64_t i = lo + s * 32 + lane;
-        v[s] = i < hi ? ids[i] : -1;
-        wv[s] = i < hi ? w[i] : 0.0f;
-    }
-    __syncthreads();
-    bool bad = false;
-    warp_walk<OR_WALK ? kWalkOr : kWalkBallot>(v, lo, hi, E, cntw + warp * E, pm + warp * E,
-                                               bad);
-    if (__any_sync(kFull, bad) && lane == 0)
-        atomicOr(status, MOE_STATUS_BAD_ID);
-    __syncthreads();
-    // per expert: warp counts -> prefix over warps, the block's total, and
-    // an exclusive scan of the totals over the experts (contiguous runs of J
-    // experts per thread, then warp shuffles and warp totals)
-    const int32_t *brow = bcnt + int64_t(blockIdx.x) * E;
-    const int32_t *grow = bcnt + (int64_t(nblk) + blockIdx.x / kPlanGroupBlocks) * E;
-    const int J = (E + kPThreads - 1) / kPThreads;
-    const int e0 = min(E, tid * J), e1 = min(E, e0 + J);
-    int tsum = 0;
-    for (int e = e0; e < e1; ++e) {
-        int run = 0;
+        for (int s = 0; s < kPSteps; ++s) {
+            const int64_t i = blo + s * 32 + lane;
+            v[s] = i < bhi ? ids[i] : -1;
+        }
+    };
+    // CTA c places blocks c, c + gridDim.x, ... (grid: the CTAs the GPU holds
+    // at once); the next block's ids are loaded while this block's runs are
+    // written out
+    load_ids(blockIdx.x);
+    for (int b = blockIdx.x; b < nblk; b += gridDim.x) {
+        const int64_t blk_lo = int64_t(b) * kPlanBlockEntries;
+        const int64_t lo = blk_lo + warp * kPSteps * 32;
+        const int64_t hi = min(n, lo + kPSteps * 32);
+#pragma unroll
+        for (int s = 0; s < kPSteps; ++s) {
+            const int64_t i = lo + s * 32 + lane;
+            wv[s] = i < hi ? w[i] : 0.0f;
+        }
+        __syncthreads();
+        bool bad = false;
+        warp_walk<OR_WALK ? kWalkOr : kWalkBallot>(v, lo, hi, E, cntw + warp * E, pm + warp * E,
+                                                   bad);
+        if (__any_sync(kFull, bad) && lane == 0)
+            atomicOr(status, MOE_STATUS_BAD_ID);
+        __syncthreads();
+        // per expert: warp counts -> prefix over warps, the block's total, and
+        // an exclusive scan of the totals over the experts (contiguous runs of J
+        // experts per thread, then warp shuffles and warp totals)
+        const int32_t *brow = bcnt + int64_t(b) * E;
+        const int32_t *grow = bcnt + (int64_t(nblk) + b / kPlanGroupBlocks) * E;
+        const int J = (E + kPThreads - 1) / kPThreads;
+        const int e0 = min(E, tid * J), e1 = min(E, e0 + J);
+        int tsum = 0;
+        for (int e = e0; e < e1; ++e) {
+            int run = 0;
+#pragma unroll
+            for (int w2 = 0; w2 < kPWarps; ++w2) {
+                const int t = cntw[w2 * E + e];
+                cntw[w2 * E + e] = uint16_t(run);
+                run += t;
+            }
+            loc[e] = run;  // the block's count for now
+            tsum += run;
+            s_off[e] = offsets[e];
+            rowbase[e] = s_off[e] + grow[e] + brow[e];
+        }
+        if (tid == 0)
+            s_off[E] = offsets[E];
+        int sc = tsum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(kFull, sc, o);
+            if (lane >= o)
+                sc += t;
+        }
+        if (lane == 31)
+            warp_tot[warp] = sc;
+        __syncthreads();
+        int slot0 = sc - tsum, total = 0;
 #pragma unroll
         for (int w2 = 0; w2 < kPWarps; ++w2) {
-            const int t = cntw[w2 * E + e];
-            cntw[w2 * E + e] = uint16_t(run);
-            run += t;
+            slot0 += w2 < warp ? warp_tot[w2] : 0;
+            total += warp_tot[w2];
         }
-        loc[e] = run;  // the block's count for now
-        tsum += run;
-        s_off[e] = offsets[e];
-        rowbase[e] = s_off[e] + grow[e] + brow[e];
-    }
-    if (tid == 0)
-        s_off[E] = offsets[E];
-    int sc = tsum;
+        for (int e = e0; e < e1; ++e) {
+            const int c = loc[e];
+            loc[e] = slot0;
+            slot0 += c;
+        }
+        __syncthreads();
+        // each entry: its rank in the block, pos in flat order, its sorted slot
+        const uint16_t *mycnt = cntw + warp * E;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(kFull, sc, o);
-        if (lane >= o)
-            sc += t;
-    }
-    if (lane == 31)
-        warp_tot[warp] = sc;
-    __syncthreads();
-    int slot0 = sc - tsum, total = 0;
-#pragma unroll
-    for (int w2 = 0; w2 < kPWarps; ++w2) {
-        slot0 += w2 < warp ? warp_tot[w2] : 0;
-        total += warp_tot[w2];
-    }
-    for (int e = e0; e < e1; ++e) {
-        const int c = loc[e];
-        loc[e] = slot0;
-        slot0 += c;
-    }
-    __syncthreads();
-    // each entry: its rank in the block, pos in flat order, its sorted slot
-    const uint16_t *mycnt = cntw + warp * E;
-#pragma unroll
-    for (int s = 0; s < kPSteps; ++s) {
-        const int64_t i = lo + s * 32 + lane;
-        if (i < hi) {
-            const int p = v[s];
-            if (p >= 0) {
-                const int e = p & 0xffff, r = mycnt[e] + (p >> 16);
-                const int row = rowbase[e] + r;
-                pos[i] = row;
-                const int slot = loc[e] + r;
-                s_row[slot] = row;
-                s_w[slot] = wv[s];
-                s_li[slot] = uint16_t(i - blk_lo);
-            } else {
-                pos[i] = -1;
+        for (int s = 0; s < kPSteps; ++s) {
+            const int64_t i = lo + s * 32 + lane;
+            if (i < hi) {
+                const int p = v[s];
+                if (p >= 0) {
+                    const int e = p & 0xffff, r = mycnt[e] + (p >> 16);
+                    const int row = rowbase[e] + r;
+                    pos[i] = row;
+                    const int slot = loc[e] + r;
+                    s_row[slot] = row;
+                    s_w[slot] = wv[s];
+                    s_li[slot] = uint16_t(i - blk_lo);
+                } else {
+                    pos[i] = -1;
+                }
             }
         }
-    }
-    __syncthreads();
-    for (int j = tid; j < total; j += kPThreads) {
-        const int row = s_row[j];
-        if (row < cap) {
-            srt_tok[row] = int32_t(div_k(uint32_t(blk_lo + s_li[j]), kd));
-            srt_w[row] = s_w[j];
+        __syncthreads();
+        zero_warp_counts(cntw, E);  // the lane words are left zero by every step
+        if (b + int(gridDim.x) < nblk)
+            load_ids(b + gridDim.x);
+        for (int j = tid; j < total; j += kPThreads) {
+            const int row = s_row[j];
+            if (row < cap) {
+                srt_tok[row] = int32_t(div_k(uint32_t(blk_lo + s_li[j]), kd));
+                srt_w[row] = s_w[j];
+            }
         }
     }
     // tile table, spread over the grid
@@ -786,7 +804,16 @@ cudaError_t launch_plan(const int32_t *ids, const float *w, int T, int k, int E,
                      counts, E, tm, cap, offsets, srt_tok, srt_w, tile_expert, status, nblk == 0);
     if (err != cudaSuccess || nblk == 0)
         return err;
-    return launch_pdl(or_walk ? k_place_blocks<true> : k_place_blocks<false>, dim3(nblk),
+    int per_sm = 0;  // resident place CTAs per SM for this E (shared memory and registers)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm, or_walk ? k_place_blocks<true> : k_place_blocks<false>, kPThreads,
+            place_smem_bytes(E, or_walk)) != cudaSuccess ||
+        per_sm < 1) {
+        cudaGetLastError();  // a failed query is not the caller's error
+        per_sm = 1;
+    }
+    const int pgrid = std::min(nblk, device_sm_count() * per_sm);
+    return launch_pdl(or_walk ? k_place_blocks<true> : k_place_blocks<false>, dim3(pgrid),
                       dim3(kPThreads), place_smem_bytes(E, or_walk), stream, ids, w, n,
                       make_divk(uint32_t(k)), E, tm, cap, static_cast<const int32_t *>(offsets),
                       static_cast<const int32_t *>(bcnt), nblk, pos, srt_tok, srt_w,
