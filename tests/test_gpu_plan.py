@@ -222,3 +222,15 @@ def test_plan_walk_switch(E, T):
     ids[rng.random(ids.shape) < 0.05] = -1
     w = rng.standard_normal(ids.shape).astype(np.float32)
     check(ids, w, E, 16)
+
+
+@pytest.mark.parametrize("T,k,E", [(30001, 3, 700), (12000, 7, 300), (2000, 37, 1500), (300, 255, 512)])
+def test_plan_multi_kernel_odd_k(T, k, E):
+    # above the one-launch size with k not a power of two: the token index
+    # of each row is the flat index divided by k (by a multiply-high), the
+    # walk runs on shared-memory lane words (E <= 1024) or ballots (E = 1500)
+    rng = np.random.default_rng(T + 97 * k)
+    ids = rng.integers(0, E, size=(T, k), dtype=np.int32)
+    ids[rng.random(ids.shape) < 0.03] = -1
+    w = rng.standard_normal((T, k)).astype(np.float32)
+    check(ids, w, E, 16)
