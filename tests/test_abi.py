@@ -224,3 +224,32 @@ def test_moe_layer_holds_either_weight_form():
 def test_status_strings(lib):
     for code in (0, -1, -2, -3, -4, -5, -6, -7, 99):
         assert isinstance(B.status_str(code), str) and B.status_str(code)
+
+
+def test_plan_workspace_holds_block_and_group_counts(lib):
+    # one row of E int32 per block of 4096 entries and one per group of 256
+    # blocks, after the 256-byte header
+    for T, k, E in [(1, 1, 1), (2048, 10, 512), (104858, 10, 512), (1 << 20, 10, 512),
+                    (65537, 4, 4096), (70001, 2, 256)]:
+        nblk = -(-(T * k) // 4096)
+        rows = nblk + -(-nblk // 256)
+        want = 256 + -(-(rows * E * 4) // 256) * 256
+        assert B.plan_workspace_bytes(T, k, E) == want, (T, k, E)
+
+
+def noalloc_call(lib, T, k, E, status):
+    tm = 16
+    return lib.moe_plan_noalloc(FAKE, FAKE, T, k, E, tm, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                B.capacity(T, k, E, tm), status, None)
+
+
+@pytest.mark.parametrize("E,entries", [(512, 517 * 4096), (4096, 64 * 4096)])
+def test_noalloc_limit_boundary(lib, E, entries):
+    # (blocks + groups) x E <= MOE_PLAN_NOALLOC_MAX_COUNTS: at the limit the
+    # size check passes (the misaligned status word is the first error, so
+    # nothing is enqueued); one entry more needs another block row
+    k = 4 if E == 4096 else 1
+    T = entries // k
+    assert noalloc_call(lib, T, k, E, FAKE + 2) == B.MOE_ERR_ALIGN
+    T1 = (entries + k) // k
+    assert noalloc_call(lib, T1, k, E, FAKE + 2) == B.MOE_ERR_WORKSPACE
