@@ -140,8 +140,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // Slots of ensure_smem_limit's per-device cache.
 enum SmemSlot {
-    kSlotPlace = 0,
-    kSlotPlaceOr,
+    kSlotPlaceOr = 0,      // the large-input place kernel with shared-memory lane words
+    kSlotPlaceBallot0,     // ... with ballots, for ids of 0 .. 12 bits
+    kSlotPlaceBallot12 = kSlotPlaceBallot0 + 12,
     kSlotHist,
     kSlotGateUp,
     kSlotGateUpRows,

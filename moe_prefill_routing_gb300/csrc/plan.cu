@@ -24,13 +24,13 @@
 //    ranks its share, then, through distributed shared memory and hardware
 //    cluster barriers, each CTA scans a share of the experts and hands every
 //    CTA the first row of each expert for its share of entries.
-// Larger inputs, where the plan is bound by its HBM traffic, run four
-// kernels over blocks of 4096 entries, chained with programmatic dependent
-// launch: count (each block's count per expert), column scan (per expert,
-// the rows of the earlier blocks of the same group of 256 blocks, and each
-// group's total), expert scan (the groups' totals prefixed, offsets, tail
-// rows), place (the ranks walked again, in registers, the scatter and the
-// tile table).
+// Larger inputs run four kernels over blocks of 4096 entries, chained with
+// programmatic dependent launch: count (each block's count per expert),
+// column scan (per expert, the rows of the earlier blocks of the same group
+// of 256 blocks, and each group's total), expert scan (the groups' totals
+// prefixed, counts, offsets), place (the ranks walked again, the block's
+// entries put in expert order in shared memory and written out run after
+// run, pos, the tail rows and the tile table).
 // The ranks are recomputed rather than stored between the passes, so the
 // entries are read twice and pos, srt_tok and srt_w written once.
 #include "../../include/moe_prefill.h"
@@ -52,13 +52,6 @@ constexpr int kPSteps = 16;
 static_assert(kPWarps * kPSteps * 32 == kPlanBlockEntries, "entries per block");
 constexpr int kColThreads = 1024;  // column scan: 32 warps x 32 experts
 constexpr int kScanThreads = 1024;
-
-// 16 * E bytes of per-warp 16-bit counters: E vectors of 16 bytes.
-__device__ __forceinline__ void zero_warp_counts(uint16_t *cntw, int E)
-{
-    for (int v = threadIdx.x; v < E; v += kPThreads)
-        reinterpret_cast<uint4 *>(cntw)[v] = make_uint4(0u, 0u, 0u, 0u);
-}
 
 // Count: bcnt[b][e] = entries of block b (kPlanBlockEntries flat entries)
 // routed to expert e.  Only the totals matter here, so shared-memory atomics
@@ -153,24 +146,19 @@ __global__ void __launch_bounds__(kColThreads)
 
 // Expert scan (one CTA): counts[e] = the sum of the groups' totals, each
 // total replaced by the rows of e in the earlier groups; offsets[e] = sum
-// over e' < e of counts[e'] rounded up to tm, offsets[E] = R_pad; the tail
-// rows [offsets[e] + counts[e], offsets[e + 1]) get srt_tok = -1 and srt_w =
-// +0; with fill_tiles (no place kernel follows, i.e. no entries)
-// tile_expert[t] = e for the tiles of e.  Resets the status word (the place
-// adds bad-id bits after).
+// over e' < e of counts[e'] rounded up to tm, offsets[E] = R_pad.  Resets the
+// status word (the place kernel adds bad-id bits after).  The tail rows and
+// the tile table are the place kernel's, which runs over the whole GPU.
 __global__ void __launch_bounds__(kScanThreads)
     k_scan_experts(int32_t *__restrict__ gsum, int ngroups, int32_t *__restrict__ counts, int E,
                    int tm, int64_t cap, int32_t *__restrict__ offsets,
-                   int32_t *__restrict__ srt_tok, float *__restrict__ srt_w,
-                   int32_t *__restrict__ tile_expert, uint32_t *__restrict__ status,
-                   bool fill_tiles)
+                   uint32_t *__restrict__ status)
 {
     __shared__ int warp_incl[kScanThreads / 32];
     pdl_launch_dependents();
     pdl_wait();
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
-    const int64_t n_tiles_cap = cap / tm;
     int64_t carry = 0;  // padded rows of the experts before this slice
     for (int base = 0; base < E; base += kScanThreads) {
         const int e = base + tid;
@@ -215,16 +203,8 @@ __global__ void __launch_bounds__(kScanThreads)
         const int64_t off = carry + (v - P) + (warp > 0 ? warp_incl[warp - 1] : 0);
         const int slice_total = warp_incl[kScanThreads / 32 - 1];
         __syncthreads();  // warp_incl is reused by the next slice
-        if (e < E) {
+        if (e < E)
             offsets[e] = int32_t(off);
-            for (int64_t r = off + c; r < off + P && r < cap; ++r) {
-                srt_tok[r] = -1;
-                srt_w[r] = 0.0f;
-            }
-            if (fill_tiles)
-                for (int64_t t = off / tm; t < (off + P) / tm && t < n_tiles_cap; ++t)
-                    tile_expert[t] = e;
-        }
         carry += slice_total;
     }
     if (tid == 0) {
@@ -259,35 +239,13 @@ __device__ __forceinline__ uint32_t div_k(uint32_t n, DivK d)
 }
 
 // A warp walks its range 32 entries (one step) at a time; the lanes of a
-// step that hold the same expert are found in one of three ways.  kWalkOr
+// step that hold the same expert are found in one of two ways.  kWalkOr
 // (E <= kOrWalkMaxE): each warp keeps a 32-bit word per expert in shared
 // memory, every lane ORs its bit into its expert's word and reads back the
 // whole set (one shared atomic and one load per step).  Above that the
-// per-warp words would not fit: kWalkBallot intersects one ballot per bit of
-// the id (plus one for validity), kWalkMatch uses __match_any_sync; measured,
-// the first is faster in the place kernel of large inputs, the second in the
-// one-launch cluster plan.
-constexpr int kWalkOr = 0, kWalkBallot = 1, kWalkMatch = 2;
+// per-warp words would not fit and kWalkMatch uses __match_any_sync.
+constexpr int kWalkOr = 0, kWalkMatch = 2;
 constexpr int kOrWalkMaxE = 1024;
-constexpr int kMaxIdBits = 12;  // ids < MOE_MAX_EXPERTS = 4096
-static_assert(MOE_MAX_EXPERTS <= (1 << kMaxIdBits), "id bits");
-
-// Place (each CTA loops over blocks, the grid being the CTAs the GPU holds
-// at once): block b walks its entries again (same ranges, same ranks),
-// prefixes the warps' counts per expert, and gives each entry row = offsets[e] +
-// (rows of e in earlier blocks) + (its rank among the block's entries of e).
-// A block's entries of one expert fill consecutive rows, so their rows,
-// weights and block-local indices are first put in shared memory in expert
-// order and then written out run after run: neighbouring lanes write
-// neighbouring rows of srt_tok and srt_w (pos keeps flat order).  The kernel
-// also fills the tile table: tile t belongs to the expert whose rows hold
-// row t * tm.
-constexpr size_t place_smem_bytes(int E, bool or_walk)
-{
-    return size_t(kPWarps) * E * (sizeof(uint16_t) + (or_walk ? sizeof(uint32_t) : 0)) +
-           size_t(3 * E + 2) * sizeof(int) +
-           size_t(kPlanBlockEntries) * (sizeof(int) + sizeof(float) + sizeof(uint16_t));
-}
 
 // Rank of each entry of this warp's range [lo, hi) (at most kPSteps * 32
 // entries) among the earlier entries of the range with the same expert, with
@@ -300,7 +258,6 @@ __device__ __forceinline__ void warp_walk(int (&v)[kPSteps], int64_t lo, int64_t
                                           uint16_t *mycnt, uint32_t *mypm, bool &bad)
 {
     const uint32_t lane = threadIdx.x & 31, lt = lanemask_lt();
-    const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;
 #pragma unroll
     for (int s = 0; s < kPSteps; ++s) {
         if (lo + s * 32 < hi) {  // the same for the whole warp
@@ -314,19 +271,8 @@ __device__ __forceinline__ void warp_walk(int (&v)[kPSteps], int64_t lo, int64_t
                     atomicOr(&mypm[e], 1u << lane);
                 __syncwarp();
                 peers = ok ? mypm[e] : (1u << lane);
-            } else if (WALK == kWalkMatch) {
-                peers = __match_any_sync(kFull, ok ? uint32_t(e) : (0x80000000u | lane));
             } else {
-                const uint32_t vb = __ballot_sync(kFull, ok);
-                peers = ok ? vb : (1u << lane);
-#pragma unroll
-                for (int bit = 0; bit < kMaxIdBits; ++bit) {
-                    if (bit < nbits) {  // the same for the whole warp
-                        const bool set = (uint32_t(e) >> bit) & 1u;
-                        const uint32_t bb = __ballot_sync(kFull, set);
-                        peers &= set ? bb : ~bb;
-                    }
-                }
+                peers = __match_any_sync(kFull, ok ? uint32_t(e) : (0x80000000u | lane));
             }
             // every lane reads its expert's running count (lanes of one
             // expert read the same word), then the lowest of them moves it on
@@ -345,148 +291,329 @@ __device__ __forceinline__ void warp_walk(int (&v)[kPSteps], int64_t lo, int64_t
     }
 }
 
-// 80 registers a thread: three CTAs of 256 threads per SM.
-template <bool OR_WALK>
-__global__ void __launch_bounds__(kPThreads, 3)
+// ---- place for large inputs -------------------------------------------------------
+//
+// Each CTA loops over blocks of kPlanBlockEntries flat entries (the grid being
+// the CTAs the GPU holds at once).  A block is placed in four phases:
+//  - walk: each warp walks its 512 entries 32 at a time; the lanes of a step
+//    holding the same expert are found either through per-warp lane words in
+//    shared memory (each lane ORs its bit into its expert's word) or from
+//    ballots: one per bit of the id, combined per group of 5 bits into, for
+//    lane b, the lanes whose digit is b, and read back with one shuffle per
+//    group.  Each lane reads its expert's running count in this warp (shared
+//    memory), the lowest lane of the set moves it on, and popc of the lower
+//    lanes of the set gives the entry's rank in the warp's range;
+//  - per expert (a thread per contiguous slice of experts): the warps'
+//    counts prefixed over the warps, the block's count, its exclusive scan
+//    over the experts (the start of the expert's run in the block's
+//    expert-sorted order), and the row of the run's first slot, so that
+//    row = slot + delta[e];
+//  - each entry: slot = its warp's first slot for the expert + its rank;
+//    pos (flat order, coalesced) = slot + delta[e]; the entry's key goes to
+//    slot in shared memory;
+//  - write-out: slot j of the sorted block to row j + delta[e], so that
+//    neighbouring lanes write neighbouring rows of srt_tok and srt_w.
+// The next block's ids, weights and count rows are copied into shared memory
+// (cp.async) while the current one is placed.
+constexpr int kQThreads = 256;
+constexpr int kQWarps = kQThreads / 32;
+constexpr int kQSteps = kPlanBlockEntries / kQThreads;  // 16 entries a lane
+constexpr int kLiBits = 12;                              // local index in a block
+static_assert(kPlanBlockEntries == (1 << kLiBits), "keys are (expert << 12) | local index");
+static_assert(kQWarps == 8, "counter vectors: E (counts) and 2 * E (lane words) of 16 bytes");
+static_assert(MOE_MAX_EXPERTS <= (1 << (32 - kLiBits)), "expert ids fit in a key");
+constexpr int kMaxIdBits = 12;  // ids < MOE_MAX_EXPERTS = 4096
+static_assert(MOE_MAX_EXPERTS <= (1 << kMaxIdBits), "id bits");
+// The OR walk's lane words share the sorted keys' buffer (the walk ends
+// before the first key is placed): 8 warps x E words fit in it for E <= 512.
+constexpr int kPlaceOrWalkMaxE = 512;
+
+// ids, weights and sorted keys (a word per entry; the OR walk's per-warp
+// lane words share the keys' buffer), the per-warp running counts (16 bits),
+// then the block's count row (then the runs' deltas), its group's row and the
+// offsets.
+constexpr size_t place_smem_bytes(int E)
+{
+    return size_t(3) * kPlanBlockEntries * sizeof(uint32_t) + size_t(kQWarps) * E * sizeof(uint16_t) +
+           size_t(3 * E + 1) * sizeof(int);
+}
+static_assert(kQWarps * 512 <= kPlanBlockEntries, "lane words of the OR walk fit in the keys' buffer");
+
+__device__ __forceinline__ void cp_async4(void *sdst, const void *gsrc)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(sdst)), "l"(gsrc)
+                 : "memory");
+}
+
+// 16 bytes, of which the first src_bytes are read (the rest are zero-filled).
+__device__ __forceinline__ void cp_async16(void *sdst, const void *gsrc, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(sdst)),
+                 "l"(gsrc), "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Waits until at most one committed group of this thread is still in flight.
+__device__ __forceinline__ void cp_async_wait_all_but_one()
+{
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+
+// The nb (<= kPlanBlockEntries) words src[0, nb) into dst; vec: src is
+// 16-byte aligned, so 16-byte copies (the last one partial).
+__device__ __forceinline__ void copy_block_words(uint32_t *dst, const void *src, int nb, bool vec)
+{
+    const uint32_t *s = static_cast<const uint32_t *>(src);
+    if (vec) {
+        for (int c = threadIdx.x; c * 4 < nb; c += kQThreads)
+            cp_async16(dst + 4 * c, s + 4 * c, uint32_t(min(4, nb - 4 * c)) * 4u);
+    } else {
+        for (int i = threadIdx.x; i < nb; i += kQThreads)
+            cp_async4(dst + i, s + i);
+    }
+}
+
+// The lanes of this step holding a valid id equal to this lane's (for a valid
+// lane), from ballots: for each group of up to 5 id bits, lane b forms the set
+// of valid lanes whose digit in that group is b (lsel[i] is all ones where bit
+// i of the lane index is 0), and every lane reads the set of its own digit
+// from that lane.  NBITS: bits of an id (ids < 2^NBITS).
+template <int NBITS>
+__device__ __forceinline__ uint32_t ballot_peers(uint32_t e, bool ok,
+                                                 const uint32_t (&lsel)[5])
+{
+    const uint32_t vb = __ballot_sync(kFull, ok);
+    uint32_t peers = vb;
+#pragma unroll
+    for (int g = 0; g * 5 < NBITS; ++g) {
+        constexpr int kMaxW = 5;
+        const int wg = NBITS - 5 * g < kMaxW ? NBITS - 5 * g : kMaxW;
+        uint32_t m = vb;
+#pragma unroll
+        for (int bit = 0; bit < kMaxW; ++bit)
+            if (bit < wg)
+                m &= __ballot_sync(kFull, (e >> (5 * g + bit)) & 1u) ^ lsel[bit];
+        peers &= __shfl_sync(kFull, m, int((e >> (5 * g)) & ((1u << wg) - 1u)));
+    }
+    return peers;
+}
+
+template <int NBITS, bool OR_WALK>
+__global__ void __launch_bounds__(kQThreads, 3)
     k_place_blocks(const int32_t *__restrict__ ids, const float *__restrict__ w, int64_t n,
                    DivK kd, int E, int tm, int64_t cap, const int32_t *__restrict__ offsets,
-                   const int32_t *__restrict__ bcnt, int nblk, int32_t *__restrict__ pos,
-                   int32_t *__restrict__ srt_tok, float *__restrict__ srt_w,
-                   int32_t *__restrict__ tile_expert, uint32_t *__restrict__ status)
+                   const int32_t *__restrict__ counts, const int32_t *__restrict__ bcnt, int nblk,
+                   int32_t *__restrict__ pos, int32_t *__restrict__ srt_tok,
+                   float *__restrict__ srt_w, int32_t *__restrict__ tile_expert,
+                   uint32_t *__restrict__ status, bool vec_in)
 {
     extern __shared__ __align__(16) uint8_t psm[];
-    uint16_t *cntw = reinterpret_cast<uint16_t *>(psm);  // [8][E]
-    uint32_t *pm = reinterpret_cast<uint32_t *>(psm + kPWarps * E * sizeof(uint16_t));  // [8][E]
-    int *rowbase = reinterpret_cast<int *>(
-        psm + kPWarps * E * (sizeof(uint16_t) + (OR_WALK ? sizeof(uint32_t) : 0)));  // [E]
-    int *loc = rowbase + E;      // [E + 1] block-local first slot of each expert
-    int *s_off = loc + E + 1;    // [E + 1] offsets
-    int *s_row = s_off + E + 1;  // [4096] the block's entries in expert order: row,
-    float *s_w = reinterpret_cast<float *>(s_row + kPlanBlockEntries);       // weight,
-    uint16_t *s_li = reinterpret_cast<uint16_t *>(s_w + kPlanBlockEntries);  // local index
-    __shared__ int warp_tot[kPWarps];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint32_t *s_ids = reinterpret_cast<uint32_t *>(psm);  // [4096] the block's ids
+    float *s_w = reinterpret_cast<float *>(s_ids + kPlanBlockEntries);             // weights
+    uint32_t *sorted = reinterpret_cast<uint32_t *>(s_w + kPlanBlockEntries);      // keys
+    uint32_t *pm = sorted;  // [8][E] lane words of the OR walk, during the walk only
+    uint16_t *cntw = reinterpret_cast<uint16_t *>(sorted + kPlanBlockEntries);     // [8][E]
+    int *s_brow = reinterpret_cast<int *>(cntw + kQWarps * E);
+    int *s_grow = s_brow + E;  // [E] block's count row, then delta; group's row
+    int *s_off = s_grow + E;   // [E + 1]
+    __shared__ int warp_tot[kQWarps];
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const uint32_t lane = tid & 31, lt = lanemask_lt();
+    uint32_t lsel[5];
+#pragma unroll
+    for (int bit = 0; bit < 5; ++bit)
+        lsel[bit] = (lane >> bit) & 1u ? 0u : kFull;
     pdl_launch_dependents();
-    zero_warp_counts(cntw, E);
-    if (OR_WALK)
-        for (int v = tid; v < 2 * E; v += kPThreads)
+    for (int v = tid; v < E; v += kQThreads)  // counts: E vectors of 16 bytes
+        reinterpret_cast<uint4 *>(cntw)[v] = make_uint4(0u, 0u, 0u, 0u);
+    if (OR_WALK)  // lane words: 2 * E vectors
+        for (int v = tid; v < 2 * E; v += kQThreads)
             reinterpret_cast<uint4 *>(pm)[v] = make_uint4(0u, 0u, 0u, 0u);
     // everything is read after the wait: this launch may begin before the
     // count kernel's own wait for whatever wrote the ids has ended
     pdl_wait();
-    int v[kPSteps];
-    float wv[kPSteps];
-    auto load_ids = [&](int bb) {
-        const int64_t blo = int64_t(bb) * kPlanBlockEntries + warp * kPSteps * 32;
-        const int64_t bhi = min(n, blo + kPSteps * 32);
-#pragma unroll
-        for (int s = 0; s < kPSteps; ++s) {
-            const int64_t i = blo + s * 32 + lane;
-            v[s] = i < bhi ? ids[i] : -1;
-        }
+    for (int e = tid; e <= E; e += kQThreads)
+        s_off[e] = offsets[e];
+    auto block_len = [&](int bb) {
+        return int(min(int64_t(kPlanBlockEntries), n - int64_t(bb) * kPlanBlockEntries));
     };
-    // CTA c places blocks c, c + gridDim.x, ... (grid: the CTAs the GPU holds
-    // at once); the next block's ids are loaded while this block's runs are
-    // written out
-    load_ids(blockIdx.x);
+    if (int(blockIdx.x) < nblk) {
+        const int64_t lo = int64_t(blockIdx.x) * kPlanBlockEntries;
+        copy_block_words(s_ids, ids + lo, block_len(blockIdx.x), vec_in);
+        cp_async_commit();
+        copy_block_words(reinterpret_cast<uint32_t *>(s_w), w + lo, block_len(blockIdx.x), vec_in);
+        cp_async_commit();
+    }
+    uint16_t *mycnt = cntw + warp * E;
+    uint32_t *mypm = pm + warp * E;
+    const int J = (E + kQThreads - 1) / kQThreads;  // experts per thread in the scans
+    const int e0 = min(E, tid * J), e1 = min(E, e0 + J);
+    bool bad = false;
     for (int b = blockIdx.x; b < nblk; b += gridDim.x) {
         const int64_t blk_lo = int64_t(b) * kPlanBlockEntries;
-        const int64_t lo = blk_lo + warp * kPSteps * 32;
-        const int64_t hi = min(n, lo + kPSteps * 32);
-#pragma unroll
-        for (int s = 0; s < kPSteps; ++s) {
-            const int64_t i = lo + s * 32 + lane;
-            wv[s] = i < hi ? w[i] : 0.0f;
+        const int nb = block_len(b);
+        const int next = b + int(gridDim.x);
+        cp_async_wait_all_but_one();  // this block's ids (its weights may be in flight)
+        __syncthreads();              // ... every thread's; the counters are zero
+        {
+            const int32_t *brow = bcnt + int64_t(b) * E;
+            const int32_t *grow = bcnt + (int64_t(nblk) + b / kPlanGroupBlocks) * E;
+            for (int e = tid; e < E; e += kQThreads) {
+                cp_async4(&s_brow[e], brow + e);
+                cp_async4(&s_grow[e], grow + e);
+            }
+            cp_async_commit();
         }
-        __syncthreads();
-        bool bad = false;
-        warp_walk<OR_WALK ? kWalkOr : kWalkBallot>(v, lo, hi, E, cntw + warp * E, pm + warp * E,
-                                                   bad);
-        if (__any_sync(kFull, bad) && lane == 0)
-            atomicOr(status, MOE_STATUS_BAD_ID);
-        __syncthreads();
-        // per expert: warp counts -> prefix over warps, the block's total, and
-        // an exclusive scan of the totals over the experts (contiguous runs of J
-        // experts per thread, then warp shuffles and warp totals)
-        const int32_t *brow = bcnt + int64_t(b) * E;
-        const int32_t *grow = bcnt + (int64_t(nblk) + b / kPlanGroupBlocks) * E;
-        const int J = (E + kPThreads - 1) / kPThreads;
-        const int e0 = min(E, tid * J), e1 = min(E, e0 + J);
+        // ---- walk: each entry's rank in its warp's range ----------------------
+        const int lo = warp * (kQSteps * 32);  // the warp's range in the block
+        int v[kQSteps];  // (rank << 16) | expert, or -1
+#pragma unroll
+        for (int s = 0; s < kQSteps; ++s) {
+            const int li = lo + s * 32 + int(lane);
+            const bool in = li < nb;
+            const int e = in ? int(s_ids[li]) : -1;
+            const bool ok = e >= 0 && e < E;
+            bad |= in && !ok && e != -1;
+            if (lo + s * 32 < nb) {  // the same for the whole warp
+                uint32_t peers;
+                if (OR_WALK) {
+                    if (ok)
+                        atomicOr(&mypm[e], 1u << lane);
+                    __syncwarp();
+                    peers = ok ? mypm[e] : 0u;
+                } else {
+                    peers = ballot_peers<NBITS>(uint32_t(e), ok, lsel);
+                }
+                // every lane reads its expert's running count (lanes of one
+                // expert read the same word), then the lowest of them moves it on
+                const int first = ok ? int(mycnt[e]) : 0;
+                __syncwarp();
+                if (ok && (peers & lt) == 0u) {
+                    mycnt[e] = uint16_t(first + __popc(peers));
+                    if (OR_WALK)
+                        mypm[e] = 0u;
+                }
+                v[s] = ok ? ((first + __popc(peers & lt)) << 16) | e : -1;
+                __syncwarp();
+            } else {
+                v[s] = -1;
+            }
+        }
+        __syncthreads();  // every warp's counts; every id read
+        if (next < nblk)  // the next block's ids may come in
+            copy_block_words(s_ids, ids + int64_t(next) * kPlanBlockEntries, block_len(next),
+                             vec_in);
+        cp_async_commit();
+        // ---- per expert: warps prefixed, the run's start and its row delta -----
+        // (warp 0's first slot for an expert is the run's start: until the
+        // scan over the experts is known, its word holds the block's count)
         int tsum = 0;
         for (int e = e0; e < e1; ++e) {
             int run = 0;
 #pragma unroll
-            for (int w2 = 0; w2 < kPWarps; ++w2) {
+            for (int w2 = 0; w2 < kQWarps; ++w2) {
                 const int t = cntw[w2 * E + e];
                 cntw[w2 * E + e] = uint16_t(run);
                 run += t;
             }
-            loc[e] = run;  // the block's count for now
+            cntw[e] = uint16_t(run);
             tsum += run;
-            s_off[e] = offsets[e];
-            rowbase[e] = s_off[e] + grow[e] + brow[e];
         }
-        if (tid == 0)
-            s_off[E] = offsets[E];
-        int sc = tsum;
+        int sc = tsum;  // scan of the block's counts over the experts
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int t = __shfl_up_sync(kFull, sc, o);
-            if (lane >= o)
+            if (int(lane) >= o)
                 sc += t;
         }
         if (lane == 31)
             warp_tot[warp] = sc;
+        cp_async_wait_all_but_one();  // this block's weights and count rows
         __syncthreads();
-        int slot0 = sc - tsum, total = 0;
+        int start = sc - tsum, nv = 0;
 #pragma unroll
-        for (int w2 = 0; w2 < kPWarps; ++w2) {
-            slot0 += w2 < warp ? warp_tot[w2] : 0;
-            total += warp_tot[w2];
+        for (int w2 = 0; w2 < kQWarps; ++w2) {
+            start += w2 < warp ? warp_tot[w2] : 0;
+            nv += warp_tot[w2];
         }
         for (int e = e0; e < e1; ++e) {
-            const int c = loc[e];
-            loc[e] = slot0;
-            slot0 += c;
-        }
-        __syncthreads();
-        // each entry: its rank in the block, pos in flat order, its sorted slot
-        const uint16_t *mycnt = cntw + warp * E;
+            const int c = cntw[e];
+            cntw[e] = uint16_t(start);
 #pragma unroll
-        for (int s = 0; s < kPSteps; ++s) {
-            const int64_t i = lo + s * 32 + lane;
-            if (i < hi) {
+            for (int w2 = 1; w2 < kQWarps; ++w2)
+                cntw[w2 * E + e] += uint16_t(start);
+            // the run's first row less its first slot: offsets + rows of the
+            // earlier groups + rows of the group's earlier blocks - start
+            s_brow[e] += s_off[e] + s_grow[e] - start;
+            start += c;
+        }
+        __syncthreads();
+        // ---- each entry: its slot, pos, and its key in expert order -------------
+#pragma unroll
+        for (int s = 0; s < kQSteps; ++s) {
+            const int li = lo + s * 32 + int(lane);
+            if (li < nb) {
                 const int p = v[s];
+                int row = -1;
                 if (p >= 0) {
-                    const int e = p & 0xffff, r = mycnt[e] + (p >> 16);
-                    const int row = rowbase[e] + r;
-                    pos[i] = row;
-                    const int slot = loc[e] + r;
-                    s_row[slot] = row;
-                    s_w[slot] = wv[s];
-                    s_li[slot] = uint16_t(i - blk_lo);
-                } else {
-                    pos[i] = -1;
+                    const int e = p & 0xffff;
+                    const int slot = int(mycnt[e]) + (p >> 16);
+                    row = slot + s_brow[e];
+                    sorted[slot] = (uint32_t(e) << kLiBits) | uint32_t(li);
                 }
+                pos[blk_lo + li] = row;
             }
         }
         __syncthreads();
-        zero_warp_counts(cntw, E);  // the lane words are left zero by every step
-        if (b + int(gridDim.x) < nblk)
-            load_ids(b + gridDim.x);
-        for (int j = tid; j < total; j += kPThreads) {
-            const int row = s_row[j];
-            if (row < cap) {
-                srt_tok[row] = int32_t(div_k(uint32_t(blk_lo + s_li[j]), kd));
-                srt_w[row] = s_w[j];
+        for (int q = tid; q < E; q += kQThreads)  // counters for the next block
+            reinterpret_cast<uint4 *>(cntw)[q] = make_uint4(0u, 0u, 0u, 0u);
+        // ---- write-out: slot j to row j + delta, neighbouring lanes neighbouring rows
+        uint32_t key[kQSteps];
+#pragma unroll
+        for (int u = 0; u < kQSteps; ++u) {
+            const int j = u * kQThreads + tid;
+            key[u] = j < nv ? sorted[j] : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kQSteps; ++u) {
+            const int j = u * kQThreads + tid;
+            const uint32_t li = key[u] & ((1u << kLiBits) - 1u);
+            const int row = j + s_brow[key[u] >> kLiBits];
+            const float wt = s_w[li];
+            if (j < nv && row < cap) {
+                srt_tok[row] = int32_t(div_k(uint32_t(blk_lo) + li, kd));
+                srt_w[row] = wt;
             }
         }
+        __syncthreads();
+        if (OR_WALK)  // the keys' buffer holds the next walk's lane words: zero
+            for (int q = tid; q < 2 * E; q += kQThreads)
+                reinterpret_cast<uint4 *>(pm)[q] = make_uint4(0u, 0u, 0u, 0u);
+        if (next < nblk)  // every weight of this block has been read
+            copy_block_words(reinterpret_cast<uint32_t *>(s_w),
+                             w + int64_t(next) * kPlanBlockEntries, block_len(next), vec_in);
+        cp_async_commit();
     }
-    // tile table, spread over the grid
+    asm volatile("cp.async.wait_group 0;" ::: "memory");  // no copy outlives the CTA
+    if (__any_sync(kFull, bad) && lane == 0)
+        atomicOr(status, MOE_STATUS_BAD_ID);
+    // tail rows of each expert (srt_tok = -1, srt_w = +0) and the tile table,
+    // spread over the grid
+    for (int e = int(blockIdx.x) * kQThreads + tid; e < E; e += int(gridDim.x) * kQThreads)
+        for (int64_t r = int64_t(s_off[e]) + counts[e]; r < s_off[e + 1] && r < cap; ++r) {
+            srt_tok[r] = -1;
+            srt_w[r] = 0.0f;
+        }
     const int64_t R = min(int64_t(s_off[E]), cap);
     const int64_t ntiles = R / tm;
-    for (int64_t t = int64_t(blockIdx.x) * kPThreads + tid; t < ntiles;
-         t += int64_t(gridDim.x) * kPThreads) {
+    for (int64_t t = int64_t(blockIdx.x) * kQThreads + tid; t < ntiles;
+         t += int64_t(gridDim.x) * kQThreads) {
         const int64_t r = t * tm;
         int l = 0, h = E - 1;  // the last e with offsets[e] <= r
         while (l < h) {
@@ -782,15 +909,28 @@ cudaError_t launch_plan(const int32_t *ids, const float *w, int T, int k, int E,
     const int ngroups = plan_num_groups(nblk);
     int32_t *gsum = bcnt + int64_t(nblk) * E;  // [ngroups][E] after the blocks' rows
     const size_t cnt_smem = size_t(E) * sizeof(int);
-    const bool or_walk = E <= kOrWalkMaxE;
-    const void *place_fn = or_walk ? reinterpret_cast<const void *>(k_place_blocks<true>)
-                                   : reinterpret_cast<const void *>(k_place_blocks<false>);
-    // the opt-in size covers every E this instantiation takes
-    const size_t max_place_smem = or_walk ? place_smem_bytes(kOrWalkMaxE, true)
-                                          : place_smem_bytes(MOE_MAX_EXPERTS, false);
+    // the place kernel: lanes of one expert from shared-memory lane words
+    // (E <= kPlaceOrWalkMaxE) or from ballots on the id's bits
+    const bool or_walk = E <= kPlaceOrWalkMaxE;
+    const int nbits = E > 1 ? 32 - __builtin_clz(unsigned(E - 1)) : 0;
+    using PlaceFn = void (*)(const int32_t *, const float *, int64_t, DivK, int, int, int64_t,
+                             const int32_t *, const int32_t *, const int32_t *, int, int32_t *,
+                             int32_t *, float *, int32_t *, uint32_t *, bool);
+    static constexpr PlaceFn kBallot[kMaxIdBits + 1] = {
+        k_place_blocks<0, false>,  k_place_blocks<1, false>,  k_place_blocks<2, false>,
+        k_place_blocks<3, false>,  k_place_blocks<4, false>,  k_place_blocks<5, false>,
+        k_place_blocks<6, false>,  k_place_blocks<7, false>,  k_place_blocks<8, false>,
+        k_place_blocks<9, false>,  k_place_blocks<10, false>, k_place_blocks<11, false>,
+        k_place_blocks<12, false>};
+    const PlaceFn place_fn = or_walk ? k_place_blocks<0, true> : kBallot[nbits];
+    const size_t place_smem = place_smem_bytes(E);
     cudaError_t err;
     if (nblk > 0) {
-        err = ensure_smem_limit(place_fn, or_walk ? kSlotPlaceOr : kSlotPlace, max_place_smem);
+        // the opt-in size covers every E of this kernel's instantiation
+        err = or_walk ? ensure_smem_limit(reinterpret_cast<const void *>(place_fn), kSlotPlaceOr,
+                                          place_smem_bytes(kPlaceOrWalkMaxE))
+                      : ensure_smem_limit(reinterpret_cast<const void *>(place_fn),
+                                          kSlotPlaceBallot0 + nbits, place_smem_bytes(1 << nbits));
         if (err == cudaSuccess)
             err = launch_pdl(k_count, dim3(std::min(nblk, device_sm_count() * kCountCtasPerSm)),
                              dim3(kPThreads), cnt_smem, stream, ids, n, nblk, E, bcnt);
@@ -800,24 +940,25 @@ cudaError_t launch_plan(const int32_t *ids, const float *w, int T, int k, int E,
         if (err != cudaSuccess)
             return err;
     }
+    // with no entries every expert is empty: no tail rows, no tiles
     err = launch_pdl(k_scan_experts, dim3(1), dim3(kScanThreads), 0, stream, gsum, ngroups,
-                     counts, E, tm, cap, offsets, srt_tok, srt_w, tile_expert, status, nblk == 0);
+                     counts, E, tm, cap, offsets, status);
     if (err != cudaSuccess || nblk == 0)
         return err;
     int per_sm = 0;  // resident place CTAs per SM for this E (shared memory and registers)
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &per_sm, or_walk ? k_place_blocks<true> : k_place_blocks<false>, kPThreads,
-            place_smem_bytes(E, or_walk)) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, place_fn, kQThreads, place_smem) !=
+            cudaSuccess ||
         per_sm < 1) {
         cudaGetLastError();  // a failed query is not the caller's error
         per_sm = 1;
     }
     const int pgrid = std::min(nblk, device_sm_count() * per_sm);
-    return launch_pdl(or_walk ? k_place_blocks<true> : k_place_blocks<false>, dim3(pgrid),
-                      dim3(kPThreads), place_smem_bytes(E, or_walk), stream, ids, w, n,
+    const bool vec_in =
+        ((reinterpret_cast<uintptr_t>(ids) | reinterpret_cast<uintptr_t>(w)) & 15) == 0;
+    return launch_pdl(place_fn, dim3(pgrid), dim3(kQThreads), place_smem, stream, ids, w, n,
                       make_divk(uint32_t(k)), E, tm, cap, static_cast<const int32_t *>(offsets),
-                      static_cast<const int32_t *>(bcnt), nblk, pos, srt_tok, srt_w,
-                      tile_expert, status);
+                      static_cast<const int32_t *>(counts), static_cast<const int32_t *>(bcnt),
+                      nblk, pos, srt_tok, srt_w, tile_expert, status, vec_in);
 }
 
 }  // namespace moe

@@ -198,7 +198,8 @@ def test_plan_column_scan_group_boundaries(n_entries):
     # the column scan prefixes block counts inside groups of 256 blocks of
     # 4096 entries and the expert scan adds the groups' totals: exactly one
     # full group, one full group plus a ragged block, two full groups
-    # (k = 4, E = 1000: the shared-memory OR walk; E = 2000: the ballot walk)
+    # (k = 4; E = 1000 and 2000: the place kernel finds the lanes of one
+    # expert from ballots on two and three groups of id bits)
     k = 4
     T = n_entries // k
     for E in (1000, 2000):
@@ -212,10 +213,11 @@ def test_plan_column_scan_group_boundaries(n_entries):
 @pytest.mark.parametrize("E", [1024, 1025])
 @pytest.mark.parametrize("T", [1000, 20000])
 def test_plan_walk_switch(E, T):
-    # up to 1024 experts the lanes of one expert are found through per-warp
-    # words in shared memory, above that by ballots (multi-kernel plan) or
-    # __match_any_sync (one-launch plan); T = 1000 runs the one-launch plan,
-    # T = 20000 the multi-kernel plan (k = 8)
+    # up to 1024 experts the one-launch plan finds the lanes of one expert
+    # through per-warp words in shared memory, above that by
+    # __match_any_sync; the multi-kernel plan uses the words up to 512
+    # experts and ballots on groups of 5 id bits above; T = 1000 runs the
+    # one-launch plan, T = 20000 the multi-kernel plan (k = 8)
     rng = np.random.default_rng(E * 7 + T)
     ids = rng.integers(0, E, size=(T, 8), dtype=np.int32)
     ids[:, 0] = E - 1  # the largest id in every token
@@ -227,10 +229,59 @@ def test_plan_walk_switch(E, T):
 @pytest.mark.parametrize("T,k,E", [(30001, 3, 700), (12000, 7, 300), (2000, 37, 1500), (300, 255, 512)])
 def test_plan_multi_kernel_odd_k(T, k, E):
     # above the one-launch size with k not a power of two: the token index
-    # of each row is the flat index divided by k (by a multiply-high), the
-    # walk runs on shared-memory lane words (E <= 1024) or ballots (E = 1500)
+    # of each row is the flat index divided by k (by a multiply-high); the
+    # lanes of one expert come from shared-memory words (E <= 512) or from
+    # ballots on two (E <= 1024) or three groups of id bits (E = 1500)
     rng = np.random.default_rng(T + 97 * k)
     ids = rng.integers(0, E, size=(T, k), dtype=np.int32)
     ids[rng.random(ids.shape) < 0.03] = -1
     w = rng.standard_normal((T, k)).astype(np.float32)
     check(ids, w, E, 16)
+
+
+@pytest.mark.parametrize("E", [1, 2, 31, 32, 33, 512, 513, 1024, 1025, 4096])
+def test_plan_multi_kernel_expert_counts(E):
+    # above the one-launch size the place kernel finds the lanes of one
+    # expert in a 32-entry step from per-warp words in shared memory (E <=
+    # 512) or from one ballot per id bit, combined in groups of 5 bits (one
+    # group up to 32 experts, two up to 1024, three above): both sides of
+    # each switch, one expert, and the largest expert count (20001 x 4
+    # entries, the last block ragged, skipped slots)
+    T, k = 20001, 4
+    rng = np.random.default_rng(E + 11)
+    ids = rng.integers(0, E, size=(T, k), dtype=np.int32)
+    ids[rng.random(ids.shape) < 0.03] = -1
+    ids[7, :] = E - 1
+    w = rng.standard_normal((T, k)).astype(np.float32)
+    check(ids, w, E, 16)
+
+
+def test_plan_multi_kernel_unaligned_buffers():
+    # ids, w and pos starting 4 bytes past a 16-byte boundary: the place
+    # kernel then copies ids and weights into shared memory 4 bytes at a time
+    T, k, E, tm = 30001, 3, 500, 16
+    rng = np.random.default_rng(21)
+    ids = rng.integers(0, E, size=(T, k), dtype=np.int32)
+    ids[rng.random(ids.shape) < 0.02] = -1
+    w = rng.standard_normal((T, k)).astype(np.float32)
+    n = T * k
+    ids_buf = torch.zeros(n + 4, dtype=torch.int32, device="cuda")
+    w_buf = torch.zeros(n + 4, dtype=torch.float32, device="cuda")
+    pos_buf = torch.full((n + 4,), int(POISON_I), dtype=torch.int32, device="cuda")
+    ids_d = ids_buf[1:n + 1].view(T, k)
+    w_d = w_buf[1:n + 1].view(T, k)
+    ids_d.copy_(torch.from_numpy(ids))
+    w_d.copy_(torch.from_numpy(w))
+    pos_d = pos_buf[1:n + 1].view(T, k)
+    assert ids_d.data_ptr() % 16 == 4 and pos_d.data_ptr() % 16 == 4
+    cap = B.capacity(T, k, E, tm)
+    o = B.plan(ids_d, w_d, E, tm, cap=cap, out={"pos": pos_d})
+    assert B.read_status(o["ws"]) == 0
+    ref = oracle.plan(ids, w, E, tm)
+    R = ref["R_pad"]
+    assert o["offsets"].cpu().tolist() == ref["offsets"].tolist()
+    assert np.array_equal(o["srt_tok"][:R].cpu().numpy(), ref["srt_tok"])
+    assert np.array_equal(o["srt_w"][:R].cpu().numpy().view(np.uint32), ref["srt_w"].view(np.uint32))
+    assert np.array_equal(pos_d.cpu().numpy(), ref["pos"])
+    assert int(pos_buf[0]) == int(POISON_I) and int(pos_buf[n + 1]) == int(POISON_I)
+    assert np.array_equal(o["tile_expert"][:R // tm].cpu().numpy(), ref["tile_expert"])
