@@ -21,7 +21,8 @@ entries (plan_sweep), the plan + gather configuration with fp16 rows
 ``--impl reference`` times the CPU oracle itself (the only reference this
 method has) on bounded samples of the same workload.
 
-Multi-GPU (torchrun): every rank runs its own independent layer on its own
+Multi-GPU (torchrun, or ``--gpus N`` alone, which starts the N ranks through
+torchrun on this node): every rank runs its own independent layer on its own
 chunk of tokens (weak scaling, no collective on the data path); rank 0
 prints the line with the max time over ranks.
 """
@@ -566,6 +567,21 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def relaunch_ranks(n: int) -> int:
+    """Runs this same command as n ranks under torch.distributed.run on this
+    node and returns its exit code (rank 0 prints the line)."""
+    import socket
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node",
+           str(n), "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.abspath(__file__), *sys.argv[1:]]
+    log(f"starting {n} ranks: {' '.join(cmd)}")
+    return subprocess.run(cmd).returncode
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -592,7 +608,15 @@ def main():
         ap.error("--warmup must be >= 3")
     if not W.workload(args.workload).ffn:
         ap.error("that workload has no expert FFN (plan + gather only)")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # N ranks were asked for without a launcher: start them, one process
+        # per GPU, through torchrun on this node (rendezvous on 127.0.0.1)
+        sys.exit(relaunch_ranks(args.gpus))
     rank, world, local = replicas.init_from_env(backend="nccl" if args.impl == "native" else "gloo")
+    if world != args.gpus:
+        ap.error(f"--gpus {args.gpus} but the launcher started {world} ranks")
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)

@@ -158,15 +158,19 @@ MOE_API int moe_plan(const int32_t *ids, const float *w, int T, int k, int E, in
  *
  * Arguments are those of moe_plan, without ws / ws_bytes and with
  *   status   uint32* device word that receives the MOE_STATUS_* bits of this
- *            call (reset by the call), or NULL to leave them in the library.
+ *            call (reset by the call), or NULL to leave them in a word inside
+ *            the library's array, which the caller cannot read: pass a word
+ *            whenever a bad id or an overflow must be detected.
  * Limit: (B + ceil(B / 256)) x E <= MOE_PLAN_NOALLOC_MAX_COUNTS with
  * B = ceil(T*k / 4096) (one row of E counts per block of 4096 entries and
  * one per group of 256 blocks): T*k up to 2M entries with E = 512, up to
  * 262144 with E = 4096.  Larger sizes return MOE_ERR_WORKSPACE.
  *
  * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any
- * stream capture.  Every call on a device shares the same array and leaves
+ * device, with that device current) and keeps it for the life of the
+ * process; make that first call before any stream capture, and do not use
+ * this entry point after a cudaDeviceReset of that device (the array may
+ * then sit at another address).  Every call on a device shares the same array and leaves
  * its contents behind; nothing in it has to start at zero (every count the
  * kernels read is written first by the same call), but calls that overlap on
  * the GPU (on different streams without ordering) race on it and must not

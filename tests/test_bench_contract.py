@@ -43,3 +43,16 @@ def test_reference_arm_two_ranks_prints_once():
     assert r.returncode == 0, r.stderr[-2000:]
     lines = _json_lines(r.stdout)
     assert len(lines) == 1 and lines[0]["n_gpus"] == 2
+
+
+def test_gpus_flag_without_launcher_starts_that_many_ranks():
+    # --gpus 2 without torchrun: bench.py starts the two ranks itself and
+    # rank 0 alone prints, with n_gpus = 2 (never a silent single rank)
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "1",
+                        "--gpus", "2", "--steps", "1", "--warmup", "3"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600,
+                       env={k: v for k, v in os.environ.items()
+                            if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")})
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1 and lines[0]["n_gpus"] == 2 and lines[0]["impl"] == "reference"

@@ -168,3 +168,34 @@ def test_ffn_wait_limit_stops_cleanly_and_reports():
     assert int(status.item()) & B.STATUS_TIMEOUT
     assert 1.0 < elapsed < 60.0
     run_case(inp, wl.E, wl.d, wl.f, wl.tm, Wg, Wu, Wd)
+
+
+@pytest.mark.parametrize("T,d,E,k,f,tm", [
+    (100, 192, 5, 3, 192, 16),   # ragged M tiles on both GEMMs (192 = 128 + 64)
+    (300, 128, 2, 1, 256, 32),   # experts over 128 rows
+    (257, 256, 6, 4, 704, 16),   # f = 5.5 x 128
+])
+def test_expert_ffn_entry_point(T, d, E, k, f, tm):
+    # moe_expert_ffn (gate/up and down in one call, H kept in the caller's
+    # buffer) through the C ABI: H against the oracle's fp64 h, Ys against
+    # the oracle's fp64 job output w * (h Wd), on every real row; pad rows 0
+    inp = W.make_layer(T, d, E, k, f, tm=tm, seed=7 * T + f, skip_frac=0.1)
+    p, xs, real, row_e = staged_inputs(inp, E, tm)
+    cap = B.capacity(T, k, E, tm)
+    Wg, Wu, Wd = (dev16(inp[n]) for n in ("Wg", "Wu", "Wd"))
+    H0 = torch.full((cap, f), -7.0, dtype=torch.bfloat16, device="cuda")
+    Y0 = torch.full((cap, d), -7.0, dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    H, Ys = B.expert_ffn(dev16(to_cap(xs, cap)), Wg, Wu, Wd, dev(p["offsets"]),
+                         dev(to_cap(p["srt_w"], cap)), cap, H=H0, Ys=Y0, status=status)
+    torch.cuda.synchronize()
+    assert H.data_ptr() == H0.data_ptr() and Ys.data_ptr() == Y0.data_ptr()
+    assert int(status.item()) == 0
+    h_ref, ys_ref = oracle.expert_rows(xs, real, row_e[real], p["srt_w"][real], *inputs_host(inp))
+    Hh, Yh = host16(H), host16(Ys)
+    ok, err, bound = layer_tolerance(W.bits_to_float(Hh[real], "bf16").astype(np.float64), h_ref)
+    assert ok, f"H: max err {err} > {bound}"
+    ok, err, bound = layer_tolerance(W.bits_to_float(Yh[real], "bf16").astype(np.float64), ys_ref)
+    assert ok, f"Ys: max err {err} > {bound}"
+    pad = np.nonzero(p["srt_tok"] < 0)[0]
+    assert len(pad) > 0 and np.all(Hh[pad] == 0) and np.all((Yh[pad] & 0x7FFF) == 0)

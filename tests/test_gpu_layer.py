@@ -1,8 +1,9 @@
 """moe_layer_forward (plan -> gather -> gate/up -> down -> combine in one call)
 vs the oracle: max|y - ref| <= 1e-2 * max|ref| + 1e-3, bf16 operands with
-fp32 accumulation.  Full outputs on small shapes; at the workloads' full sizes,
-in the same launch configuration the benchmark times, sampled tokens that
-the oracle computes one by one.  The plan and the gathered rows left in the
+fp32 accumulation.  Full outputs on small shapes and on the full-size
+layers (the first chunk of the long prompt included), in the same launch
+configuration the benchmark times; on the other long-prompt chunks, sampled
+tokens that the oracle computes one by one.  The plan and the gathered rows left in the
 workspace are also checked bit for bit."""
 import numpy as np
 import pytest
@@ -82,10 +83,29 @@ def test_layer_shapes_full_output(T, d, E, k, f, tm, skip):
     check_workspace_plan(ws, inp, E, d, f, tm)
 
 
-@pytest.mark.parametrize("cfg,chunk", [(3, 0), (4, 0), (5, 0), (5, 5)])
-def test_layer_workloads_sampled_tokens(cfg, chunk):
+@pytest.mark.parametrize("cfg,chunk", [(3, 0), (4, 0), (5, 0)])
+def test_layer_workloads_full_output(cfg, chunk):
+    # every token of the full-size layers (the full page-1-scale layer, the
+    # 256-expert layer, the first chunk of the long prompt), in the launch
+    # configuration the benchmark times, against the oracle run on all tokens
     wl = W.workload(cfg)
-    inp = dict(inputs(cfg)) if chunk == 0 else W.make_inputs(cfg, chunk=chunk, weights=False)
+    inp = inputs(cfg)
+    y, ws = run_layer(inp, *dev_weights(cfg), wl.tm)
+    ref = oracle.layer(inp["x"], inp["ids"], inp["w"], inp["Wg"], inp["Wu"], inp["Wd"])
+    got = host_f(y)
+    assert got.shape == ref.shape == (wl.T, wl.d)
+    ok, err, bound = layer_tolerance(got, ref)
+    assert ok, (err, bound)
+    assert B.read_status(ws) == 0
+    print(f"cfg {cfg} chunk {chunk}: all {wl.T} tokens, max err {err:.3e} (bound {bound:.3e}), "
+          f"rel-L2 {rel_l2(got, ref):.3e}")
+
+
+@pytest.mark.parametrize("cfg,chunk", [(5, 5)])
+def test_layer_workloads_sampled_tokens(cfg, chunk):
+    # the other chunks of the long prompt: tokens the oracle computes one by one
+    wl = W.workload(cfg)
+    inp = W.make_inputs(cfg, chunk=chunk, weights=False)
     host_w = inputs(cfg)
     y, ws = run_layer(inp, *dev_weights(cfg), wl.tm)
     toks = sample_tokens(inp["ids"], 40, seed=cfg)
