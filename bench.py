@@ -14,9 +14,14 @@ Printed: ONE JSON line with rows/s (T*k routed rows per layer), the plan's
 microseconds per layer, per-stage times, the roofline of the dominant kernel
 (the gate/up GEMM), the end-to-end rows/s through host buffers, SM clocks
 sampled during the timed region, and the CPU oracle timed on a bounded
-sample on this host's cores.  Beside them: the plan alone on 1M and 10M
-entries (plan_sweep), the plan + gather configuration with fp16 rows
-(plan_gather), and the same layer on 8-bit operands (fp8_layer).
+sample on this host's cores, and how far the layer lands from the oracle
+(accuracy_vs_oracle).  Beside them: the plan alone on 1M and 10M entries
+(plan_sweep), the plan + gather configuration with fp16 rows (plan_gather),
+the same layer on 8-bit operands (fp8_layer, with its own error against the
+fp64 oracle), and every other layer workload timed the same way (workloads:
+the tiny layer, the 256-expert layer, and the long prompt as its 8 chunks of
+4096 tokens per step), each with per-stage times, its gate/up roofline and
+the oracle on this host's cores.
 
 ``--impl reference`` times the CPU oracle itself (the only reference this
 method has) on bounded samples of the same workload.
@@ -186,7 +191,7 @@ def d16(a, dev):
 
 # ---- CPU oracle timing ----------------------------------------------------------
 
-def oracle_sample(inp, wl, budget_s, nthreads):
+def oracle_sample(inp, wl, budget_s, nthreads, with_output=False):
     """Times the oracle on a bounded sample of the workload: the full plan
     (single-threaded by definition) and the layer for the first n tokens,
     n chosen to take about budget_s.  Returns rows/s and a description."""
@@ -203,13 +208,29 @@ def oracle_sample(inp, wl, budget_s, nthreads):
     n = int(max(len(pilot), min(wl.T, budget_s / max(per_tok, 1e-9))))
     toks = np.arange(n, dtype=np.int32)
     t = time.perf_counter()
-    oracle.layer(*args, x_dtype=wl.x_dtype, tokens=toks, nthreads=nthreads)
+    y_ref = oracle.layer(*args, x_dtype=wl.x_dtype, tokens=toks, nthreads=nthreads)
     t_layer = time.perf_counter() - t
     secs = t_layer + t_plan * n / wl.T
     rows = n * wl.k
-    return rows / secs, secs, f"plan of all {wl.T * wl.k} rows (1 thread) + fp64 FFN/combine of " \
-                              f"the first {n} tokens ({rows} rows) on {nthreads} threads; " \
-                              f"plan time prorated per row"
+    if with_output:
+        return rows / secs, secs, _sample_desc(wl, n, rows, nthreads), toks, y_ref
+    return rows / secs, secs, _sample_desc(wl, n, rows, nthreads)
+
+
+def _sample_desc(wl, n, rows, nthreads):
+    return (f"plan of all {wl.T * wl.k} rows (1 thread) + fp64 FFN/combine of the first {n} "
+            f"tokens ({rows} rows) on {nthreads} threads; plan time prorated per row")
+
+
+def error_vs_oracle(y_dev, toks, y_ref):
+    """max |y - oracle| and rel-L2 on the oracle's tokens, with the layer bound
+    1e-2 * max|oracle| + 1e-3."""
+    y = y_dev.float().cpu().numpy().astype(np.float64)[toks]
+    err = float(np.max(np.abs(y - y_ref)))
+    nrm = float(np.linalg.norm(y_ref))
+    return {"tokens": int(len(toks)), "max_abs_err": err,
+            "rel_l2": float(np.linalg.norm(y - y_ref)) / nrm if nrm > 0 else 0.0,
+            "bound": 1e-2 * float(np.max(np.abs(y_ref))) + 1e-3}
 
 
 # ---- native arm ------------------------------------------------------------------
@@ -375,6 +396,7 @@ def run_native(args, rank, world, local):
             raise RuntimeError("device status set in the E4M3 layer")
         ms8 = timed(lambda: layer8.forward(x, ids, w, y=y), args.steps)
         total8 = replicas.max_over_ranks(sum(ms8), world, dev)
+        y8 = layer8.forward(x, ids, w).clone()
         alg8 = algorithmic(wl, inp["ids"], wbytes=1, abytes=1)
         fp8 = {"value": args.steps * rows * world / (total8 / 1e3), "unit": "rows/s",
                "ms_per_step": statistics.mean(ms8), "steps": args.steps,
@@ -528,10 +550,128 @@ def run_native(args, rank, world, local):
     if world == 1 and not args.no_cpu_baseline and not e4m3:
         nth = os.cpu_count() or 1
         log("timing the CPU oracle on a bounded sample ...")
-        v, secs, desc = oracle_sample(inp, wl, args.cpu_budget, nth)
+        v, secs, desc, toks, y_ref = oracle_sample(inp, wl, args.cpu_budget, nth, with_output=True)
         line["cpu_baseline"] = {"value": v, "unit": "rows/s", "cores": nth, "kind": "oracle",
                                 "sample": desc, "seconds": secs}
+        # how far each arithmetic lands from the fp64 oracle (bf16 weights) on
+        # the oracle's tokens: the bf16 layer and, beside it, the 8-bit one
+        y16 = layer.forward(x, ids, w)
+        line["accuracy_vs_oracle"] = {"bf16_layer": error_vs_oracle(y16, toks, y_ref)}
+        if fp8 is not None:
+            fp8["accuracy_vs_oracle"] = error_vs_oracle(y8, toks, y_ref)
+            line["accuracy_vs_oracle"]["fp8_layer"] = fp8["accuracy_vs_oracle"]
+    if world == 1 and not args.no_workloads and not e4m3:
+        line["workloads"] = other_workloads(args, dev, flush, stream)
     print(json.dumps(line), flush=True)
+
+
+# ---- the other layer workloads ------------------------------------------------------
+
+def other_workloads(args, dev, flush, stream):
+    """Every other layer workload, each timed like the headline: the tiny
+    layer, the 256-expert layer and the long prompt (its 8 chunks of 4096
+    tokens per step).  Per workload: routed rows/s, per-stage times, the
+    gate/up kernel's roofline and the oracle on this host's cores."""
+    out = {}
+    hbm, tflops, peak_src = peaks()
+    for idx in (1, 4, 5):
+        wl = W.workload(idx)
+        log(f"workload {wl.name} ...")
+        chunks = [W.make_inputs(wl, seed=0, chunk=c, weights=(c == 0)) for c in range(wl.n_chunks)]
+        inp = chunks[0]
+        Wg, Wu, Wd = (d16(inp[n], dev) for n in ("Wg", "Wu", "Wd"))
+        layer = B.MoeLayer(Wg, Wu, Wd, tm=wl.tm)
+        xs_d = [d16(c["x"], dev) for c in chunks]
+        ids_d = [torch.from_numpy(c["ids"]).to(dev) for c in chunks]
+        w_d = [torch.from_numpy(c["w"]).to(dev) for c in chunks]
+        y = torch.empty((wl.T, wl.d), dtype=torch.bfloat16, device=dev)
+
+        def step():
+            for c in range(wl.n_chunks):
+                layer.forward(xs_d[c], ids_d[c], w_d[c], y=y)
+
+        for i in range(args.warmup):
+            flush.fill_(i & 0xFF)
+            step()
+        torch.cuda.synchronize(dev)
+        if B.read_status(layer._ws) != 0:
+            raise RuntimeError(f"device status set in workload {wl.name}")
+        K = max(3, args.steps)
+        ms = []
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_ev.record(stream)
+            step()
+            b_ev.record(stream)
+            ms.append((a_ev, b_ev))
+        torch.cuda.synchronize(dev)
+        ms = [a_ev.elapsed_time(b_ev) for a_ev, b_ev in ms]
+        rows = wl.T * wl.k * wl.n_chunks
+        # stages of chunk 0, each through its own entry point, L2 flushed first
+        cap = B.capacity(wl.T, wl.k, wl.E, wl.tm)
+        x0, i0, w0 = xs_d[0], ids_d[0], w_d[0]
+        o = B.plan(i0, w0, wl.E, wl.tm, cap=cap)
+        xs = B.gather(x0, o["srt_tok"], o["offsets"], wl.E, cap)
+        H = torch.empty((cap, wl.f), dtype=torch.bfloat16, device=dev)
+        Ys = torch.empty((cap, wl.d), dtype=torch.bfloat16, device=dev)
+        stages = ("plan", "gather", "gate_up", "down", "combine")
+        calls = (lambda: B.plan(i0, w0, wl.E, wl.tm, cap=cap, out=o),
+                 lambda: B.gather(x0, o["srt_tok"], o["offsets"], wl.E, cap, xs=xs),
+                 lambda: B.ffn_gate_up(xs, Wg, Wu, o["offsets"], cap, H=H),
+                 lambda: B.ffn_down(H, Wd, o["offsets"], o["srt_w"], cap, Ys=Ys),
+                 lambda: B.combine(Ys, o["pos"], y=y))
+        per = {st: [] for st in stages}
+        for i in range(min(K, 50) + 3):
+            flush.fill_(i & 0xFF)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+            ev[0].record(stream)
+            for j, c in enumerate(calls):
+                c()
+                ev[j + 1].record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= 3:
+                for j, st in enumerate(stages):
+                    per[st].append(ev[j].elapsed_time(ev[j + 1]) * 1e3)
+        stage_us = {st: statistics.median(v) for st, v in per.items()}
+        alg = algorithmic(wl, inp["ids"])
+        t_gu = statistics.mean(per["gate_up"]) * 1e-6
+        tensor_bound = alg["gate_up_flops"] / (tflops * 1e12) > alg["gate_up"] / (hbm * 1e9)
+        if tensor_bound:
+            achieved, peak, unit = alg["gate_up_flops"] / t_gu / 1e12, tflops, "TFLOP/s"
+        else:
+            achieved, peak, unit = alg["gate_up"] / t_gu / 1e9, hbm, "GB/s"
+        entry = {
+            "workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k, "f": wl.f,
+            "tm": wl.tm, "routing": ROUTING[wl.routing], "chunks_per_step": wl.n_chunks,
+            "value": K * rows / (sum(ms) / 1e3), "unit": "rows/s",
+            "ms_per_step": statistics.mean(ms), "steps": K,
+            "active_experts_chunk0": alg["active"], "R_pad_chunk0": alg["R_pad"],
+            "stages_us_chunk0": stage_us,
+            "layer_hbm_gbs_chunk0": alg["layer"] / (statistics.mean(ms) / wl.n_chunks / 1e3) / 1e9,
+            "roofline": {"kernel": "k_ffn<gate/up> (tcgen05 grouped GEMM + SwiGLU), chunk 0",
+                         "bound": "tensor" if tensor_bound else "hbm", "achieved": achieved,
+                         "peak": peak, "unit": unit, "frac": achieved / peak,
+                         "peak_source": peak_src,
+                         "algorithmic_bytes_per_launch": alg["gate_up"],
+                         "algorithmic_flops_per_launch": alg["gate_up_flops"],
+                         "tensor_floor_us": alg["gate_up_flops"] / (tflops * 1e12) * 1e6,
+                         "hbm_floor_us": alg["gate_up"] / (hbm * 1e9) * 1e6},
+            "l2": "flushed before every timed step (256 MiB write)",
+            "gpu_launches": KERNELS_PER_LAYER * wl.n_chunks * K,
+        }
+        if not args.no_cpu_baseline:
+            nth = os.cpu_count() or 1
+            v, secs, desc, toks, y_ref = oracle_sample(inp, wl, args.workload_cpu_budget, nth,
+                                                       with_output=True)
+            entry["cpu_baseline"] = {"value": v, "unit": "rows/s", "cores": nth,
+                                     "kind": "oracle", "sample": "chunk 0: " + desc,
+                                     "seconds": secs}
+            entry["accuracy_vs_oracle"] = error_vs_oracle(layer.forward(x0, i0, w0), toks, y_ref)
+        out[str(idx)] = entry
+        del layer, Wg, Wu, Wd, xs_d, ids_d, w_d, y, o, xs, H, Ys, chunks, inp
+        torch.cuda.empty_cache()
+    return out
 
 
 # ---- reference arm: the CPU oracle ------------------------------------------------
@@ -599,6 +739,10 @@ def main():
                     help="skip the plan + gather configuration (T=2048, E=512, fp16 rows)")
     ap.add_argument("--no-fp8", action="store_true",
                     help="skip the E4M3 layer measured beside the bf16 one")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other layer workloads (tiny, 256-expert, long prompt)")
+    ap.add_argument("--workload-cpu-budget", type=float, default=6.0,
+                    help="seconds of oracle work for each other workload's cpu_baseline")
     ap.add_argument("--weights", choices=("bf16", "e4m3", "f8"), default="bf16",
                     help="expert weights: bf16 (the default measurement), E4M3 codes with "
                          "per-feature scales (bf16 activations), or f8: E4M3 weights and E4M3 "
