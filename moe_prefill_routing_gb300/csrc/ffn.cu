@@ -70,11 +70,9 @@ constexpr int BM = 128;                           // MMA M: output features per 
 constexpr int BK = 64;                            // K per stage: 64 bf16 = one 128-byte row
 constexpr int BN = 128;                           // max rows per unit (MMA N)
 constexpr int UMMA_K = 16;                        // K of one kind::f16 MMA
-constexpr int kBoxRows = 16;                      // rows per activation TMA box
 constexpr uint32_t kABoxBytes = 64 * BK * 2;      // 64 features x 64 K rows
 constexpr uint32_t kATileBytes = 2 * kABoxBytes;  // 128 features
 constexpr uint32_t kBTileBytes = BN * BK * 2;     // 128 rows x 64 K
-constexpr uint32_t kBBoxBytes = kBoxRows * BK * 2;
 constexpr int kThreads = 192;      // producer, MMA, four epilogue warps
 constexpr int kConvThreads = 256;  // eight warps widening E4M3 tiles (W8)
 constexpr int kThreadsW8 = kThreads + kConvThreads;
@@ -100,6 +98,18 @@ constexpr int kConvSlots = 2;
 constexpr uint32_t kConvSlotBytes = 2 * kATileBytes;
 
 enum WeightMode : int { kBf16 = 0, kWiden = 1, kNative = 2 };
+
+// Tensor maps of the B rows: boxes of 128, 64, 32 and 16 rows (h[i] holds
+// 128 >> i rows).  A unit's rows arrive in ONE copy per stage, of the
+// smallest box that holds them (at most twice the rows): measured, the
+// number of TMA copies per stage, not their bytes, bounded the ring's intake
+// (eight 16-row boxes per stage: long-prompt gate/up 390 us; one 128-row
+// box: 289 us; exact boxes of 128/64/32/16 rows, up to four: 304 us).
+// With gathered rows (tma_gather4) h[0] is the token-row map.
+constexpr int kRowMaps = 4;
+struct RowMaps {
+    CUtensorMap h[kRowMaps];
+};
 
 template <int WM>
 struct Cfg {
@@ -281,7 +291,7 @@ __device__ __forceinline__ void widen_e4m3x16(const uint4 v, uint4 &lo, uint4 &h
 template <bool GATED, bool GATHER, int WM>
 __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
     k_ffn(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
-          const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_out,
+          const __grid_constant__ RowMaps map_b, const __grid_constant__ CUtensorMap map_out,
           const FfnArgs p)
 {
     constexpr bool W8 = WM == kWiden, A8 = WM == kNative, SCALED = WM != kBf16;
@@ -325,7 +335,8 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
         prefetch_tmap(&map_a0);
         if (GATED)
             prefetch_tmap(&map_a1);
-        prefetch_tmap(&map_b);
+        for (int i = 0; i < (GATHER ? 1 : kRowMaps); ++i)
+            prefetch_tmap(&map_b.h[i]);
         prefetch_tmap(&map_out);
     }
     if (warp == 1) {
@@ -376,7 +387,11 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                     W8 ? (1u + uint32_t(tile_base(m0, 1) < p.M)) * kA8TileBytes
                     : A8 ? (1u + uint32_t(tile_base(m0, 1) < p.M)) * kATileBytes  // 128 x 128 codes
                          : boxes * kABoxBytes;
-                const uint32_t bytes = a_bytes + uint32_t(w.nrows) * uint32_t(BK * 2);
+                // B: one copy of the smallest 16/32/64/128-row box holding the
+                // unit's rows (128-byte rows in every mode)
+                const int box_i = w.nrows > BN / 2 ? 0 : w.nrows > BN / 4 ? 1 : w.nrows > BN / 8 ? 2 : 3;
+                const uint32_t b_rows = GATHER ? uint32_t(w.nrows) : uint32_t(BN >> box_i);
+                const uint32_t bytes = a_bytes + b_rows * uint32_t(BK * 2);
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag)) {
                         ok = false;
@@ -412,12 +427,13 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                     uint8_t *sb = sa + (W8 ? 2 * kA8TileBytes : 2 * kATileBytes);
                     if (GATHER) {
                         for (int j = 0; j < w.nrows; j += 4)
-                            tma_gather4(sb + j * (BK * 2), &map_b, fb, k0, row_tok[j],
+                            tma_gather4(sb + j * (BK * 2), &map_b.h[0], fb, k0, row_tok[j],
                                         row_tok[j + 1], row_tok[j + 2], row_tok[j + 3]);
                     } else {
-                        for (int j = 0; j < w.nrows / kBoxRows; ++j)
-                            tma_load_2d(sb + j * kBBoxBytes, &map_b, fb, k0,
-                                        w.row0 + j * kBoxRows);
+                        // the unit's rows in one box of 16, 32, 64 or 128 rows, the
+                        // smallest that holds them; rows past the unit (the next
+                        // expert's, or zero past cap) are loaded and not used
+                        tma_load_2d(sb, &map_b.h[box_i], fb, k0, w.row0);
                     }
                     issued |= 1u << stage;
                     issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -817,27 +833,39 @@ cudaError_t weight_map_e4m3_kmajor(CUtensorMap *m, const void *Wq, int E, int K,
     return encode_bf16(m, Wq, 3, dims, strides, box, false, true);
 }
 
-// E4M3 rows [cap, K] (K contiguous): boxes of 16 rows x 128 K codes.
-cudaError_t rows_map_e4m3(CUtensorMap *m, const void *X, int64_t cap, int K)
+// E4M3 rows [cap, K] (K contiguous): boxes of 128, 64, 32, 16 rows x 128 K codes.
+cudaError_t rows_map_e4m3(RowMaps *m, const void *X, int64_t cap, int K)
 {
     const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(cap)};
     const cuuint64_t strides[1] = {cuuint64_t(K)};
-    const cuuint32_t box[2] = {128, kBoxRows};
-    return encode_bf16(m, X, 2, dims, strides, box, false, true);
+    for (int i = 0; i < kRowMaps; ++i) {
+        const cuuint32_t box[2] = {128, cuuint32_t(BN >> i)};
+        const cudaError_t e = encode_bf16(&m->h[i], X, 2, dims, strides, box, false, true);
+        if (e != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
 }
 
-// Rows [cap, K] (K contiguous): boxes of 16 rows x 64 K.
-cudaError_t rows_map(CUtensorMap *m, const void *X, int64_t cap, int K)
+// Rows [cap, K] (K contiguous): boxes of 128, 64, 32, 16 rows x 64 K.
+cudaError_t rows_map(RowMaps *m, const void *X, int64_t cap, int K)
 {
     const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(cap)};
     const cuuint64_t strides[1] = {cuuint64_t(K) * 2};
-    const cuuint32_t box[2] = {BK, kBoxRows};
-    return encode_bf16(m, X, 2, dims, strides, box);
+    for (int i = 0; i < kRowMaps; ++i) {
+        const cuuint32_t box[2] = {BK, cuuint32_t(BN >> i)};
+        const cudaError_t e = encode_bf16(&m->h[i], X, 2, dims, strides, box);
+        if (e != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
 }
 
-// Token rows [T, K] read four at a time by index: one-row boxes of 64 K.
-cudaError_t token_rows_map(CUtensorMap *m, const void *X, int T, int K)
+// Token rows [T, K] read four at a time by index: one-row boxes of 64 K
+// (in h[0]; the other maps are unused).
+cudaError_t token_rows_map(RowMaps *rm, const void *X, int T, int K)
 {
+    CUtensorMap *m = &rm->h[0];
     const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(T)};
     const cuuint64_t strides[1] = {cuuint64_t(K) * 2};
     const cuuint32_t box[2] = {BK, 1};
@@ -860,7 +888,8 @@ cudaError_t launch_ffn_gate_up(const void *xs, const void *Wg, const void *Wu,
                                const int32_t *offsets, int E, int d, int f, int64_t cap,
                                void *H, uint32_t *status, cudaStream_t stream, int stall_cta)
 {
-    CUtensorMap mg, mu, mx, mo;
+    CUtensorMap mg, mu, mo;
+    RowMaps mx;
     cudaError_t err;
     if ((err = weight_map(&mg, Wg, E, d, f)) != cudaSuccess ||
         (err = weight_map(&mu, Wu, E, d, f)) != cudaSuccess ||
@@ -882,7 +911,8 @@ cudaError_t launch_ffn_gate_up_rows(const void *x, int T, const int32_t *srt_tok
                                     const void *Wu, const int32_t *offsets, int E, int d, int f,
                                     int64_t cap, void *H, uint32_t *status, cudaStream_t stream)
 {
-    CUtensorMap mg, mu, mx, mo;
+    CUtensorMap mg, mu, mo;
+    RowMaps mx;
     cudaError_t err;
     if ((err = weight_map(&mg, Wg, E, d, f)) != cudaSuccess ||
         (err = weight_map(&mu, Wu, E, d, f)) != cudaSuccess ||
@@ -904,7 +934,8 @@ cudaError_t launch_ffn_down(const void *H, const void *Wd, const int32_t *offset
                             const float *srt_w, int E, int d, int f, int64_t cap, void *Ys,
                             uint32_t *status, cudaStream_t stream)
 {
-    CUtensorMap mw, mh, mo;
+    CUtensorMap mw, mo;
+    RowMaps mh;
     cudaError_t err;
     if ((err = weight_map(&mw, Wd, E, f, d)) != cudaSuccess ||
         (err = rows_map(&mh, H, cap, f)) != cudaSuccess ||
@@ -926,7 +957,8 @@ cudaError_t launch_ffn_gate_up_e4m3(const void *xs, const uint8_t *Wg, const flo
                                     int E, int d, int f, int64_t cap, void *H, uint32_t *status,
                                     cudaStream_t stream)
 {
-    CUtensorMap mg, mu, mx, mo;
+    CUtensorMap mg, mu, mo;
+    RowMaps mx;
     cudaError_t err;
     if ((err = weight_map_e4m3(&mg, Wg, E, d, f)) != cudaSuccess ||
         (err = weight_map_e4m3(&mu, Wu, E, d, f)) != cudaSuccess ||
@@ -949,7 +981,8 @@ cudaError_t launch_ffn_gate_up_native(const uint8_t *xs8, const int32_t *xexp, c
                                       const int32_t *offsets, int E, int d, int f, int64_t cap,
                                       void *H, uint32_t *status, cudaStream_t stream)
 {
-    CUtensorMap mg, mu, mx, mo;
+    CUtensorMap mg, mu, mo;
+    RowMaps mx;
     cudaError_t err;
     if ((err = weight_map_e4m3_kmajor(&mg, Wg, E, d, f)) != cudaSuccess ||
         (err = weight_map_e4m3_kmajor(&mu, Wu, E, d, f)) != cudaSuccess ||
@@ -972,7 +1005,8 @@ cudaError_t launch_ffn_down_native(const uint8_t *H8, const int32_t *hexp, const
                                    int E, int d, int f, int64_t cap, void *Ys, uint32_t *status,
                                    cudaStream_t stream)
 {
-    CUtensorMap mw, mh, mo;
+    CUtensorMap mw, mo;
+    RowMaps mh;
     cudaError_t err;
     if ((err = weight_map_e4m3_kmajor(&mw, Wd, E, f, d)) != cudaSuccess ||
         (err = rows_map_e4m3(&mh, H8, cap, f)) != cudaSuccess ||
@@ -993,7 +1027,8 @@ cudaError_t launch_ffn_down_e4m3(const void *H, const uint8_t *Wd, const float *
                                  const int32_t *offsets, const float *srt_w, int E, int d, int f,
                                  int64_t cap, void *Ys, uint32_t *status, cudaStream_t stream)
 {
-    CUtensorMap mw, mh, mo;
+    CUtensorMap mw, mo;
+    RowMaps mh;
     cudaError_t err;
     if ((err = weight_map_e4m3(&mw, Wd, E, f, d)) != cudaSuccess ||
         (err = rows_map(&mh, H, cap, f)) != cudaSuccess ||
