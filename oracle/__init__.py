@@ -22,7 +22,12 @@ function cites the passage it follows in the C source:
   (expert, output feature) ("Round 4 Track C ...", section 2 runs the
   experts from quantized packs; E4M3 is the OCP 8-bit floating point
   format).  ``layer`` and ``expert_rows`` take such weights as
-  ``(codes, scales)`` pairs in place of bf16 arrays.
+  ``(codes, scales)`` pairs in place of bf16 arrays;
+* ``quantize_mxfp4`` / ``dequantize_mxfp4`` -- expert weights as 4-bit
+  MXFP4 (the OCP Microscaling format: E2M1 codes in blocks of 32 along the
+  reduction axis with a power-of-two scale each); the dequantized weights
+  are exact bf16 values, so the layer on MXFP4 weights is ``layer`` on
+  them.
 
 Pins (CPU tests): brute force on tiny inputs, closed forms, a dense numpy
 cross-check for a single expert, invariants, and hand-worked fixtures under
@@ -91,6 +96,12 @@ def _load():
             lib.oracle_e4m3_encode.argtypes = [C.c_float]
             lib.oracle_quantize_e4m3.restype = None
             lib.oracle_quantize_e4m3.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P]
+            lib.oracle_e2m1_value.restype = C.c_double
+            lib.oracle_e2m1_value.argtypes = [C.c_uint8]
+            lib.oracle_quantize_mxfp4.restype = None
+            lib.oracle_quantize_mxfp4.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P]
+            lib.oracle_dequantize_mxfp4.restype = C.c_int
+            lib.oracle_dequantize_mxfp4.argtypes = [P, P, C.c_int, C.c_int, C.c_int, P]
             lib.oracle_layer_tokens_e4m3.restype = C.c_int
             lib.oracle_layer_tokens_e4m3.argtypes = [P, C.c_int, P, P, P, P, P, P, P, P,
                                                      C.c_int, C.c_int, C.c_int, C.c_int,
@@ -292,6 +303,43 @@ def dequantize_e4m3(q, s) -> np.ndarray:
     table = np.array([e4m3_value(c) for c in range(256)], np.float64)
     q = np.asarray(q, np.uint8)
     return table[q] * np.asarray(s, np.float64)[:, None, :]
+
+
+def e2m1_value(c: int) -> float:
+    """Value of a 4-bit E2M1 code (OCP MX): 1 sign, 2 exponent bits (bias
+    1), 1 mantissa bit; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6."""
+    return float(_load().oracle_e2m1_value(int(c) & 0xF))
+
+
+def quantize_mxfp4(W):
+    """bf16 weights [E, K, M] -> MXFP4 along K: (codes uint8 [E, K, M/2], two
+    4-bit E2M1 codes a byte, feature m even in the low nibble; scale
+    exponents uint8 [E, K/32, M], scale = 2^(S-127)).  Per block of 32 k:
+    x = floor(log2(max|W|)) - 2 clamped to [-127, 127] (-127 for a zero
+    block), S = x + 127, code = nearest E2M1 to W / 2^x (ties to even,
+    saturated at 6).  K must be a multiple of 32, M even."""
+    W = _c(W, np.uint16)
+    E, K, M = W.shape
+    if K % 32 or M % 2:
+        raise OracleError("MXFP4 needs K % 32 == 0 and M even")
+    codes = np.zeros((E, K, M // 2), np.uint8)
+    scales = np.empty((E, K // 32, M), np.uint8)
+    _load().oracle_quantize_mxfp4(_p(W), E, K, M, _p(codes), _p(scales))
+    return codes, scales
+
+
+def dequantize_mxfp4(codes, scales) -> np.ndarray:
+    """The dequantized weights e2m1(code) * 2^(S-127) as bf16 bit patterns
+    [E, K, M] (exact for S <= 252: every such value is a bf16 value).  The
+    layer on MXFP4 weights is the bf16 layer on these weights."""
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    E, K, M2 = codes.shape
+    W = np.empty((E, K, 2 * M2), np.uint16)
+    rc = _load().oracle_dequantize_mxfp4(_p(codes), _p(scales), E, K, 2 * M2, _p(W))
+    if rc != 0:
+        raise OracleError("MXFP4 value outside bf16 (scale exponent above 252)")
+    return W
 
 
 def quantize_rows_e4m3(x):

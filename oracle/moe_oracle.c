@@ -24,7 +24,11 @@
  *       here is 8-bit floating point E4M3 (the OCP 8-bit floating point
  *       format: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
  *       infinities, S.1111.111 = NaN, largest finite 448) with one fp32
- *       scale per expert and output feature.
+ *       scale per expert and output feature; and 4-bit MXFP4 (the OCP
+ *       Microscaling format: E2M1 elements -- 1 sign, 2 exponent bits with
+ *       bias 1, 1 mantissa bit, magnitudes 0 .. 6 -- in blocks of 32 along
+ *       the reduction axis sharing a power-of-two scale 2^(S-127), S an
+ *       unsigned 8-bit exponent).
  *
  * Readings taken where the pages leave a step open:
  *  - flat entry i = t*k + j (token-major); ties inside an expert keep
@@ -168,6 +172,126 @@ void oracle_quantize_e4m3(const uint16_t *W, int E, int K, int M, uint8_t *q, fl
             }
         }
     }
+}
+
+/* ---- MXFP4 weights [P1 sec. 2; the OCP Microscaling (MX) MXFP4 format] ---- */
+
+/* Value of an E2M1 (4-bit) code: 1 sign bit, 2 exponent bits (bias 1), 1
+ * mantissa bit; exponent field 0 is subnormal (m/2), the rest normal
+ * ((1 + m/2) * 2^(e-1)).  Magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; no
+ * infinities, no NaN. */
+static double e2m1_value(uint8_t c)
+{
+    int sign = (c >> 3) & 1, ex = (c >> 1) & 3, man = c & 1;
+    double v = ex == 0 ? 0.5 * man : ldexp(1.0 + 0.5 * man, ex - 1);
+    return sign ? -v : v;
+}
+
+/* Nearest E2M1 code to v, ties to the even code (the one whose mantissa
+ * bit is 0), magnitudes past 6 saturated to 6; the sign is kept (a
+ * negative value that rounds to zero gives -0).  A search over the eight
+ * non-negative magnitudes, which increase with their codes. */
+static uint8_t e2m1_encode(double v)
+{
+    uint8_t sign = signbit(v) ? 0x8 : 0x0;
+    double a = fabs(v);
+    int c, best = 0;
+    if (a >= 6.0)
+        return (uint8_t)(sign | 0x7);
+    for (c = 1; c <= 7; c++) {
+        double lo = e2m1_value((uint8_t)(c - 1)), hi = e2m1_value((uint8_t)c);
+        if (a > hi)
+            continue;
+        /* lo <= a <= hi */
+        if (a - lo < hi - a)
+            best = c - 1;
+        else if (a - lo > hi - a)
+            best = c;
+        else /* a tie: the code whose mantissa bit is 0 */
+            best = (c & 1) ? c - 1 : c;
+        break;
+    }
+    return (uint8_t)(sign | best);
+}
+
+#define MX_BLOCK 32
+#define E2M1_EMAX 2 /* exponent of the largest E2M1 normal: 6 = 1.5 * 2^2 */
+
+/*
+ * Quantize bf16 weights W [E][K][M] (M the output feature, contiguous) to
+ * MXFP4 along the reduction axis K: for each expert e, output feature m and
+ * block b of 32 consecutive k (K a multiple of 32, M even):
+ *   amax = max |W| over the block
+ *   x = floor(log2(amax)) - 2, clamped to [-127, 127]; x = -127 when amax = 0
+ *   scales[e][b][m] = x + 127 (an 8-bit power-of-two exponent, E8M0)
+ *   code = e2m1_encode(W / 2^x) (exact division by a power of two)
+ * so the dequantized weight is e2m1_value(code) * 2^x.  Codes are packed two
+ * per byte along M: byte codes[e][k][m/2] holds feature m (even) in its low
+ * four bits and feature m + 1 in its high four bits.  W must be finite.
+ */
+void oracle_quantize_mxfp4(const uint16_t *W, int E, int K, int M, uint8_t *codes,
+                           uint8_t *scales)
+{
+    long e, b, k, m;
+    for (e = 0; e < E; e++) {
+        for (b = 0; b < K / MX_BLOCK; b++) {
+            for (m = 0; m < M; m++) {
+                double amax = 0.0;
+                int x = -127, fe;
+                for (k = b * MX_BLOCK; k < (b + 1) * MX_BLOCK; k++) {
+                    double a = fabs(bf16_value(W[(e * K + k) * M + m]));
+                    if (a > amax)
+                        amax = a;
+                }
+                if (amax > 0.0) {
+                    frexp(amax, &fe); /* amax = f * 2^fe, f in [0.5, 1): floor(log2) = fe - 1 */
+                    x = fe - 1 - E2M1_EMAX;
+                    if (x < -127)
+                        x = -127;
+                    if (x > 127)
+                        x = 127;
+                }
+                scales[(e * (K / MX_BLOCK) + b) * M + m] = (uint8_t)(x + 127);
+                for (k = b * MX_BLOCK; k < (b + 1) * MX_BLOCK; k++) {
+                    uint8_t c = e2m1_encode(ldexp(bf16_value(W[(e * K + k) * M + m]), -x));
+                    uint8_t *byte = &codes[(e * K + k) * (M / 2) + m / 2];
+                    if ((m & 1) == 0)
+                        *byte = (uint8_t)((*byte & 0xf0) | c);
+                    else
+                        *byte = (uint8_t)((*byte & 0x0f) | (c << 4));
+                }
+            }
+        }
+    }
+}
+
+/*
+ * The dequantized weights e2m1_value(code) * 2^(scale - 127) as bf16 bit
+ * patterns W [E][K][M].  Every such value with scale <= 252 is a bf16 value
+ * (at most two significant bits, exponent inside bf16's range), so this is
+ * exact; returns ORC_ERR_ARG if some value is not (a scale byte above 252).
+ */
+int oracle_dequantize_mxfp4(const uint8_t *codes, const uint8_t *scales, int E, int K, int M,
+                            uint16_t *W)
+{
+    long e, k, m;
+    for (e = 0; e < E; e++)
+        for (k = 0; k < K; k++)
+            for (m = 0; m < M; m++) {
+                uint8_t byte = codes[(e * K + k) * (M / 2) + m / 2];
+                uint8_t c = (m & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xf);
+                int s = scales[(e * (K / MX_BLOCK) + k / MX_BLOCK) * M + m];
+                double v = ldexp(e2m1_value(c), s - 127);
+                float f = (float)v;
+                uint32_t u;
+                if (s > 252 || (double)f != v)
+                    return ORC_ERR_ARG;
+                memcpy(&u, &f, sizeof u);
+                if (u & 0xffffu)
+                    return ORC_ERR_ARG;
+                W[(e * K + k) * M + m] = (uint16_t)(u >> 16);
+            }
+    return ORC_OK;
 }
 
 /*
@@ -742,3 +866,5 @@ double oracle_round_bf16(double v) { return to_bf16(v); }
 double oracle_value16(uint16_t b, int is_f16) { return value16(b, is_f16); }
 double oracle_e4m3_value(uint8_t c) { return e4m3_value(c); }
 uint8_t oracle_e4m3_encode(float v) { return e4m3_encode(v); }
+double oracle_e2m1_value(uint8_t c) { return e2m1_value(c); }
+uint8_t oracle_e2m1_encode(double v) { return e2m1_encode(v); }

@@ -45,6 +45,21 @@ MUTANTS = {
     "down_codes_from_fp64_h": ("        hq[n] = a8 ? to_bf16(h[n]) : h[n];", "        hq[n] = h[n];"),
     "quantize_amax_axis": ("float a = (float)fabs(bf16_value(W[(e * K + k) * M + m]));",
                            "float a = (float)fabs(bf16_value(W[(e * K + m % K) * M + k % M]));"),
+    "e2m1_emax": ("#define E2M1_EMAX 2", "#define E2M1_EMAX 3"),
+    "e2m1_subnormal_step": ("double v = ex == 0 ? 0.5 * man : ldexp(1.0 + 0.5 * man, ex - 1);",
+                            "double v = ex == 0 ? 0.25 * man : ldexp(1.0 + 0.5 * man, ex - 1);"),
+    "e2m1_exponent_bias": ("double v = ex == 0 ? 0.5 * man : ldexp(1.0 + 0.5 * man, ex - 1);",
+                           "double v = ex == 0 ? 0.5 * man : ldexp(1.0 + 0.5 * man, ex);"),
+    "e2m1_ties_up": ("            best = (c & 1) ? c - 1 : c;", "            best = c;"),
+    "e2m1_no_saturation": ("    if (a >= 6.0)\n        return (uint8_t)(sign | 0x7);",
+                           "    if (a >= 8.0)\n        return (uint8_t)(sign | 0x7);"),
+    "mx_scale_bias": ("scales[(e * (K / MX_BLOCK) + b) * M + m] = (uint8_t)(x + 127);",
+                      "scales[(e * (K / MX_BLOCK) + b) * M + m] = (uint8_t)(x + 126);"),
+    "mx_nibble_order": ("            if ((m & 1) == 0)\n                        *byte",
+                        "            if ((m & 1) == 1)\n                        *byte"),
+    "mx_block_along_m": ("double a = fabs(bf16_value(W[(e * K + k) * M + m]));",
+                         "double a = fabs(bf16_value(W[(e * K + b * MX_BLOCK + (k % MX_BLOCK)) * M + (m / MX_BLOCK) * MX_BLOCK + (k % MX_BLOCK) % M]));"),
+    "mx_exponent_from_ceil": ("x = fe - 1 - E2M1_EMAX;", "x = fe - E2M1_EMAX;"),
 }
 
 
@@ -62,6 +77,7 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(HERE, "test_oracle_plan.py"),
                         os.path.join(HERE, "test_oracle_layer.py"),
-                        os.path.join(HERE, "test_oracle_e4m3.py")],
+                        os.path.join(HERE, "test_oracle_e4m3.py"),
+                        os.path.join(HERE, "test_oracle_mxfp4.py")],
                        env=env, capture_output=True, text=True, cwd=os.path.dirname(HERE))
     assert r.returncode != 0, f"planted mistake {name} passed every pin:\n{r.stdout[-2000:]}"
