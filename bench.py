@@ -17,8 +17,9 @@ sampled during the timed region, and the CPU oracle timed on a bounded
 sample on this host's cores, and how far the layer lands from the oracle
 (accuracy_vs_oracle).  Beside them: the plan alone on 1M and 10M entries
 (plan_sweep), the plan + gather configuration with fp16 rows (plan_gather),
-the same layer on 8-bit operands (fp8_layer, with its own error against the
-fp64 oracle), and every other layer workload timed the same way (workloads:
+the same layer on 8-bit operands (fp8_layer) and on MXFP4 4-bit weights
+(mxfp4_layer), each with its own error against the fp64 oracle, and every
+other layer workload timed the same way (workloads:
 the tiny layer, the 256-expert layer, and the long prompt as its 8 chunks of
 4096 tokens per step), each with per-stage times, its gate/up roofline and
 the oracle on this host's cores.
@@ -407,6 +408,47 @@ def run_native(args, rank, world, local):
                "gpu_launches": (KERNELS_PER_LAYER + 1) * args.steps}
         del layer8
 
+    # MXFP4 expert weights (4-bit E2M1 codes, power-of-two scale per 32 along
+    # K; decoded to bf16 in shared memory, bf16 activations), timed the same way
+    mx4 = None
+    if not e4m3 and not args.no_fp8:
+        layer4 = B.MoeLayer.quantized_mxfp4(Wg, Wu, Wd, tm=wl.tm)
+        for i in range(args.warmup):
+            flush.fill_(i & 0xFF)
+            layer4.forward(x, ids, w, y=y)
+        torch.cuda.synchronize(dev)
+        if B.read_status(layer4._ws) != 0:
+            raise RuntimeError("device status set in the MXFP4 layer")
+        ms4 = timed(lambda: layer4.forward(x, ids, w, y=y), args.steps)
+        total4 = replicas.max_over_ranks(sum(ms4), world, dev)
+        y4 = layer4.forward(x, ids, w).clone()
+        o4 = B.plan(ids, w, wl.E, wl.tm, cap=cap)
+        xs4 = B.gather(x, o4["srt_tok"], o4["offsets"], wl.E, cap)
+        H4 = torch.empty((cap, wl.f), dtype=torch.bfloat16, device=dev)
+        Ys4 = torch.empty((cap, wl.d), dtype=torch.bfloat16, device=dev)
+        gu4, dn4 = [], []
+        for i in range(min(args.steps, 50) + 3):
+            flush.fill_(i & 0xFF)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            ev[0].record(stream)
+            B.ffn_gate_up_mxfp4(xs4, layer4.Wg, layer4.Wu, o4["offsets"], cap, H=H4)
+            ev[1].record(stream)
+            B.ffn_down_mxfp4(H4, layer4.Wd, o4["offsets"], o4["srt_w"], cap, Ys=Ys4)
+            ev[2].record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= 3:
+                gu4.append(ev[0].elapsed_time(ev[1]) * 1e3)
+                dn4.append(ev[1].elapsed_time(ev[2]) * 1e3)
+        mx4 = {"value": args.steps * rows * world / (total4 / 1e3), "unit": "rows/s",
+               "ms_per_step": statistics.mean(ms4), "steps": args.steps,
+               "gate_up_us": statistics.median(gu4), "down_us": statistics.median(dn4),
+               "arithmetic": "MXFP4 weights (4-bit E2M1 codes, power-of-two scale per 32 along "
+                             "K, decoded exactly to bf16 in shared memory); bf16 activations, "
+                             "fp32 accumulation; bf16 H, Ys, y",
+               "weight_bytes_active": alg["active"] * 3 * wl.d * wl.f // 2,
+               "gpu_launches": KERNELS_PER_LAYER * args.steps}
+        del layer4, o4, xs4, H4, Ys4
+
     # the plan alone on large inputs, where its HBM traffic is what bounds it:
     # T*k = 1M and 10M entries, E = 512, ids uniform over the experts (drawn on
     # the device from a seeded generator), L2 flushed before each call
@@ -545,6 +587,7 @@ def run_native(args, rank, world, local):
                       f"({alg['weights'] / 1e9:.2f} GB > 129 MB L2)"},
         "clocks": clk,
         "fp8_layer": fp8,
+        "mxfp4_layer": mx4,
         "gpu_launches": (KERNELS_PER_LAYER + int(f8)) * args.steps,
     }
     if world == 1 and not args.no_cpu_baseline and not e4m3:
@@ -560,6 +603,9 @@ def run_native(args, rank, world, local):
         if fp8 is not None:
             fp8["accuracy_vs_oracle"] = error_vs_oracle(y8, toks, y_ref)
             line["accuracy_vs_oracle"]["fp8_layer"] = fp8["accuracy_vs_oracle"]
+        if mx4 is not None:
+            mx4["accuracy_vs_oracle"] = error_vs_oracle(y4, toks, y_ref)
+            line["accuracy_vs_oracle"]["mxfp4_layer"] = mx4["accuracy_vs_oracle"]
     if world == 1 and not args.no_workloads and not e4m3:
         line["workloads"] = other_workloads(args, dev, flush, stream)
     print(json.dumps(line), flush=True)
@@ -738,7 +784,7 @@ def main():
     ap.add_argument("--no-plan-gather", action="store_true",
                     help="skip the plan + gather configuration (T=2048, E=512, fp16 rows)")
     ap.add_argument("--no-fp8", action="store_true",
-                    help="skip the E4M3 layer measured beside the bf16 one")
+                    help="skip the E4M3 and MXFP4 layers measured beside the bf16 one")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the other layer workloads (tiny, 256-expert, long prompt)")
     ap.add_argument("--workload-cpu-budget", type=float, default=6.0,

@@ -397,6 +397,52 @@ MOE_API int moe_layer_forward_f8(const void *x, const int32_t *ids, const float 
                                  size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * MXFP4 expert weights (4 bits a weight).  The same page (section 2) runs
+ * experts from 4-bit block formats; here the 4-bit form is MXFP4 of the OCP
+ * Microscaling (MX) specification: E2M1 elements (1 sign, 2 exponent bits
+ * with bias 1, 1 mantissa bit; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6) in
+ * blocks of 32 along K (the reduction axis), each block of each expert and
+ * output feature sharing a power-of-two scale 2^(S-127), S one byte:
+ *   x = floor(log2(max |W| over the block)) - 2, clamped to [-127, 127]
+ *       (-127 for a block of zeros); S = x + 127
+ *   code = E2M1 nearest to W / 2^x (ties to the even code, past 6
+ *          saturated, the sign kept)
+ * and the weight the GEMMs use is value(code) * 2^x, which is exactly a bf16
+ * value.  Activations, H, Ys and y stay bf16, accumulation fp32: the layer
+ * on MXFP4 weights is the bf16 layer on the dequantized weights.  The GEMMs
+ * load the 4-bit codes and the scales with TMA and decode them to bf16 in
+ * shared memory.
+ *
+ * moe_quantize_mxfp4 -- W bf16 [E, K, M] (M = output features, contiguous;
+ * K a multiple of 32, M even; 4-byte aligned) -> codes uint8 [E, K, M/2]
+ * (feature m even in the low four bits of byte m/2, m + 1 in the high four)
+ * and scales uint8 [E, K/32, M] (S; 2-byte aligned).  W must be finite.  A
+ * one-time preparation, not part of the layer.
+ *
+ * moe_ffn_gate_up_mxfp4 / moe_ffn_down_mxfp4 -- moe_ffn_gate_up /
+ * moe_ffn_down with MXFP4 weights: Wg, Wu codes [E, d, f/2] with scales
+ * xg, xu [E, d/32, f]; Wd codes [E, f, d/2] with scales xd [E, f/32, d]
+ * (codes and scales 16-byte aligned).  Everything else as in the bf16 calls.
+ *
+ * moe_layer_forward_mxfp4 -- moe_layer_forward with MXFP4 weights (as
+ * above); same workspace (moe_workspace_bytes) and outputs.
+ */
+MOE_API int moe_quantize_mxfp4(const void *W, int E, int K, int M, uint8_t *codes,
+                               uint8_t *scales, moe_stream_t stream);
+MOE_API int moe_ffn_gate_up_mxfp4(const void *xs, const uint8_t *Wg, const uint8_t *xg,
+                                  const uint8_t *Wu, const uint8_t *xu, const int32_t *offsets,
+                                  int E, int d, int f, int64_t cap, void *H, uint32_t *status,
+                                  moe_stream_t stream);
+MOE_API int moe_ffn_down_mxfp4(const void *H, const uint8_t *Wd, const uint8_t *xd,
+                               const int32_t *offsets, const float *srt_w, int E, int d, int f,
+                               int64_t cap, void *Ys, uint32_t *status, moe_stream_t stream);
+MOE_API int moe_layer_forward_mxfp4(const void *x, const int32_t *ids, const float *w,
+                                    const uint8_t *Wg, const uint8_t *xg, const uint8_t *Wu,
+                                    const uint8_t *xu, const uint8_t *Wd, const uint8_t *xd,
+                                    int T, int d, int E, int k, int f, int tm, void *y, void *ws,
+                                    size_t ws_bytes, moe_stream_t stream);
+
+/*
  * moe_prefill_forward_host -- moe_layer_forward over n_chunks prefill
  * chunks of T tokens each, taken from and returned to HOST memory.  The
  * pages run the layer chunk by chunk over a prompt ("Round 4 Track C:

@@ -9,6 +9,7 @@ from __future__ import annotations
 import ctypes as C
 import os
 import threading
+from typing import NamedTuple
 
 import torch
 
@@ -91,6 +92,19 @@ _SIGS = {
                                          C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int,
                                          C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_size_t,
                                          C.c_void_p]),
+    "moe_quantize_mxfp4": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p,
+                                     C.c_void_p, C.c_void_p]),
+    "moe_ffn_gate_up_mxfp4": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                        C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
+                                        C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p]),
+    "moe_ffn_down_mxfp4": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                     C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int64,
+                                     C.c_void_p, C.c_void_p, C.c_void_p]),
+    "moe_layer_forward_mxfp4": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                          C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                          C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int,
+                                          C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_size_t,
+                                          C.c_void_p]),
     "moe_read_status": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p]),
     "moe_selftest_wait_limit": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                           C.c_int, C.c_int, C.c_int, C.c_int64, C.c_void_p,
@@ -497,6 +511,71 @@ def layer_forward_e4m3(x, ids, w, Wg, Wu, Wd, tm: int, y=None, ws=None, act_e4m3
     return y
 
 
+class Mxfp4(NamedTuple):
+    """MXFP4 weights of one projection: codes uint8 [E, K, M/2] (two 4-bit
+    E2M1 codes a byte, feature m even in the low four bits) and scale
+    exponents uint8 [E, K/32, M] (scale 2^(S-127) per block of 32 along K)."""
+    codes: torch.Tensor
+    scales: torch.Tensor
+
+
+def quantize_mxfp4(W) -> Mxfp4:
+    """moe_quantize_mxfp4: bf16 W [E, K, M] -> Mxfp4(codes, scales)."""
+    E, K, M = W.shape
+    codes = torch.empty((E, K, M // 2), dtype=torch.uint8, device=W.device)
+    scales = torch.empty((E, K // 32, M), dtype=torch.uint8, device=W.device)
+    with torch.cuda.device(W.device):
+        rc = lib().moe_quantize_mxfp4(_ptr(W), E, K, M, _ptr(codes), _ptr(scales),
+                                      _stream(W.device))
+    _check("moe_quantize_mxfp4", rc)
+    return Mxfp4(codes, scales)
+
+
+def ffn_gate_up_mxfp4(xs, Wg: Mxfp4, Wu: Mxfp4, offsets, cap: int, H=None, status=None):
+    E, d, f2 = Wg.codes.shape
+    f = 2 * f2
+    if H is None:
+        H = torch.empty((max(cap, 1), f), dtype=torch.bfloat16, device=xs.device)
+    with torch.cuda.device(xs.device):
+        rc = lib().moe_ffn_gate_up_mxfp4(_ptr(xs), _ptr(Wg.codes), _ptr(Wg.scales),
+                                         _ptr(Wu.codes), _ptr(Wu.scales), _ptr(offsets), E, d, f,
+                                         cap, _ptr(H), _ptr(status), _stream(xs.device))
+    _check("moe_ffn_gate_up_mxfp4", rc)
+    return H
+
+
+def ffn_down_mxfp4(H, Wd: Mxfp4, offsets, srt_w, cap: int, Ys=None, status=None):
+    E, f, d2 = Wd.codes.shape
+    d = 2 * d2
+    if Ys is None:
+        Ys = torch.empty((max(cap, 1), d), dtype=torch.bfloat16, device=H.device)
+    with torch.cuda.device(H.device):
+        rc = lib().moe_ffn_down_mxfp4(_ptr(H), _ptr(Wd.codes), _ptr(Wd.scales), _ptr(offsets),
+                                      _ptr(srt_w), E, d, f, cap, _ptr(Ys), _ptr(status),
+                                      _stream(H.device))
+    _check("moe_ffn_down_mxfp4", rc)
+    return Ys
+
+
+def layer_forward_mxfp4(x, ids, w, Wg: Mxfp4, Wu: Mxfp4, Wd: Mxfp4, tm: int, y=None, ws=None):
+    """moe_layer_forward_mxfp4 with MXFP4 weights."""
+    T, d = x.shape
+    k = ids.shape[1]
+    E, f = Wg.codes.shape[0], Wg.scales.shape[2]
+    dev = x.device
+    if y is None:
+        y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    if ws is None:
+        ws = torch.empty(workspace_bytes(T, d, E, k, f, tm), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = lib().moe_layer_forward_mxfp4(_ptr(x), _ptr(ids), _ptr(w), _ptr(Wg.codes),
+                                           _ptr(Wg.scales), _ptr(Wu.codes), _ptr(Wu.scales),
+                                           _ptr(Wd.codes), _ptr(Wd.scales), T, d, E, k, f, tm,
+                                           _ptr(y), _ptr(ws), ws.numel(), _stream(dev))
+    _check("moe_layer_forward_mxfp4", rc)
+    return y
+
+
 def selftest_wait_limit(xs, Wg, Wu, offsets, cap: int, status, cta: int = 0, H=None):
     """Gate/up GEMM with CTA `cta` made to wait for bytes that never come:
     its bounded waits run out, it stops, and `status` gets STATUS_TIMEOUT."""
@@ -524,7 +603,9 @@ class MoeLayer:
     """A routed MoE layer with its expert weights resident in HBM.
 
     The weights are bf16 tensors or, all three, (E4M3 codes, fp32 scales)
-    pairs from ``quantize_e4m3`` (``MoeLayer.quantized`` makes them).
+    pairs from ``quantize_e4m3`` (``MoeLayer.quantized`` makes them), or, all
+    three, ``Mxfp4`` weights from ``quantize_mxfp4``
+    (``MoeLayer.quantized_mxfp4``).
     ``forward`` takes device inputs.  ``forward_host`` (one chunk) and
     ``forward_host_chunks`` (a sequence of chunks) take pinned host inputs
     and go through moe_prefill_forward_host: the inputs are copied in and y
@@ -533,6 +614,17 @@ class MoeLayer:
 
     def __init__(self, Wg, Wu, Wd, tm: int = 16, act_e4m3: bool = False):
         self.Wg, self.Wu, self.Wd, self.tm = Wg, Wu, Wd, tm
+        self.mxfp4 = isinstance(Wg, Mxfp4)
+        if self.mxfp4:
+            if act_e4m3 or not (isinstance(Wu, Mxfp4) and isinstance(Wd, Mxfp4)):
+                raise ValueError("MXFP4 weights: all three projections, bf16 activations")
+            self.tm, self.act_e4m3, self.e4m3 = tm, False, False
+            self.E, self.f = Wd.codes.shape[0], Wd.codes.shape[1]
+            self.d = 2 * Wd.codes.shape[2]
+            self.device = Wd.codes.device
+            self._ws = None
+            self._host_ws = None
+            return
         self.e4m3 = isinstance(Wg, tuple)
         self.act_e4m3 = bool(act_e4m3)
         if self.act_e4m3 and not self.e4m3:
@@ -552,6 +644,11 @@ class MoeLayer:
         return cls(quantize_e4m3(Wg, kmajor=act_e4m3), quantize_e4m3(Wu, kmajor=act_e4m3),
                    quantize_e4m3(Wd, kmajor=act_e4m3), tm=tm, act_e4m3=act_e4m3)
 
+    @classmethod
+    def quantized_mxfp4(cls, Wg, Wu, Wd, tm: int = 16):
+        """The same layer with its bf16 weights quantized to MXFP4 on the device."""
+        return cls(quantize_mxfp4(Wg), quantize_mxfp4(Wu), quantize_mxfp4(Wd), tm=tm)
+
     def workspace(self, T: int, k: int):
         n = workspace_bytes(T, self.d, self.E, k, self.f, self.tm)
         if self._ws is None or self._ws.numel() < n:
@@ -561,6 +658,8 @@ class MoeLayer:
     def forward(self, x, ids, w, y=None):
         T = x.shape[0]
         ws = self.workspace(T, ids.shape[1])
+        if self.mxfp4:
+            return layer_forward_mxfp4(x, ids, w, self.Wg, self.Wu, self.Wd, self.tm, y=y, ws=ws)
         if self.e4m3:
             return layer_forward_e4m3(x, ids, w, self.Wg, self.Wu, self.Wd, self.tm, y=y, ws=ws,
                                       act_e4m3=self.act_e4m3)
@@ -575,7 +674,10 @@ class MoeLayer:
     def forward_host_chunks(self, x_hs, ids_hs, w_hs, y_hs):
         """A sequence of prefill chunks of equal T from host memory: chunk
         c+1's inputs are copied in and chunk c-1's y copied out while chunk
-        c runs.  Asynchronous on the current stream."""
+        c runs.  Asynchronous on the current stream.  (The host entry point
+        takes bf16 or E4M3 weights; an MXFP4 layer runs through ``forward``.)"""
+        if self.mxfp4:
+            raise ValueError("moe_prefill_forward_host takes bf16 or E4M3 weights, not MXFP4")
         T, k = ids_hs[0].shape
         n = prefill_host_workspace_bytes(T, self.d, self.E, k, self.f, self.tm)
         if self._host_ws is None or self._host_ws.numel() < n:

@@ -273,23 +273,25 @@ int moe_workspace_layout(int T, int d, int E, int k, int f, int tm, size_t *out)
 }
 
 // The expert weights of a layer: bf16, or E4M3 codes with per-feature scales
-// (act_e4m3: Wg, Wu K-major and the gate/up rows in E4M3 too).
+// (act_e4m3: Wg, Wu K-major and the gate/up rows in E4M3 too), or MXFP4
+// codes with per-block scale exponents (xg, xu, xd).
 struct LayerWeights {
     const void *Wg, *Wu, *Wd;
-    const float *sg, *su, *sd;  // all null for bf16
+    const float *sg, *su, *sd;  // E4M3 scales; null otherwise
     bool act_e4m3;
+    const uint8_t *xg = nullptr, *xu = nullptr, *xd = nullptr;  // MXFP4 scale exponents
 };
 
 static int layer_forward(const void *x, const int32_t *ids, const float *w,
                          const LayerWeights &W, int T, int d, int E, int k, int f, int tm, void *y,
                          void *ws, size_t ws_bytes, moe_stream_t stream)
 {
-    const bool e4m3 = W.sg != nullptr;
+    const bool e4m3 = W.sg != nullptr, mx4 = W.xg != nullptr;
     if (!base_sizes_ok(T, k, E) || tm < 16 || tm > MOE_MAX_TM || tm % 16 != 0 || d <= 0 ||
         f <= 0 || d % 64 != 0 || f % 64 != 0)
         return MOE_ERR_SHAPE;
     if (!W.Wg || !W.Wu || !W.Wd || !ws || (T > 0 && (!x || !ids || !w || !y)) ||
-        (e4m3 && (!W.su || !W.sd)))
+        (e4m3 && (!W.su || !W.sd)) || (mx4 && (!W.xu || !W.xd)))
         return MOE_ERR_NULL;
     size_t L[MOE_WS_FIELDS];
     int rc = layout(T, d, E, k, f, tm, L);
@@ -299,7 +301,8 @@ static int layer_forward(const void *x, const int32_t *ids, const float *w,
         return MOE_ERR_WORKSPACE;
     if (!aligned(ws, 256) || !aligned(x, 16) || !aligned(y, 16) || !aligned(W.Wg, 16) ||
         !aligned(W.Wu, 16) || !aligned(W.Wd, 16) || !aligned(ids, 4) || !aligned(w, 4) ||
-        !aligned(W.sg, 4) || !aligned(W.su, 4) || !aligned(W.sd, 4))
+        !aligned(W.sg, 4) || !aligned(W.su, 4) || !aligned(W.sd, 4) || !aligned(W.xg, 16) ||
+        !aligned(W.xu, 16) || !aligned(W.xd, 16))
         return MOE_ERR_ALIGN;
     if (T == 0)
         return MOE_OK;
@@ -335,6 +338,8 @@ static int layer_forward(const void *x, const int32_t *ids, const float *w,
     if (e == cudaSuccess)
         e = W.act_e4m3 ? moe::launch_ffn_gate_up_native(xs8, xexp, qg, W.sg, qu, W.su, offsets, E,
                                                         d, f, cap, H, status, s)
+            : mx4      ? moe::launch_ffn_gate_up_mxfp4(xs, qg, W.xg, qu, W.xu, offsets, E, d, f,
+                                                       cap, H, status, s)
             : e4m3     ? moe::launch_ffn_gate_up_e4m3(xs, qg, W.sg, qu, W.su, offsets, E, d, f, cap,
                                                       H, status, s)
                        : moe::launch_ffn_gate_up(xs, W.Wg, W.Wu, offsets, E, d, f, cap, H, status,
@@ -349,6 +354,8 @@ static int layer_forward(const void *x, const int32_t *ids, const float *w,
     if (e == cudaSuccess)
         e = W.act_e4m3 ? moe::launch_ffn_down_native(h8, hexp, qd, W.sd, offsets, srt_w, E, d, f,
                                                      cap, Ys, status, s)
+            : mx4      ? moe::launch_ffn_down_mxfp4(H, qd, W.xd, offsets, srt_w, E, d, f, cap, Ys,
+                                                    status, s)
             : e4m3     ? moe::launch_ffn_down_e4m3(H, qd, W.sd, offsets, srt_w, E, d, f, cap, Ys,
                                                    status, s)
                        : moe::launch_ffn_down(H, W.Wd, offsets, srt_w, E, d, f, cap, Ys, status,
@@ -386,6 +393,63 @@ int moe_layer_forward_f8(const void *x, const int32_t *ids, const float *w, cons
         return MOE_ERR_NULL;
     const LayerWeights W{Wg, Wu, Wd, sg, su, sd, true};
     return layer_forward(x, ids, w, W, T, d, E, k, f, tm, y, ws, ws_bytes, stream);
+}
+
+int moe_layer_forward_mxfp4(const void *x, const int32_t *ids, const float *w,
+                            const uint8_t *Wg, const uint8_t *xg, const uint8_t *Wu,
+                            const uint8_t *xu, const uint8_t *Wd, const uint8_t *xd, int T, int d,
+                            int E, int k, int f, int tm, void *y, void *ws, size_t ws_bytes,
+                            moe_stream_t stream)
+{
+    if (!xg)
+        return MOE_ERR_NULL;
+    LayerWeights W{Wg, Wu, Wd, nullptr, nullptr, nullptr, false};
+    W.xg = xg;
+    W.xu = xu;
+    W.xd = xd;
+    return layer_forward(x, ids, w, W, T, d, E, k, f, tm, y, ws, ws_bytes, stream);
+}
+
+int moe_quantize_mxfp4(const void *W, int E, int K, int M, uint8_t *codes, uint8_t *scales,
+                       moe_stream_t stream)
+{
+    if (E < 1 || E > MOE_MAX_EXPERTS || K < 32 || M < 2 || K % 32 != 0 || M % 2 != 0)
+        return MOE_ERR_SHAPE;
+    if (!W || !codes || !scales)
+        return MOE_ERR_NULL;
+    if (!aligned(W, 4) || !aligned(scales, 2))
+        return MOE_ERR_ALIGN;
+    return cuda_rc(moe::launch_quantize_mxfp4(W, E, K, M, codes, scales, as_stream(stream)));
+}
+
+int moe_ffn_gate_up_mxfp4(const void *xs, const uint8_t *Wg, const uint8_t *xg, const uint8_t *Wu,
+                          const uint8_t *xu, const int32_t *offsets, int E, int d, int f,
+                          int64_t cap, void *H, uint32_t *status, moe_stream_t stream)
+{
+    int rc = ffn_checks(xs, Wg, Wu, offsets, E, d, f, cap, H);
+    if (rc == MOE_OK && (!xg || !xu))
+        rc = MOE_ERR_NULL;
+    if (rc == MOE_OK && (!aligned(xg, 16) || !aligned(xu, 16) || !aligned(status, 4)))
+        rc = MOE_ERR_ALIGN;
+    if (rc != MOE_OK || cap == 0)
+        return rc;
+    return cuda_rc(moe::launch_ffn_gate_up_mxfp4(xs, Wg, xg, Wu, xu, offsets, E, d, f, cap, H,
+                                                 status, as_stream(stream)));
+}
+
+int moe_ffn_down_mxfp4(const void *H, const uint8_t *Wd, const uint8_t *xd, const int32_t *offsets,
+                       const float *srt_w, int E, int d, int f, int64_t cap, void *Ys,
+                       uint32_t *status, moe_stream_t stream)
+{
+    int rc = ffn_checks(H, Wd, srt_w, offsets, E, d, f, cap, Ys);
+    if (rc == MOE_OK && !xd)
+        rc = MOE_ERR_NULL;
+    if (rc == MOE_OK && (!aligned(xd, 16) || !aligned(status, 4)))
+        rc = MOE_ERR_ALIGN;
+    if (rc != MOE_OK || cap == 0)
+        return rc;
+    return cuda_rc(moe::launch_ffn_down_mxfp4(H, Wd, xd, offsets, srt_w, E, d, f, cap, Ys, status,
+                                              as_stream(stream)));
 }
 
 int moe_quantize_e4m3(const void *W, int E, int K, int M, uint8_t *q, float *scale, int kmajor,

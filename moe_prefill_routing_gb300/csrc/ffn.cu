@@ -97,7 +97,20 @@ constexpr uint32_t kStageBytesW8 = 2 * kA8TileBytes + kBTileBytes;
 constexpr int kConvSlots = 2;
 constexpr uint32_t kConvSlotBytes = 2 * kATileBytes;
 
-enum WeightMode : int { kBf16 = 0, kWiden = 1, kNative = 2 };
+enum WeightMode : int { kBf16 = 0, kWiden = 1, kNative = 2, kMx4 = 3 };
+
+// kMx4: MXFP4 weights -- 4-bit E2M1 codes, two per byte along the output
+// features ([E, K, M/2]), and one power-of-two scale 2^(S-127) per (expert,
+// block of 32 along K, output feature) ([E, K/32, M] exponent bytes).  A
+// stage holds the B rows first (16 KB, 1024-byte aligned), then per A tile
+// the codes (64 K rows x 64 bytes) and the scales (2 blocks x 128 bytes).
+// The widening warps decode code x 2^(S-127) into the same bf16 tiles the
+// other widening mode writes (exact: every such value is a bf16 value), and
+// the same bf16 MMAs run; the epilogue applies no scale.
+constexpr uint32_t kMx4CodeBytes = BM / 2 * BK;   // 4 KB: 128 features x 64 K, 4 bits each
+constexpr uint32_t kMx4ScaleBytes = BM * (BK / 32);  // 256 B: 128 features x 2 blocks
+constexpr uint32_t kMx4TileBytes = kMx4CodeBytes + kMx4ScaleBytes;
+constexpr uint32_t kStageBytesMx4 = (kBTileBytes + 2 * kMx4TileBytes + 1023) / 1024 * 1024;
 
 // Tensor maps of the B rows: boxes of 128, 64, 32 and 16 rows (h[i] holds
 // 128 >> i rows).  A unit's rows arrive in ONE copy per stage, of the
@@ -113,9 +126,14 @@ struct RowMaps {
 
 template <int WM>
 struct Cfg {
-    static constexpr bool kW8 = WM == kWiden;
+    static constexpr bool kW8 = WM == kWiden || WM == kMx4;  // widening warps
     static constexpr int kThreadsK = kW8 ? kThreadsW8 : kThreads;
-    static constexpr uint32_t kStageB = kW8 ? kStageBytesW8 : kStageBytes;
+    static constexpr uint32_t kStageB =
+        WM == kMx4 ? kStageBytesMx4 : kW8 ? kStageBytesW8 : kStageBytes;
+    // where the A tiles and the B rows sit in a stage
+    static constexpr uint32_t kAOff = WM == kMx4 ? kBTileBytes : 0u;
+    static constexpr uint32_t kBOff =
+        WM == kMx4 ? 0u : WM == kWiden ? 2 * kA8TileBytes : 2 * kATileBytes;
     static constexpr uint32_t kRingBytes =
         kStages * kStageB + (kW8 ? kConvSlots * kConvSlotBytes : 0u);
     static constexpr int kKStep = WM == kNative ? 128 : BK;  // K elements per stage
@@ -169,6 +187,7 @@ constexpr size_t ffn_smem_bytes(int E)
 static_assert(ffn_smem_bytes<kBf16>(MOE_MAX_EXPERTS) <= 227 * 1024, "shared memory per CTA");
 static_assert(ffn_smem_bytes<kWiden>(MOE_MAX_EXPERTS) <= 227 * 1024, "shared memory per CTA");
 static_assert(ffn_smem_bytes<kNative>(MOE_MAX_EXPERTS) <= 227 * 1024, "shared memory per CTA");
+static_assert(ffn_smem_bytes<kMx4>(MOE_MAX_EXPERTS) <= 227 * 1024, "shared memory per CTA");
 
 // Bounded wait that ignores the abort flag (used while stopping).
 __device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity)
@@ -285,16 +304,80 @@ __device__ __forceinline__ void widen_e4m3x16(const uint4 v, uint4 &lo, uint4 &h
     hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// 2^(S-127) as an fp32 value, exactly (S = 0: the subnormal 2^-127).
+__device__ __forceinline__ float mx_scale(uint32_t S)
+{
+    return __uint_as_float(S ? S << 23 : 0x00400000u);
+}
+
+// E2M1 code n (1 sign, 2 exponent bits with bias 1, 1 mantissa bit) times
+// the fp32 scale x = 2^(S-127): the code's magnitude built as fp32 bits
+// (exponent field 0: 0 or 0.5; otherwise (1 + m/2) * 2^(e-1)), then one
+// exact multiply by the power of two.
+__device__ __forceinline__ float e2m1_scaled(uint32_t n, float x)
+{
+    const uint32_t e = (n >> 1) & 3u, m = n & 1u;
+    uint32_t bits = e ? ((e + 126u) << 23) | (m << 22) : (m ? 0x3F000000u : 0u);
+    bits |= (n & 8u) << 28;
+    return __uint_as_float(bits) * x;
+}
+
+// One stage of MXFP4 A tiles (nt of them) -> bf16 tiles of a widening slot,
+// in the layout a 128-byte-swizzled TMA load of bf16 weights would produce.
+// Task g of the stage (ct, ct + 256, ...): tile g >> 8, K row r = (g >> 2) &
+// 63, 16-byte chunk c = g & 3 of the row's 64 code bytes = features 32c ..
+// 32c + 31 (byte b: feature 32c + 2b in its low four bits, + 1 in its high);
+// their scales sit in scale row r / 32.  Output chunk i (features 32c + 8i
+// .. + 7) goes to 64-feature box c >> 1, 16-byte chunk 4 (c & 1) + i of row r,
+// at that index XOR (r mod 8).
+__device__ __forceinline__ void widen_mx4_stage(const uint8_t *src, uint8_t *dst, int ct, int nt)
+{
+    constexpr int kTasks = BK * 4;  // per tile
+#pragma unroll
+    for (int q = 0; q < 2 * kTasks / kConvThreads; ++q) {
+        const int g = ct + q * kConvThreads;
+        if (g >= kTasks * nt)
+            break;
+        const int t = g / kTasks, r = (g >> 2) & (BK - 1), c = g & 3;
+        const uint8_t *tile = src + t * kMx4TileBytes;
+        const uint4 cv = *reinterpret_cast<const uint4 *>(tile + r * (BM / 2) + c * 16);
+        const uint8_t *srow = tile + kMx4CodeBytes + (r >> 5) * BM + 32 * c;
+        const uint4 s01 = *reinterpret_cast<const uint4 *>(srow);
+        const uint4 s23 = *reinterpret_cast<const uint4 *>(srow + 16);
+        const uint32_t code[4] = {cv.x, cv.y, cv.z, cv.w};
+        const uint32_t sc[8] = {s01.x, s01.y, s01.z, s01.w, s23.x, s23.y, s23.z, s23.w};
+        uint8_t *row = dst + t * kATileBytes + (c >> 1) * kABoxBytes + r * 128;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {  // features 32c + 8i .. + 7: code word i, scale words 2i, 2i+1
+            uint32_t o[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {  // features 8i + 2h, 8i + 2h + 1
+                const uint32_t byte = (code[i] >> (8 * h)) & 0xffu;
+                const uint32_t sw = sc[2 * i + (h >> 1)];
+                const float v0 = e2m1_scaled(byte & 0xfu, mx_scale((sw >> (16 * (h & 1))) & 0xffu));
+                const float v1 = e2m1_scaled(byte >> 4, mx_scale((sw >> (16 * (h & 1) + 8)) & 0xffu));
+                const __nv_bfloat162 b = __floats2bfloat162_rn(v0, v1);
+                o[h] = *reinterpret_cast<const uint32_t *>(&b);
+            }
+            const int j = 4 * (c & 1) + i;
+            *reinterpret_cast<uint4 *>(row + ((j ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
 // GATHER: the B rows of a unit are token rows of x fetched by index
 // (srt_tok, four rows per TMA gather4) instead of consecutive rows of xs.
 // WM: weight mode (kBf16, kWiden, kNative), see the top of this file.
+// map_s0, map_s1: kMx4 only, the scale exponents of A tiles 0 and 1.
 template <bool GATED, bool GATHER, int WM>
 __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
     k_ffn(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
           const __grid_constant__ RowMaps map_b, const __grid_constant__ CUtensorMap map_out,
+          const __grid_constant__ CUtensorMap map_s0, const __grid_constant__ CUtensorMap map_s1,
           const FfnArgs p)
 {
-    constexpr bool W8 = WM == kWiden, A8 = WM == kNative, SCALED = WM != kBf16;
+    constexpr bool W8 = Cfg<WM>::kW8, A8 = WM == kNative, MX4 = WM == kMx4;
+    constexpr bool SCALED = WM == kWiden || WM == kNative;  // scales in the epilogue
     static_assert(!(GATHER && SCALED), "gathered rows come with bf16 weights only");
     constexpr int S = kStages;
     constexpr int UM = Kind<GATED>::kUnitM;
@@ -338,6 +421,11 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
         for (int i = 0; i < (GATHER ? 1 : kRowMaps); ++i)
             prefetch_tmap(&map_b.h[i]);
         prefetch_tmap(&map_out);
+        if (MX4) {
+            prefetch_tmap(&map_s0);
+            if (GATED)
+                prefetch_tmap(&map_s1);
+        }
     }
     if (warp == 1) {
         tmem_alloc(&ctl->tmem_base, kTmemCols);
@@ -384,7 +472,8 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                 // kWiden: one E4M3 box of 128 features per A tile that starts
                 // inside M (features past M are zero-filled and still counted)
                 const uint32_t a_bytes =
-                    W8 ? (1u + uint32_t(tile_base(m0, 1) < p.M)) * kA8TileBytes
+                    MX4  ? (1u + uint32_t(tile_base(m0, 1) < p.M)) * kMx4TileBytes
+                    : W8 ? (1u + uint32_t(tile_base(m0, 1) < p.M)) * kA8TileBytes
                     : A8 ? (1u + uint32_t(tile_base(m0, 1) < p.M)) * kATileBytes  // 128 x 128 codes
                          : boxes * kABoxBytes;
                 // B: one copy of the smallest 16/32/64/128-row box holding the
@@ -400,12 +489,21 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                     uint64_t *fb = &ctl->full[stage];
                     mbar_arrive_expect_tx(fb, bytes + stall_bytes);
                     stall_bytes = 0;
-                    uint8_t *sa = smem + stage * SB;
+                    uint8_t *sa = smem + stage * SB + Cfg<WM>::kAOff;
                     const int k0 = kb * Cfg<WM>::kKStep;
 #pragma unroll
                     for (int t = 0; t < 2; ++t) {
                         const CUtensorMap *m = (GATED && t == 1) ? &map_a1 : &map_a0;
-                        if (W8) {
+                        if (MX4) {
+                            // codes [E, K, M/2]: (byte column, k, expert); scales
+                            // [E, K/32, M]: (feature, block, expert)
+                            if (tile_base(m0, t) < p.M) {
+                                uint8_t *st = sa + t * kMx4TileBytes;
+                                tma_load_3d(st, m, fb, tile_base(m0, t) / 2, k0, w.e);
+                                tma_load_3d(st + kMx4CodeBytes, (GATED && t == 1) ? &map_s1 : &map_s0,
+                                            fb, tile_base(m0, t), k0 / 32, w.e);
+                            }
+                        } else if (W8) {
                             if (tile_base(m0, t) < p.M)
                                 tma_load_3d(sa + t * kA8TileBytes, m, fb, tile_base(m0, t), k0,
                                             w.e);
@@ -424,7 +522,7 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                             }
                         }
                     }
-                    uint8_t *sb = sa + (W8 ? 2 * kA8TileBytes : 2 * kATileBytes);
+                    uint8_t *sb = smem + stage * SB + Cfg<WM>::kBOff;
                     if (GATHER) {
                         for (int j = 0; j < w.nrows; j += 4)
                             tma_gather4(sb + j * (BK * 2), &map_b.h[0], fb, k0, row_tok[j],
@@ -488,7 +586,7 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                     tc_fence_after_sync();
                     const uint32_t sst = smem_u32(smem + stage * SB);
                     const uint32_t sa = W8 ? smem_u32(conv + cslot * kConvSlotBytes) : sst;
-                    const uint32_t sb = sst + (W8 ? 2 * kA8TileBytes : 2 * kATileBytes);
+                    const uint32_t sb = sst + Cfg<WM>::kBOff;
                     if (A8) {
                         // both operands K-major 128-byte rows; K = 32 codes (32 bytes)
                         // per instruction, four per stage
@@ -559,8 +657,11 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                     ok = false;
                     break;
                 }
-                const uint8_t *src = smem + stage * SB;
+                const uint8_t *src = smem + stage * SB + Cfg<WM>::kAOff;
                 uint8_t *dst = conv + cslot * kConvSlotBytes;
+                if (MX4) {
+                    widen_mx4_stage(src, dst, ct, nt);
+                } else {
                 // a tile is 64 K rows x 8 chunks of 16 codes.  Chunk c of row
                 // r (features 16c..16c+15)
                 // becomes the 16-byte chunks 2(c&3) and 2(c&3)+1 of row r of
@@ -589,6 +690,7 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                         *reinterpret_cast<uint4 *>(row + ((j0 ^ (r & 7)) << 4)) = lo;
                         *reinterpret_cast<uint4 *>(row + (((j0 + 1) ^ (r & 7)) << 4)) = hi;
                     }
+                }
                 }
                 fence_proxy_async_smem();  // the widened tiles -> visible to the MMAs
                 mbar_arrive(&ctl->conv_full[cslot]);
@@ -847,6 +949,26 @@ cudaError_t rows_map_e4m3(RowMaps *m, const void *X, int64_t cap, int K)
     return cudaSuccess;
 }
 
+// MXFP4 codes [E, K, M/2] (two features a byte): unswizzled boxes of 64
+// bytes (128 features) x 64 K rows of one expert.
+cudaError_t mx4_code_map(CUtensorMap *m, const void *Wq, int E, int K, int M)
+{
+    const cuuint64_t dims[3] = {cuuint64_t(M / 2), cuuint64_t(K), cuuint64_t(E)};
+    const cuuint64_t strides[2] = {cuuint64_t(M / 2), cuuint64_t(M / 2) * K};
+    const cuuint32_t box[3] = {BM / 2, BK, 1};
+    return encode_bf16(m, Wq, 3, dims, strides, box, true, true);
+}
+
+// MXFP4 scale exponents [E, K/32, M]: unswizzled boxes of 128 features x 2
+// blocks (64 K) of one expert.
+cudaError_t mx4_scale_map(CUtensorMap *m, const void *S, int E, int K, int M)
+{
+    const cuuint64_t dims[3] = {cuuint64_t(M), cuuint64_t(K / 32), cuuint64_t(E)};
+    const cuuint64_t strides[2] = {cuuint64_t(M), cuuint64_t(M) * (K / 32)};
+    const cuuint32_t box[3] = {BM, BK / 32, 1};
+    return encode_bf16(m, S, 3, dims, strides, box, true, true);
+}
+
 // Rows [cap, K] (K contiguous): boxes of 128, 64, 32, 16 rows x 64 K.
 cudaError_t rows_map(RowMaps *m, const void *X, int64_t cap, int K)
 {
@@ -904,7 +1026,7 @@ cudaError_t launch_ffn_gate_up(const void *xs, const void *Wg, const void *Wu,
     const FfnArgs a{offsets, nullptr, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f,
                     stall_cta, nullptr, nullptr, nullptr};
     return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<kBf16>(E),
-                      stream, mg, mu, mx, mo, a);
+                      stream, mg, mu, mx, mo, mo, mo, a);
 }
 
 cudaError_t launch_ffn_gate_up_rows(const void *x, int T, const int32_t *srt_tok, const void *Wg,
@@ -927,7 +1049,7 @@ cudaError_t launch_ffn_gate_up_rows(const void *x, int T, const int32_t *srt_tok
     const FfnArgs a{offsets, srt_tok, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f,
                     -1, nullptr, nullptr, nullptr};
     return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<kBf16>(E),
-                      stream, mg, mu, mx, mo, a);
+                      stream, mg, mu, mx, mo, mo, mo, a);
 }
 
 cudaError_t launch_ffn_down(const void *H, const void *Wd, const int32_t *offsets,
@@ -949,7 +1071,7 @@ cudaError_t launch_ffn_down(const void *H, const void *Wd, const int32_t *offset
     const FfnArgs a{offsets, nullptr, srt_w, static_cast<uint16_t *>(Ys), status, cap, E, f, d,
                     -1, nullptr, nullptr, nullptr};
     return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<kBf16>(E),
-                      stream, mw, mw, mh, mo, a);
+                      stream, mw, mw, mh, mo, mo, mo, a);
 }
 
 cudaError_t launch_ffn_gate_up_e4m3(const void *xs, const uint8_t *Wg, const float *sg,
@@ -973,7 +1095,7 @@ cudaError_t launch_ffn_gate_up_e4m3(const void *xs, const uint8_t *Wg, const flo
     const FfnArgs a{offsets, nullptr, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f,
                     -1, sg, su, nullptr};
     return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreadsW8), ffn_smem_bytes<kWiden>(E),
-                      stream, mg, mu, mx, mo, a);
+                      stream, mg, mu, mx, mo, mo, mo, a);
 }
 
 cudaError_t launch_ffn_gate_up_native(const uint8_t *xs8, const int32_t *xexp, const uint8_t *Wg,
@@ -997,7 +1119,7 @@ cudaError_t launch_ffn_gate_up_native(const uint8_t *xs8, const int32_t *xexp, c
     const FfnArgs a{offsets, nullptr, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f,
                     -1, sg, su, xexp};
     return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<kNative>(E),
-                      stream, mg, mu, mx, mo, a);
+                      stream, mg, mu, mx, mo, mo, mo, a);
 }
 
 cudaError_t launch_ffn_down_native(const uint8_t *H8, const int32_t *hexp, const uint8_t *Wd,
@@ -1020,7 +1142,7 @@ cudaError_t launch_ffn_down_native(const uint8_t *H8, const int32_t *hexp, const
     const FfnArgs a{offsets, nullptr, srt_w, static_cast<uint16_t *>(Ys), status, cap, E, f, d,
                     -1, sd, sd, hexp};
     return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<kNative>(E),
-                      stream, mw, mw, mh, mo, a);
+                      stream, mw, mw, mh, mo, mo, mo, a);
 }
 
 cudaError_t launch_ffn_down_e4m3(const void *H, const uint8_t *Wd, const float *sd,
@@ -1042,7 +1164,56 @@ cudaError_t launch_ffn_down_e4m3(const void *H, const uint8_t *Wd, const float *
     const FfnArgs a{offsets, nullptr, srt_w, static_cast<uint16_t *>(Ys), status, cap, E, f, d,
                     -1, sd, sd, nullptr};
     return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreadsW8), ffn_smem_bytes<kWiden>(E),
-                      stream, mw, mw, mh, mo, a);
+                      stream, mw, mw, mh, mo, mo, mo, a);
+}
+
+cudaError_t launch_ffn_gate_up_mxfp4(const void *xs, const uint8_t *Wg, const uint8_t *sg,
+                                     const uint8_t *Wu, const uint8_t *su, const int32_t *offsets,
+                                     int E, int d, int f, int64_t cap, void *H, uint32_t *status,
+                                     cudaStream_t stream)
+{
+    CUtensorMap mg, mu, msg, msu, mo;
+    RowMaps mx;
+    cudaError_t err;
+    if ((err = mx4_code_map(&mg, Wg, E, d, f)) != cudaSuccess ||
+        (err = mx4_code_map(&mu, Wu, E, d, f)) != cudaSuccess ||
+        (err = mx4_scale_map(&msg, sg, E, d, f)) != cudaSuccess ||
+        (err = mx4_scale_map(&msu, su, E, d, f)) != cudaSuccess ||
+        (err = rows_map(&mx, xs, cap, d)) != cudaSuccess ||
+        (err = out_map(&mo, H, cap, f, Kind<true>::kUnitM)) != cudaSuccess)
+        return err;
+    auto kern = k_ffn<true, false, kMx4>;
+    err = ensure_smem_limit(reinterpret_cast<const void *>(kern), kSlotGateUpMx4,
+                            ffn_smem_bytes<kMx4>(MOE_MAX_EXPERTS));
+    if (err != cudaSuccess)
+        return err;
+    const FfnArgs a{offsets, nullptr, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f,
+                    -1, nullptr, nullptr, nullptr};
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreadsW8), ffn_smem_bytes<kMx4>(E),
+                      stream, mg, mu, mx, mo, msg, msu, a);
+}
+
+cudaError_t launch_ffn_down_mxfp4(const void *H, const uint8_t *Wd, const uint8_t *sd,
+                                  const int32_t *offsets, const float *srt_w, int E, int d, int f,
+                                  int64_t cap, void *Ys, uint32_t *status, cudaStream_t stream)
+{
+    CUtensorMap mw, msd, mo;
+    RowMaps mh;
+    cudaError_t err;
+    if ((err = mx4_code_map(&mw, Wd, E, f, d)) != cudaSuccess ||
+        (err = mx4_scale_map(&msd, sd, E, f, d)) != cudaSuccess ||
+        (err = rows_map(&mh, H, cap, f)) != cudaSuccess ||
+        (err = out_map(&mo, Ys, cap, d, Kind<false>::kUnitM)) != cudaSuccess)
+        return err;
+    auto kern = k_ffn<false, false, kMx4>;
+    err = ensure_smem_limit(reinterpret_cast<const void *>(kern), kSlotDownMx4,
+                            ffn_smem_bytes<kMx4>(MOE_MAX_EXPERTS));
+    if (err != cudaSuccess)
+        return err;
+    const FfnArgs a{offsets, nullptr, srt_w, static_cast<uint16_t *>(Ys), status, cap, E, f, d,
+                    -1, nullptr, nullptr, nullptr};
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreadsW8), ffn_smem_bytes<kMx4>(E),
+                      stream, mw, mw, mh, mo, msd, msd, a);
 }
 
 }  // namespace moe

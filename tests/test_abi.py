@@ -253,3 +253,24 @@ def test_noalloc_limit_boundary(lib, E, entries):
     assert noalloc_call(lib, T, k, E, FAKE + 2) == B.MOE_ERR_ALIGN
     T1 = (entries + k) // k
     assert noalloc_call(lib, T1, k, E, FAKE + 2) == B.MOE_ERR_WORKSPACE
+
+
+def test_mxfp4_argument_checks(lib):
+    FAKEP = 1 << 20
+    # K a multiple of 32 and M even; null and misaligned pointers
+    assert lib.moe_quantize_mxfp4(FAKEP, 2, 48, 64, FAKEP, FAKEP, None) == B.MOE_ERR_SHAPE
+    assert lib.moe_quantize_mxfp4(FAKEP, 2, 64, 63, FAKEP, FAKEP, None) == B.MOE_ERR_SHAPE
+    assert lib.moe_quantize_mxfp4(None, 2, 64, 64, FAKEP, FAKEP, None) == B.MOE_ERR_NULL
+    assert lib.moe_quantize_mxfp4(FAKEP, 2, 64, 64, FAKEP, FAKEP + 1, None) == B.MOE_ERR_ALIGN
+    # GEMMs: d and f multiples of 64, scale exponents present and 16-byte aligned
+    args = (FAKEP, FAKEP, FAKEP, FAKEP, FAKEP, FAKEP)
+    assert lib.moe_ffn_gate_up_mxfp4(*args, 4, 96, 64, 64, FAKEP, None, None) == B.MOE_ERR_SHAPE
+    assert lib.moe_ffn_gate_up_mxfp4(FAKEP, FAKEP, None, FAKEP, FAKEP, FAKEP, 4, 64, 64, 64,
+                                     FAKEP, None, None) == B.MOE_ERR_NULL
+    assert lib.moe_ffn_gate_up_mxfp4(FAKEP, FAKEP, FAKEP + 8, FAKEP, FAKEP, FAKEP, 4, 64, 64, 64,
+                                     FAKEP, None, None) == B.MOE_ERR_ALIGN
+    assert lib.moe_ffn_down_mxfp4(FAKEP, FAKEP, None, FAKEP, FAKEP, 4, 64, 64, 64, FAKEP, None,
+                                  None) == B.MOE_ERR_NULL
+    assert lib.moe_layer_forward_mxfp4(FAKEP, FAKEP, FAKEP, FAKEP, None, FAKEP, FAKEP, FAKEP,
+                                       FAKEP, 8, 64, 4, 2, 64, 16, FAKEP, FAKEP, 1 << 30,
+                                       None) == B.MOE_ERR_NULL
