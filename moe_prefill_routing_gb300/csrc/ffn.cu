@@ -58,6 +58,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cudaTypedefs.h>
 
@@ -310,58 +311,42 @@ __device__ __forceinline__ float mx_scale(uint32_t S)
     return __uint_as_float(S ? S << 23 : 0x00400000u);
 }
 
-// E2M1 code n (1 sign, 2 exponent bits with bias 1, 1 mantissa bit) times
-// the fp32 scale x = 2^(S-127): the code's magnitude built as fp32 bits
-// (exponent field 0: 0 or 0.5; otherwise (1 + m/2) * 2^(e-1)), then one
-// exact multiply by the power of two.
-__device__ __forceinline__ float e2m1_scaled(uint32_t n, float x)
-{
-    const uint32_t e = (n >> 1) & 3u, m = n & 1u;
-    uint32_t bits = e ? ((e + 126u) << 23) | (m << 22) : (m ? 0x3F000000u : 0u);
-    bits |= (n & 8u) << 28;
-    return __uint_as_float(bits) * x;
-}
-
 // One stage of MXFP4 A tiles (nt of them) -> bf16 tiles of a widening slot,
 // in the layout a 128-byte-swizzled TMA load of bf16 weights would produce.
-// Task g of the stage (ct, ct + 256, ...): tile g >> 8, K row r = (g >> 2) &
-// 63, 16-byte chunk c = g & 3 of the row's 64 code bytes = features 32c ..
-// 32c + 31 (byte b: feature 32c + 2b in its low four bits, + 1 in its high);
-// their scales sit in scale row r / 32.  Output chunk i (features 32c + 8i
-// .. + 7) goes to 64-feature box c >> 1, 16-byte chunk 4 (c & 1) + i of row r,
-// at that index XOR (r mod 8).
+// Thread ct takes tile ct >> 7, the 8 K rows 8 rg .. 8 rg + 7 (rg = (ct >> 4)
+// & 7, all in scale block rg >> 2) and the 8 features 8 fg .. 8 fg + 7 (fg =
+// ct & 15): per row one 4-byte word of codes (byte b: feature 8 fg + 2b in
+// its low four bits, + 1 in its high), decoded two codes at a time by the
+// hardware's E2M1 -> f16 conversion (exact) and scaled by the features' 8
+// powers of two (computed once); each row's 8 bf16 values are one 16-byte
+// chunk, chunk fg & 7 of 64-feature box fg >> 3, at that index XOR (r mod 8).
 __device__ __forceinline__ void widen_mx4_stage(const uint8_t *src, uint8_t *dst, int ct, int nt)
 {
-    constexpr int kTasks = BK * 4;  // per tile
+    const int t = ct >> 7, rg = (ct >> 4) & 7, fg = ct & 15;
+    if (t >= nt)
+        return;
+    const uint8_t *tile = src + t * kMx4TileBytes;
+    const uint2 sb = *reinterpret_cast<const uint2 *>(tile + kMx4CodeBytes + (rg >> 2) * BM + 8 * fg);
+    float x[8];
 #pragma unroll
-    for (int q = 0; q < 2 * kTasks / kConvThreads; ++q) {
-        const int g = ct + q * kConvThreads;
-        if (g >= kTasks * nt)
-            break;
-        const int t = g / kTasks, r = (g >> 2) & (BK - 1), c = g & 3;
-        const uint8_t *tile = src + t * kMx4TileBytes;
-        const uint4 cv = *reinterpret_cast<const uint4 *>(tile + r * (BM / 2) + c * 16);
-        const uint8_t *srow = tile + kMx4CodeBytes + (r >> 5) * BM + 32 * c;
-        const uint4 s01 = *reinterpret_cast<const uint4 *>(srow);
-        const uint4 s23 = *reinterpret_cast<const uint4 *>(srow + 16);
-        const uint32_t code[4] = {cv.x, cv.y, cv.z, cv.w};
-        const uint32_t sc[8] = {s01.x, s01.y, s01.z, s01.w, s23.x, s23.y, s23.z, s23.w};
-        uint8_t *row = dst + t * kATileBytes + (c >> 1) * kABoxBytes + r * 128;
+    for (int i = 0; i < 8; ++i)
+        x[i] = mx_scale(((i < 4 ? sb.x : sb.y) >> (8 * (i & 3))) & 0xffu);
+    uint8_t *box = dst + t * kATileBytes + (fg >> 3) * kABoxBytes;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {  // features 32c + 8i .. + 7: code word i, scale words 2i, 2i+1
-            uint32_t o[4];
+    for (int i = 0; i < 8; ++i) {
+        const int r = 8 * rg + i;
+        const uint32_t cw = *reinterpret_cast<const uint32_t *>(tile + r * (BM / 2) + 4 * fg);
+        uint32_t o[4];
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {  // features 8i + 2h, 8i + 2h + 1
-                const uint32_t byte = (code[i] >> (8 * h)) & 0xffu;
-                const uint32_t sw = sc[2 * i + (h >> 1)];
-                const float v0 = e2m1_scaled(byte & 0xfu, mx_scale((sw >> (16 * (h & 1))) & 0xffu));
-                const float v1 = e2m1_scaled(byte >> 4, mx_scale((sw >> (16 * (h & 1) + 8)) & 0xffu));
-                const __nv_bfloat162 b = __floats2bfloat162_rn(v0, v1);
-                o[h] = *reinterpret_cast<const uint32_t *>(&b);
-            }
-            const int j = 4 * (c & 1) + i;
-            *reinterpret_cast<uint4 *>(row + ((j ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        for (int b = 0; b < 4; ++b) {
+            const __half2 h = __half2(__nv_cvt_fp4x2_to_halfraw2(
+                static_cast<__nv_fp4x2_storage_t>((cw >> (8 * b)) & 0xffu), __NV_E2M1));
+            const float2 f = __half22float2(h);
+            const __nv_bfloat162 v = __floats2bfloat162_rn(f.x * x[2 * b], f.y * x[2 * b + 1]);
+            o[b] = *reinterpret_cast<const uint32_t *>(&v);
         }
+        *reinterpret_cast<uint4 *>(box + r * 128 + (((fg & 7) ^ (r & 7)) << 4)) =
+            make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
