@@ -285,3 +285,28 @@ def test_plan_multi_kernel_unaligned_buffers():
     assert np.array_equal(pos_d.cpu().numpy(), ref["pos"])
     assert int(pos_buf[0]) == int(POISON_I) and int(pos_buf[n + 1]) == int(POISON_I)
     assert np.array_equal(o["tile_expert"][:R // tm].cpu().numpy(), ref["tile_expert"])
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_plan_multi_kernel_random_shapes(seed):
+    # above the one-launch size with random shapes: expert counts from 1 to
+    # 4096, tm from 1 to 256, Zipf-skewed or uniform ids, skipped slots and a
+    # few bad ids, T*k from 65K to 700K entries (ragged last block)
+    rng = np.random.default_rng(1000 + seed)
+    E = int(rng.choice([1, 7, 96, 500, 1024, 1031, 4096]))
+    k = int(rng.integers(1, 12))
+    T = int(rng.integers(65536 // k + 1, 700000 // k))
+    tm = int(rng.choice([1, 16, 48, 256]))
+    if seed % 2:
+        pop = 1.0 / np.arange(1, E + 1) ** 1.2
+        ids = rng.choice(E, size=(T, k), p=pop / pop.sum()).astype(np.int32)
+    else:
+        ids = rng.integers(0, E, size=(T, k), dtype=np.int32)
+    ids[rng.random(ids.shape) < 0.03] = -1
+    bad = rng.random(ids.shape) < 1e-5
+    ids[bad] = E + 5
+    w = rng.standard_normal((T, k)).astype(np.float32)
+    g, status = gpu_plan(ids, w, E, tm)
+    assert bool(status & B.STATUS_BAD_ID) == bool(bad.any())
+    fixed = np.where(ids >= E, -1, ids).astype(np.int32)
+    assert_same_plan(g, oracle.plan(fixed, w, E, tm), tm)
