@@ -74,15 +74,24 @@ constexpr int UMMA_K = 16;                        // K of one kind::f16 MMA
 constexpr uint32_t kABoxBytes = 64 * BK * 2;      // 64 features x 64 K rows
 constexpr uint32_t kATileBytes = 2 * kABoxBytes;  // 128 features
 constexpr uint32_t kBTileBytes = BN * BK * 2;     // 128 rows x 64 K
-constexpr int kThreads = 192;      // producer, MMA, four epilogue warps
-constexpr int kConvThreads = 256;  // eight warps widening E4M3 tiles (W8)
-constexpr int kThreadsW8 = kThreads + kConvThreads;
-constexpr int kMaxWarps = kThreadsW8 / 32;
+constexpr int kThreads = 192;      // producer, MMA (A tile 0), four epilogue warps
+constexpr int kConvThreads = 256;     // eight warps widening E4M3 tiles (W8)
+constexpr int kConvThreadsMx4 = 256;  // warps decoding MXFP4 tiles
+// One more warp, the last of the CTA, issues the MMAs of A tile 1.  Measured
+// on GB300, a thread that waits on a stage's mbarrier and then issues that
+// stage's MMAs cannot keep the tensor pipe busy once the MMAs are short (a
+// unit of <= 128 rows): eight MMAs of 128 x 64 x 16 with the wait and the
+// commit took 720 cycles a stage from one thread, 512 when two threads each
+// waited and issued the MMAs of one accumulator.
+constexpr int kIssuers = 2;
+constexpr int kMaxWarps =
+    (kThreads + (kConvThreads > kConvThreadsMx4 ? kConvThreads : kConvThreadsMx4)) / 32 + 1;
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for the stop path
 
 constexpr int kStages = 4;
+constexpr int kStagesMx4 = 4;
 constexpr uint32_t kStageBytes = 2 * kATileBytes + kBTileBytes;  // two A tiles + one B tile
 constexpr uint32_t kAccCols = 2 * BN;                            // two accumulators per buffer
 constexpr uint32_t kTmemCols = 2 * kAccCols;                     // double-buffered
@@ -128,7 +137,10 @@ struct RowMaps {
 template <int WM>
 struct Cfg {
     static constexpr bool kW8 = WM == kWiden || WM == kMx4;  // widening warps
-    static constexpr int kThreadsK = kW8 ? kThreadsW8 : kThreads;
+    static constexpr int kConvT = WM == kMx4 ? kConvThreadsMx4 : kConvThreads;
+    static constexpr int kThreadsK = (kW8 ? kThreads + kConvT : kThreads) + 32;
+    static constexpr int kMmaWarp1 = kThreadsK / 32 - 1;  // issues the MMAs of A tile 1
+    static constexpr int kS = WM == kMx4 ? kStagesMx4 : kStages;  // stages in the ring
     static constexpr uint32_t kStageB =
         WM == kMx4 ? kStageBytesMx4 : kW8 ? kStageBytesW8 : kStageBytes;
     // where the A tiles and the B rows sit in a stage
@@ -136,7 +148,7 @@ struct Cfg {
     static constexpr uint32_t kBOff =
         WM == kMx4 ? 0u : WM == kWiden ? 2 * kA8TileBytes : 2 * kATileBytes;
     static constexpr uint32_t kRingBytes =
-        kStages * kStageB + (kW8 ? kConvSlots * kConvSlotBytes : 0u);
+        kS * kStageB + (kW8 ? kConvSlots * kConvSlotBytes : 0u);
     static constexpr int kKStep = WM == kNative ? 128 : BK;  // K elements per stage
 };
 
@@ -153,7 +165,7 @@ struct Ctrl {
     uint64_t empty[S];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
-    uint64_t conv_full[kConvSlots];   // kWiden: widened A tiles ready (kConvThreads arrivals)
+    uint64_t conv_full[kConvSlots];   // W8: widened A tiles ready (Cfg::kConvT arrivals)
     uint64_t conv_empty[kConvSlots];  // kWiden: the MMAs are done with a slot
     uint64_t mma_done;
     uint32_t tmem_base;
@@ -182,7 +194,7 @@ struct FfnArgs {
 template <int WM>
 constexpr size_t ffn_smem_bytes(int E)
 {
-    return 1024 + size_t(Cfg<WM>::kRingBytes) + kStgBytes + sizeof(Ctrl<kStages>) +
+    return 1024 + size_t(Cfg<WM>::kRingBytes) + kStgBytes + sizeof(Ctrl<Cfg<WM>::kS>) +
            2 * BN * sizeof(int) + size_t(E + 1) * sizeof(int);
 }
 static_assert(ffn_smem_bytes<kBf16>(MOE_MAX_EXPERTS) <= 227 * 1024, "shared memory per CTA");
@@ -320,21 +332,26 @@ __device__ __forceinline__ float mx_scale(uint32_t S)
 // hardware's E2M1 -> f16 conversion (exact) and scaled by the features' 8
 // powers of two (computed once); each row's 8 bf16 values are one 16-byte
 // chunk, chunk fg & 7 of 64-feature box fg >> 3, at that index XOR (r mod 8).
+template <int NT>
 __device__ __forceinline__ void widen_mx4_stage(const uint8_t *src, uint8_t *dst, int ct, int nt)
 {
-    const int t = ct >> 7, rg = (ct >> 4) & 7, fg = ct & 15;
+    constexpr int kRows = 2 * BK * 16 / NT;  // K rows per thread (16 threads span a row)
+    constexpr int kGroups = BK / kRows;      // row groups per tile
+    static_assert(kRows * kGroups == BK && kRows <= 32 && 32 % kRows == 0, "decode split");
+    const int t = ct / (16 * kGroups), rg = (ct >> 4) % kGroups, fg = ct & 15;
     if (t >= nt)
         return;
     const uint8_t *tile = src + t * kMx4TileBytes;
-    const uint2 sb = *reinterpret_cast<const uint2 *>(tile + kMx4CodeBytes + (rg >> 2) * BM + 8 * fg);
+    const uint2 sb = *reinterpret_cast<const uint2 *>(tile + kMx4CodeBytes +
+                                                      (kRows * rg / 32) * BM + 8 * fg);
     float x[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
         x[i] = mx_scale(((i < 4 ? sb.x : sb.y) >> (8 * (i & 3))) & 0xffu);
     uint8_t *box = dst + t * kATileBytes + (fg >> 3) * kABoxBytes;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int r = 8 * rg + i;
+    for (int i = 0; i < kRows; ++i) {
+        const int r = kRows * rg + i;
         const uint32_t cw = *reinterpret_cast<const uint32_t *>(tile + r * (BM / 2) + 4 * fg);
         uint32_t o[4];
 #pragma unroll
@@ -364,7 +381,7 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
     constexpr bool W8 = Cfg<WM>::kW8, A8 = WM == kNative, MX4 = WM == kMx4;
     constexpr bool SCALED = WM == kWiden || WM == kNative;  // scales in the epilogue
     static_assert(!(GATHER && SCALED), "gathered rows come with bf16 weights only");
-    constexpr int S = kStages;
+    constexpr int S = Cfg<WM>::kS;
     constexpr int UM = Kind<GATED>::kUnitM;
     constexpr uint32_t SB = Cfg<WM>::kStageB;
     extern __shared__ uint8_t smem_raw[];
@@ -384,17 +401,17 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&ctl->full[s], 1);
-            mbar_init(&ctl->empty[s], 1);
+            mbar_init(&ctl->empty[s], kIssuers);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&ctl->tmem_full[b], 1);
+            mbar_init(&ctl->tmem_full[b], kIssuers);
             mbar_init(&ctl->tmem_empty[b], kEpiThreads);
         }
         for (int c = 0; c < kConvSlots; ++c) {
-            mbar_init(&ctl->conv_full[c], kConvThreads);
-            mbar_init(&ctl->conv_empty[c], 1);
+            mbar_init(&ctl->conv_full[c], Cfg<WM>::kConvT);
+            mbar_init(&ctl->conv_empty[c], kIssuers);
         }
-        mbar_init(&ctl->mma_done, 1);
+        mbar_init(&ctl->mma_done, kIssuers);
         ctl->abort_flag = 0;
         ctl->epi_stop = 0;
         fence_mbar_init();
@@ -544,8 +561,9 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                         mbar_drain(&ctl->full[s], (issued_par >> s) & 1u);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ---- MMA issuer ----
+    } else if (warp == 1 || warp == Cfg<WM>::kMmaWarp1) {
+        // ---- MMA issuers: warp 1 for A tile 0, the last warp for A tile 1 ----
+        const int tsel = warp == 1 ? 0 : 1;
         if (lane == 0) {
             int stage = 0, abuf = 0, cslot = 0;
             uint32_t phase = 0, aphase = 0, cphase = 0;
@@ -553,13 +571,14 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
             for (int64_t u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
                 const Unit w = map_unit(u, n_mt, chunk_start, p.E, p.offsets);
                 const int m0 = w.mt * UM;
-                const bool use1 = tile_base(m0, 1) < p.M;  // second A tile holds real features
+                // this issuer's A tile holds real features (tile 0 always does)
+                const bool mine = tsel == 0 || tile_base(m0, 1) < p.M;
                 if (!mbar_wait(&ctl->tmem_empty[abuf], aphase ^ 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t d0 = tmem_base + uint32_t(abuf) * kAccCols;
+                const uint32_t d0 = tmem_base + uint32_t(abuf) * kAccCols + uint32_t(tsel) * BN;
                 const uint32_t idesc = A8 ? idesc_e4m3_f32(BM, uint32_t(w.nrows))
                                           : idesc_bf16_f32(BM, uint32_t(w.nrows), 1u, 0u);
                 for (int kb = 0; kb < nk; ++kb) {
@@ -570,37 +589,28 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                     }
                     tc_fence_after_sync();
                     const uint32_t sst = smem_u32(smem + stage * SB);
-                    const uint32_t sa = W8 ? smem_u32(conv + cslot * kConvSlotBytes) : sst;
+                    const uint32_t sa = (W8 ? smem_u32(conv + cslot * kConvSlotBytes) : sst) +
+                                        uint32_t(tsel) * kATileBytes;  // this issuer's A tile
                     const uint32_t sb = sst + Cfg<WM>::kBOff;
-                    if (A8) {
+                    if (!mine) {
+                        // no MMAs; the commits below still count this issuer's arrival
+                    } else if (A8) {
                         // both operands K-major 128-byte rows; K = 32 codes (32 bytes)
                         // per instruction, four per stage
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t bdesc = smem_desc_sw128(sb + kk * 32, 16, 1024);
-                            const uint32_t acc = (kb | kk) != 0;
-                            tc_mma_f8(d0, smem_desc_sw128(sa + kk * 32, 16, 1024), bdesc, idesc,
-                                      acc);
-                            if (use1)
-                                tc_mma_f8(d0 + BN,
-                                          smem_desc_sw128(sa + kATileBytes + kk * 32, 16, 1024),
-                                          bdesc, idesc, acc);
-                        }
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc_mma_f8(d0, smem_desc_sw128(sa + kk * 32, 16, 1024),
+                                      smem_desc_sw128(sb + kk * 32, 16, 1024), idesc,
+                                      (kb | kk) != 0);
                     } else {
 #pragma unroll
-                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                            // B: K-major rows of 128 B; the K step moves 32 B inside the row.
-                            const uint64_t bdesc = smem_desc_sw128(sb + kk * UMMA_K * 2, 16, 1024);
-                            // A: MN-major, one 128-byte row per K index; the K step moves 16 rows.
-                            const uint32_t acc = (kb | kk) != 0;
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                            // A: MN-major, one 128-byte row per K index, the K step moves
+                            // 16 rows; B: K-major rows of 128 B, the K step moves 32 B
+                            // inside the row.
                             tc_mma_f16(d0, smem_desc_sw128(sa + kk * UMMA_K * 128, kABoxBytes, 1024),
-                                       bdesc, idesc, acc);
-                            if (use1)
-                                tc_mma_f16(d0 + BN,
-                                           smem_desc_sw128(sa + kATileBytes + kk * UMMA_K * 128,
-                                                           kABoxBytes, 1024),
-                                           bdesc, idesc, acc);
-                        }
+                                       smem_desc_sw128(sb + kk * UMMA_K * 2, 16, 1024), idesc,
+                                       (kb | kk) != 0);
                     }
                     tc_commit(&ctl->empty[stage]);  // frees the stage once these MMAs finish
                     if (++stage == S) {
@@ -629,7 +639,7 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
         __syncwarp();
     } else if (W8 && warp >= kThreads / 32) {
         // ---- widening (W8): E4M3 A tiles of a stage -> bf16 tiles of a slot ----
-        const int ct = int(threadIdx.x) - kThreads;  // 0..kConvThreads-1
+        const int ct = int(threadIdx.x) - kThreads;  // 0 .. Cfg<WM>::kConvT - 1
         int stage = 0, cslot = 0;
         uint32_t phase = 0, cphase = 0;
         bool ok = true;
@@ -645,7 +655,7 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                 const uint8_t *src = smem + stage * SB + Cfg<WM>::kAOff;
                 uint8_t *dst = conv + cslot * kConvSlotBytes;
                 if (MX4) {
-                    widen_mx4_stage(src, dst, ct, nt);
+                    widen_mx4_stage<Cfg<WM>::kConvT>(src, dst, ct, nt);
                 } else {
                 // a tile is 64 K rows x 8 chunks of 16 codes.  Chunk c of row
                 // r (features 16c..16c+15)
@@ -1010,7 +1020,7 @@ cudaError_t launch_ffn_gate_up(const void *xs, const void *Wg, const void *Wu,
         return err;
     const FfnArgs a{offsets, nullptr, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f,
                     stall_cta, nullptr, nullptr, nullptr};
-    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<kBf16>(E),
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(Cfg<kBf16>::kThreadsK), ffn_smem_bytes<kBf16>(E),
                       stream, mg, mu, mx, mo, mo, mo, a);
 }
 
@@ -1033,7 +1043,7 @@ cudaError_t launch_ffn_gate_up_rows(const void *x, int T, const int32_t *srt_tok
         return err;
     const FfnArgs a{offsets, srt_tok, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f,
                     -1, nullptr, nullptr, nullptr};
-    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<kBf16>(E),
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(Cfg<kBf16>::kThreadsK), ffn_smem_bytes<kBf16>(E),
                       stream, mg, mu, mx, mo, mo, mo, a);
 }
 
@@ -1055,7 +1065,7 @@ cudaError_t launch_ffn_down(const void *H, const void *Wd, const int32_t *offset
         return err;
     const FfnArgs a{offsets, nullptr, srt_w, static_cast<uint16_t *>(Ys), status, cap, E, f, d,
                     -1, nullptr, nullptr, nullptr};
-    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<kBf16>(E),
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(Cfg<kBf16>::kThreadsK), ffn_smem_bytes<kBf16>(E),
                       stream, mw, mw, mh, mo, mo, mo, a);
 }
 
@@ -1079,7 +1089,7 @@ cudaError_t launch_ffn_gate_up_e4m3(const void *xs, const uint8_t *Wg, const flo
         return err;
     const FfnArgs a{offsets, nullptr, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f,
                     -1, sg, su, nullptr};
-    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreadsW8), ffn_smem_bytes<kWiden>(E),
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(Cfg<kWiden>::kThreadsK), ffn_smem_bytes<kWiden>(E),
                       stream, mg, mu, mx, mo, mo, mo, a);
 }
 
@@ -1103,7 +1113,7 @@ cudaError_t launch_ffn_gate_up_native(const uint8_t *xs8, const int32_t *xexp, c
         return err;
     const FfnArgs a{offsets, nullptr, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f,
                     -1, sg, su, xexp};
-    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<kNative>(E),
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(Cfg<kNative>::kThreadsK), ffn_smem_bytes<kNative>(E),
                       stream, mg, mu, mx, mo, mo, mo, a);
 }
 
@@ -1126,7 +1136,7 @@ cudaError_t launch_ffn_down_native(const uint8_t *H8, const int32_t *hexp, const
         return err;
     const FfnArgs a{offsets, nullptr, srt_w, static_cast<uint16_t *>(Ys), status, cap, E, f, d,
                     -1, sd, sd, hexp};
-    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreads), ffn_smem_bytes<kNative>(E),
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(Cfg<kNative>::kThreadsK), ffn_smem_bytes<kNative>(E),
                       stream, mw, mw, mh, mo, mo, mo, a);
 }
 
@@ -1148,7 +1158,7 @@ cudaError_t launch_ffn_down_e4m3(const void *H, const uint8_t *Wd, const float *
         return err;
     const FfnArgs a{offsets, nullptr, srt_w, static_cast<uint16_t *>(Ys), status, cap, E, f, d,
                     -1, sd, sd, nullptr};
-    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreadsW8), ffn_smem_bytes<kWiden>(E),
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(Cfg<kWiden>::kThreadsK), ffn_smem_bytes<kWiden>(E),
                       stream, mw, mw, mh, mo, mo, mo, a);
 }
 
@@ -1174,7 +1184,7 @@ cudaError_t launch_ffn_gate_up_mxfp4(const void *xs, const uint8_t *Wg, const ui
         return err;
     const FfnArgs a{offsets, nullptr, nullptr, static_cast<uint16_t *>(H), status, cap, E, d, f,
                     -1, nullptr, nullptr, nullptr};
-    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreadsW8), ffn_smem_bytes<kMx4>(E),
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(Cfg<kMx4>::kThreadsK), ffn_smem_bytes<kMx4>(E),
                       stream, mg, mu, mx, mo, msg, msu, a);
 }
 
@@ -1197,7 +1207,7 @@ cudaError_t launch_ffn_down_mxfp4(const void *H, const uint8_t *Wd, const uint8_
         return err;
     const FfnArgs a{offsets, nullptr, srt_w, static_cast<uint16_t *>(Ys), status, cap, E, f, d,
                     -1, nullptr, nullptr, nullptr};
-    return launch_pdl(kern, dim3(device_sm_count()), dim3(kThreadsW8), ffn_smem_bytes<kMx4>(E),
+    return launch_pdl(kern, dim3(device_sm_count()), dim3(Cfg<kMx4>::kThreadsK), ffn_smem_bytes<kMx4>(E),
                       stream, mw, mw, mh, mo, msd, msd, a);
 }
 

@@ -9,7 +9,8 @@ whole layer once through the stage entry points, then runs the chosen stage
 ``--iters`` more times.  Every stage call goes through the C ABI.  With
 ``--weights f8`` the gather, gate/up and down stages are the E4M3-operand
 ones (weights quantized on the device first; down includes the pass that
-makes H's rows E4M3).  ``--plan-entries N`` runs the plan alone on N flat
+makes H's rows E4M3); with ``--weights mxfp4`` gate/up, down and the layer
+run on MXFP4 weights (quantized on the device first), rows in bf16.  ``--plan-entries N`` runs the plan alone on N flat
 entries (k = 10, E = 512, tm = 16, ids uniform over the experts and drawn
 on the device, as in the bench's plan sweep).
 """
@@ -35,7 +36,7 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=0, help="override T (0: the workload's)")
     ap.add_argument("--stage", choices=STAGES, default="gate_up")
     ap.add_argument("--iters", type=int, default=3)
-    ap.add_argument("--weights", choices=("bf16", "f8"), default="bf16")
+    ap.add_argument("--weights", choices=("bf16", "f8", "mxfp4"), default="bf16")
     ap.add_argument("--plan-entries", type=int, default=0,
                     help="run only the plan on this many uniform entries")
     a = ap.parse_args(argv)
@@ -60,6 +61,7 @@ def main(argv=None):
     o = B.plan(ids, w, wl.E, wl.tm, cap=cap)
     xs = B.gather(x, o["srt_tok"], o["offsets"], wl.E, cap)
     f8 = a.weights == "f8"
+    mx4 = a.weights == "mxfp4"
     if not plan_only:
         Wg, Wu, Wd = (d16(inp[n]) for n in ("Wg", "Wu", "Wd"))
         H, Ys = B.expert_ffn(xs, Wg, Wu, Wd, o["offsets"], o["srt_w"], cap)
@@ -68,6 +70,8 @@ def main(argv=None):
             Wg, Wu, Wd = (B.quantize_e4m3(t, kmajor=True) for t in (Wg, Wu, Wd))
             x8, xe = B.gather_e4m3(x, o["srt_tok"], o["offsets"], wl.E, cap)
             H8, he = B.rows_e4m3(H, o["offsets"], wl.E, cap)
+        if mx4:
+            Wg, Wu, Wd = (B.quantize_mxfp4(t) for t in (Wg, Wu, Wd))
     calls = {
         "plan": lambda: B.plan(ids, w, wl.E, wl.tm, cap=cap, out=o),
         "gather": lambda: B.gather(x, o["srt_tok"], o["offsets"], wl.E, cap, xs=xs),
@@ -88,6 +92,12 @@ def main(argv=None):
             "down": down_f8,
             "layer": lambda: B.layer_forward_e4m3(x, ids, w, Wg, Wu, Wd, wl.tm, y=y,
                                                   act_e4m3=True),
+        })
+    if mx4 and not plan_only:
+        calls.update({
+            "gate_up": lambda: B.ffn_gate_up_mxfp4(xs, Wg, Wu, o["offsets"], cap, H=H),
+            "down": lambda: B.ffn_down_mxfp4(H, Wd, o["offsets"], o["srt_w"], cap, Ys=Ys),
+            "layer": lambda: B.layer_forward_mxfp4(x, ids, w, Wg, Wu, Wd, wl.tm, y=y),
         })
     for _ in range(a.iters):
         calls[a.stage]()
