@@ -409,7 +409,7 @@ def run_native(args, rank, world, local):
         del layer8
 
     # MXFP4 expert weights (4-bit E2M1 codes, power-of-two scale per 32 along
-    # K; decoded to bf16 in shared memory, bf16 activations), timed the same way
+    # K; decoded to bf16 into tensor memory, bf16 activations), timed the same way
     mx4 = None
     if not e4m3 and not args.no_fp8:
         layer4 = B.MoeLayer.quantized_mxfp4(Wg, Wu, Wd, tm=wl.tm)
@@ -443,7 +443,7 @@ def run_native(args, rank, world, local):
                "ms_per_step": statistics.mean(ms4), "steps": args.steps,
                "gate_up_us": statistics.median(gu4), "down_us": statistics.median(dn4),
                "arithmetic": "MXFP4 weights (4-bit E2M1 codes, power-of-two scale per 32 along "
-                             "K, decoded exactly to bf16 in shared memory); bf16 activations, "
+                             "K, decoded exactly to bf16 into tensor memory); bf16 activations, "
                              "fp32 accumulation; bf16 H, Ys, y",
                "weight_bytes_active": alg["active"] * 3 * wl.d * wl.f // 2,
                "gpu_launches": KERNELS_PER_LAYER * args.steps}

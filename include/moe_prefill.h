@@ -410,18 +410,19 @@ MOE_API int moe_layer_forward_f8(const void *x, const int32_t *ids, const float 
  * and the weight the GEMMs use is value(code) * 2^x, which is exactly a bf16
  * value.  Activations, H, Ys and y stay bf16, accumulation fp32: the layer
  * on MXFP4 weights is the bf16 layer on the dequantized weights.  The GEMMs
- * load the 4-bit codes and the scales with TMA and decode them to bf16 in
- * shared memory.
+ * load the 4-bit codes and the scales with TMA and decode them to bf16 into
+ * tensor memory, where the tensor cores read them.
  *
  * moe_quantize_mxfp4 -- W bf16 [E, K, M] (M = output features, contiguous;
- * K a multiple of 32, M even; 4-byte aligned) -> codes uint8 [E, K, M/2]
- * (feature m even in the low four bits of byte m/2, m + 1 in the high four)
- * and scales uint8 [E, K/32, M] (S; 2-byte aligned).  W must be finite.  A
- * one-time preparation, not part of the layer.
+ * K a multiple of 32, M even; 4-byte aligned) -> codes uint8 [E, M, K/2]
+ * (each output feature's codes contiguous along K: k even in the low four
+ * bits of byte k/2, k + 1 in the high four; 16-byte aligned) and scales
+ * uint8 [E, K/32, M] (S).  W must be finite.  A one-time preparation, not
+ * part of the layer.
  *
  * moe_ffn_gate_up_mxfp4 / moe_ffn_down_mxfp4 -- moe_ffn_gate_up /
- * moe_ffn_down with MXFP4 weights: Wg, Wu codes [E, d, f/2] with scales
- * xg, xu [E, d/32, f]; Wd codes [E, f, d/2] with scales xd [E, f/32, d]
+ * moe_ffn_down with MXFP4 weights: Wg, Wu codes [E, f, d/2] with scales
+ * xg, xu [E, d/32, f]; Wd codes [E, d, f/2] with scales xd [E, f/32, d]
  * (codes and scales 16-byte aligned).  Everything else as in the bf16 calls.
  *
  * moe_layer_forward_mxfp4 -- moe_layer_forward with MXFP4 weights (as

@@ -512,8 +512,8 @@ def layer_forward_e4m3(x, ids, w, Wg, Wu, Wd, tm: int, y=None, ws=None, act_e4m3
 
 
 class Mxfp4(NamedTuple):
-    """MXFP4 weights of one projection: codes uint8 [E, K, M/2] (two 4-bit
-    E2M1 codes a byte, feature m even in the low four bits) and scale
+    """MXFP4 weights of one projection: codes uint8 [E, M, K/2] (two 4-bit
+    E2M1 codes a byte along K, k even in the low four bits) and scale
     exponents uint8 [E, K/32, M] (scale 2^(S-127) per block of 32 along K)."""
     codes: torch.Tensor
     scales: torch.Tensor
@@ -522,7 +522,7 @@ class Mxfp4(NamedTuple):
 def quantize_mxfp4(W) -> Mxfp4:
     """moe_quantize_mxfp4: bf16 W [E, K, M] -> Mxfp4(codes, scales)."""
     E, K, M = W.shape
-    codes = torch.empty((E, K, M // 2), dtype=torch.uint8, device=W.device)
+    codes = torch.empty((E, M, K // 2), dtype=torch.uint8, device=W.device)
     scales = torch.empty((E, K // 32, M), dtype=torch.uint8, device=W.device)
     with torch.cuda.device(W.device):
         rc = lib().moe_quantize_mxfp4(_ptr(W), E, K, M, _ptr(codes), _ptr(scales),
@@ -532,8 +532,8 @@ def quantize_mxfp4(W) -> Mxfp4:
 
 
 def ffn_gate_up_mxfp4(xs, Wg: Mxfp4, Wu: Mxfp4, offsets, cap: int, H=None, status=None):
-    E, d, f2 = Wg.codes.shape
-    f = 2 * f2
+    E, f, d2 = Wg.codes.shape
+    d = 2 * d2
     if H is None:
         H = torch.empty((max(cap, 1), f), dtype=torch.bfloat16, device=xs.device)
     with torch.cuda.device(xs.device):
@@ -545,8 +545,8 @@ def ffn_gate_up_mxfp4(xs, Wg: Mxfp4, Wu: Mxfp4, offsets, cap: int, H=None, statu
 
 
 def ffn_down_mxfp4(H, Wd: Mxfp4, offsets, srt_w, cap: int, Ys=None, status=None):
-    E, f, d2 = Wd.codes.shape
-    d = 2 * d2
+    E, d, f2 = Wd.codes.shape
+    f = 2 * f2
     if Ys is None:
         Ys = torch.empty((max(cap, 1), d), dtype=torch.bfloat16, device=H.device)
     with torch.cuda.device(H.device):
@@ -619,8 +619,9 @@ class MoeLayer:
             if act_e4m3 or not (isinstance(Wu, Mxfp4) and isinstance(Wd, Mxfp4)):
                 raise ValueError("MXFP4 weights: all three projections, bf16 activations")
             self.tm, self.act_e4m3, self.e4m3 = tm, False, False
-            self.E, self.f = Wd.codes.shape[0], Wd.codes.shape[1]
-            self.d = 2 * Wd.codes.shape[2]
+            # Wd codes [E, d, f/2]
+            self.E, self.d = Wd.codes.shape[0], Wd.codes.shape[1]
+            self.f = 2 * Wd.codes.shape[2]
             self.device = Wd.codes.device
             self._ws = None
             self._host_ws = None

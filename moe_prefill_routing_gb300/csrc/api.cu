@@ -417,7 +417,7 @@ int moe_quantize_mxfp4(const void *W, int E, int K, int M, uint8_t *codes, uint8
         return MOE_ERR_SHAPE;
     if (!W || !codes || !scales)
         return MOE_ERR_NULL;
-    if (!aligned(W, 4) || !aligned(scales, 2))
+    if (!aligned(W, 4) || !aligned(codes, 16))
         return MOE_ERR_ALIGN;
     return cuda_rc(moe::launch_quantize_mxfp4(W, E, K, M, codes, scales, as_stream(stream)));
 }

@@ -91,7 +91,7 @@ constexpr uint32_t kFull = 0xffffffffu;
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for the stop path
 
 constexpr int kStages = 4;
-constexpr int kStagesMx4 = 4;
+constexpr int kStagesMx4 = 7;  // no widened tiles in shared memory: room for more stages
 constexpr uint32_t kStageBytes = 2 * kATileBytes + kBTileBytes;  // two A tiles + one B tile
 constexpr uint32_t kAccCols = 2 * BN;                            // two accumulators per buffer
 constexpr uint32_t kTmemCols = 2 * kAccCols;                     // double-buffered
@@ -106,18 +106,29 @@ constexpr uint32_t kA8TileBytes = BM * BK;                       // 8 KB
 constexpr uint32_t kStageBytesW8 = 2 * kA8TileBytes + kBTileBytes;
 constexpr int kConvSlots = 2;
 constexpr uint32_t kConvSlotBytes = 2 * kATileBytes;
+constexpr int kMx4Slots = 4;      // kMx4: decoded A tiles in tensor memory, four slots
+constexpr uint32_t kMx4SlotCol = kAccCols;       // first TMEM column of the slots (256)
+constexpr uint32_t kMx4SlotCols = 2 * (BK / 2);     // a slot: two tiles of 64 K = 32 columns
+constexpr int kMaxSlots = kConvSlots > kMx4Slots ? kConvSlots : kMx4Slots;
 
 enum WeightMode : int { kBf16 = 0, kWiden = 1, kNative = 2, kMx4 = 3 };
 
-// kMx4: MXFP4 weights -- 4-bit E2M1 codes, two per byte along the output
-// features ([E, K, M/2]), and one power-of-two scale 2^(S-127) per (expert,
-// block of 32 along K, output feature) ([E, K/32, M] exponent bytes).  A
-// stage holds the B rows first (16 KB, 1024-byte aligned), then per A tile
-// the codes (64 K rows x 64 bytes) and the scales (2 blocks x 128 bytes).
-// The widening warps decode code x 2^(S-127) into the same bf16 tiles the
-// other widening mode writes (exact: every such value is a bf16 value), and
-// the same bf16 MMAs run; the epilogue applies no scale.
-constexpr uint32_t kMx4CodeBytes = BM / 2 * BK;   // 4 KB: 128 features x 64 K, 4 bits each
+// kMx4: MXFP4 weights -- 4-bit E2M1 codes, two per byte along K (the
+// reduction axis; [E, M, K/2], k even in the low four bits), and one
+// power-of-two scale 2^(S-127) per (expert, block of 32 along K, output
+// feature) ([E, K/32, M] exponent bytes).  A stage holds the B rows first
+// (16 KB, 1024-byte aligned), then per A tile the codes (128 features x 32
+// bytes) and the scales (2 blocks x 128 bytes).  The decoding warps turn
+// code x 2^(S-127) into bf16 (exact: every such value is a bf16 value) and
+// write each A tile straight into tensor memory (tcgen05.st: lane = output
+// feature, one 32-bit column per two K), where the MMAs read it as their A
+// operand ([a_tmem] form); B stays in shared memory.  The decoded tiles
+// never pass through shared memory, whose bandwidth bounded the design that
+// staged them there (the stores, the MMAs' A reads and the TMA writes all
+// shared it).  Tensor memory then holds one accumulator buffer (columns 0 ..
+// 255) and four decoded-A slots (256 .. 511); the epilogue of a unit and the
+// next unit's MMAs do not overlap.  The epilogue applies no scale.
+constexpr uint32_t kMx4CodeBytes = BM * BK / 2;   // 4 KB: 128 features x 64 K, 4 bits each
 constexpr uint32_t kMx4ScaleBytes = BM * (BK / 32);  // 256 B: 128 features x 2 blocks
 constexpr uint32_t kMx4TileBytes = kMx4CodeBytes + kMx4ScaleBytes;
 constexpr uint32_t kStageBytesMx4 = (kBTileBytes + 2 * kMx4TileBytes + 1023) / 1024 * 1024;
@@ -148,7 +159,9 @@ struct Cfg {
     static constexpr uint32_t kBOff =
         WM == kMx4 ? 0u : WM == kWiden ? 2 * kA8TileBytes : 2 * kATileBytes;
     static constexpr uint32_t kRingBytes =
-        kS * kStageB + (kW8 ? kConvSlots * kConvSlotBytes : 0u);
+        kS * kStageB + (WM == kWiden ? kConvSlots * kConvSlotBytes : 0u);
+    static constexpr int kSlots = WM == kMx4 ? kMx4Slots : kConvSlots;  // widened-tile slots
+    static constexpr int kAccBufs = WM == kMx4 ? 1 : 2;  // accumulator buffers in TMEM
     static constexpr int kKStep = WM == kNative ? 128 : BK;  // K elements per stage
 };
 
@@ -165,8 +178,8 @@ struct Ctrl {
     uint64_t empty[S];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
-    uint64_t conv_full[kConvSlots];   // W8: widened A tiles ready (Cfg::kConvT arrivals)
-    uint64_t conv_empty[kConvSlots];  // kWiden: the MMAs are done with a slot
+    uint64_t conv_full[kMaxSlots];   // W8: widened A tiles ready (one arrival per warp)
+    uint64_t conv_empty[kMaxSlots];  // W8: the MMAs are done with a slot
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -323,48 +336,95 @@ __device__ __forceinline__ float mx_scale(uint32_t S)
     return __uint_as_float(S ? S << 23 : 0x00400000u);
 }
 
-// One stage of MXFP4 A tiles (nt of them) -> bf16 tiles of a widening slot,
-// in the layout a 128-byte-swizzled TMA load of bf16 weights would produce.
-// Thread ct takes tile ct >> 7, the 8 K rows 8 rg .. 8 rg + 7 (rg = (ct >> 4)
-// & 7, all in scale block rg >> 2) and the 8 features 8 fg .. 8 fg + 7 (fg =
-// ct & 15): per row one 4-byte word of codes (byte b: feature 8 fg + 2b in
-// its low four bits, + 1 in its high), decoded two codes at a time by the
-// hardware's E2M1 -> f16 conversion (exact) and scaled by the features' 8
-// powers of two (computed once); each row's 8 bf16 values are one 16-byte
-// chunk, chunk fg & 7 of 64-feature box fg >> 3, at that index XOR (r mod 8).
-template <int NT>
-__device__ __forceinline__ void widen_mx4_stage(const uint8_t *src, uint8_t *dst, int ct, int nt)
+// Two E2M1 codes of one byte (k even in the low four bits) -> the bf16 pair
+// value(code) x 2^-126 (low half: the even k), exactly: the three magnitude
+// bits (e1 e0 m) placed at bf16 bits 8..6 are the exponent field e1 e0 and
+// the mantissa's top bit, which reads value(code) x 2^-126 for every code
+// (e = 0 lands on the subnormal 2^-127 = 0.5 x 2^-126), and the sign at bit
+// 15.  Four bytes of w at once: byte b of ev / od holds the even / odd code
+// of pair b; __byte_perm brings pair b's two codes to bytes 0 and 2.
+__device__ __forceinline__ uint32_t e2m1_pair_bits(uint32_t ev, uint32_t od, int b)
 {
-    constexpr int kRows = 2 * BK * 16 / NT;  // K rows per thread (16 threads span a row)
-    constexpr int kGroups = BK / kRows;      // row groups per tile
-    static_assert(kRows * kGroups == BK && kRows <= 32 && 32 % kRows == 0, "decode split");
-    const int t = ct / (16 * kGroups), rg = (ct >> 4) % kGroups, fg = ct & 15;
+    const uint32_t wb = __byte_perm(ev, od, 0x4400u + 0x1111u * uint32_t(b));
+    return ((wb << 6) & 0x01C001C0u) | ((wb << 12) & 0x80008000u);
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&v)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+        "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+        "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait()
+{
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// One stage of an MXFP4 A tile -> bf16 in tensor memory.  Decoding thread
+// ct (eight warps) takes tile ct >> 7 and output feature m = 32 (warp mod 4)
+// + lane, the TMEM lane its warp may write: the feature's 64 codes of the
+// stage (32 bytes) and its two block scales, 64 bf16 values = 32 columns at
+// slot + 32 t (column j: k = 2j low, 2j + 1 high), one tcgen05.st.  The
+// value is code x 2^(S-127): from the bit placement above times the bf16
+// 2^(S-1) (one bf16x2 multiply, exact while S <= 128: weights below 8 in
+// magnitude); a block with a larger S takes the f16 conversion and an fp32
+// multiply, exact as well.
+__device__ __forceinline__ void decode_mx4_tile(const uint8_t *src, int ct, int nt,
+                                                uint32_t slot_taddr)
+{
+    // a warp may write only its own quadrant of TMEM lanes: warp index mod 4
+    const int t = ct >> 7, lane = ct & 31, q = int(threadIdx.x >> 5) & 3;
     if (t >= nt)
         return;
+    const int m = 32 * q + lane;
     const uint8_t *tile = src + t * kMx4TileBytes;
-    const uint2 sb = *reinterpret_cast<const uint2 *>(tile + kMx4CodeBytes +
-                                                      (kRows * rg / 32) * BM + 8 * fg);
-    float x[8];
+    // the feature's 32 bytes in two 16-byte loads, the halves in a lane-dependent
+    // order so that each quarter-warp covers all 32 banks
+    const int h0 = (lane >> 2) & 1;
+    const uint4 c0 = *reinterpret_cast<const uint4 *>(tile + m * 32 + 16 * h0);
+    const uint4 c1 = *reinterpret_cast<const uint4 *>(tile + m * 32 + 16 * (h0 ^ 1));
+    const uint4 lo = h0 ? c1 : c0, hi = h0 ? c0 : c1;  // k 0..31 (block 0), 32..63 (block 1)
+    const uint32_t s0 = tile[kMx4CodeBytes + m], s1 = tile[kMx4CodeBytes + BM + m];
+    const uint32_t cw[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    uint32_t v[32];
+    if (s0 <= 128u && s1 <= 128u) {
+        const uint32_t sc0 = ((s0 + 126u) << 7) * 0x10001u, sc1 = ((s1 + 126u) << 7) * 0x10001u;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-        x[i] = mx_scale(((i < 4 ? sb.x : sb.y) >> (8 * (i & 3))) & 0xffu);
-    uint8_t *box = dst + t * kATileBytes + (fg >> 3) * kABoxBytes;
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t ev = cw[i] & 0x0F0F0F0Fu, od = (cw[i] >> 4) & 0x0F0F0F0Fu;
+            const uint32_t sc = i < 4 ? sc0 : sc1;
 #pragma unroll
-    for (int i = 0; i < kRows; ++i) {
-        const int r = kRows * rg + i;
-        const uint32_t cw = *reinterpret_cast<const uint32_t *>(tile + r * (BM / 2) + 4 * fg);
-        uint32_t o[4];
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const __half2 h = __half2(__nv_cvt_fp4x2_to_halfraw2(
-                static_cast<__nv_fp4x2_storage_t>((cw >> (8 * b)) & 0xffu), __NV_E2M1));
-            const float2 f = __half22float2(h);
-            const __nv_bfloat162 v = __floats2bfloat162_rn(f.x * x[2 * b], f.y * x[2 * b + 1]);
-            o[b] = *reinterpret_cast<const uint32_t *>(&v);
+            for (int b = 0; b < 4; ++b) {
+                const uint32_t u = e2m1_pair_bits(ev, od, b);
+                const __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&u),
+                                                 *reinterpret_cast<const __nv_bfloat162 *>(&sc));
+                v[4 * i + b] = *reinterpret_cast<const uint32_t *>(&r);
+            }
         }
-        *reinterpret_cast<uint4 *>(box + r * 128 + (((fg & 7) ^ (r & 7)) << 4)) =
-            make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+        const float x0 = mx_scale(s0), x1 = mx_scale(s1);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float x = i < 4 ? x0 : x1;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const float2 f = __half22float2(__half2(__nv_cvt_fp4x2_to_halfraw2(
+                    static_cast<__nv_fp4x2_storage_t>((cw[i] >> (8 * b)) & 0xffu), __NV_E2M1)));
+                const __nv_bfloat162 r = __floats2bfloat162_rn(f.x * x, f.y * x);
+                v[4 * i + b] = *reinterpret_cast<const uint32_t *>(&r);
+            }
+        }
     }
+    tmem_st_32x32b_x32(slot_taddr + (uint32_t(32 * q) << 16) + uint32_t(t) * (BK / 2), v);
+    tmem_st_wait();
 }
 
 // GATHER: the B rows of a unit are token rows of x fetched by index
@@ -407,8 +467,8 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
             mbar_init(&ctl->tmem_full[b], kIssuers);
             mbar_init(&ctl->tmem_empty[b], kEpiThreads);
         }
-        for (int c = 0; c < kConvSlots; ++c) {
-            mbar_init(&ctl->conv_full[c], Cfg<WM>::kConvT);
+        for (int c = 0; c < Cfg<WM>::kSlots; ++c) {
+            mbar_init(&ctl->conv_full[c], Cfg<WM>::kConvT / 32);
             mbar_init(&ctl->conv_empty[c], kIssuers);
         }
         mbar_init(&ctl->mma_done, kIssuers);
@@ -497,11 +557,11 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                     for (int t = 0; t < 2; ++t) {
                         const CUtensorMap *m = (GATED && t == 1) ? &map_a1 : &map_a0;
                         if (MX4) {
-                            // codes [E, K, M/2]: (byte column, k, expert); scales
-                            // [E, K/32, M]: (feature, block, expert)
+                            // codes [E, M, K/2]: (byte column along K, feature,
+                            // expert); scales [E, K/32, M]: (feature, block, expert)
                             if (tile_base(m0, t) < p.M) {
                                 uint8_t *st = sa + t * kMx4TileBytes;
-                                tma_load_3d(st, m, fb, tile_base(m0, t) / 2, k0, w.e);
+                                tma_load_3d(st, m, fb, k0 / 2, tile_base(m0, t), w.e);
                                 tma_load_3d(st + kMx4CodeBytes, (GATED && t == 1) ? &map_s1 : &map_s0,
                                             fb, tile_base(m0, t), k0 / 32, w.e);
                             }
@@ -579,8 +639,10 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d0 = tmem_base + uint32_t(abuf) * kAccCols + uint32_t(tsel) * BN;
+                // kMx4: this issuer's decoded A tile in the slot's TMEM columns
+                const uint32_t a_tm = tmem_base + kMx4SlotCol + uint32_t(tsel) * (BK / 2);
                 const uint32_t idesc = A8 ? idesc_e4m3_f32(BM, uint32_t(w.nrows))
-                                          : idesc_bf16_f32(BM, uint32_t(w.nrows), 1u, 0u);
+                                          : idesc_bf16_f32(BM, uint32_t(w.nrows), MX4 ? 0u : 1u, 0u);
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait(&ctl->full[stage], phase, abort_flag) ||
                         (W8 && !mbar_wait(&ctl->conv_full[cslot], cphase, abort_flag))) {
@@ -594,6 +656,13 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                     const uint32_t sb = sst + Cfg<WM>::kBOff;
                     if (!mine) {
                         // no MMAs; the commits below still count this issuer's arrival
+                    } else if (MX4) {
+                        // A from tensor memory: K = 16 (8 columns) per instruction
+#pragma unroll
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                            tc_mma_f16_tmem_a(d0, a_tm + uint32_t(cslot) * kMx4SlotCols + kk * 8,
+                                              smem_desc_sw128(sb + kk * UMMA_K * 2, 16, 1024),
+                                              idesc, (kb | kk) != 0);
                     } else if (A8) {
                         // both operands K-major 128-byte rows; K = 32 codes (32 bytes)
                         // per instruction, four per stage
@@ -619,7 +688,7 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                     }
                     if (W8) {
                         tc_commit(&ctl->conv_empty[cslot]);
-                        if (++cslot == kConvSlots) {
+                        if (++cslot == Cfg<WM>::kSlots) {
                             cslot = 0;
                             cphase ^= 1u;
                         }
@@ -628,9 +697,10 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                 if (!ok)
                     break;
                 tc_commit(&ctl->tmem_full[abuf]);
-                abuf ^= 1;
-                if (abuf == 0)
+                if (++abuf == Cfg<WM>::kAccBufs) {
+                    abuf = 0;
                     aphase ^= 1u;
+                }
             }
             // all MMAs issued here have completed once this arrives
             tc_commit(&ctl->mma_done);
@@ -655,7 +725,10 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                 const uint8_t *src = smem + stage * SB + Cfg<WM>::kAOff;
                 uint8_t *dst = conv + cslot * kConvSlotBytes;
                 if (MX4) {
-                    widen_mx4_stage<Cfg<WM>::kConvT>(src, dst, ct, nt);
+                    // the MMAs that last read this slot's columns are done
+                    tc_fence_after_sync();
+                    decode_mx4_tile(src, ct, nt,
+                                    tmem_base + kMx4SlotCol + uint32_t(cslot) * kMx4SlotCols);
                 } else {
                 // a tile is 64 K rows x 8 chunks of 16 codes.  Chunk c of row
                 // r (features 16c..16c+15)
@@ -687,13 +760,18 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                     }
                 }
                 }
-                fence_proxy_async_smem();  // the widened tiles -> visible to the MMAs
-                mbar_arrive(&ctl->conv_full[cslot]);
+                if (MX4)
+                    tc_fence_before_sync();  // this thread's tensor-memory stores, done
+                else
+                    fence_proxy_async_smem();  // the widened tiles -> visible to the MMAs
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&ctl->conv_full[cslot]);
                 if (++stage == S) {
                     stage = 0;
                     phase ^= 1u;
                 }
-                if (++cslot == kConvSlots) {
+                if (++cslot == Cfg<WM>::kSlots) {
                     cslot = 0;
                     cphase ^= 1u;
                 }
@@ -847,9 +925,10 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
             }
             tc_fence_before_sync();
             mbar_arrive(&ctl->tmem_empty[abuf]);
-            abuf ^= 1;
-            if (abuf == 0)
+            if (++abuf == Cfg<WM>::kAccBufs) {
+                abuf = 0;
                 aphase ^= 1u;
+            }
         }
         if (et == 0)
             bulk_wait<0>();  // every store written before the CTA (and its smem) goes
@@ -944,13 +1023,13 @@ cudaError_t rows_map_e4m3(RowMaps *m, const void *X, int64_t cap, int K)
     return cudaSuccess;
 }
 
-// MXFP4 codes [E, K, M/2] (two features a byte): unswizzled boxes of 64
-// bytes (128 features) x 64 K rows of one expert.
+// MXFP4 codes [E, M, K/2] (two K a byte): unswizzled boxes of 32 bytes (64
+// K) x 128 features of one expert.
 cudaError_t mx4_code_map(CUtensorMap *m, const void *Wq, int E, int K, int M)
 {
-    const cuuint64_t dims[3] = {cuuint64_t(M / 2), cuuint64_t(K), cuuint64_t(E)};
-    const cuuint64_t strides[2] = {cuuint64_t(M / 2), cuuint64_t(M / 2) * K};
-    const cuuint32_t box[3] = {BM / 2, BK, 1};
+    const cuuint64_t dims[3] = {cuuint64_t(K / 2), cuuint64_t(M), cuuint64_t(E)};
+    const cuuint64_t strides[2] = {cuuint64_t(K / 2), cuuint64_t(K / 2) * M};
+    const cuuint32_t box[3] = {BK / 2, BM, 1};
     return encode_bf16(m, Wq, 3, dims, strides, box, true, true);
 }
 

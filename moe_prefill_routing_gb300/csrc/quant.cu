@@ -108,7 +108,8 @@ cudaError_t launch_quantize_e4m3(const void *W, int E, int K, int M, uint8_t *q,
 //       block of zeros
 //   code = the E2M1 value nearest to W / 2^x, ties to the even code (mantissa
 //       bit 0), past 6 saturated, the sign kept
-// Codes are packed two a byte along M (feature m even in the low four bits).
+// Codes are packed two a byte along K ([E, M, K/2], k even in the low four
+// bits): each output feature's codes are contiguous, 16 bytes a block.
 
 namespace {
 
@@ -122,46 +123,40 @@ __device__ __forceinline__ uint32_t e2m1_code(float a)
            uint32_t(a >= 1.75f) + uint32_t(a > 2.5f) + uint32_t(a >= 3.5f) + uint32_t(a > 5.0f);
 }
 
-// One thread per (expert, block of 32 k, pair of features 2t, 2t + 1).
+// One thread per (expert, block of 32 k, output feature m): the block's 32
+// weights (stride M, coalesced across the threads), its exponent, its 32
+// codes as one 16-byte store.
 __global__ void __launch_bounds__(kQuantThreads)
     k_quant_mxfp4(const __nv_bfloat16 *__restrict__ W, int K, int M,
                   uint8_t *__restrict__ codes, uint8_t *__restrict__ scales)
 {
-    const int t = blockIdx.x * kQuantThreads + threadIdx.x;  // feature pair
+    const int m = blockIdx.x * kQuantThreads + threadIdx.x;  // output feature
     const int b = blockIdx.y;                                // block along K
     const int64_t e = blockIdx.z;
-    if (2 * t >= M)
+    if (m >= M)
         return;
-    const __nv_bfloat162 *src =
-        reinterpret_cast<const __nv_bfloat162 *>(W + (e * K + int64_t(b) * 32) * M) + t;
-    float v0[32], v1[32];
-    float a0 = 0.0f, a1 = 0.0f;
+    const __nv_bfloat16 *src = W + (e * K + int64_t(b) * 32) * M + m;
+    float v[32];
+    float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        const float2 v = __bfloat1622float2(src[int64_t(i) * (M / 2)]);
-        v0[i] = v.x;
-        v1[i] = v.y;
-        a0 = fmaxf(a0, fabsf(v.x));
-        a1 = fmaxf(a1, fabsf(v.y));
+        v[i] = __bfloat162float(src[int64_t(i) * M]);
+        amax = fmaxf(amax, fabsf(v[i]));
     }
     // x from the exponent field of the block maximum (a subnormal or zero
     // maximum clamps to -127)
-    auto exponent = [](float amax) {
-        const int f = int((__float_as_uint(amax) >> 23) & 0xffu);
-        return f == 0 ? -127 : max(-127, min(127, f - 127 - 2));
-    };
-    const int x0 = exponent(a0), x1 = exponent(a1);
-    const float r0 = __uint_as_float(uint32_t(127 - x0) << 23);  // 2^-x, exact (x <= 125 here)
-    const float r1 = __uint_as_float(uint32_t(127 - x1) << 23);
-    uint8_t *out = codes + (e * K + int64_t(b) * 32) * (M / 2) + t;
+    const int f = int((__float_as_uint(amax) >> 23) & 0xffu);
+    const int x = f == 0 ? -127 : max(-127, min(127, f - 127 - 2));
+    const float r = __uint_as_float(uint32_t(127 - x) << 23);  // 2^-x, exact (x <= 125 here)
+    uint32_t word[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        const uint32_t c0 = e2m1_code(fabsf(v0[i]) * r0) | (signbit(v0[i]) ? 8u : 0u);
-        const uint32_t c1 = e2m1_code(fabsf(v1[i]) * r1) | (signbit(v1[i]) ? 8u : 0u);
-        out[int64_t(i) * (M / 2)] = uint8_t(c0 | (c1 << 4));
+        const uint32_t c = e2m1_code(fabsf(v[i]) * r) | (signbit(v[i]) ? 8u : 0u);
+        word[i >> 3] |= c << (4 * (i & 7));
     }
-    *reinterpret_cast<uint16_t *>(scales + (e * (K / 32) + b) * int64_t(M) + 2 * t) =
-        uint16_t((x0 + 127) | ((x1 + 127) << 8));
+    *reinterpret_cast<uint4 *>(codes + (e * M + m) * int64_t(K / 2) + 16 * b) =
+        make_uint4(word[0], word[1], word[2], word[3]);
+    scales[(e * (K / 32) + b) * int64_t(M) + m] = uint8_t(x + 127);
 }
 
 }  // namespace
@@ -169,7 +164,7 @@ __global__ void __launch_bounds__(kQuantThreads)
 cudaError_t launch_quantize_mxfp4(const void *W, int E, int K, int M, uint8_t *codes,
                                   uint8_t *scales, cudaStream_t stream)
 {
-    const dim3 grid(unsigned((M / 2 + kQuantThreads - 1) / kQuantThreads), unsigned(K / 32),
+    const dim3 grid(unsigned((M + kQuantThreads - 1) / kQuantThreads), unsigned(K / 32),
                     unsigned(E));
     k_quant_mxfp4<<<grid, kQuantThreads, 0, stream>>>(static_cast<const __nv_bfloat16 *>(W), K, M,
                                                       codes, scales);

@@ -261,7 +261,8 @@ def test_mxfp4_argument_checks(lib):
     assert lib.moe_quantize_mxfp4(FAKEP, 2, 48, 64, FAKEP, FAKEP, None) == B.MOE_ERR_SHAPE
     assert lib.moe_quantize_mxfp4(FAKEP, 2, 64, 63, FAKEP, FAKEP, None) == B.MOE_ERR_SHAPE
     assert lib.moe_quantize_mxfp4(None, 2, 64, 64, FAKEP, FAKEP, None) == B.MOE_ERR_NULL
-    assert lib.moe_quantize_mxfp4(FAKEP, 2, 64, 64, FAKEP, FAKEP + 1, None) == B.MOE_ERR_ALIGN
+    assert lib.moe_quantize_mxfp4(FAKEP, 2, 64, 64, FAKEP + 8, FAKEP, None) == B.MOE_ERR_ALIGN
+    assert lib.moe_quantize_mxfp4(FAKEP + 2, 2, 64, 64, FAKEP, FAKEP, None) == B.MOE_ERR_ALIGN
     # GEMMs: d and f multiples of 64, scale exponents present and 16-byte aligned
     args = (FAKEP, FAKEP, FAKEP, FAKEP, FAKEP, FAKEP)
     assert lib.moe_ffn_gate_up_mxfp4(*args, 4, 96, 64, 64, FAKEP, None, None) == B.MOE_ERR_SHAPE

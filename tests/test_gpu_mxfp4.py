@@ -3,11 +3,18 @@
 moe_quantize_mxfp4 must give the oracle's codes and scale exponents bit for
 bit.  Every dequantized MXFP4 weight is a bf16 value, so the GEMMs on MXFP4
 weights must equal the bf16 GEMMs on the oracle's dequantized weights bit
-for bit: that pins the in-shared-memory decoding (the 4-bit codes, their
-nibble order, the per-block scales and the swizzled bf16 layout they are
-written in).  The whole layer is checked against the oracle's layer on the
-dequantized weights (the layer bar) and against the bf16 layer on them (bit
-for bit)."""
+for bit: that pins the decoding into tensor memory (the 4-bit codes, their
+nibble order, the per-block scales and the lane / column layout the MMAs
+read them in).
+
+The library stores codes K-major ([E, M, K/2], k even in the low nibble);
+the oracle's are [E, K, M/2] (feature m even in the low nibble).
+``kmajor`` turns the oracle's into the library's layout (a pure
+re-arrangement of the same 4-bit codes).
+
+The whole layer is checked against the oracle's layer on the dequantized
+weights (the layer bar) and against the bf16 layer on them (bit for
+bit)."""
 import numpy as np
 import pytest
 import torch
@@ -19,6 +26,16 @@ from moe_prefill_routing_gb300 import workload as W
 from helpers import dev, dev16, host16, host_f, inputs, layer_tolerance, sample_tokens
 
 pytestmark = pytest.mark.gpu
+
+
+def kmajor(codes):
+    """Oracle codes [E, K, M/2] -> [E, M, K/2] (k even in the low nibble)."""
+    E, K, M2 = codes.shape
+    nib = np.empty((E, K, 2 * M2), dtype=np.uint8)
+    nib[:, :, 0::2] = codes & 0x0F
+    nib[:, :, 1::2] = codes >> 4
+    t = np.ascontiguousarray(nib.transpose(0, 2, 1))  # [E, M, K]
+    return np.ascontiguousarray(t[:, :, 0::2] | (t[:, :, 1::2] << 4))
 
 
 def gpu_quantize(bits):
@@ -42,7 +59,7 @@ def test_quantize_matches_oracle_bitwise(E, K, M, std):
     c, s = gpu_quantize(bits)
     co, so = oracle.quantize_mxfp4(bits)
     assert np.array_equal(s, so)
-    assert np.array_equal(c, co)
+    assert np.array_equal(c, kmajor(co))
 
 
 def test_quantize_workload_weights_sampled_experts():
@@ -51,13 +68,13 @@ def test_quantize_workload_weights_sampled_experts():
     c, s = gpu_quantize(inp["Wd"])
     for e in (0, 77, wl.E - 1):
         co, so = oracle.quantize_mxfp4(inp["Wd"][e:e + 1])
-        assert np.array_equal(c[e:e + 1], co) and np.array_equal(s[e:e + 1], so)
+        assert np.array_equal(c[e:e + 1], kmajor(co)) and np.array_equal(s[e:e + 1], so)
 
 
 def mx_dev(bits):
     """Oracle MXFP4 weights on the device, and their dequantized bf16 weights."""
     codes, scales = oracle.quantize_mxfp4(bits)
-    return B.Mxfp4(dev(codes), dev(scales)), dev16(oracle.dequantize_mxfp4(codes, scales))
+    return B.Mxfp4(dev(kmajor(codes)), dev(scales)), dev16(oracle.dequantize_mxfp4(codes, scales))
 
 
 def staged(inp, E, tm):
