@@ -341,12 +341,16 @@ __device__ __forceinline__ float mx_scale(uint32_t S)
 // bits (e1 e0 m) placed at bf16 bits 8..6 are the exponent field e1 e0 and
 // the mantissa's top bit, which reads value(code) x 2^-126 for every code
 // (e = 0 lands on the subnormal 2^-127 = 0.5 x 2^-126), and the sign at bit
-// 15.  Four bytes of w at once: byte b of ev / od holds the even / odd code
-// of pair b; __byte_perm brings pair b's two codes to bytes 0 and 2.
+// 15.  ev / od hold the even / odd codes of two pairs in bytes 0 and 1
+// (bytes 2 and 3 zero); __byte_perm brings pair b's two codes to bytes 0
+// and 2 with zero bytes 1 and 3, so that one multiply by 2^6 + 2^12 lays
+// each code at bits 6..9 and, again, 12..15 of its half without carries;
+// the mask keeps the magnitude from the first copy and the sign from the
+// second.
 __device__ __forceinline__ uint32_t e2m1_pair_bits(uint32_t ev, uint32_t od, int b)
 {
-    const uint32_t wb = __byte_perm(ev, od, 0x4400u + 0x1111u * uint32_t(b));
-    return ((wb << 6) & 0x01C001C0u) | ((wb << 12) & 0x80008000u);
+    const uint32_t wb = __byte_perm(ev, od, b ? 0x6521u : 0x6420u);
+    return (wb * 0x1040u) & 0x81C081C0u;
 }
 
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&v)[32])
@@ -399,11 +403,12 @@ __device__ __forceinline__ void decode_mx4_tile(const uint8_t *src, int ct, int 
         const uint32_t sc0 = ((s0 + 126u) << 7) * 0x10001u, sc1 = ((s1 + 126u) << 7) * 0x10001u;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const uint32_t ev = cw[i] & 0x0F0F0F0Fu, od = (cw[i] >> 4) & 0x0F0F0F0Fu;
             const uint32_t sc = i < 4 ? sc0 : sc1;
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
-                const uint32_t u = e2m1_pair_bits(ev, od, b);
+                const uint32_t half = b < 2 ? cw[i] : cw[i] >> 16;  // pairs b & 1 of this half
+                const uint32_t u =
+                    e2m1_pair_bits(half & 0x0F0Fu, (half >> 4) & 0x0F0Fu, b & 1);
                 const __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&u),
                                                  *reinterpret_cast<const __nv_bfloat162 *>(&sc));
                 v[4 * i + b] = *reinterpret_cast<const uint32_t *>(&r);
@@ -644,7 +649,10 @@ __global__ void __launch_bounds__(Cfg<WM>::kThreadsK, 1)
                 const uint32_t idesc = A8 ? idesc_e4m3_f32(BM, uint32_t(w.nrows))
                                           : idesc_bf16_f32(BM, uint32_t(w.nrows), MX4 ? 0u : 1u, 0u);
                 for (int kb = 0; kb < nk; ++kb) {
-                    if (!mbar_wait(&ctl->full[stage], phase, abort_flag) ||
+                    // kMx4: the decoding warps arrive on conv_full only after they
+                    // saw the stage full (its B rows with its codes), so the
+                    // issuers wait on conv_full alone
+                    if ((!MX4 && !mbar_wait(&ctl->full[stage], phase, abort_flag)) ||
                         (W8 && !mbar_wait(&ctl->conv_full[cslot], cphase, abort_flag))) {
                         ok = false;
                         break;
