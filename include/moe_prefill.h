@@ -415,9 +415,10 @@ MOE_API int moe_layer_forward_f8(const void *x, const int32_t *ids, const float 
  *
  * moe_quantize_mxfp4 -- W bf16 [E, K, M] (M = output features, contiguous;
  * K a multiple of 32, M even; 4-byte aligned) -> codes uint8 [E, M, K/2]
- * (each output feature's codes contiguous along K: k even in the low four
- * bits of byte k/2, k + 1 in the high four; 16-byte aligned) and scales
- * uint8 [E, K/32, M] (S).  W must be finite.  A one-time preparation, not
+ * (each output feature's codes contiguous along K, eight to a little-endian
+ * 32-bit word: the word of k = 8i .. 8i + 7 holds k = 8i + 2j in bits
+ * 4j .. 4j + 3 and k = 8i + 2j + 1 in bits 16 + 4j .. 19 + 4j; 16-byte
+ * aligned) and scales uint8 [E, K/32, M] (S).  W must be finite.  A one-time preparation, not
  * part of the layer.
  *
  * moe_ffn_gate_up_mxfp4 / moe_ffn_down_mxfp4 -- moe_ffn_gate_up /

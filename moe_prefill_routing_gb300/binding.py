@@ -512,8 +512,9 @@ def layer_forward_e4m3(x, ids, w, Wg, Wu, Wd, tm: int, y=None, ws=None, act_e4m3
 
 
 class Mxfp4(NamedTuple):
-    """MXFP4 weights of one projection: codes uint8 [E, M, K/2] (two 4-bit
-    E2M1 codes a byte along K, k even in the low four bits) and scale
+    """MXFP4 weights of one projection: codes uint8 [E, M, K/2] (4-bit E2M1
+    codes along K, eight to a 32-bit word: k = 8i + 2j at bits 4j.., its odd
+    neighbour 16 bits higher) and scale
     exponents uint8 [E, K/32, M] (scale 2^(S-127) per block of 32 along K)."""
     codes: torch.Tensor
     scales: torch.Tensor

@@ -114,7 +114,8 @@ constexpr int kMaxSlots = kConvSlots > kMx4Slots ? kConvSlots : kMx4Slots;
 enum WeightMode : int { kBf16 = 0, kWiden = 1, kNative = 2, kMx4 = 3 };
 
 // kMx4: MXFP4 weights -- 4-bit E2M1 codes, two per byte along K (the
-// reduction axis; [E, M, K/2], k even in the low four bits), and one
+// reduction axis; [E, M, K/2], eight codes to a 32-bit word: k = 8i + 2j at
+// bits 4j .. 4j + 3, k = 8i + 2j + 1 at bits 16 + 4j .. 19 + 4j), and one
 // power-of-two scale 2^(S-127) per (expert, block of 32 along K, output
 // feature) ([E, K/32, M] exponent bytes).  A stage holds the B rows first
 // (16 KB, 1024-byte aligned), then per A tile the codes (128 features x 32
@@ -336,21 +337,29 @@ __device__ __forceinline__ float mx_scale(uint32_t S)
     return __uint_as_float(S ? S << 23 : 0x00400000u);
 }
 
-// Two E2M1 codes of one byte (k even in the low four bits) -> the bf16 pair
+// Two E2M1 codes (pair j of a code word: k even and odd) -> the bf16 pair
 // value(code) x 2^-126 (low half: the even k), exactly: the three magnitude
 // bits (e1 e0 m) placed at bf16 bits 8..6 are the exponent field e1 e0 and
 // the mantissa's top bit, which reads value(code) x 2^-126 for every code
 // (e = 0 lands on the subnormal 2^-127 = 0.5 x 2^-126), and the sign at bit
-// 15.  ev / od hold the even / odd codes of two pairs in bytes 0 and 1
-// (bytes 2 and 3 zero); __byte_perm brings pair b's two codes to bytes 0
-// and 2 with zero bytes 1 and 3, so that one multiply by 2^6 + 2^12 lays
-// each code at bits 6..9 and, again, 12..15 of its half without carries;
-// the mask keeps the magnitude from the first copy and the sign from the
-// second.
-__device__ __forceinline__ uint32_t e2m1_pair_bits(uint32_t ev, uint32_t od, int b)
+// 15.  A code word holds pair j's even code at bits 4j..4j+3 and its odd
+// code 16 bits higher; masked out (w & 0x000F000F << 4j) and multiplied by
+// 2^(6-4j) + 2^(12-4j) (j = 0, 1; the word shifted right by 8 first for
+// j = 2, 3), each code lands at bits 6..9 and, again, 12..15 of its half
+// without carries; the final mask keeps the magnitude from the first copy
+// and the sign from the second.
+__device__ __forceinline__ uint32_t e2m1_pair_bits(uint32_t w, int j)
 {
-    const uint32_t wb = __byte_perm(ev, od, b ? 0x6521u : 0x6420u);
-    return (wb * 0x1040u) & 0x81C081C0u;
+    const uint32_t x = (j & 2) ? w >> 8 : w;
+    return (j & 1) ? ((x & 0x00F000F0u) * 0x104u) & 0x81C081C0u
+                   : ((x & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;
+}
+
+// Pair j of a code word as the two-code byte (the even k in the low four
+// bits) the f16 conversion takes.
+__device__ __forceinline__ uint32_t e2m1_pair_byte(uint32_t w, int j)
+{
+    return ((w >> (4 * j)) & 0xFu) | (((w >> (16 + 4 * j)) & 0xFu) << 4);
 }
 
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&v)[32])
@@ -406,9 +415,7 @@ __device__ __forceinline__ void decode_mx4_tile(const uint8_t *src, int ct, int 
             const uint32_t sc = i < 4 ? sc0 : sc1;
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
-                const uint32_t half = b < 2 ? cw[i] : cw[i] >> 16;  // pairs b & 1 of this half
-                const uint32_t u =
-                    e2m1_pair_bits(half & 0x0F0Fu, (half >> 4) & 0x0F0Fu, b & 1);
+                const uint32_t u = e2m1_pair_bits(cw[i], b);
                 const __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&u),
                                                  *reinterpret_cast<const __nv_bfloat162 *>(&sc));
                 v[4 * i + b] = *reinterpret_cast<const uint32_t *>(&r);
@@ -422,7 +429,7 @@ __device__ __forceinline__ void decode_mx4_tile(const uint8_t *src, int ct, int 
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
                 const float2 f = __half22float2(__half2(__nv_cvt_fp4x2_to_halfraw2(
-                    static_cast<__nv_fp4x2_storage_t>((cw[i] >> (8 * b)) & 0xffu), __NV_E2M1)));
+                    static_cast<__nv_fp4x2_storage_t>(e2m1_pair_byte(cw[i], b)), __NV_E2M1)));
                 const __nv_bfloat162 r = __floats2bfloat162_rn(f.x * x, f.y * x);
                 v[4 * i + b] = *reinterpret_cast<const uint32_t *>(&r);
             }

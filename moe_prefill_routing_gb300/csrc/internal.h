@@ -110,9 +110,9 @@ cudaError_t launch_ffn_down_e4m3(const void *H, const uint8_t *Wd, const float *
                                  const int32_t *offsets, const float *srt_w, int E, int d, int f,
                                  int64_t cap, void *Ys, uint32_t *status, cudaStream_t stream);
 
-// MXFP4 weights: codes [E, M, K/2] (two 4-bit E2M1 codes a byte, k even in
-// the low four bits) and scale exponents [E, K/32, M] (2^(S-127)); see
-// quant.cu.  The GEMMs decode them to bf16 into tensor memory.
+// MXFP4 weights: codes [E, M, K/2] (4-bit E2M1 codes along K, eight to a
+// 32-bit word in the order quant.cu gives) and scale exponents [E, K/32, M]
+// (2^(S-127)); see quant.cu.  The GEMMs decode them to bf16 into tensor memory.
 cudaError_t launch_quantize_mxfp4(const void *W, int E, int K, int M, uint8_t *codes,
                                   uint8_t *scales, cudaStream_t stream);
 cudaError_t launch_ffn_gate_up_mxfp4(const void *xs, const uint8_t *Wg, const uint8_t *sg,

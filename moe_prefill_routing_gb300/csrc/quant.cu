@@ -108,8 +108,11 @@ cudaError_t launch_quantize_e4m3(const void *W, int E, int K, int M, uint8_t *q,
 //       block of zeros
 //   code = the E2M1 value nearest to W / 2^x, ties to the even code (mantissa
 //       bit 0), past 6 saturated, the sign kept
-// Codes are packed two a byte along K ([E, M, K/2], k even in the low four
-// bits): each output feature's codes are contiguous, 16 bytes a block.
+// Codes are stored along K ([E, M, K/2] bytes: each output feature's codes
+// contiguous, 16 bytes a block), eight to a 32-bit word (little-endian): the
+// word of k = 8i .. 8i + 7 holds k = 8i + 2j in bits 4j .. 4j + 3 and
+// k = 8i + 2j + 1 in bits 16 + 4j .. 19 + 4j (j = 0..3), the order in which
+// the GEMMs' decode takes them apart with one mask each.
 
 namespace {
 
@@ -152,7 +155,7 @@ __global__ void __launch_bounds__(kQuantThreads)
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         const uint32_t c = e2m1_code(fabsf(v[i]) * r) | (signbit(v[i]) ? 8u : 0u);
-        word[i >> 3] |= c << (4 * (i & 7));
+        word[i >> 3] |= c << (4 * ((i & 7) >> 1) + 16 * (i & 1));
     }
     *reinterpret_cast<uint4 *>(codes + (e * M + m) * int64_t(K / 2) + 16 * b) =
         make_uint4(word[0], word[1], word[2], word[3]);

@@ -7,8 +7,9 @@ for bit: that pins the decoding into tensor memory (the 4-bit codes, their
 nibble order, the per-block scales and the lane / column layout the MMAs
 read them in).
 
-The library stores codes K-major ([E, M, K/2], k even in the low nibble);
-the oracle's are [E, K, M/2] (feature m even in the low nibble).
+The library stores codes along K ([E, M, K/2] bytes, eight codes to a
+little-endian 32-bit word: k = 8i + 2j at bits 4j, k = 8i + 2j + 1 at bits
+16 + 4j); the oracle's are [E, K, M/2] (feature m even in the low nibble).
 ``kmajor`` turns the oracle's into the library's layout (a pure
 re-arrangement of the same 4-bit codes).
 
@@ -29,13 +30,17 @@ pytestmark = pytest.mark.gpu
 
 
 def kmajor(codes):
-    """Oracle codes [E, K, M/2] -> [E, M, K/2] (k even in the low nibble)."""
+    """Oracle codes [E, K, M/2] -> the library's [E, M, K/2]: per group of
+    eight k, bytes (k0 | k2 << 4, k4 | k6 << 4, k1 | k3 << 4, k5 | k7 << 4)."""
     E, K, M2 = codes.shape
     nib = np.empty((E, K, 2 * M2), dtype=np.uint8)
     nib[:, :, 0::2] = codes & 0x0F
     nib[:, :, 1::2] = codes >> 4
-    t = np.ascontiguousarray(nib.transpose(0, 2, 1))  # [E, M, K]
-    return np.ascontiguousarray(t[:, :, 0::2] | (t[:, :, 1::2] << 4))
+    t = nib.transpose(0, 2, 1).reshape(E, 2 * M2, K // 8, 8)  # [E, M, K/8, 8]
+    out = np.empty((E, 2 * M2, K // 8, 4), dtype=np.uint8)
+    for b, (lo, hi) in enumerate(((0, 2), (4, 6), (1, 3), (5, 7))):
+        out[..., b] = t[..., lo] | (t[..., hi] << 4)
+    return np.ascontiguousarray(out.reshape(E, 2 * M2, K // 2))
 
 
 def gpu_quantize(bits):
@@ -118,6 +123,31 @@ def test_gemms_equal_bf16_gemms_on_dequantized_weights(T, d, E, k, f, tm):
     ok, err, bound = layer_tolerance(
         W.bits_to_float(host16(H4)[real], "bf16").astype(np.float64), h_ref)
     assert ok, (err, bound)
+
+
+def test_gemms_large_weights_take_the_fp32_scaling():
+    # blocks with |W| >= 8 (S > 128) decode through the f16 conversion and an
+    # fp32 multiply; mixed with ordinary blocks in the same tiles
+    T, d, E, k, f, tm = 120, 128, 3, 2, 192, 16
+    inp = W.make_layer(T, d, E, k, f, tm=tm, seed=77, skip_frac=0.0)
+    for n in ("Wg", "Wu", "Wd"):
+        Wf = W.bits_to_float(inp[n], "bf16").astype(np.float32)
+        Wf[:, :, ::3] *= 4000.0      # every third output feature: |W| up to ~300
+        inp[n] = W.bf16_bits(Wf)
+    p, xs = staged(inp, E, tm)
+    cap = B.capacity(T, k, E, tm)
+    offsets = dev(p["offsets"])
+    (mg, g16), (mu, u16), (md, d16w) = (mx_dev(inp[n]) for n in ("Wg", "Wu", "Wd"))
+    assert int(mg.scales.max()) > 128 and int(mg.scales.min()) <= 128
+    xs_d = dev16(to_cap(xs, cap))
+    R = p["R_pad"]
+    H4 = B.ffn_gate_up_mxfp4(xs_d, mg, mu, offsets, cap)
+    H16 = B.ffn_gate_up(xs_d, g16, u16, offsets, cap)
+    assert torch.equal(H4[:R].view(torch.int16), H16[:R].view(torch.int16))
+    srt_w = dev(to_cap(p["srt_w"], cap))
+    Y4 = B.ffn_down_mxfp4(H16, md, offsets, srt_w, cap)
+    Y16 = B.ffn_down(H16, d16w, offsets, srt_w, cap)
+    assert torch.equal(Y4[:R].view(torch.int16), Y16[:R].view(torch.int16))
 
 
 def layer_case(inp, tm, tokens=None):
