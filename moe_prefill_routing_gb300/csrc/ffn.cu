@@ -108,7 +108,7 @@ constexpr int kConvSlots = 2;
 constexpr uint32_t kConvSlotBytes = 2 * kATileBytes;
 constexpr int kMx4Slots = 4;      // kMx4: decoded A tiles in tensor memory, four slots
 constexpr uint32_t kMx4SlotCol = kAccCols;       // first TMEM column of the slots (256)
-constexpr uint32_t kMx4SlotCols = 2 * (BK / 2);     // a slot: two tiles of 64 K = 32 columns
+constexpr uint32_t kMx4SlotCols = 2 * (BK / 2);  // a slot: two tiles of 32 columns (64 K each)
 constexpr int kMaxSlots = kConvSlots > kMx4Slots ? kConvSlots : kMx4Slots;
 
 enum WeightMode : int { kBf16 = 0, kWiden = 1, kNative = 2, kMx4 = 3 };
@@ -124,9 +124,9 @@ enum WeightMode : int { kBf16 = 0, kWiden = 1, kNative = 2, kMx4 = 3 };
 // write each A tile straight into tensor memory (tcgen05.st: lane = output
 // feature, one 32-bit column per two K), where the MMAs read it as their A
 // operand ([a_tmem] form); B stays in shared memory.  The decoded tiles
-// never pass through shared memory, whose bandwidth bounded the design that
-// staged them there (the stores, the MMAs' A reads and the TMA writes all
-// shared it).  Tensor memory then holds one accumulator buffer (columns 0 ..
+// never pass through shared memory (staging them there, swizzled for the
+// MMAs, measured 398 against 316 us for the full layer's gate/up with the
+// same decode).  Tensor memory then holds one accumulator buffer (columns 0 ..
 // 255) and four decoded-A slots (256 .. 511); the epilogue of a unit and the
 // next unit's MMAs do not overlap.  The epilogue applies no scale.
 constexpr uint32_t kMx4CodeBytes = BM * BK / 2;   // 4 KB: 128 features x 64 K, 4 bits each
