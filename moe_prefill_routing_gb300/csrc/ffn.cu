@@ -125,8 +125,8 @@ enum WeightMode : int { kBf16 = 0, kWiden = 1, kNative = 2, kMx4 = 3 };
 // feature, one 32-bit column per two K), where the MMAs read it as their A
 // operand ([a_tmem] form); B stays in shared memory.  The decoded tiles
 // never pass through shared memory (staging them there, swizzled for the
-// MMAs, measured 398 against 316 us for the full layer's gate/up with the
-// same decode).  Tensor memory then holds one accumulator buffer (columns 0 ..
+// MMAs, measured 398-404 us against 316 us for the full layer's gate/up,
+// with either decode).  Tensor memory then holds one accumulator buffer (columns 0 ..
 // 255) and four decoded-A slots (256 .. 511); the epilogue of a unit and the
 // next unit's MMAs do not overlap.  The epilogue applies no scale.
 constexpr uint32_t kMx4CodeBytes = BM * BK / 2;   // 4 KB: 128 features x 64 K, 4 bits each
